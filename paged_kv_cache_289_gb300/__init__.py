@@ -1,1 +1,199 @@
-"""libpagedkv Python binding (filled in with the C-ABI library)."""
+"""Python binding of libpagedkv (the C ABI in include/pagedkv.h).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors are torch CUDA tensors (PyTorch supplies device memory and streams);
+their data pointers go straight to the C entry points of the same names.
+There is no CPU fallback: if the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "PkvError", "lib", "library_path", "BF16", "FP8_E4M3", "DEVERR_WAIT_TIMEOUT",
+    "DEVERR_SEQ_CLAMPED", "DEVERR_BLOCK_RANGE", "compute_slot_mapping", "kv_cache_write",
+    "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn", "prefix_block_hash",
+    "device_num_sms", "read_device_error",
+]
+
+BF16 = 0
+FP8_E4M3 = 1
+DEVERR_WAIT_TIMEOUT = 0x1
+DEVERR_SEQ_CLAMPED = 0x2
+DEVERR_BLOCK_RANGE = 0x4
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "lib", "libpagedkv.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class PkvError(RuntimeError):
+    def __init__(self, fn, status):
+        name = lib().pkv_status_string(status).decode() if _lib is not None else str(status)
+        super().__init__(f"{fn} failed: {name} ({status})")
+        self.status = status
+
+
+def lib():
+    """Load libpagedkv.so (built by __graft_entry__.build())."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(library_path):
+                raise RuntimeError(
+                    f"libpagedkv.so is not built ({library_path}); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(library_path)
+            p, i, i64, u64, f, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64,
+                                     ctypes.c_uint64, ctypes.c_float, ctypes.c_size_t)
+            L.pkv_status_string.restype = ctypes.c_char_p
+            L.pkv_status_string.argtypes = [i]
+            L.pkv_version.restype = i
+            L.pkv_version.argtypes = []
+            L.pkv_device_num_sms.restype = i
+            L.pkv_device_num_sms.argtypes = [p]
+            L.pkv_compute_slot_mapping.restype = i
+            L.pkv_compute_slot_mapping.argtypes = [p, i, p, p, i, i, p, p]
+            L.pkv_kv_cache_write.restype = i
+            L.pkv_kv_cache_write.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, p, p]
+            L.pkv_decode_workspace_size.restype = sz
+            L.pkv_decode_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.pkv_paged_decode_attn.restype = i
+            L.pkv_paged_decode_attn.argtypes = [p, p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
+                                                p, p, sz, p]
+            L.pkv_prefix_block_hash.restype = i
+            L.pkv_prefix_block_hash.argtypes = [p, p, i, i, u64, p, p, p]
+            _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise PkvError(fn, status)
+
+
+def _need(t, name, dtypes, contiguous=True):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtypes and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _cache_dtype(t):
+    return FP8_E4M3 if t.element_size() == 1 else BF16
+
+
+def device_num_sms() -> int:
+    n = ctypes.c_int(0)
+    _check("pkv_device_num_sms", lib().pkv_device_num_sms(ctypes.byref(n)))
+    return n.value
+
+
+def compute_slot_mapping(block_table, positions, block_size, req_idx=None, out=None, stream=None):
+    """slot[t] = block_table[r][pos/BS]*BS + pos%BS (r = req_idx[t], or t); -1 for pos < 0."""
+    import torch
+    _need(block_table, "block_table", (torch.int32,))
+    _need(positions, "positions", (torch.int32,))
+    if req_idx is not None:
+        _need(req_idx, "req_idx", (torch.int32,))
+    T = positions.shape[0]
+    if out is None:
+        out = torch.empty(T, dtype=torch.int64, device=positions.device)
+    _check("pkv_compute_slot_mapping", lib().pkv_compute_slot_mapping(
+        _ptr(block_table), block_table.shape[1], _ptr(req_idx), _ptr(positions), T, block_size,
+        _ptr(out), _stream(stream)))
+    return out
+
+
+def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None, stream=None):
+    """Write new K/V rows [T, Hkv, D] (bf16) into the paged caches [NB, Hkv, BS, D]."""
+    import torch
+    _need(k, "k", (torch.bfloat16,))
+    _need(v, "v", (torch.bfloat16,))
+    _need(slot_mapping, "slot_mapping", (torch.int64,))
+    _need(k_cache, "k_cache", None)
+    _need(v_cache, "v_cache", None)
+    T, Hkv, D = k.shape
+    NB, _, BS, _ = k_cache.shape
+    _check("pkv_kv_cache_write", lib().pkv_kv_cache_write(
+        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, BS, NB, _cache_dtype(k_cache),
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _stream(stream)))
+
+
+def decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype,
+                          num_sms=0) -> int:
+    return int(lib().pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                               block_size, cache_dtype, num_sms))
+
+
+def alloc_decode_workspace(batch, num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype,
+                           device="cuda"):
+    """A zeroed workspace of the size the decode call needs (its first word is the
+    sticky device error word)."""
+    import torch
+    n = decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype)
+    if n == 0:
+        raise PkvError("pkv_decode_workspace_size", -2)
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def read_device_error(workspace) -> int:
+    """The device error word (PKV_DEVERR_* bits) of a decode workspace (synchronises)."""
+    return int(workspace[:4].view(__import__("torch").int32).item()) & 0xFFFFFFFF
+
+
+def paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, scale, out=None, k_scale=None,
+                      v_scale=None, workspace=None, stream=None):
+    """out[r, hq] = softmax(scale * q[r, hq] K_r^T) V_r over the paged caches."""
+    import torch
+    _need(q, "q", (torch.bfloat16,))
+    _need(k_cache, "k_cache", None)
+    _need(v_cache, "v_cache", None)
+    _need(block_table, "block_table", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    N, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_cache.shape
+    dt = _cache_dtype(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_decode_workspace(N, Hq, Hkv, D, BS, dt, device=q.device)
+    _check("pkv_paged_decode_attn", lib().pkv_paged_decode_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D, BS, NB, dt, float(scale), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def prefix_block_hash(tokens, offsets, block_size, hash_offsets, num_hashes, seed=0, out=None,
+                      stream=None):
+    """Chained block hashes of CSR token sequences; returns an int64 tensor holding the
+    uint64 bit patterns, laid out by `hash_offsets`."""
+    import torch
+    _need(tokens, "tokens", (torch.int32,))
+    _need(offsets, "offsets", (torch.int64,))
+    _need(hash_offsets, "hash_offsets", (torch.int64,))
+    if out is None:
+        out = torch.empty(max(int(num_hashes), 1), dtype=torch.int64, device=tokens.device)
+    _check("pkv_prefix_block_hash", lib().pkv_prefix_block_hash(
+        _ptr(tokens), _ptr(offsets), offsets.shape[0] - 1, block_size,
+        int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out), _ptr(hash_offsets), _stream(stream)))
+    return out[:num_hashes]

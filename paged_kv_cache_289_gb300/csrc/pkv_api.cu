@@ -1,0 +1,161 @@
+// pkv_api.cu -- the extern "C" entry points of libpagedkv.
+//
+// Every entry point validates its host-side scalars and pointer alignment
+// first and launches nothing when a check fails.  No entry point synchronises
+// the device or copies device memory to the host.
+#include <stdint.h>
+
+#include "pkv_internal.cuh"
+
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool shape_supported(int Hq, int Hkv, int D, int BS, int dtype) {
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > pkv::kGroupPad) return false;
+    if (BS != 16 && BS != 32) return false;
+    if (dtype == PKV_BF16) return D == 64 || D == 128;
+    if (dtype == PKV_FP8_E4M3) return D == 128;
+    return false;
+}
+
+int current_num_sms(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    *out = n;
+    return PKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_status_string(int status) {
+    switch (status) {
+        case PKV_OK: return "PKV_OK";
+        case PKV_ERR_INVALID_ARG: return "PKV_ERR_INVALID_ARG";
+        case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
+        case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
+        case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        default: return "PKV_UNKNOWN_STATUS";
+    }
+}
+
+int pkv_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+int pkv_device_num_sms(int* num_sms) {
+    if (!num_sms) return PKV_ERR_INVALID_ARG;
+    return current_num_sms(num_sms);
+}
+
+int pkv_compute_slot_mapping(const int32_t* block_table, int max_blocks_per_seq,
+                             const int32_t* req_idx, const int32_t* positions, int num_tokens,
+                             int block_size, int64_t* slot_mapping, pkv_stream_t stream) {
+    if (num_tokens < 0 || block_size <= 0 || max_blocks_per_seq <= 0) return PKV_ERR_INVALID_ARG;
+    if (num_tokens == 0) return PKV_OK;
+    if (!block_table || !positions || !slot_mapping) return PKV_ERR_INVALID_ARG;
+    cudaError_t e = pkv::slot_mapping_launch(block_table, max_blocks_per_seq, req_idx, positions,
+                                             num_tokens, block_size, slot_mapping,
+                                             reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping, int num_tokens,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks,
+                       int cache_dtype, void* k_cache, void* v_cache, const float* k_scale,
+                       const float* v_scale, pkv_stream_t stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
+    if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PKV_ERR_INVALID_ARG;
+    cudaError_t e = pkv::cache_write_launch(
+        k, v, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, num_blocks,
+        cache_dtype == PKV_FP8_E4M3, k_cache, v_cache, k_scale, v_scale,
+        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int cache_dtype, int num_sms) {
+    if (batch < 0 || batch > pkv::kMaxBatch) return 0;
+    if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype)) return 0;
+    if (num_sms <= 0 && current_num_sms(&num_sms) != PKV_OK) return 0;
+    return pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
+                                       cache_dtype == PKV_FP8_E4M3, num_sms);
+}
+
+int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                          const float* k_scale, const float* v_scale,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                          int head_dim, int block_size, int num_blocks, int cache_dtype,
+                          float scale, void* out, void* workspace, size_t workspace_bytes,
+                          pkv_stream_t stream) {
+    if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+    if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype))
+        return PKV_ERR_UNSUPPORTED;
+    if (batch > pkv::kMaxBatch) return PKV_ERR_UNSUPPORTED;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PKV_ERR_INVALID_ARG;
+    // flat page index and TMA row coordinates are int32
+    const int64_t rows = ((int64_t)num_blocks + 1) * num_kv_heads * block_size;
+    const int64_t max_pages = (int64_t)batch * num_kv_heads * max_blocks_per_seq;
+    if (rows >= (int64_t)1 << 31 || max_pages >= (int64_t)1 << 31 ||
+        (int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 31)
+        return PKV_ERR_UNSUPPORTED;
+    int num_sms = 0;
+    if (current_num_sms(&num_sms) != PKV_OK) return PKV_ERR_CUDA;
+    const size_t need = pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
+                                                    cache_dtype == PKV_FP8_E4M3, num_sms);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
+    pkv::DecodeLaunch L;
+    L.q = q;
+    L.k_cache = k_cache;
+    L.v_cache = v_cache;
+    L.k_scale = k_scale;
+    L.v_scale = v_scale;
+    L.block_table = block_table;
+    L.seq_lens = seq_lens;
+    L.out = out;
+    L.workspace = workspace;
+    L.N = batch;
+    L.Hq = num_q_heads;
+    L.Hkv = num_kv_heads;
+    L.D = head_dim;
+    L.BS = block_size;
+    L.MB = max_blocks_per_seq;
+    L.NB = num_blocks;
+    L.fp8 = cache_dtype == PKV_FP8_E4M3;
+    L.scale = scale;
+    L.num_sms = num_sms;
+    return pkv::decode_launch(L, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pkv_prefix_block_hash(const int32_t* tokens, const int64_t* offsets, int num_seqs,
+                          int block_size, uint64_t seed, uint64_t* hashes,
+                          const int64_t* hash_offsets, pkv_stream_t stream) {
+    if (num_seqs < 0 || block_size <= 0 || block_size > 1024) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!tokens || !offsets || !hashes || !hash_offsets) return PKV_ERR_INVALID_ARG;
+    cudaError_t e = pkv::prefix_hash_launch(tokens, offsets, num_seqs, block_size, seed, hashes,
+                                            hash_offsets, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,730 @@
+// pkv_decode.cu -- paged GQA decode attention for sm_103a.
+//
+// Computes, for every request r and query head hq (kv head h = hq / G),
+//     out[r][hq] = softmax(scale * q K_r^T) V_r
+// where K_r / V_r are the request's pages gathered through its block table
+// ("深入LLM推理：从KV Cache到PD分离的Serving全景解析", sections "KV Cache：Transformer
+// 的循环状态" and "PagedAttention与Cache管理"), with an online (running max / sum)
+// softmax ("GPU推理深度拆解：KV Cache视角", 算子优化要点) and the KV length split
+// across warps when the batch is small (same note: batch-1 decode leaves SMs idle).
+//
+// Work decomposition.  Unit u = (request r, kv head h) owns np_r = ceil(seq_r / BS)
+// pages.  All units' pages form one flat list of P items (request-major, then
+// head, then page).  A persistent grid of W warps (one CTA per SM) cuts the list
+// into W equal contiguous ranges, so every warp streams the same number of bytes
+// whatever the length mix.  A warp walks its range unit by unit ("segments");
+// a segment that covers a whole unit writes the bf16 output directly, otherwise
+// it writes an unnormalised partial (o, running max m, sum l) to workspace slot
+// u + w (unique: unit and warp ranges are both ordered).  A second kernel merges
+// the partials of split units with log-sum-exp weights.
+//
+// Per-warp pipeline.  Each warp owns `stages` shared-memory stages of one
+// (block, head) K page + V page.  Lane 0 issues 2-D bulk tensor copies (TMA,
+// 128-byte swizzle, box = 128 bytes x BS rows) that complete on the stage's
+// mbarrier; all lanes wait on it (bounded), compute, and the stage is refilled
+// with the page `stages` ahead.  Block ids for the next 32 pages are looked up
+// one batch ahead (one lane per page), so the issue path never waits on the
+// block table.
+//
+// Math per page (tensor cores, mma.sync m16n8k16, fp32 accumulators):
+//   S^T[t][g] = K[t][:] . Q[g][:]     A = K page tile (16 tokens x 16 d, ldmatrix),
+//                                     B = Q^T of the GQA group (8 heads, registers)
+//   O^T[d][g] += V^T[d][t] P^T[t][g]  A = V page tile (ldmatrix.trans), B = P^T from
+//                                     the S^T accumulators via movmatrix.trans
+// FP8 (E4M3) pages are widened to fp16 in registers (cvt e4m3x2 -> f16x2); the
+// per-(block, head) K scale multiplies S, the V scale multiplies the page's P.V
+// contribution, so neither scale is rounded into an fp16 operand.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+struct DecodeArgs {
+    const uint16_t* q;
+    uint16_t* out;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const float* k_scale;
+    const float* v_scale;
+    uint32_t* err;
+    int32_t* g_prefix;
+    float* partials;
+    int N, Hq, Hkv, G, MB, NB;
+    float scale_log2;   // scale * log2(e): scores kept in the log2 domain
+    int stages;
+    int total_warps;
+};
+
+template <int D, int BS, bool FP8>
+struct Cfg {
+    static constexpr int ELT = FP8 ? 1 : 2;
+    static constexpr int ROW_BYTES = D * ELT;
+    static constexpr int CH = ROW_BYTES / 128;            // 128-byte column chunks per row
+    static constexpr int CH_ELEMS = 128 / ELT;            // elements per chunk
+    static constexpr int PAGE_BYTES = BS * ROW_BYTES;     // one K (or V) page
+    static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
+    static constexpr int MT = BS / 16;                    // 16-token tiles per page
+    static constexpr int KS = D / 16;                     // QK k-steps
+    static constexpr int DT = D / 16;                     // PV d-tiles
+    static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle lines");
+    static_assert(BS % 16 == 0, "block size must be a multiple of 16");
+};
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Byte offset of 16-byte chunk `kc` of token row `t` inside a page laid out by
+// TMA with 128-byte swizzle: column chunk region, then rows of 128 bytes whose
+// 16-byte units are XOR-permuted by (row mod 8).
+template <int BS>
+__device__ __forceinline__ uint32_t swz(int t, int kc) {
+    return (uint32_t)((kc >> 3) * (BS * 128) + t * 128 + (((kc & 7) ^ (t & 7)) << 4));
+}
+
+// Per-lane description of one page of a 32-page batch.
+struct PageBatch {
+    int id;        // physical block (NB = out of range sentinel)
+    int r, h;      // unit
+    uint32_t fl;   // valid tokens | first << 8 | last << 9
+    float ks, vs;  // FP8 scales
+};
+
+template <int BS, bool FP8>
+__device__ __forceinline__ void load_batch(PageBatch& b, int xbeg, int x1,
+                                           const int32_t* s_prefix, const int32_t* s_seq,
+                                           const DecodeArgs& a, uint32_t& errbits) {
+    const int lane = threadIdx.x & 31;
+    const int x = xbeg + lane;
+    b.id = a.NB; b.r = 0; b.h = 0; b.fl = 0; b.ks = 1.f; b.vs = 1.f;
+    if (x >= x1) return;
+    int lo = 0, hi = a.N;   // s_prefix[lo] <= x < s_prefix[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_prefix[mid] <= x) lo = mid; else hi = mid;
+    }
+    const int r = lo;
+    const int np = (s_prefix[r + 1] - s_prefix[r]) / a.Hkv;
+    const int off = x - s_prefix[r];
+    const int h = off / np;
+    const int j = off - h * np;
+    int id = __ldg(a.block_table + (int64_t)r * a.MB + j);
+    if (id < 0 || id >= a.NB) {
+        errbits |= PKV_DEVERR_BLOCK_RANGE;
+        id = a.NB;   // TMA of rows past the tensor end reads zeros
+    }
+    const int ntok = min(BS, s_seq[r] - j * BS);
+    b.id = id;
+    b.r = r;
+    b.h = h;
+    b.fl = (uint32_t)ntok | ((j == 0) ? 0x100u : 0u) | ((j == np - 1) ? 0x200u : 0u);
+    if (FP8 && id < a.NB) {
+        b.ks = __ldg(a.k_scale + (int64_t)id * a.Hkv + h);
+        b.vs = __ldg(a.v_scale + (int64_t)id * a.Hkv + h);
+    }
+}
+
+template <int D, int BS, bool FP8>
+__global__ void __launch_bounds__(256, 1)
+    pkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
+                      const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
+    using C = Cfg<D, BS, FP8>;
+    extern __shared__ uint8_t smem_raw[];
+    const int NW = blockDim.x >> 5;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int S = a.stages;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* basep = smem_raw + (base - raw);
+    const uint32_t stage0 = base + (uint32_t)(warp * S * C::STAGE_BYTES);
+    const uint32_t bars = base + (uint32_t)(NW * S * C::STAGE_BYTES) + (uint32_t)(warp * S * 8);
+    int32_t* s_prefix = reinterpret_cast<int32_t*>(basep + NW * S * C::STAGE_BYTES + NW * S * 8);
+    int32_t* s_seq = s_prefix + (a.N + 1);
+
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(bars + 8u * s, 1);
+        fence_mbar_init();
+    }
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmK);
+        prefetch_tensormap(&tmV);
+    }
+
+    // ---- page prefix over requests (every CTA computes its own copy) ----
+    uint32_t errbits = 0;
+    const int maxlen = a.MB * BS;
+    for (int i = threadIdx.x; i < a.N; i += blockDim.x) {
+        const int s = __ldg(a.seq_lens + i);
+        const int c = min(max(s, 0), maxlen);
+        if (c != s) errbits |= PKV_DEVERR_SEQ_CLAMPED;
+        s_seq[i] = c;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int running = 0;
+        for (int b0 = 0; b0 < a.N; b0 += 32) {
+            const int i = b0 + lane;
+            int v = (i < a.N) ? a.Hkv * ((s_seq[i] + BS - 1) / BS) : 0;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += n;
+            }
+            if (i < a.N) s_prefix[i + 1] = running + v;
+            running += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) s_prefix[0] = 0;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i <= a.N; i += blockDim.x) a.g_prefix[i] = s_prefix[i];
+    }
+
+    const int P = s_prefix[a.N];
+    const int W = a.total_warps;
+    const int gw = blockIdx.x * NW + warp;
+    const int x0 = (int)(((int64_t)gw * P) / W);
+    const int x1 = (int)(((int64_t)(gw + 1) * P) / W);
+    const int count = x1 - x0;
+    if (count <= 0) {
+        if (blockIdx.x == 0 && errbits) atomicOr(a.err, errbits);
+        return;
+    }
+
+    PageBatch cur, nxt;
+    load_batch<BS, FP8>(cur, x0, x1, s_prefix, s_seq, a, errbits);
+    load_batch<BS, FP8>(nxt, x0 + 32, x1, s_prefix, s_seq, a, errbits);
+    int cb = 0;   // batch index held in `cur`
+    const uint64_t policy = l2_policy_evict_first();
+
+    auto issue = [&](int i) {
+        const int bi = i >> 5;
+        const int src = i & 31;
+        const int id = __shfl_sync(0xffffffffu, bi == cb ? cur.id : nxt.id, src);
+        const int h = __shfl_sync(0xffffffffu, bi == cb ? cur.h : nxt.h, src);
+        if (lane == 0) {
+            const int s = i % S;
+            const uint32_t bar = bars + 8u * s;
+            const uint32_t dst = stage0 + (uint32_t)(s * C::STAGE_BYTES);
+            const int y = (id * a.Hkv + h) * BS;
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+#pragma unroll
+            for (int ch = 0; ch < C::CH; ++ch)
+                tma_load_2d_hint(dst + ch * (BS * 128), &tmK, ch * C::CH_ELEMS, y, bar, policy);
+#pragma unroll
+            for (int ch = 0; ch < C::CH; ++ch)
+                tma_load_2d_hint(dst + C::PAGE_BYTES + ch * (BS * 128), &tmV, ch * C::CH_ELEMS, y,
+                                 bar, policy);
+        }
+    };
+
+    const int npro = min(S, count);
+    for (int i = 0; i < npro; ++i) issue(i);
+
+    const int g = lane >> 2;   // mma row group: head column of B / token row of A
+    const int c = lane & 3;
+
+    float o[C::DT][4];
+    float ot[FP8 ? C::DT : 1][4];
+    uint32_t qf[C::KS][2];
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float qscale = a.scale_log2;
+    bool seg_full = false;
+    int seg_r = 0, seg_h = 0;
+
+    for (int i = 0; i < count; ++i) {
+        if (i > 0 && (i & 31) == 0) {
+            cur = nxt;
+            ++cb;
+            load_batch<BS, FP8>(nxt, x0 + (cb + 1) * 32, x1, s_prefix, s_seq, a, errbits);
+        }
+        const int src = i & 31;
+        const int r = __shfl_sync(0xffffffffu, cur.r, src);
+        const int h = __shfl_sync(0xffffffffu, cur.h, src);
+        const uint32_t fl = __shfl_sync(0xffffffffu, cur.fl, src);
+        float ks = 1.f, vs = 1.f;
+        if (FP8) {
+            ks = __shfl_sync(0xffffffffu, cur.ks, src);
+            vs = __shfl_sync(0xffffffffu, cur.vs, src);
+        }
+        const int ntok = (int)(fl & 0xFFu);
+        const bool first = (fl >> 8) & 1u;
+        const bool last = (fl >> 9) & 1u;
+
+        // ---- segment start: load the GQA group's queries as mma B fragments ----
+        if (i == 0 || first) {
+            seg_full = first;
+            seg_r = r;
+            seg_h = h;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+#pragma unroll
+            for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
+            const uint16_t* qrow = a.q + ((int64_t)r * a.Hq + (int64_t)h * a.G + g) * D;
+            const bool gv = g < a.G;
+            if (!FP8) {
+#pragma unroll
+                for (int ks2 = 0; ks2 < C::KS; ++ks2) {
+                    qf[ks2][0] = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 2 * c)) : 0u;
+                    qf[ks2][1] = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 8 + 2 * c)) : 0u;
+                }
+                qscale = a.scale_log2;
+            } else {
+                // k-slot mapping for E4M3 A fragments: slots 2c,2c+1 <-> d = 4c,4c+1 and
+                // slots 8+2c,9+2c <-> d = 4c+2,4c+3 of each 16-d step.
+                uint2 raw_q[C::KS];
+                float amax = 0.f;
+#pragma unroll
+                for (int ks2 = 0; ks2 < C::KS; ++ks2) {
+                    raw_q[ks2] = gv ? __ldg(reinterpret_cast<const uint2*>(qrow + ks2 * 16 + 4 * c))
+                                    : make_uint2(0u, 0u);
+                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo_to_f32(raw_q[ks2].x)),
+                                                   fabsf(bf16_hi_to_f32(raw_q[ks2].x))),
+                                             fmaxf(fabsf(bf16_lo_to_f32(raw_q[ks2].y)),
+                                                   fabsf(bf16_hi_to_f32(raw_q[ks2].y)))));
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+                // power of two putting the largest |q| in [2^14, 2^15): exact rescale
+                // (E >= 15 keeps both 2^(141-E) and 2^(E-141) normal binary32 numbers)
+                int E = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+                E = max(E, 15);
+                const float sc = __uint_as_float((uint32_t)(268 - E) << 23);
+                const float inv_sc = __uint_as_float((uint32_t)(E - 14) << 23);
+#pragma unroll
+                for (int ks2 = 0; ks2 < C::KS; ++ks2) {
+                    qf[ks2][0] = pack_f16x2(bf16_lo_to_f32(raw_q[ks2].x) * sc,
+                                            bf16_hi_to_f32(raw_q[ks2].x) * sc);
+                    qf[ks2][1] = pack_f16x2(bf16_lo_to_f32(raw_q[ks2].y) * sc,
+                                            bf16_hi_to_f32(raw_q[ks2].y) * sc);
+                }
+                qscale = a.scale_log2 * inv_sc;
+            }
+        }
+
+        // ---- wait for the page ----
+        const int s = i % S;
+        const uint32_t par = (uint32_t)((i / S) & 1);
+        bool ok = mbar_wait_bounded(bars + 8u * s, par, kWaitLimitNs);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) {
+            if (lane == 0) atomicOr(a.err, PKV_DEVERR_WAIT_TIMEOUT | errbits);
+            for (int k = i; k < min(i + S, count); ++k)
+                (void)mbar_wait_bounded(bars + 8u * (k % S), (uint32_t)((k / S) & 1), kWaitLimitNs);
+            __syncwarp();
+            return;
+        }
+        const uint32_t kpg = stage0 + (uint32_t)(s * C::STAGE_BYTES);
+        const uint32_t vpg = kpg + C::PAGE_BYTES;
+
+        // rows past the request's length hold stale data: zero them in V so that
+        // P = 0 times them stays 0 even if they hold NaN patterns
+        if (ntok < BS) {
+            uint8_t* vp = basep + (vpg - base);
+            const int units = (BS - ntok) * C::CH * 8;   // 16-byte units
+            for (int u = lane; u < units; u += 32) {
+                const int ch = u / ((BS - ntok) * 8);
+                const int rem = u - ch * ((BS - ntok) * 8);
+                const int t = ntok + rem / 8;
+                const int k16 = rem & 7;
+                *reinterpret_cast<uint4*>(vp + ch * (BS * 128) + t * 128 + k16 * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            __syncwarp();
+        }
+
+        // ---- S^T = K Q^T (tokens x heads) ----
+        float sacc[C::MT][4];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+            const int t = mt * 16 + (lane & 15);
+            if (!FP8) {
+#pragma unroll
+                for (int ks2 = 0; ks2 < C::KS; ++ks2) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(kpg + swz<BS>(t, 2 * ks2 + (lane >> 4)), a0, a1, a2, a3);
+                    if (ks2 & 1) mma_bf16(e1, a0, a1, a2, a3, qf[ks2][0], qf[ks2][1]);
+                    else         mma_bf16(e0, a0, a1, a2, a3, qf[ks2][0], qf[ks2][1]);
+                }
+            } else {
+#pragma unroll
+                for (int kp = 0; kp < C::KS / 2; ++kp) {
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(kpg + swz<BS>(t, 2 * kp + (lane >> 4)), r0, r1, r2, r3);
+                    mma_f16(e0, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1),
+                            e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16),
+                            qf[2 * kp][0], qf[2 * kp][1]);
+                    mma_f16(e1, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3),
+                            e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16),
+                            qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sacc[mt][e] = e0[e] + e1[e];
+        }
+
+        // ---- online softmax (log2 domain), heads 2c and 2c+1 of this lane ----
+        const float sc_page = FP8 ? qscale * ks : qscale;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int tok = mt * 16 + g + ((e & 2) ? 8 : 0);
+                const float v = sacc[mt][e] * sc_page;
+                sacc[mt][e] = (tok < ntok) ? v : -INFINITY;
+            }
+            mx0 = fmaxf(mx0, fmaxf(sacc[mt][0], sacc[mt][2]));
+            mx1 = fmaxf(mx1, fmaxf(sacc[mt][1], sacc[mt][3]));
+        }
+#pragma unroll
+        for (int o2 = 4; o2 < 32; o2 <<= 1) {
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        float ps0 = 0.f, ps1 = 0.f;
+        uint32_t pb[C::MT][2];
+#pragma unroll
+        for (int mt = 0; mt < C::MT; ++mt) {
+            const float p0 = exp2f(sacc[mt][0] - mn0), p1 = exp2f(sacc[mt][1] - mn1);
+            const float p2 = exp2f(sacc[mt][2] - mn0), p3 = exp2f(sacc[mt][3] - mn1);
+            ps0 += p0 + p2;
+            ps1 += p1 + p3;
+            if (!FP8) {
+                pb[mt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+                pb[mt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+            } else {
+                pb[mt][0] = movmatrix_trans(pack_f16x2(p0, p1));
+                pb[mt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+            }
+        }
+        l0 = l0 * al0 + ps0;
+        l1 = l1 * al1 + ps1;
+#pragma unroll
+        for (int dt = 0; dt < C::DT; ++dt) {
+            o[dt][0] *= al0;
+            o[dt][2] *= al0;
+            o[dt][1] *= al1;
+            o[dt][3] *= al1;
+        }
+
+        // ---- O^T += V^T P^T ----
+        if (!FP8) {
+#pragma unroll
+            for (int dt = 0; dt < C::DT; ++dt) {
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    const int t = mt * 16 + (lane & 7) + ((lane >> 4) << 3);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4_trans(vpg + swz<BS>(t, 2 * dt + ((lane >> 3) & 1)), a0, a1, a2, a3);
+                    mma_bf16(o[dt], a0, a1, a2, a3, pb[mt][0], pb[mt][1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ot[dt][e] = 0.f;
+#pragma unroll
+            for (int dp = 0; dp < C::DT / 2; ++dp) {
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    const int t = mt * 16 + (lane & 15);
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(vpg + swz<BS>(t, 2 * dp + (lane >> 4)), r0, r1, r2, r3);
+#pragma unroll
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t x = movmatrix_trans(half ? r2 : r0);   // tokens 0-7
+                        const uint32_t y = movmatrix_trans(half ? r3 : r1);   // tokens 8-15
+                        mma_f16(ot[2 * dp + half],
+                                e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0020)),
+                                e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0031)),
+                                e4m3x2_to_f16x2(__byte_perm(y, 0u, 0x0020)),
+                                e4m3x2_to_f16x2(__byte_perm(y, 0u, 0x0031)),
+                                pb[mt][0], pb[mt][1]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) o[dt][e] = fmaf(vs, ot[dt][e], o[dt][e]);
+        }
+
+        // ---- segment end ----
+        if (last || i == count - 1) {
+            float L0 = l0, L1 = l1;
+#pragma unroll
+            for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                L0 += __shfl_xor_sync(0xffffffffu, L0, o2);
+                L1 += __shfl_xor_sync(0xffffffffu, L1, o2);
+            }
+            const int g0 = 2 * c, g1 = 2 * c + 1;
+            if (seg_full && last) {
+                const float inv0 = 1.f / L0, inv1 = 1.f / L1;
+                uint16_t* ob = a.out + ((int64_t)seg_r * a.Hq + (int64_t)seg_h * a.G) * D;
+#pragma unroll
+                for (int dt = 0; dt < C::DT; ++dt) {
+                    if (!FP8) {
+                        const int d = dt * 16 + g;
+                        if (g0 < a.G) {
+                            ob[g0 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][0] * inv0));
+                            ob[g0 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][2] * inv0));
+                        }
+                        if (g1 < a.G) {
+                            ob[g1 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][1] * inv1));
+                            ob[g1 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][3] * inv1));
+                        }
+                    } else {
+                        const int d = dt * 16 + 2 * g;
+                        if (g0 < a.G)
+                            *reinterpret_cast<uint32_t*>(ob + g0 * D + d) =
+                                pack_bf16x2(o[dt][0] * inv0, o[dt][2] * inv0);
+                        if (g1 < a.G)
+                            *reinterpret_cast<uint32_t*>(ob + g1 * D + d) =
+                                pack_bf16x2(o[dt][1] * inv1, o[dt][3] * inv1);
+                    }
+                }
+            } else {
+                const int64_t slot = (int64_t)seg_r * a.Hkv + seg_h + gw;
+                float* ps = a.partials + slot * (kGroupPad * (D + 4));
+#pragma unroll
+                for (int dt = 0; dt < C::DT; ++dt) {
+                    if (!FP8) {
+                        const int d = dt * 16 + g;
+                        ps[g0 * (D + 4) + d] = o[dt][0];
+                        ps[g0 * (D + 4) + d + 8] = o[dt][2];
+                        ps[g1 * (D + 4) + d] = o[dt][1];
+                        ps[g1 * (D + 4) + d + 8] = o[dt][3];
+                    } else {
+                        const int d = dt * 16 + 2 * g;
+                        *reinterpret_cast<float2*>(ps + g0 * (D + 4) + d) = make_float2(o[dt][0], o[dt][2]);
+                        *reinterpret_cast<float2*>(ps + g1 * (D + 4) + d) = make_float2(o[dt][1], o[dt][3]);
+                    }
+                }
+                if (g == 0) {
+                    *reinterpret_cast<float2*>(ps + g0 * (D + 4) + D) = make_float2(m0, L0);
+                    *reinterpret_cast<float2*>(ps + g1 * (D + 4) + D) = make_float2(m1, L1);
+                }
+            }
+        }
+
+        // every lane orders its generic accesses of this stage (ldmatrix reads, the
+        // zero fill) before the async-proxy refill lane 0 is about to issue
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (i + S < count) issue(i + S);
+    }
+    if (errbits) atomicOr(a.err, errbits);
+}
+
+// Merge the partials of every unit that was split across warps:
+//   M = max_w m_w,  out = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w
+// (the log-sum-exp merge of online softmax; "GPU推理深度拆解：KV Cache视角",
+// 系统层：Context Parallel -- the same merge ring attention uses).
+template <int D>
+__global__ void __launch_bounds__(128)
+    pkv_decode_reduce_kernel(const DecodeArgs a, int block_size) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int u = blockIdx.x * (blockDim.x >> 5) + warp;
+    if (u >= a.N * a.Hkv) return;
+    const int r = u / a.Hkv;
+    const int h = u - r * a.Hkv;
+    const int P = a.g_prefix[a.N];
+    const int base_r = a.g_prefix[r];
+    const int np = (a.g_prefix[r + 1] - base_r) / a.Hkv;
+    constexpr int PER = D / 32;   // d values per lane
+    uint16_t* ob = a.out + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D;
+    if (np == 0) {
+        for (int gg = 0; gg < a.G; ++gg)
+#pragma unroll
+            for (int k = 0; k < PER; ++k) ob[gg * D + lane * PER + k] = 0;
+        return;
+    }
+    const int64_t W = a.total_warps;
+    const int64_t U = (int64_t)base_r + (int64_t)h * np;
+    const int64_t E = U + np - 1;
+    const int64_t wf = ((U + 1) * W - 1) / P;
+    const int64_t wl = ((E + 1) * W - 1) / P;
+    if (wf == wl) return;   // the unit was finished inside one warp
+    for (int gg = 0; gg < a.G; ++gg) {
+        float M = -INFINITY;
+        for (int64_t w = wf; w <= wl; ++w) {
+            const float* ps = a.partials + (u + w) * (kGroupPad * (D + 4)) + gg * (D + 4);
+            M = fmaxf(M, ps[D]);
+        }
+        float acc[PER];
+#pragma unroll
+        for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+        float L = 0.f;
+        for (int64_t w = wf; w <= wl; ++w) {
+            const float* ps = a.partials + (u + w) * (kGroupPad * (D + 4)) + gg * (D + 4);
+            const float wt = exp2f(ps[D] - M);
+            L = fmaf(wt, ps[D + 1], L);
+            if constexpr (PER == 4) {
+                const float4 v = *reinterpret_cast<const float4*>(ps + lane * 4);
+                acc[0] = fmaf(wt, v.x, acc[0]);
+                acc[1] = fmaf(wt, v.y, acc[1]);
+                acc[2] = fmaf(wt, v.z, acc[2]);
+                acc[3] = fmaf(wt, v.w, acc[3]);
+            } else {
+                const float2 v = *reinterpret_cast<const float2*>(ps + lane * 2);
+                acc[0] = fmaf(wt, v.x, acc[0]);
+                acc[1] = fmaf(wt, v.y, acc[1]);
+            }
+        }
+        const float inv = 1.f / L;
+#pragma unroll
+        for (int k = 0; k < PER; k += 2)
+            *reinterpret_cast<uint32_t*>(ob + gg * D + lane * PER + k) =
+                pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult qr;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+int env_int(const char* name, int dflt) {
+    const char* v = getenv(name);
+    if (!v || !*v) return dflt;
+    return atoi(v);
+}
+
+}  // namespace
+
+// The CTA shape for a (dtype, D, BS): `warps` independent pipelines of `stages`
+// pages each, sized to keep about 192 KB of pages in flight per SM.
+DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch) {
+    DecodePlan p;
+    const int elt = fp8 ? 1 : 2;
+    p.stage_bytes = 2 * block_size * head_dim * elt;
+    p.warps = env_int("PKV_DECODE_WARPS", 4);
+    if (p.warps < 1) p.warps = 1;
+    if (p.warps > 8) p.warps = 8;
+    int stages = env_int("PKV_DECODE_STAGES", 0);
+    if (stages <= 0) stages = 196608 / (p.warps * p.stage_bytes);
+    if (stages > 16) stages = 16;
+    if (stages < 2) stages = 2;
+    const int fixed = 1024 + (int)align_up(4 * (2 * (int64_t)batch + 1), 16);
+    while (stages > 2 &&
+           fixed + p.warps * stages * (p.stage_bytes + 8) > 232448)
+        --stages;
+    p.stages = stages;
+    p.smem_bytes = fixed + p.warps * stages * (p.stage_bytes + 8);
+    p.ctas_per_sm = 1;
+    p.total_warps = num_sms * p.ctas_per_sm * p.warps;
+    return p;
+}
+
+
+template <int D, int BS, bool FP8>
+static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const DecodeArgs& args, cudaStream_t st) {
+    auto kern = pkv_decode_kernel<D, BS, FP8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         plan.smem_bytes);
+    if (e != cudaSuccess) return e;
+    const int grid = L.num_sms * plan.ctas_per_sm;
+    kern<<<grid, plan.warps * 32, plan.smem_bytes, st>>>(tk, tv, args);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int units = L.N * L.Hkv;
+    pkv_decode_reduce_kernel<D><<<(units + 3) / 4, 128, 0, st>>>(args, BS);
+    return cudaGetLastError();
+}
+
+static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, int BS,
+                             int64_t rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const int elt = fp8 ? 1 : 2;
+    cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)(D * elt)};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)BS};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// Returns a pkv_status.  Arguments are validated by the caller.
+int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
+    const DecodePlan plan = decode_plan(L.fp8, L.D, L.BS, L.num_sms, L.N);
+    const WorkspaceLayout WL = workspace_layout(L.N, L.Hkv, L.D, plan.total_warps);
+    const int64_t rows = (int64_t)L.NB * L.Hkv * L.BS;
+    alignas(64) CUtensorMap tk, tv;
+    if (!encode_cache_map(&tk, L.k_cache, L.fp8, L.D, L.BS, rows) ||
+        !encode_cache_map(&tv, L.v_cache, L.fp8, L.D, L.BS, rows))
+        return PKV_ERR_CUDA;
+    DecodeArgs a;
+    uint8_t* ws = static_cast<uint8_t*>(L.workspace);
+    a.q = static_cast<const uint16_t*>(L.q);
+    a.out = static_cast<uint16_t*>(L.out);
+    a.block_table = L.block_table;
+    a.seq_lens = L.seq_lens;
+    a.k_scale = L.k_scale;
+    a.v_scale = L.v_scale;
+    a.err = reinterpret_cast<uint32_t*>(ws);
+    a.g_prefix = reinterpret_cast<int32_t*>(ws + WL.prefix_off);
+    a.partials = reinterpret_cast<float*>(ws + WL.partial_off);
+    a.N = L.N;
+    a.Hq = L.Hq;
+    a.Hkv = L.Hkv;
+    a.G = L.Hq / L.Hkv;
+    a.MB = L.MB;
+    a.NB = L.NB;
+    a.scale_log2 = L.scale * 1.4426950408889634f;
+    a.stages = plan.stages;
+    a.total_warps = plan.total_warps;
+    cudaError_t e = cudaErrorInvalidValue;
+    if (!L.fp8) {
+        if (L.D == 128 && L.BS == 16) e = launch_t<128, 16, false>(L, plan, tk, tv, a, st);
+        else if (L.D == 128 && L.BS == 32) e = launch_t<128, 32, false>(L, plan, tk, tv, a, st);
+        else if (L.D == 64 && L.BS == 16) e = launch_t<64, 16, false>(L, plan, tk, tv, a, st);
+        else if (L.D == 64 && L.BS == 32) e = launch_t<64, 32, false>(L, plan, tk, tv, a, st);
+        else return PKV_ERR_UNSUPPORTED;
+    } else {
+        if (L.D == 128 && L.BS == 16) e = launch_t<128, 16, true>(L, plan, tk, tv, a, st);
+        else if (L.D == 128 && L.BS == 32) e = launch_t<128, 32, true>(L, plan, tk, tv, a, st);
+        else return PKV_ERR_UNSUPPORTED;
+    }
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int head_dim, int block_size, int fp8,
+                              int num_sms) {
+    const DecodePlan plan = decode_plan(fp8, head_dim, block_size, num_sms, batch);
+    return (size_t)workspace_layout(batch, num_kv_heads, head_dim, plan.total_warps).total;
+}
+
+}  // namespace pkv

@@ -1,0 +1,248 @@
+// pkv_internal.cuh -- device helpers shared by the libpagedkv kernels (sm_103a).
+//
+// Thin inline-PTX wrappers: mbarrier waits with a time limit, bulk tensor
+// copies (TMA), ldmatrix / movmatrix, mma.sync m16n8k16 and the fp8/fp16/bf16
+// packs.  No math library internals are re-implemented here: exponentials use
+// the CUDA exp2f function and conversions use the hardware cvt instructions.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+// ---------------------------------------------------------------- launch plan
+// The decode kernel's CTA shape for one (dtype, head_dim, block_size).  Chosen
+// on the host; the same numbers size the workspace.
+struct DecodePlan {
+    int warps;          // independent consumer warps per CTA (each its own pipeline)
+    int stages;         // pages in flight per warp
+    int ctas_per_sm;    // resident CTAs per SM (persistent grid = SMs * ctas_per_sm)
+    int stage_bytes;    // K page + V page of one (block, head)
+    int smem_bytes;     // dynamic shared memory per CTA
+    int total_warps;    // grid warps = W
+};
+
+constexpr int kGroupPad = 8;                 // query heads per GQA group padded to mma N = 8
+constexpr int kMaxBatch = 16384;             // requests (page-prefix table lives in smem)
+constexpr uint32_t kWorkspaceHeader = 256;   // error word + reserved
+
+__host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Byte offsets inside the decode workspace.
+struct WorkspaceLayout {
+    int64_t prefix_off;    // int32 [N + 1] page prefix over requests (x Hkv)
+    int64_t partial_off;   // fp32 [slots][kGroupPad][D + 4]
+    int64_t slots;         // N * Hkv + W
+    int64_t total;
+};
+
+__host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int num_kv_heads,
+                                                            int head_dim, int total_warps) {
+    WorkspaceLayout L;
+    L.prefix_off = kWorkspaceHeader;
+    L.partial_off = align_up(L.prefix_off + 4 * (int64_t)(batch + 1), 256);
+    L.slots = (int64_t)batch * num_kv_heads + total_warps;
+    L.total = L.partial_off + L.slots * kGroupPad * (head_dim + 4) * 4;
+    return L;
+}
+
+// ---------------------------------------------------------------- host launchers
+struct DecodeLaunch {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const float* k_scale;
+    const float* v_scale;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    void* out;
+    void* workspace;
+    int N, Hq, Hkv, D, BS, MB, NB, fp8;
+    float scale;
+    int num_sms;
+};
+
+DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch);
+int decode_launch(const DecodeLaunch& L, cudaStream_t st);
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int head_dim, int block_size, int fp8,
+                              int num_sms);
+cudaError_t slot_mapping_launch(const int32_t* block_table, int MB, const int32_t* req_idx,
+                                const int32_t* positions, int T, int BS, int64_t* out,
+                                cudaStream_t st);
+cudaError_t cache_write_launch(const void* k, const void* v, const int64_t* slots, int T,
+                               int Hkv, int D, int BS, int NB, int fp8, void* k_cache,
+                               void* v_cache, const float* k_scale, const float* v_scale,
+                               cudaStream_t st);
+cudaError_t prefix_hash_launch(const int32_t* tokens, const int64_t* offsets, int num_seqs, int B,
+                               uint64_t seed, uint64_t* hashes, const int64_t* hash_offsets,
+                               cudaStream_t st);
+
+// ---------------------------------------------------------------- smem / sync
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns` of wall
+// time (measured with %globaltimer).  Returns false on time-out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// 2-D tiled bulk tensor copy global -> shared, completion on an mbarrier.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Same, with an L2 cache policy (evict-first for streamed pages).
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, int x,
+                                                 int y, uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- fragments
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held one row-pair per thread.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// D = A(16x16, row) * B(16x8, col) + D, bf16 inputs, fp32 accumulators.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Same with fp16 inputs.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two E4M3 bytes (low 16 bits of x, low byte first) -> fp16x2, exact.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+    uint32_t y;
+    asm volatile(
+        "{\n\t.reg .b16 lo, hi;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, lo;\n\t}"
+        : "=r"(y)
+        : "r"(x));
+    return y;
+}
+
+// Two fp32 -> E4M3x2 with round-to-nearest-even and saturation to +-448;
+// `lo` lands in the low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+    uint16_t y;
+    asm volatile("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(y) : "f"(hi), "f"(lo));
+    return y;
+}
+
+// Two fp32 -> packed bf16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t y;
+    asm volatile("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(hi), "f"(lo));
+    return y;
+}
+
+// Two fp32 -> packed fp16x2 (round to nearest even), `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t y;
+    asm volatile("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(y) : "f"(hi), "f"(lo));
+    return y;
+}
+
+__device__ __forceinline__ float bf16_lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16_hi_to_f32(uint32_t x) {
+    return __uint_as_float(x & 0xFFFF0000u);
+}
+
+}  // namespace pkv

@@ -118,9 +118,11 @@ def _tokens(rng, seq_lens, vocab):
     return toks, offs
 
 
-def make(cfg: int, seed: int | None = None, small: bool = False) -> Workload:
+def make(cfg: int, seed: int | None = None, small: bool = False,
+         batch: int | None = None) -> Workload:
     """Workload `cfg` (1..5).  `small=True` keeps the head/dim/block shape but
-    shrinks batch and lengths so the fp64 oracle finishes in seconds."""
+    shrinks batch and lengths so the fp64 oracle finishes in seconds.  `batch`
+    overrides the number of requests of workloads 2, 4 and 5 (same length law)."""
     seed = cfg if seed is None else seed
     rng = np.random.default_rng(seed)
     if cfg == 1:
@@ -142,6 +144,7 @@ def make(cfg: int, seed: int | None = None, small: bool = False) -> Workload:
             N, lo, hi = 8, 64, 700
         else:
             N, lo, hi = 64, 1024, 8192
+        N = batch or N
         seq = rng.integers(lo, hi + 1, size=N).astype(np.int32)
         Hq, Hkv, D, BS = 64, 8, 128, 16
         bt, NB = _assign_blocks(rng, seq, BS)
@@ -163,6 +166,7 @@ def make(cfg: int, seed: int | None = None, small: bool = False) -> Workload:
             N, prefix, tlo, thi = 12, 512, 16, 200
         else:
             N, prefix, tlo, thi = 128, 4096, 256, 1024
+        N = batch or N
         Hq, Hkv, D, BS = 32, 8, 128, 16
         tails = rng.integers(tlo, thi + 1, size=N).astype(np.int32)
         seq = (prefix + tails).astype(np.int32)
@@ -196,6 +200,7 @@ def make(cfg: int, seed: int | None = None, small: bool = False) -> Workload:
             N, lo, hi = 16, 128, 2048
         else:
             N, lo, hi = 256, 128, 16384
+        N = batch or N
         seq = np.exp(rng.uniform(math.log(lo), math.log(hi), size=N)).astype(np.int64)
         seq = np.clip(seq, lo, hi).astype(np.int32)
         Hq, Hkv, D, BS = 64, 8, 128, 32

@@ -160,6 +160,35 @@ PKV_API int pkv_paged_decode_attn(const void *q, const void *k_cache, const void
                           size_t workspace_bytes, pkv_stream_t stream);
 
 /*
+ * Paged decode attention that allocates nothing.  The sources describe no such
+ * call: it exists for callers that cannot call cudaMalloc -- for example a plugin
+ * hosted by an engine that owns all device memory and offers no workspace hook,
+ * or code on a latency-critical path where cudaMalloc's implicit device
+ * synchronisation is not acceptable.  Same arguments and results as
+ * pkv_paged_decode_attn without the workspace: the scratch is a 16 MiB static
+ * device array inside the library, which every GPU that loads the library holds
+ * until the process exits.
+ *   - Shapes whose pkv_decode_workspace_size exceeds 16 MiB return
+ *     PKV_ERR_WORKSPACE and launch nothing (at head_dim 128 on a 152-SM GPU:
+ *     batch * num_kv_heads up to about 3,300).
+ *   - The first call on a device, made with that device current, looks up the
+ *     array's device address (cudaGetSymbolAddress); make that first call before
+ *     any stream capture.
+ *   - Every call shares the one array and it keeps the last call's contents;
+ *     nothing in it needs to start at zero.  Calls that overlap on the GPU (other
+ *     streams, other threads) race on it: serialise them.  The device error word
+ *     of this variant stays inside the shared array and is not reported.
+ */
+PKV_API int pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache,
+                                          const void *v_cache, const float *k_scale,
+                                          const float *v_scale, const int32_t *block_table,
+                                          int max_blocks_per_seq, const int32_t *seq_lens,
+                                          int batch, int num_q_heads, int num_kv_heads,
+                                          int head_dim, int block_size, int num_blocks,
+                                          int cache_dtype, float scale, void *out,
+                                          pkv_stream_t stream);
+
+/*
  * Chained prefix block hash ([P3] "优化一：Prefix Cache", 工作原理：按块哈希):
  *     h_0 = seed,   h_i = H(h_{i-1}, tokens of block i),   i = 1 .. floor(L_s / B)
  * with H(p, blk) = fmix64(p XOR FNV1a64(little-endian bytes of the block's int32

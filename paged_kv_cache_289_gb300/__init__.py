@@ -14,7 +14,8 @@ import threading
 __all__ = [
     "PkvError", "lib", "library_path", "BF16", "FP8_E4M3", "DEVERR_WAIT_TIMEOUT",
     "DEVERR_SEQ_CLAMPED", "DEVERR_BLOCK_RANGE", "compute_slot_mapping", "kv_cache_write",
-    "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn", "prefix_block_hash",
+    "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn",
+    "paged_decode_attn_noalloc", "prefix_block_hash",
     "device_num_sms", "read_device_error",
 ]
 
@@ -64,6 +65,9 @@ def lib():
             L.pkv_paged_decode_attn.restype = i
             L.pkv_paged_decode_attn.argtypes = [p, p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
                                                 p, p, sz, p]
+            L.pkv_paged_decode_attn_noalloc.restype = i
+            L.pkv_paged_decode_attn_noalloc.argtypes = [p, p, p, p, p, p, i, p, i, i, i, i, i, i,
+                                                        i, f, p, p]
             L.pkv_prefix_block_hash.restype = i
             L.pkv_prefix_block_hash.argtypes = [p, p, i, i, u64, p, p, p]
             _lib = L
@@ -180,6 +184,27 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, scale, out=Non
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D, BS, NB, dt, float(scale), _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale, out=None,
+                              k_scale=None, v_scale=None, stream=None):
+    """Same as paged_decode_attn, for callers that cannot allocate: the library's static
+    device scratch replaces the workspace (calls must not overlap on the GPU)."""
+    import torch
+    _need(q, "q", (torch.bfloat16,))
+    _need(k_cache, "k_cache", None)
+    _need(v_cache, "v_cache", None)
+    _need(block_table, "block_table", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    N, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _check("pkv_paged_decode_attn_noalloc", lib().pkv_paged_decode_attn_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D, BS, NB, _cache_dtype(k_cache),
+        float(scale), _ptr(out), _stream(stream)))
     return out
 
 

@@ -148,8 +148,11 @@ PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_
  * Requirements: q, out, caches, workspace 16-byte aligned; workspace_bytes >=
  *   pkv_decode_workspace_size(...) for the same shape and device.
  * The work is one flat list of (request, kv head, page) items split evenly over
- * a persistent grid of warps; units that span warps are merged by a second
- * kernel with log-sum-exp weights.  Two launches, no host synchronisation.
+ * a persistent grid of warps; for a unit that spans warps, the last of them to
+ * finish merges the partial results with log-sum-exp weights.  One launch, no
+ * host synchronisation.  The workspace's arrival counters carry a per-call tag,
+ * so the workspace needs no clearing between calls; calls that share a
+ * workspace must not overlap on the GPU.
  */
 PKV_API int pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
                           const float *k_scale, const float *v_scale,

@@ -15,8 +15,9 @@
 // whatever the length mix.  A warp walks its range unit by unit ("segments");
 // a segment that covers a whole unit writes the bf16 output directly, otherwise
 // it writes an unnormalised partial (o, running max m, sum l) to workspace slot
-// u + w (unique: unit and warp ranges are both ordered).  A second kernel merges
-// the partials of split units with log-sum-exp weights.
+// u + w (unique: unit and warp ranges are both ordered) and arrives on the unit's
+// counter; the warp that arrives last merges the unit's partials with log-sum-exp
+// weights and writes the output.  Nobody waits for anybody: one launch per call.
 //
 // Per-warp pipeline.  Each warp owns `stages` shared-memory stages of one
 // (block, head) K page + V page.  Lane 0 issues 2-D bulk tensor copies (TMA,
@@ -38,6 +39,8 @@
 #include <cuda_fp16.h>
 #include <math.h>
 
+#include <atomic>
+
 #include "pkv_internal.cuh"
 
 namespace pkv {
@@ -50,12 +53,13 @@ struct DecodeArgs {
     const float* k_scale;
     const float* v_scale;
     uint32_t* err;
-    int32_t* g_prefix;
+    unsigned long long* counters;   // per unit: epoch << 32 | warps arrived
     float* partials;
     int N, Hq, Hkv, G, MB, NB;
     float scale_log2;   // scale * log2(e): scores kept in the log2 domain
     int stages;
     int total_warps;
+    uint32_t epoch;     // differs between calls (graph replays reuse one; counters reset)
 };
 
 template <int D, int BS, bool FP8>
@@ -125,6 +129,87 @@ __device__ __forceinline__ void load_batch(PageBatch& b, int xbeg, int x1,
     }
 }
 
+// Count one arrival on a split unit's counter and return the number of warps that
+// have arrived in this call.  The counter holds (epoch << 32 | count); a counter
+// left by another call (other epoch, or garbage) restarts at 1, so the workspace
+// never needs clearing.  Only the few warps sharing the unit contend.
+__device__ __forceinline__ uint32_t counter_arrive(unsigned long long* p, uint32_t epoch,
+                                                   uint32_t& errbits) {
+    unsigned long long old = atomicAdd(p, 0ull);
+    for (int it = 0; it < (1 << 16); ++it) {
+        const unsigned long long nv = ((uint32_t)(old >> 32) == epoch)
+                                          ? old + 1ull
+                                          : (((unsigned long long)epoch << 32) | 1ull);
+        const unsigned long long seen = atomicCAS(p, old, nv);
+        if (seen == old) return (uint32_t)nv;
+        old = seen;
+    }
+    errbits |= PKV_DEVERR_WAIT_TIMEOUT;
+    return 0u;
+}
+
+// Log-sum-exp merge of unit u's partials written by warps wf..wl (slots u + w):
+//   M = max_w m_w,  out = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w
+// ("GPU推理深度拆解：KV Cache视角", 系统层：Context Parallel: the online-softmax merge
+// that ring attention also uses).  Lanes 0..7 reduce (m, l) per head; then every lane
+// accumulates D/32 output columns of all heads.  Partials are read through L2 (.cg):
+// they were written by other SMs during this launch.
+template <int D>
+__device__ __noinline__ void merge_unit(const float* partials, uint16_t* out, int Hq, int G,
+                                        int64_t u, int wf, int wl, int r, int h) {
+    constexpr int PER = D / 32;
+    constexpr int SLOT = kGroupPad * (D + 4);
+    const int lane = threadIdx.x & 31;
+    const float* base = partials + (u + wf) * SLOT;
+    const int n = wl - wf + 1;
+    float M = -INFINITY, L = 0.f;
+    if (lane < kGroupPad) {
+        for (int k = 0; k < n; ++k) M = fmaxf(M, __ldcg(base + (int64_t)k * SLOT + lane * (D + 4) + D));
+        for (int k = 0; k < n; ++k) {
+            const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+                base + (int64_t)k * SLOT + lane * (D + 4) + D));
+            L = fmaf(exp2f(ml.x - M), ml.y, L);
+        }
+    }
+    float Mh[kGroupPad];
+#pragma unroll
+    for (int gg = 0; gg < kGroupPad; ++gg) Mh[gg] = __shfl_sync(0xffffffffu, M, gg);
+    float acc[kGroupPad][PER];
+#pragma unroll
+    for (int gg = 0; gg < kGroupPad; ++gg)
+#pragma unroll
+        for (int k = 0; k < PER; ++k) acc[gg][k] = 0.f;
+    for (int k = 0; k < n; ++k) {
+        const float* ps = base + (int64_t)k * SLOT;
+#pragma unroll
+        for (int gg = 0; gg < kGroupPad; ++gg) {
+            if (gg >= G) break;
+            const float wt = exp2f(__ldcg(ps + gg * (D + 4) + D) - Mh[gg]);
+            if constexpr (PER == 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + gg * (D + 4) + lane * 4));
+                acc[gg][0] = fmaf(wt, v.x, acc[gg][0]);
+                acc[gg][1] = fmaf(wt, v.y, acc[gg][1]);
+                acc[gg][2] = fmaf(wt, v.z, acc[gg][2]);
+                acc[gg][3] = fmaf(wt, v.w, acc[gg][3]);
+            } else {
+                const float2 v = __ldcg(reinterpret_cast<const float2*>(ps + gg * (D + 4) + lane * 2));
+                acc[gg][0] = fmaf(wt, v.x, acc[gg][0]);
+                acc[gg][1] = fmaf(wt, v.y, acc[gg][1]);
+            }
+        }
+    }
+    uint16_t* ob = out + ((int64_t)r * Hq + (int64_t)h * G) * D;
+#pragma unroll
+    for (int gg = 0; gg < kGroupPad; ++gg) {
+        const float inv = 1.f / __shfl_sync(0xffffffffu, L, gg);
+        if (gg >= G) continue;
+#pragma unroll
+        for (int k = 0; k < PER; k += 2)
+            *reinterpret_cast<uint32_t*>(ob + gg * D + lane * PER + k) =
+                pack_bf16x2(acc[gg][k] * inv, acc[gg][k + 1] * inv);
+    }
+}
+
 template <int D, int BS, bool FP8>
 __global__ void __launch_bounds__(256, 1)
     pkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
@@ -179,8 +264,11 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) s_prefix[0] = 0;
     }
     __syncthreads();
-    if (blockIdx.x == 0) {
-        for (int i = threadIdx.x; i <= a.N; i += blockDim.x) a.g_prefix[i] = s_prefix[i];
+    // requests with no cached tokens get zero output rows (grid-strided over requests)
+    for (int r = blockIdx.x; r < a.N; r += gridDim.x) {
+        if (s_seq[r] != 0) continue;
+        uint4* ob = reinterpret_cast<uint4*>(a.out + (int64_t)r * a.Hq * D);
+        for (int k = threadIdx.x; k < a.Hq * D / 8; k += blockDim.x) ob[k] = make_uint4(0u, 0u, 0u, 0u);
     }
 
     const int P = s_prefix[a.N];
@@ -518,6 +606,25 @@ __global__ void __launch_bounds__(256, 1)
                     *reinterpret_cast<float2*>(ps + g0 * (D + 4) + D) = make_float2(m0, L0);
                     *reinterpret_cast<float2*>(ps + g1 * (D + 4) + D) = make_float2(m1, L1);
                 }
+                // arrive on the unit's counter; the last of its warps merges
+                const int64_t u = (int64_t)seg_r * a.Hkv + seg_h;
+                const int np_u = (s_prefix[seg_r + 1] - s_prefix[seg_r]) / a.Hkv;
+                const int64_t U = (int64_t)s_prefix[seg_r] + (int64_t)seg_h * np_u;
+                const int64_t E = U + np_u - 1;
+                const int wf = (int)(((U + 1) * W - 1) / P);
+                const int wl = (int)(((E + 1) * W - 1) / P);
+                __syncwarp();
+                uint32_t arrived = 0;
+                if (lane == 0) {
+                    __threadfence();
+                    arrived = counter_arrive(a.counters + u, a.epoch, errbits);
+                }
+                arrived = __shfl_sync(0xffffffffu, arrived, 0);
+                if (arrived == (uint32_t)(wl - wf + 1)) {
+                    __threadfence();
+                    merge_unit<D>(a.partials, a.out, a.Hq, a.G, u, wf, wl, seg_r, seg_h);
+                    if (lane == 0) atomicExch(a.counters + u, (unsigned long long)a.epoch << 32);
+                }
             }
         }
 
@@ -528,70 +635,6 @@ __global__ void __launch_bounds__(256, 1)
         if (i + S < count) issue(i + S);
     }
     if (errbits) atomicOr(a.err, errbits);
-}
-
-// Merge the partials of every unit that was split across warps:
-//   M = max_w m_w,  out = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w
-// (the log-sum-exp merge of online softmax; "GPU推理深度拆解：KV Cache视角",
-// 系统层：Context Parallel -- the same merge ring attention uses).
-template <int D>
-__global__ void __launch_bounds__(128)
-    pkv_decode_reduce_kernel(const DecodeArgs a, int block_size) {
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int u = blockIdx.x * (blockDim.x >> 5) + warp;
-    if (u >= a.N * a.Hkv) return;
-    const int r = u / a.Hkv;
-    const int h = u - r * a.Hkv;
-    const int P = a.g_prefix[a.N];
-    const int base_r = a.g_prefix[r];
-    const int np = (a.g_prefix[r + 1] - base_r) / a.Hkv;
-    constexpr int PER = D / 32;   // d values per lane
-    uint16_t* ob = a.out + ((int64_t)r * a.Hq + (int64_t)h * a.G) * D;
-    if (np == 0) {
-        for (int gg = 0; gg < a.G; ++gg)
-#pragma unroll
-            for (int k = 0; k < PER; ++k) ob[gg * D + lane * PER + k] = 0;
-        return;
-    }
-    const int64_t W = a.total_warps;
-    const int64_t U = (int64_t)base_r + (int64_t)h * np;
-    const int64_t E = U + np - 1;
-    const int64_t wf = ((U + 1) * W - 1) / P;
-    const int64_t wl = ((E + 1) * W - 1) / P;
-    if (wf == wl) return;   // the unit was finished inside one warp
-    for (int gg = 0; gg < a.G; ++gg) {
-        float M = -INFINITY;
-        for (int64_t w = wf; w <= wl; ++w) {
-            const float* ps = a.partials + (u + w) * (kGroupPad * (D + 4)) + gg * (D + 4);
-            M = fmaxf(M, ps[D]);
-        }
-        float acc[PER];
-#pragma unroll
-        for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-        float L = 0.f;
-        for (int64_t w = wf; w <= wl; ++w) {
-            const float* ps = a.partials + (u + w) * (kGroupPad * (D + 4)) + gg * (D + 4);
-            const float wt = exp2f(ps[D] - M);
-            L = fmaf(wt, ps[D + 1], L);
-            if constexpr (PER == 4) {
-                const float4 v = *reinterpret_cast<const float4*>(ps + lane * 4);
-                acc[0] = fmaf(wt, v.x, acc[0]);
-                acc[1] = fmaf(wt, v.y, acc[1]);
-                acc[2] = fmaf(wt, v.z, acc[2]);
-                acc[3] = fmaf(wt, v.w, acc[3]);
-            } else {
-                const float2 v = *reinterpret_cast<const float2*>(ps + lane * 2);
-                acc[0] = fmaf(wt, v.x, acc[0]);
-                acc[1] = fmaf(wt, v.y, acc[1]);
-            }
-        }
-        const float inv = 1.f / L;
-#pragma unroll
-        for (int k = 0; k < PER; k += 2)
-            *reinterpret_cast<uint32_t*>(ob + gg * D + lane * PER + k) =
-                pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
-    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -610,6 +653,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     }
     return fn;
+}
+
+// Tag of one call for the split-unit arrival counters (never 0, so a zeroed
+// workspace holds no current tag).
+uint32_t next_epoch() {
+    static std::atomic<uint32_t> counter{0};
+    uint32_t e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    if (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    return e;
 }
 
 int env_int(const char* name, int dflt) {
@@ -654,10 +706,6 @@ static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const
     if (e != cudaSuccess) return e;
     const int grid = L.num_sms * plan.ctas_per_sm;
     kern<<<grid, plan.warps * 32, plan.smem_bytes, st>>>(tk, tv, args);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const int units = L.N * L.Hkv;
-    pkv_decode_reduce_kernel<D><<<(units + 3) / 4, 128, 0, st>>>(args, BS);
     return cudaGetLastError();
 }
 
@@ -695,7 +743,7 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     a.k_scale = L.k_scale;
     a.v_scale = L.v_scale;
     a.err = reinterpret_cast<uint32_t*>(ws);
-    a.g_prefix = reinterpret_cast<int32_t*>(ws + WL.prefix_off);
+    a.counters = reinterpret_cast<unsigned long long*>(ws + WL.counter_off);
     a.partials = reinterpret_cast<float*>(ws + WL.partial_off);
     a.N = L.N;
     a.Hq = L.Hq;
@@ -706,6 +754,7 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     a.scale_log2 = L.scale * 1.4426950408889634f;
     a.stages = plan.stages;
     a.total_warps = plan.total_warps;
+    a.epoch = next_epoch();
     cudaError_t e = cudaErrorInvalidValue;
     if (!L.fp8) {
         if (L.D == 128 && L.BS == 16) e = launch_t<128, 16, false>(L, plan, tk, tv, a, st);

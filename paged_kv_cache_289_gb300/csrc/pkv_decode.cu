@@ -272,10 +272,13 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     const int P = s_prefix[a.N];
-    const int W = a.total_warps;
+    // With fewer pages than warps only P warps get work (one page each); otherwise
+    // every warp owns at least one page, so the warps spanning a unit are exactly
+    // the ones between the warps of its first and last page.
+    const int W = min(a.total_warps, P);
     const int gw = blockIdx.x * NW + warp;
-    const int x0 = (int)(((int64_t)gw * P) / W);
-    const int x1 = (int)(((int64_t)(gw + 1) * P) / W);
+    const int x0 = gw < W ? (int)(((int64_t)gw * P) / W) : 0;
+    const int x1 = gw < W ? (int)(((int64_t)(gw + 1) * P) / W) : 0;
     const int count = x1 - x0;
     if (count <= 0) {
         if (blockIdx.x == 0 && errbits) atomicOr(a.err, errbits);

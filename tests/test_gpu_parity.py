@@ -266,3 +266,26 @@ def test_prefix_hash_long_sequence_and_odd_block_sizes():
     for B in (16, 32, 7, 1):
         got, ref = _hash_both(toks, offs, B, B)
         assert np.array_equal(got, ref)
+
+
+def test_decode_workspace_reuse_and_garbage_contents():
+    """One workspace shared by successive calls of different shapes, starting from
+    garbage bytes: the split-unit counters carry a per-call tag and partial slots are
+    written before they are read, so nothing in the workspace needs clearing."""
+    torch = torch_mod()
+    cases = [W.custom(3, 16, 2, 128, 16, [40, 5000, 700], seed=41),     # pages > warps
+             W.custom(5, 16, 2, 128, 16, [3, 17, 1, 33, 64], seed=42),  # pages < warps
+             W.make(2, small=True)]
+    n = max(pkv.decode_workspace_size(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, pkv.BF16) for wl in cases)
+    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")
+    ws[:4] = 0   # the error word
+    for rep in range(2):
+        for wl in cases:
+            d = W.host_data(wl)
+            out = pkv.paged_decode_attn(bf16_dev(d["q"]), bf16_dev(d["k_cache"]),
+                                        bf16_dev(d["v_cache"]), to_dev(wl.block_table),
+                                        to_dev(wl.seq_lens), wl.scale, workspace=ws)
+            ref = oracle.decode_attn(d["q"], d["k_cache"], d["v_cache"], wl.block_table,
+                                     wl.seq_lens, wl.scale)
+            compare(out_to_f64(out), ref, False)
+    assert pkv.read_device_error(ws) == 0

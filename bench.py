@@ -2,8 +2,9 @@
 """Benchmark of the paged-KV decode step (libpagedkv on GB300).
 
 One step = the whole hot path over one batch: slot mapping of each request's new
-token, KV cache write, paged GQA decode attention (main + LSE-merge kernels), and the
-chained prefix block hash of every request's tokens (on a side stream).
+token, KV cache write, paged GQA decode attention (one kernel; split units are merged
+inside it), and the chained prefix block hash of every request's tokens (on a side
+stream).
 
 Workload: the Llama-3.3-70B-shaped decode layer -- batch 64, 64 query / 8 KV heads,
 head_dim 128, bf16, 16-token blocks, lengths U[1024, 8192], blocks randomly permuted
@@ -308,7 +309,7 @@ def run_ours(args):
     ws = pkv.alloc_decode_workspace(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, dt_code, device=dev)
     main = torch.cuda.current_stream(dev)
     side = torch.cuda.Stream(dev)
-    launches_per_step = 5   # slot map, write, decode main, decode merge, hash
+    launches_per_step = 4   # slot map, write, decode, hash
 
     def step(q, k_new, v_new, dec_ev=None):
         pkv.compute_slot_mapping(bt, pos, wl.BS, out=slots, stream=main)
@@ -371,7 +372,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, read+write bytes)",
-                "kernel": "pkv_paged_decode_attn (pkv_decode_kernel + pkv_decode_reduce_kernel)",
+                "kernel": "pkv_paged_decode_attn (pkv_decode_kernel)",
                 "algorithmic_bytes_per_launch": alg,
                 "avg_launch_ms": round(dec_avg * 1e3, 4)}
 

@@ -15,9 +15,10 @@
 // whatever the length mix.  A warp walks its range unit by unit ("segments");
 // a segment that covers a whole unit writes the bf16 output directly, otherwise
 // it writes an unnormalised partial (o, running max m, sum l) to workspace slot
-// u + w (unique: unit and warp ranges are both ordered) and arrives on the unit's
-// counter; the warp that arrives last merges the unit's partials with log-sum-exp
-// weights and writes the output.  Nobody waits for anybody: one launch per call.
+// u + w (unique: unit and warp ranges are both ordered).  If the unit spans at most
+// kInKernelMerge warps, the warp arrives on the unit's counter and the last to
+// arrive merges the partials with log-sum-exp weights; wider units are merged by a
+// small follow-up kernel.  Nobody waits for anybody.
 //
 // Per-warp pipeline.  Each warp owns `stages` shared-memory stages of one
 // (block, head) K page + V page.  Lane 0 issues 2-D bulk tensor copies (TMA,
@@ -54,6 +55,7 @@ struct DecodeArgs {
     const float* v_scale;
     uint32_t* err;
     unsigned long long* counters;   // per unit: epoch << 32 | warps arrived
+    int32_t* g_prefix;              // page prefix over requests, for the merge kernel
     float* partials;
     int N, Hq, Hkv, G, MB, NB;
     float scale_log2;   // scale * log2(e): scores kept in the log2 domain
@@ -68,23 +70,33 @@ struct Cfg {
     static constexpr int ROW_BYTES = D * ELT;
     static constexpr int CH = ROW_BYTES / 128;            // 128-byte column chunks per row
     static constexpr int CH_ELEMS = 128 / ELT;            // elements per chunk
-    static constexpr int PAGE_BYTES = BS * ROW_BYTES;     // one K (or V) page
-    static constexpr int STAGE_BYTES = 2 * PAGE_BYTES;
-    static constexpr int MT = BS / 16;                    // 16-token tiles per page
+    static constexpr int TT = FP8 ? BS : 16;              // tokens per pipeline tile
+    static constexpr int SUB = BS / TT;                   // tiles per page (1 or 2)
+    static constexpr int TILE_BYTES = TT * ROW_BYTES;     // K (or V) part of a stage
+    static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // 8 KB at bf16 D=128 or E4M3 BS=32
+    static constexpr int MT = TT / 16;                    // 16-token mma tiles per tile
     static constexpr int KS = D / 16;                     // QK k-steps
     static constexpr int DT = D / 16;                     // PV d-tiles
     static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle lines");
     static_assert(BS % 16 == 0, "block size must be a multiple of 16");
+    static_assert(SUB == 1 || SUB == 2, "one or two tiles per page");
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+// Units split over at most this many warps are merged inside the decode kernel by
+// the last warp to finish; wider splits (long requests at small batch) are merged
+// by pkv_decode_merge_kernel, which spreads the reads over one warp per head.
+constexpr int kInKernelMerge = 6;
+// The running max of a head is raised only when a score exceeds it by more than
+// this many log2 units; until then P is taken against the stale max (P <= 2^8).
+constexpr float kRescaleSlack = 8.f;
 
-// Byte offset of 16-byte chunk `kc` of token row `t` inside a page laid out by
-// TMA with 128-byte swizzle: column chunk region, then rows of 128 bytes whose
-// 16-byte units are XOR-permuted by (row mod 8).
-template <int BS>
+// Byte offset of 16-byte chunk `kc` of token row `t` inside a tile of ROWS rows
+// laid out by TMA with 128-byte swizzle: column chunk region, then rows of 128
+// bytes whose 16-byte units are XOR-permuted by (row mod 8).
+template <int ROWS>
 __device__ __forceinline__ uint32_t swz(int t, int kc) {
-    return (uint32_t)((kc >> 3) * (BS * 128) + t * 128 + (((kc & 7) ^ (t & 7)) << 4));
+    return (uint32_t)((kc >> 3) * (ROWS * 128) + t * 128 + (((kc & 7) ^ (t & 7)) << 4));
 }
 
 // Per-lane description of one page of a 32-page batch.
@@ -211,7 +223,7 @@ __device__ __noinline__ void merge_unit(const float* partials, uint16_t* out, in
 }
 
 template <int D, int BS, bool FP8>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
     pkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
     using C = Cfg<D, BS, FP8>;
@@ -237,6 +249,7 @@ __global__ void __launch_bounds__(256, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
+    pdl_launch_dependents();   // the merge kernel may launch now; it waits for completion
 
     // ---- page prefix over requests (every CTA computes its own copy) ----
     uint32_t errbits = 0;
@@ -264,6 +277,9 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) s_prefix[0] = 0;
     }
     __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i <= a.N; i += blockDim.x) a.g_prefix[i] = s_prefix[i];
+    }
     // requests with no cached tokens get zero output rows (grid-strided over requests)
     for (int r = blockIdx.x; r < a.N; r += gridDim.x) {
         if (s_seq[r] != 0) continue;
@@ -292,28 +308,31 @@ __global__ void __launch_bounds__(256, 1)
     const uint64_t policy = l2_policy_evict_first();
 
     auto issue = [&](int i) {
-        const int bi = i >> 5;
-        const int src = i & 31;
+        const int pi = (C::SUB == 2) ? (i >> 1) : i;   // page of item i
+        const int sub = i & (C::SUB - 1);               // tile within the page
+        const int bi = pi >> 5;
+        const int src = pi & 31;
         const int id = __shfl_sync(0xffffffffu, bi == cb ? cur.id : nxt.id, src);
         const int h = __shfl_sync(0xffffffffu, bi == cb ? cur.h : nxt.h, src);
         if (lane == 0) {
             const int s = i % S;
             const uint32_t bar = bars + 8u * s;
             const uint32_t dst = stage0 + (uint32_t)(s * C::STAGE_BYTES);
-            const int y = (id * a.Hkv + h) * BS;
+            const int y = (id * a.Hkv + h) * BS + sub * C::TT;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
 #pragma unroll
             for (int ch = 0; ch < C::CH; ++ch)
-                tma_load_2d_hint(dst + ch * (BS * 128), &tmK, ch * C::CH_ELEMS, y, bar, policy);
+                tma_load_2d_hint(dst + ch * (C::TT * 128), &tmK, ch * C::CH_ELEMS, y, bar, policy);
 #pragma unroll
             for (int ch = 0; ch < C::CH; ++ch)
-                tma_load_2d_hint(dst + C::PAGE_BYTES + ch * (BS * 128), &tmV, ch * C::CH_ELEMS, y,
-                                 bar, policy);
+                tma_load_2d_hint(dst + C::TILE_BYTES + ch * (C::TT * 128), &tmV, ch * C::CH_ELEMS,
+                                 y, bar, policy);
         }
     };
 
-    const int npro = min(S, count);
+    const int total = count * C::SUB;   // pipeline items (tiles)
+    const int npro = min(S, total);
     for (int i = 0; i < npro; ++i) issue(i);
 
     const int g = lane >> 2;   // mma row group: head column of B / token row of A
@@ -327,13 +346,15 @@ __global__ void __launch_bounds__(256, 1)
     bool seg_full = false;
     int seg_r = 0, seg_h = 0;
 
-    for (int i = 0; i < count; ++i) {
-        if (i > 0 && (i & 31) == 0) {
+    for (int i = 0; i < total; ++i) {
+        const int pi = (C::SUB == 2) ? (i >> 1) : i;
+        const int sub = i & (C::SUB - 1);
+        if (sub == 0 && pi > 0 && (pi & 31) == 0) {
             cur = nxt;
             ++cb;
             load_batch<BS, FP8>(nxt, x0 + (cb + 1) * 32, x1, s_prefix, s_seq, a, errbits);
         }
-        const int src = i & 31;
+        const int src = pi & 31;
         const int r = __shfl_sync(0xffffffffu, cur.r, src);
         const int h = __shfl_sync(0xffffffffu, cur.h, src);
         const uint32_t fl = __shfl_sync(0xffffffffu, cur.fl, src);
@@ -342,9 +363,10 @@ __global__ void __launch_bounds__(256, 1)
             ks = __shfl_sync(0xffffffffu, cur.ks, src);
             vs = __shfl_sync(0xffffffffu, cur.vs, src);
         }
-        const int ntok = (int)(fl & 0xFFu);
-        const bool first = (fl >> 8) & 1u;
-        const bool last = (fl >> 9) & 1u;
+        // valid tokens of this tile (<= 0 only for the empty second half of a last page)
+        const int ntok = (int)(fl & 0xFFu) - sub * C::TT;
+        const bool first = ((fl >> 8) & 1u) && sub == 0;
+        const bool last = ((fl >> 9) & 1u) && sub == C::SUB - 1;
 
         // ---- segment start: load the GQA group's queries as mma B fragments ----
         if (i == 0 || first) {
@@ -407,25 +429,26 @@ __global__ void __launch_bounds__(256, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
             if (lane == 0) atomicOr(a.err, PKV_DEVERR_WAIT_TIMEOUT | errbits);
-            for (int k = i; k < min(i + S, count); ++k)
+            for (int k = i; k < min(i + S, total); ++k)
                 (void)mbar_wait_bounded(bars + 8u * (k % S), (uint32_t)((k / S) & 1), kWaitLimitNs);
             __syncwarp();
             return;
         }
         const uint32_t kpg = stage0 + (uint32_t)(s * C::STAGE_BYTES);
-        const uint32_t vpg = kpg + C::PAGE_BYTES;
+        const uint32_t vpg = kpg + C::TILE_BYTES;
 
         // rows past the request's length hold stale data: zero them in V so that
         // P = 0 times them stays 0 even if they hold NaN patterns
-        if (ntok < BS) {
+        if (ntok < C::TT) {
             uint8_t* vp = basep + (vpg - base);
-            const int units = (BS - ntok) * C::CH * 8;   // 16-byte units
+            const int t0 = max(ntok, 0);
+            const int units = (C::TT - t0) * C::CH * 8;   // 16-byte units
             for (int u = lane; u < units; u += 32) {
-                const int ch = u / ((BS - ntok) * 8);
-                const int rem = u - ch * ((BS - ntok) * 8);
-                const int t = ntok + rem / 8;
+                const int ch = u / ((C::TT - t0) * 8);
+                const int rem = u - ch * ((C::TT - t0) * 8);
+                const int t = t0 + rem / 8;
                 const int k16 = rem & 7;
-                *reinterpret_cast<uint4*>(vp + ch * (BS * 128) + t * 128 + k16 * 16) =
+                *reinterpret_cast<uint4*>(vp + ch * (C::TT * 128) + t * 128 + k16 * 16) =
                     make_uint4(0u, 0u, 0u, 0u);
             }
             __syncwarp();
@@ -441,7 +464,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int ks2 = 0; ks2 < C::KS; ++ks2) {
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4(kpg + swz<BS>(t, 2 * ks2 + (lane >> 4)), a0, a1, a2, a3);
+                    ldsm_x4(kpg + swz<C::TT>(t, 2 * ks2 + (lane >> 4)), a0, a1, a2, a3);
                     if (ks2 & 1) mma_bf16(e1, a0, a1, a2, a3, qf[ks2][0], qf[ks2][1]);
                     else         mma_bf16(e0, a0, a1, a2, a3, qf[ks2][0], qf[ks2][1]);
                 }
@@ -449,7 +472,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int kp = 0; kp < C::KS / 2; ++kp) {
                     uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kpg + swz<BS>(t, 2 * kp + (lane >> 4)), r0, r1, r2, r3);
+                    ldsm_x4(kpg + swz<C::TT>(t, 2 * kp + (lane >> 4)), r0, r1, r2, r3);
                     mma_f16(e0, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1),
                             e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16),
                             qf[2 * kp][0], qf[2 * kp][1]);
@@ -476,21 +499,35 @@ __global__ void __launch_bounds__(256, 1)
             mx0 = fmaxf(mx0, fmaxf(sacc[mt][0], sacc[mt][2]));
             mx1 = fmaxf(mx1, fmaxf(sacc[mt][1], sacc[mt][3]));
         }
+        // raise the running max (and rescale O and l) only when some lane's score
+        // exceeds it by more than the slack; P <= 2^kRescaleSlack otherwise
+        const bool need = (mx0 > m0 + kRescaleSlack) || (mx1 > m1 + kRescaleSlack);
+        if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-        for (int o2 = 4; o2 < 32; o2 <<= 1) {
-            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+            for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            l0 *= al0;
+            l1 *= al1;
+#pragma unroll
+            for (int dt = 0; dt < C::DT; ++dt) {
+                o[dt][0] *= al0;
+                o[dt][2] *= al0;
+                o[dt][1] *= al1;
+                o[dt][3] *= al1;
+            }
         }
-        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-        const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
         float ps0 = 0.f, ps1 = 0.f;
         uint32_t pb[C::MT][2];
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
-            const float p0 = exp2f(sacc[mt][0] - mn0), p1 = exp2f(sacc[mt][1] - mn1);
-            const float p2 = exp2f(sacc[mt][2] - mn0), p3 = exp2f(sacc[mt][3] - mn1);
+            const float p0 = exp2f(sacc[mt][0] - m0), p1 = exp2f(sacc[mt][1] - m1);
+            const float p2 = exp2f(sacc[mt][2] - m0), p3 = exp2f(sacc[mt][3] - m1);
             ps0 += p0 + p2;
             ps1 += p1 + p3;
             if (!FP8) {
@@ -501,15 +538,8 @@ __global__ void __launch_bounds__(256, 1)
                 pb[mt][1] = movmatrix_trans(pack_f16x2(p2, p3));
             }
         }
-        l0 = l0 * al0 + ps0;
-        l1 = l1 * al1 + ps1;
-#pragma unroll
-        for (int dt = 0; dt < C::DT; ++dt) {
-            o[dt][0] *= al0;
-            o[dt][2] *= al0;
-            o[dt][1] *= al1;
-            o[dt][3] *= al1;
-        }
+        l0 += ps0;
+        l1 += ps1;
 
         // ---- O^T += V^T P^T ----
         if (!FP8) {
@@ -519,7 +549,7 @@ __global__ void __launch_bounds__(256, 1)
                 for (int mt = 0; mt < C::MT; ++mt) {
                     const int t = mt * 16 + (lane & 7) + ((lane >> 4) << 3);
                     uint32_t a0, a1, a2, a3;
-                    ldsm_x4_trans(vpg + swz<BS>(t, 2 * dt + ((lane >> 3) & 1)), a0, a1, a2, a3);
+                    ldsm_x4_trans(vpg + swz<C::TT>(t, 2 * dt + ((lane >> 3) & 1)), a0, a1, a2, a3);
                     mma_bf16(o[dt], a0, a1, a2, a3, pb[mt][0], pb[mt][1]);
                 }
             }
@@ -534,7 +564,7 @@ __global__ void __launch_bounds__(256, 1)
                 for (int mt = 0; mt < C::MT; ++mt) {
                     const int t = mt * 16 + (lane & 15);
                     uint32_t r0, r1, r2, r3;
-                    ldsm_x4(vpg + swz<BS>(t, 2 * dp + (lane >> 4)), r0, r1, r2, r3);
+                    ldsm_x4(vpg + swz<C::TT>(t, 2 * dp + (lane >> 4)), r0, r1, r2, r3);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
                         const uint32_t x = movmatrix_trans(half ? r2 : r0);   // tokens 0-7
@@ -555,7 +585,7 @@ __global__ void __launch_bounds__(256, 1)
         }
 
         // ---- segment end ----
-        if (last || i == count - 1) {
+        if (last || i == total - 1) {
             float L0 = l0, L1 = l1;
 #pragma unroll
             for (int o2 = 4; o2 < 32; o2 <<= 1) {
@@ -618,11 +648,13 @@ __global__ void __launch_bounds__(256, 1)
                 const int wl = (int)(((E + 1) * W - 1) / P);
                 __syncwarp();
                 uint32_t arrived = 0;
-                if (lane == 0) {
-                    __threadfence();
-                    arrived = counter_arrive(a.counters + u, a.epoch, errbits);
+                if (wl - wf + 1 <= kInKernelMerge) {
+                    if (lane == 0) {
+                        __threadfence();
+                        arrived = counter_arrive(a.counters + u, a.epoch, errbits);
+                    }
+                    arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 }
-                arrived = __shfl_sync(0xffffffffu, arrived, 0);
                 if (arrived == (uint32_t)(wl - wf + 1)) {
                     __threadfence();
                     merge_unit<D>(a.partials, a.out, a.Hq, a.G, u, wf, wl, seg_r, seg_h);
@@ -635,9 +667,74 @@ __global__ void __launch_bounds__(256, 1)
         // zero fill) before the async-proxy refill lane 0 is about to issue
         fence_proxy_async_smem();
         __syncwarp();
-        if (i + S < count) issue(i + S);
+        if (i + S < total) issue(i + S);
     }
     if (errbits) atomicOr(a.err, errbits);
+}
+
+// Log-sum-exp merge of the units split over more than kInKernelMerge warps: one
+// CTA per unit, one warp per query head of the group, each lane D/32 columns.  The
+// loop over partials keeps several independent loads in flight.  Runs after the
+// decode kernel (programmatic dependent launch: it waits for the decode grid to
+// complete before reading).
+template <int D>
+__global__ void __launch_bounds__(kGroupPad * 32)
+    pkv_decode_merge_kernel(const DecodeArgs a) {
+    constexpr int PER = D / 32;
+    constexpr int SLOT = kGroupPad * (D + 4);
+    pdl_wait();
+    const int u = blockIdx.x;
+    const int gg = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gg >= a.G) return;
+    const int r = u / a.Hkv;
+    const int h = u - r * a.Hkv;
+    const int P = a.g_prefix[a.N];
+    const int W = min(a.total_warps, P);
+    const int np = (a.g_prefix[r + 1] - a.g_prefix[r]) / a.Hkv;
+    if (np == 0) return;
+    const int64_t U = (int64_t)a.g_prefix[r] + (int64_t)h * np;
+    const int64_t E = U + np - 1;
+    const int wf = (int)(((U + 1) * W - 1) / P);
+    const int wl = (int)(((E + 1) * W - 1) / P);
+    const int n = wl - wf + 1;
+    if (n <= kInKernelMerge) return;   // merged inside the decode kernel
+    const float* base = a.partials + ((int64_t)u + wf) * SLOT + gg * (D + 4);
+    float M = -INFINITY;
+    for (int k = lane; k < n; k += 32) M = fmaxf(M, base[(int64_t)k * SLOT + D]);
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float L = 0.f;
+    for (int k = lane; k < n; k += 32) {
+        const float2 ml = *reinterpret_cast<const float2*>(base + (int64_t)k * SLOT + D);
+        L = fmaf(exp2f(ml.x - M), ml.y, L);
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+    float acc[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+#pragma unroll 8
+    for (int k = 0; k < n; ++k) {
+        const float* ps = base + (int64_t)k * SLOT;
+        const float wt = exp2f(ps[D] - M);
+        if constexpr (PER == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(ps + lane * 4);
+            acc[0] = fmaf(wt, v.x, acc[0]);
+            acc[1] = fmaf(wt, v.y, acc[1]);
+            acc[2] = fmaf(wt, v.z, acc[2]);
+            acc[3] = fmaf(wt, v.w, acc[3]);
+        } else {
+            const float2 v = *reinterpret_cast<const float2*>(ps + lane * 2);
+            acc[0] = fmaf(wt, v.x, acc[0]);
+            acc[1] = fmaf(wt, v.y, acc[1]);
+        }
+    }
+    const float inv = 1.f / L;
+    uint16_t* ob = a.out + ((int64_t)r * a.Hq + (int64_t)h * a.G + gg) * D;
+#pragma unroll
+    for (int k = 0; k < PER; k += 2)
+        *reinterpret_cast<uint32_t*>(ob + lane * PER + k) = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
 }
 
 // ------------------------------------------------------------------ host side
@@ -680,25 +777,30 @@ int env_int(const char* name, int dflt) {
 DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch) {
     DecodePlan p;
     const int elt = fp8 ? 1 : 2;
-    p.stage_bytes = 2 * block_size * head_dim * elt;
-    p.warps = env_int("PKV_DECODE_WARPS", 4);
+    const int tile_tokens = fp8 ? block_size : 16;
+    p.stage_bytes = 2 * tile_tokens * head_dim * elt;
+    // Each warp streams its pages through its own 2-stage pipeline; the per-page
+    // instruction chain of a warp, not the bytes in flight, limits the rate, so the
+    // CTA runs several warps per SM sub-partition.  Measured on GB300: 6 warps for
+    // bf16 pages, 8 for FP8 pages (whose tiles carry twice the tokens).
+    const int max_warps = fp8 ? 8 : 12;            // register budget of the launch bounds
+    p.warps = env_int("PKV_DECODE_WARPS", fp8 ? 8 : 6);
     if (p.warps < 1) p.warps = 1;
-    if (p.warps > 8) p.warps = 8;
+    if (p.warps > max_warps) p.warps = max_warps;
     int stages = env_int("PKV_DECODE_STAGES", 0);
-    if (stages <= 0) stages = 196608 / (p.warps * p.stage_bytes);
+    if (stages <= 0) stages = 131072 / (p.warps * p.stage_bytes);
     if (stages > 16) stages = 16;
     if (stages < 2) stages = 2;
     const int fixed = 1024 + (int)align_up(4 * (2 * (int64_t)batch + 1), 16);
-    while (stages > 2 &&
-           fixed + p.warps * stages * (p.stage_bytes + 8) > 232448)
-        --stages;
+    auto bytes = [&](int w, int st) { return fixed + w * st * (p.stage_bytes + 8); };
+    while (stages > 2 && bytes(p.warps, stages) > 232448) --stages;
+    while (p.warps > 1 && bytes(p.warps, stages) > 232448) --p.warps;
     p.stages = stages;
-    p.smem_bytes = fixed + p.warps * stages * (p.stage_bytes + 8);
+    p.smem_bytes = bytes(p.warps, stages);
     p.ctas_per_sm = 1;
     p.total_warps = num_sms * p.ctas_per_sm * p.warps;
     return p;
 }
-
 
 template <int D, int BS, bool FP8>
 static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const CUtensorMap& tk,
@@ -709,7 +811,26 @@ static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const
     if (e != cudaSuccess) return e;
     const int grid = L.num_sms * plan.ctas_per_sm;
     kern<<<grid, plan.warps * 32, plan.smem_bytes, st>>>(tk, tv, args);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // the wide-split merge, launched as a programmatic dependent of the decode grid
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(L.N * L.Hkv));
+    cfg.blockDim = dim3(kGroupPad * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, pkv_decode_merge_kernel<D>, args);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        pkv_decode_merge_kernel<D><<<(unsigned)(L.N * L.Hkv), kGroupPad * 32, 0, st>>>(args);
+        e = cudaGetLastError();
+    }
+    return e;
 }
 
 static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, int BS,
@@ -719,7 +840,7 @@ static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, i
     const int elt = fp8 ? 1 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(D * elt)};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)BS};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / elt), (cuuint32_t)(fp8 ? BS : 16)};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2,
                     const_cast<void*>(base), dims, strides, box, estr,
@@ -747,6 +868,7 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     a.v_scale = L.v_scale;
     a.err = reinterpret_cast<uint32_t*>(ws);
     a.counters = reinterpret_cast<unsigned long long*>(ws + WL.counter_off);
+    a.g_prefix = reinterpret_cast<int32_t*>(ws + WL.prefix_off);
     a.partials = reinterpret_cast<float*>(ws + WL.partial_off);
     a.N = L.N;
     a.Hq = L.Hq;

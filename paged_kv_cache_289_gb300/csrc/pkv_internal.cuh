@@ -36,6 +36,7 @@ __host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + 
 // Byte offsets inside the decode workspace.
 struct WorkspaceLayout {
     int64_t counter_off;   // u64 [N * Hkv] arrival counters of split units (epoch << 32 | count)
+    int64_t prefix_off;    // int32 [N + 1] page prefix over requests (times Hkv)
     int64_t partial_off;   // fp32 [slots][kGroupPad][D + 4]: o[D], m, l, pad
     int64_t slots;         // N * Hkv + W
     int64_t total;
@@ -45,7 +46,8 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int num_k
                                                             int head_dim, int total_warps) {
     WorkspaceLayout L;
     L.counter_off = kWorkspaceHeader;
-    L.partial_off = align_up(L.counter_off + 8 * (int64_t)batch * num_kv_heads, 256);
+    L.prefix_off = align_up(L.counter_off + 8 * (int64_t)batch * num_kv_heads, 256);
+    L.partial_off = align_up(L.prefix_off + 4 * (int64_t)(batch + 1), 256);
     L.slots = (int64_t)batch * num_kv_heads + total_warps;
     L.total = L.partial_off + L.slots * kGroupPad * (head_dim + 4) * 4;
     return L;
@@ -159,6 +161,14 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+
+// Programmatic dependent launch: let the next kernel in the stream start launching,
+// and (in that kernel) wait until the kernels it depends on have completed and their
+// memory is visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");

@@ -309,7 +309,7 @@ def run_ours(args):
     ws = pkv.alloc_decode_workspace(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, dt_code, device=dev)
     main = torch.cuda.current_stream(dev)
     side = torch.cuda.Stream(dev)
-    launches_per_step = 4   # slot map, write, decode, hash
+    launches_per_step = 5   # slot map, write, decode, wide-split merge, hash
 
     def step(q, k_new, v_new, dec_ev=None):
         pkv.compute_slot_mapping(bt, pos, wl.BS, out=slots, stream=main)

@@ -249,7 +249,11 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
         prefetch_tensormap(&tmK);
         prefetch_tensormap(&tmV);
     }
-    pdl_launch_dependents();   // the merge kernel may launch now; it waits for completion
+    // programmatic dependent launch: let the merge kernel launch now (it waits for this
+    // grid to complete), and wait for the kernels before this one (e.g. the KV write)
+    // before reading anything they may have written
+    pdl_launch_dependents();
+    pdl_wait();
 
     // ---- page prefix over requests (every CTA computes its own copy) ----
     uint32_t errbits = 0;
@@ -810,27 +814,12 @@ static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const
                                          plan.smem_bytes);
     if (e != cudaSuccess) return e;
     const int grid = L.num_sms * plan.ctas_per_sm;
-    kern<<<grid, plan.warps * 32, plan.smem_bytes, st>>>(tk, tv, args);
-    e = cudaGetLastError();
+    e = launch_pdl(kern, dim3(grid), dim3(plan.warps * 32), (size_t)plan.smem_bytes, st, tk, tv,
+                   args);
     if (e != cudaSuccess) return e;
-    // the wide-split merge, launched as a programmatic dependent of the decode grid
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(L.N * L.Hkv));
-    cfg.blockDim = dim3(kGroupPad * 32);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, pkv_decode_merge_kernel<D>, args);
-    if (e != cudaSuccess) {
-        (void)cudaGetLastError();
-        pkv_decode_merge_kernel<D><<<(unsigned)(L.N * L.Hkv), kGroupPad * 32, 0, st>>>(args);
-        e = cudaGetLastError();
-    }
-    return e;
+    // the wide-split merge, a programmatic dependent of the decode grid
+    return launch_pdl(pkv_decode_merge_kernel<D>, dim3((unsigned)(L.N * L.Hkv)),
+                      dim3(kGroupPad * 32), 0, st, args);
 }
 
 static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, int BS,

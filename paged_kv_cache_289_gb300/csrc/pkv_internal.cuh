@@ -84,6 +84,32 @@ cudaError_t prefix_hash_launch(const int32_t* tokens, const int64_t* offsets, in
                                uint64_t seed, uint64_t* hashes, const int64_t* hash_offsets,
                                cudaStream_t st);
 
+// Launch `kern` as a programmatic dependent of the previous kernel in `st`: its CTAs
+// may be dispatched while that kernel finishes, and the kernel itself calls
+// griddepcontrol.wait before touching memory a predecessor may have written.  Falls
+// back to an ordinary launch where the attribute is refused.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        kern<<<grid, block, smem, st>>>(args...);
+        e = cudaGetLastError();
+    }
+    return e;
+}
+
 // ---------------------------------------------------------------- smem / sync
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256)
                             const int32_t* __restrict__ req_idx,
                             const int32_t* __restrict__ positions, int T, int BS,
                             int64_t* __restrict__ slot_mapping) {
+    pdl_launch_dependents();
+    pdl_wait();   // inputs may come from the previous kernel in the stream
     const int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     const int r = req_idx ? req_idx[t] : t;
@@ -39,6 +41,8 @@ __global__ void __launch_bounds__(256)
                            int Hkv, int D, int BS, int NB, uint8_t* __restrict__ k_cache,
                            uint8_t* __restrict__ v_cache, const float* __restrict__ k_scale,
                            const float* __restrict__ v_scale) {
+    pdl_launch_dependents();
+    pdl_wait();   // slots and rows may come from the previous kernel in the stream
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= total_chunks) return;
     const int cpr = D / 8;                       // 16-byte source chunks per row
@@ -86,9 +90,8 @@ cudaError_t slot_mapping_launch(const int32_t* block_table, int MB, const int32_
                                 const int32_t* positions, int T, int BS, int64_t* out,
                                 cudaStream_t st) {
     if (T == 0) return cudaSuccess;
-    pkv_slot_mapping_kernel<<<(T + 255) / 256, 256, 0, st>>>(block_table, MB, req_idx, positions,
-                                                             T, BS, out);
-    return cudaGetLastError();
+    return launch_pdl(pkv_slot_mapping_kernel, dim3((T + 255) / 256), dim3(256), 0, st,
+                      block_table, MB, req_idx, positions, T, BS, out);
 }
 
 cudaError_t cache_write_launch(const void* k, const void* v, const int64_t* slots, int T,
@@ -98,17 +101,16 @@ cudaError_t cache_write_launch(const void* k, const void* v, const int64_t* slot
     const int64_t chunks = (int64_t)T * Hkv * (D / 8);
     if (chunks == 0) return cudaSuccess;
     const int64_t grid = (chunks + 255) / 256;
+    const uint16_t* kk = static_cast<const uint16_t*>(k);
+    const uint16_t* vv = static_cast<const uint16_t*>(v);
+    uint8_t* kc = static_cast<uint8_t*>(k_cache);
+    uint8_t* vc = static_cast<uint8_t*>(v_cache);
     if (fp8)
-        pkv_cache_write_kernel<true><<<(unsigned)grid, 256, 0, st>>>(
-            static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), slots, chunks, Hkv,
-            D, BS, NB, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale,
-            v_scale);
-    else
-        pkv_cache_write_kernel<false><<<(unsigned)grid, 256, 0, st>>>(
-            static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), slots, chunks, Hkv,
-            D, BS, NB, static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), nullptr,
-            nullptr);
-    return cudaGetLastError();
+        return launch_pdl(pkv_cache_write_kernel<true>, dim3((unsigned)grid), dim3(256), 0, st, kk,
+                          vv, slots, chunks, Hkv, D, BS, NB, kc, vc, k_scale, v_scale);
+    return launch_pdl(pkv_cache_write_kernel<false>, dim3((unsigned)grid), dim3(256), 0, st, kk, vv,
+                      slots, chunks, Hkv, D, BS, NB, kc, vc, (const float*)nullptr,
+                      (const float*)nullptr);
 }
 
 }  // namespace pkv

@@ -63,9 +63,9 @@ def peak_hbm():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic(kernel_src_hash):
+def recorded_traffic(kernel_src_hash, workload_name):
     """Per-launch DRAM traffic of the decode launch from the committed ncu summary, if it
-    was taken on the current kernel source (else None)."""
+    was taken on the current kernel source and on this workload (else None)."""
     path = os.path.join(ROOT, "profiles", "decode_traffic.txt")
     try:
         kv = {}
@@ -75,7 +75,7 @@ def recorded_traffic(kernel_src_hash):
                 if line and not line.startswith("#") and "=" in line:
                     k, v = line.split("=", 1)
                     kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_sha256") != kernel_src_hash:
+        if kv.get("kernel_source_sha256") != kernel_src_hash or kv.get("workload") != workload_name:
             return None
         return float(kv["bytes_per_launch"])
     except Exception:
@@ -311,23 +311,27 @@ def run_ours(args):
     side = torch.cuda.Stream(dev)
     launches_per_step = 5   # slot map, write, decode, wide-split merge, hash
 
-    def step(q, k_new, v_new, dec_ev=None):
-        pkv.compute_slot_mapping(bt, pos, wl.BS, out=slots, stream=main)
-        pkv.kv_cache_write(k_new, v_new, slots, kc, vc, ks, vs, stream=main)
+    def step(I, O, dec_ev=None):
+        """One decode step on the per-step inputs I, writing the results O."""
+        pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, out=slots, stream=main)
+        pkv.kv_cache_write(I["k_new"], I["v_new"], slots, kc, vc, ks, vs, stream=main)
         side.wait_stream(main)
-        pkv.prefix_block_hash(tokens, toffs, wl.hash_block, hoffs, nh, seed=0, out=hashes,
-                              stream=side)
+        pkv.prefix_block_hash(I["tokens"], I["toffs"], wl.hash_block, I["hoffs"], nh, seed=0,
+                              out=O["hashes"], stream=side)
         if dec_ev is not None:
             dec_ev[0].record(main)
-        pkv.paged_decode_attn(q, kc, vc, bt, sl, wl.scale, out=out, k_scale=ks, v_scale=vs,
-                              workspace=ws, stream=main)
+        pkv.paged_decode_attn(I["q"], kc, vc, I["bt"], I["sl"], wl.scale, out=O["out"],
+                              k_scale=ks, v_scale=vs, workspace=ws, stream=main)
         if dec_ev is not None:
             dec_ev[1].record(main)
         main.wait_stream(side)
 
     q, k_new, v_new = dd["q"], dd["k_new"], dd["v_new"]
+    inputs = {"q": q, "k_new": k_new, "v_new": v_new, "pos": pos, "bt": bt, "sl": sl,
+              "tokens": tokens, "toffs": toffs, "hoffs": hoffs}
+    outputs = {"out": out, "hashes": hashes}
     for _ in range(max(args.warmup, 3)):
-        step(q, k_new, v_new)
+        step(inputs, outputs)
     torch.cuda.synchronize(dev)
     if world > 1:
         import torch.distributed as dist
@@ -346,7 +350,7 @@ def run_ours(args):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(main)
     for k in range(K):
-        step(q, k_new, v_new, dec_events[k])
+        step(inputs, outputs, dec_events[k])
     e1.record(main)
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -368,7 +372,7 @@ def run_ours(args):
     peak, peak_kind = peak_hbm()
     alg = decode_algorithmic_bytes(wl)
     achieved = alg / dec_avg / 1e9
-    traffic = recorded_traffic(kernel_source_hash())
+    traffic = recorded_traffic(kernel_source_hash(), wl.name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, read+write bytes)",
@@ -379,46 +383,74 @@ def run_ours(args):
     # ---------------- end to end through the public API with pinned host buffers
     e2e = None
     if not args.skip_e2e:
-        hq = dd["q"].cpu().pin_memory()
-        hk = k_new.cpu().pin_memory()
-        hv = v_new.cpu().pin_memory()
-        hpos = pos.cpu().pin_memory()
-        hbt = bt.cpu().pin_memory()
-        hsl = sl.cpu().pin_memory()
-        htok = tokens.cpu().pin_memory()
-        hto = toffs.cpu().pin_memory()
-        hho = hoffs.cpu().pin_memory()
-        hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        hhash = torch.empty(hashes.shape, dtype=hashes.dtype).pin_memory()
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-        h2d = [(dq, hq), (dk, hk), (dv, hv), (pos, hpos), (bt, hbt), (sl, hsl), (tokens, htok),
-               (toffs, hto), (hoffs, hho)]
-        bi = sum(h.numel() * h.element_size() for _, h in h2d)
-        bo = hout.numel() * hout.element_size() + hhash.numel() * hhash.element_size()
+        # Serving-style loop: every step's inputs (q, new K/V, positions, block table,
+        # lengths, tokens) go up from one packed pinned buffer and its results (out,
+        # hashes) come back, one copy each way per step.  Copies run on their own
+        # streams, double-buffered, so step k+1's upload overlaps step k's kernels.
+        def packed(tensors):
+            offs, o = {}, 0
+            for name, t in tensors.items():
+                offs[name] = (o, t.numel() * t.element_size())
+                o += (offs[name][1] + 255) // 256 * 256
+            return offs, o
 
-        def e2e_step():
-            for d_, h_ in h2d:
-                d_.copy_(h_, non_blocking=True)
-            step(dq, dk, dv)
-            hout.copy_(out, non_blocking=True)
-            hhash.copy_(hashes, non_blocking=True)
+        in_offs, in_bytes = packed(inputs)
+        out_offs, out_bytes = packed(outputs)
+        hin = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+        for name, t in inputs.items():
+            o, n = in_offs[name]
+            hin[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+        hout = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+        din = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+        dout = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
 
-        for _ in range(3):
-            e2e_step()
+        def views(buf, offs, like):
+            return {name: buf[offs[name][0]:offs[name][0] + offs[name][1]].view(t.dtype)
+                    .view(t.shape) for name, t in like.items()}
+
+        I2 = [views(din[b], in_offs, inputs) for b in range(2)]
+        O2 = [views(dout[b], out_offs, outputs) for b in range(2)]
+        up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+
+        def e2e_step(k):
+            b = k & 1
+            up.wait_event(ev_done[b])            # step k-2 finished reading set b
+            with torch.cuda.stream(up):
+                din[b].copy_(hin, non_blocking=True)
+            ev_in[b].record(up)
+            main.wait_event(ev_in[b])
+            main.wait_event(ev_out[b])           # step k-2's results of set b are home
+            step(I2[b], O2[b])
+            ev_done[b].record(main)
+            down.wait_event(ev_done[b])
+            with torch.cuda.stream(down):
+                hout[b].copy_(dout[b], non_blocking=True)
+            ev_out[b].record(down)
+
+        for k in range(4):
+            e2e_step(k)
         torch.cuda.synchronize(dev)
         if world > 1:
             dist.barrier()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(main)
-        for _ in range(K):
-            e2e_step()
+        up.wait_stream(main)                     # no upload starts before the timed region
+        for k in range(K):
+            e2e_step(k)
+        main.wait_stream(down)
         f1.record(main)
         torch.cuda.synchronize(dev)
         te = aggregate_max(f0.elapsed_time(f1) / 1e3, world, dev)
         e2e = {"value": round(total_bytes / te / 1e9, 2), "unit": UNIT,
-               "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
-               "ms_per_step": round(te / K * 1e3, 4)}
+               "h2d_bytes_per_step": int(sum(n for _, n in in_offs.values())),
+               "d2h_bytes_per_step": int(sum(n for _, n in out_offs.values())),
+               "ms_per_step": round(te / K * 1e3, 4),
+               "copies": "one packed H2D and one D2H per step on their own streams, "
+                         "double-buffered (upload of step k+1 overlaps step k)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:

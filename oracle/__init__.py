@@ -15,6 +15,7 @@ Parity status per function (what pins it, see tests/test_oracle_pins.py):
   bf16_to_double, e4m3_to_double, e4m3_from_float  -- library codecs (torch CPU) + OCP spec values
   kv_bytes                                         -- the printed 327,680 B/token and ~10 GB at 32K
   slot_mapping, kv_cache_write                     -- worked example + write/gather round trip
+  multiquery_attn                                  -- dense causal brute force, q_len = 1 case
   decode_attn / decode_rows                        -- dense brute force, permutation invariance,
                                                       GQA == replicated MHA, closed-form cases, LSE merge
   fnv1a64, fmix64                                  -- published FNV-1a and SplitMix64 test vectors
@@ -83,6 +84,9 @@ def lib():
             L.orc_decode_rows.restype = None
             L.orc_decode_rows.argtypes = [_p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i,
                                           _d, _p, _i64, _p]
+            L.orc_multiquery_attn.restype = None
+            L.orc_multiquery_attn.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i,
+                                              _i, _i, _i, _d, _p]
             L.orc_num_threads.restype = _i
             L.orc_num_threads.argtypes = []
             L.orc_fnv1a64.restype = _u64
@@ -173,6 +177,22 @@ def decode_attn(q, k_cache, v_cache, block_table, seq_lens, scale, k_scale=None,
     lib().orc_paged_decode_attn(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
                                 bt.shape[1], _ptr(sl), N, Hq, Hkv, D, BS, int(fp8),
                                 float(scale), _ptr(out))
+    return out
+
+
+def multiquery_attn(q, q_offsets, k_cache, v_cache, block_table, seq_lens, scale, k_scale=None,
+                    v_scale=None):
+    """fp64 output [T, Hq, D]: query rows q_offsets[r]..q_offsets[r+1]-1 of request r are
+    its newest tokens and attend causally (position seq_len - q_len + i and before)."""
+    q, kc, vc, ks, vs, bt, sl, fp8 = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
+                                                  k_scale, v_scale)
+    qo = _c(q_offsets, np.int32)
+    T, Hq, D = q.shape
+    Hkv, BS = kc.shape[1], kc.shape[2]
+    out = np.empty((T, Hq, D), dtype=np.float64)
+    lib().orc_multiquery_attn(_ptr(q), _ptr(qo), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
+                              bt.shape[1], _ptr(sl), qo.shape[0] - 1, Hq, Hkv, D, BS, int(fp8),
+                              float(scale), _ptr(out))
     return out
 
 

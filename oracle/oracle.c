@@ -269,6 +269,51 @@ void orc_decode_row(const uint16_t *q, const void *k_cache, const void *v_cache,
     free(s);
 }
 
+/* Multi-query paged attention: several new query tokens per request, the case of
+ * verifying speculative draft tokens in one pass ([P1] "投机解码：打破每步一token的
+ * 假设": the large model checks K drafted tokens in a single forward) with the
+ * causal rule of [P1] "KV Cache：Transformer的循环状态" (a token sees itself and
+ * everything before it).
+ * Request r owns query rows q_offsets[r] .. q_offsets[r+1]-1 (q bf16 [T][Hq][D]);
+ * with q_len = q_offsets[r+1] - q_offsets[r], its query i is the token at position
+ * seq_lens[r] - q_len + i, whose K/V are already in the cache, and it attends to
+ * the cached tokens at positions 0 .. seq_lens[r] - q_len + i.  Each row is the
+ * attention of orc_decode_row restricted to that prefix of the request; a query
+ * that sees no token gets a zero row.  out [T][Hq][D] doubles. */
+void orc_multiquery_attn(const uint16_t *q, const int32_t *q_offsets, const void *k_cache,
+                         const void *v_cache, const float *k_scale, const float *v_scale,
+                         const int32_t *block_table, int max_blocks_per_seq,
+                         const int32_t *seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int cache_is_fp8, double scale,
+                         double *out)
+{
+    int64_t T = q_offsets[batch];
+    int64_t rows = T * num_q_heads;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t row = 0; row < rows; ++row) {
+        int64_t tq = row / num_q_heads;          /* query token */
+        int hq = (int)(row % num_q_heads);
+        int r = 0;
+        while (q_offsets[r + 1] <= tq)
+            ++r;
+        int q_len = q_offsets[r + 1] - q_offsets[r];
+        int i = (int)(tq - q_offsets[r]);
+        int visible = seq_lens[r] - q_len + i + 1;  /* tokens at positions 0..pos */
+        if (visible < 0)
+            visible = 0;
+        if (visible > seq_lens[r])
+            visible = seq_lens[r];
+        /* the same computation as a single-query decode of a request whose cache
+         * holds only the visible prefix, with this row's query */
+        int32_t len1 = visible;
+        const int32_t *bt_row = block_table + (int64_t)r * max_blocks_per_seq;
+        orc_decode_row(q + tq * num_q_heads * head_dim, k_cache, v_cache, k_scale, v_scale,
+                       bt_row, max_blocks_per_seq, &len1, num_q_heads, num_kv_heads, head_dim,
+                       block_size, cache_is_fp8, scale, 0, hq, out + row * head_dim, NULL,
+                       NULL);
+    }
+}
+
 /* All rows of a batch: out [N][Hq][D] doubles.  Rows are independent, so they
  * are spread over threads; each row is computed exactly as above. */
 void orc_paged_decode_attn(const uint16_t *q, const void *k_cache, const void *v_cache,

@@ -425,3 +425,56 @@ def test_hash_prefix_sharing_workload():
 def test_hash_empty_and_short_sequences():
     out = _hash([[], [1, 2, 3], list(range(16))])
     assert len(out[0]) == 0 and len(out[1]) == 0 and len(out[2]) == 1
+
+
+# ---------------------------------------------------------------- multi-query (verify) attention
+def _dense_causal(q, qoffs, K, V, scale, G):
+    """Query i of request r (its newest tokens) over positions 0..S-q_len+i, with scipy."""
+    out = np.zeros((q.shape[0], q.shape[1], q.shape[2]))
+    for r in range(len(K)):
+        Kr = W.bf16_bits_to_f32(K[r]).astype(np.float64)
+        Vr = W.bf16_bits_to_f32(V[r]).astype(np.float64)
+        S = Kr.shape[0]
+        ql = qoffs[r + 1] - qoffs[r]
+        for i in range(ql):
+            qv = W.bf16_bits_to_f32(q[qoffs[r] + i]).astype(np.float64)
+            n = S - ql + i + 1
+            if n <= 0:
+                continue
+            for hq in range(q.shape[1]):
+                s = scale * (Kr[:n, hq // G, :] @ qv[hq])
+                out[qoffs[r] + i, hq] = scipy.special.softmax(s) @ Vr[:n, hq // G, :]
+    return out
+
+
+def test_multiquery_matches_dense_causal_bruteforce():
+    rng = np.random.default_rng(71)
+    BS, Hkv, G, D = 16, 2, 4, 64
+    lens = [1, 5, 16, 40, 77]
+    qlens = [1, 2, 4, 3, 8]
+    K = [_bf16(rng.standard_normal((S, Hkv, D))) for S in lens]
+    V = [_bf16(rng.standard_normal((S, Hkv, D))) for S in lens]
+    qoffs = np.zeros(len(lens) + 1, np.int32)
+    np.cumsum(qlens, out=qoffs[1:])
+    q = _bf16(rng.standard_normal((int(qoffs[-1]), Hkv * G, D)))
+    kc, vc, bt = _paged_from_dense(rng, K, V, BS)
+    got = oracle.multiquery_attn(q, qoffs, kc, vc, bt, np.array(lens, np.int32), 0.1)
+    ref = _dense_causal(q, qoffs, K, V, 0.1, G)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_multiquery_single_query_is_decode_and_empty_rows_are_zero():
+    wl = W.make(2, small=True)
+    d = W.host_data(wl)
+    qoffs = np.arange(wl.N + 1, dtype=np.int32)
+    got = oracle.multiquery_attn(d["q"], qoffs, d["k_cache"], d["v_cache"], wl.block_table,
+                                 wl.seq_lens, wl.scale)
+    ref = oracle.decode_attn(d["q"], d["k_cache"], d["v_cache"], wl.block_table, wl.seq_lens,
+                             wl.scale)
+    assert np.array_equal(got, ref)
+    # more queries than cached tokens: the first queries see nothing
+    q = np.repeat(d["q"][:1], 5, axis=0)
+    lens = np.array([3], np.int32)
+    got = oracle.multiquery_attn(q, np.array([0, 5], np.int32), d["k_cache"], d["v_cache"],
+                                 wl.block_table[:1], lens, wl.scale)
+    assert np.all(got[:2] == 0) and np.all(np.any(got[2:] != 0, axis=-1))

@@ -180,7 +180,8 @@ def workload_config(wl):
     return {"workload": wl.name, "batch": wl.N, "num_q_heads": wl.Hq, "num_kv_heads": wl.Hkv,
             "head_dim": wl.D, "block_size": wl.BS, "kv_dtype": "fp8_e4m3" if wl.fp8 else "bf16",
             "seq_lens": "log-uniform [128, 16384]" if wl.cfg == 5 else
-            ("uniform [1024, 8192]" if wl.cfg == 2 else "see workload"),
+            ("uniform [1024, 8192]" if wl.cfg in (2, 6) else "see workload"),
+            "query_tokens_per_request": wl.q_len,
             "mean_seq_len": round(float(wl.seq_lens.mean()), 1), "num_blocks": wl.NB,
             "kv_bytes_per_step": wl.kv_read_bytes(),
             "l2": "inputs larger than L2 (%.2f GB of pages vs 129 MB L2); no flush"
@@ -195,7 +196,7 @@ def decode_algorithmic_bytes(wl):
     b += nblk * 4                                        # block table entries read
     if wl.fp8:
         b += nblk * wl.Hkv * 2 * 4                       # K and V scales
-    b += 2 * wl.N * wl.Hq * wl.D * 2                     # q in, out
+    b += 2 * wl.N * wl.q_len * wl.Hq * wl.D * 2          # q in, out
     return b
 
 
@@ -283,7 +284,10 @@ def run_ours(args):
     dt_code = pkv.FP8_E4M3 if fp8 else pkv.BF16
     bt = torch.from_numpy(wl.block_table).to(dev)
     sl = torch.from_numpy(wl.seq_lens).to(dev)
-    pos = torch.from_numpy(wl.new_token_positions()).to(dev)
+    req_new, pos_new = wl.new_token_rows()      # the step's new tokens (q_len per request)
+    pos = torch.from_numpy(pos_new).to(dev)
+    req = torch.from_numpy(req_new).to(dev)
+    qoffs = torch.from_numpy(wl.q_offsets()).to(dev)
     if fp8:
         kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch.uint8, device=dev)
         vc = torch.zeros_like(kc)
@@ -305,29 +309,37 @@ def run_ours(args):
     nh = int(ho_np[-1])
     hashes = torch.empty(max(nh, 1), dtype=torch.int64, device=dev)
     out = torch.empty_like(dd["q"])
-    slots = torch.empty(wl.N, dtype=torch.int64, device=dev)
-    ws = pkv.alloc_decode_workspace(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, dt_code, device=dev)
+    slots = torch.empty(wl.N * wl.q_len, dtype=torch.int64, device=dev)
+    ws = torch.zeros(pkv.multiquery_workspace_size(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, dt_code,
+                                                   wl.q_len), dtype=torch.uint8, device=dev)
     main = torch.cuda.current_stream(dev)
     side = torch.cuda.Stream(dev)
     launches_per_step = 5   # slot map, write, decode, wide-split merge, hash
 
     def step(I, O, dec_ev=None):
         """One decode step on the per-step inputs I, writing the results O."""
-        pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, out=slots, stream=main)
+        pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, req_idx=I["req"], out=slots,
+                                 stream=main)
         pkv.kv_cache_write(I["k_new"], I["v_new"], slots, kc, vc, ks, vs, stream=main)
         side.wait_stream(main)
         pkv.prefix_block_hash(I["tokens"], I["toffs"], wl.hash_block, I["hoffs"], nh, seed=0,
                               out=O["hashes"], stream=side)
         if dec_ev is not None:
             dec_ev[0].record(main)
-        pkv.paged_decode_attn(I["q"], kc, vc, I["bt"], I["sl"], wl.scale, out=O["out"],
-                              k_scale=ks, v_scale=vs, workspace=ws, stream=main)
+        if wl.q_len == 1:
+            pkv.paged_decode_attn(I["q"], kc, vc, I["bt"], I["sl"], wl.scale, out=O["out"],
+                                  k_scale=ks, v_scale=vs, workspace=ws, stream=main)
+        else:
+            pkv.paged_multiquery_attn(I["q"], I["qoffs"], wl.q_len, kc, vc, I["bt"], I["sl"],
+                                      wl.scale, out=O["out"], k_scale=ks, v_scale=vs,
+                                      workspace=ws, stream=main)
         if dec_ev is not None:
             dec_ev[1].record(main)
         main.wait_stream(side)
 
     q, k_new, v_new = dd["q"], dd["k_new"], dd["v_new"]
-    inputs = {"q": q, "k_new": k_new, "v_new": v_new, "pos": pos, "bt": bt, "sl": sl,
+    inputs = {"q": q, "k_new": k_new, "v_new": v_new, "pos": pos, "req": req, "qoffs": qoffs,
+              "bt": bt, "sl": sl,
               "tokens": tokens, "toffs": toffs, "hoffs": hoffs}
     outputs = {"out": out, "hashes": hashes}
     for _ in range(max(args.warmup, 3)):
@@ -364,7 +376,7 @@ def run_ours(args):
     t_max = aggregate_max(t_total, world, dev)
     kv_bytes = wl.kv_read_bytes()
     total_bytes = aggregate_sum(float(kv_bytes) * K, world, dev)
-    total_q = aggregate_sum(float(wl.N) * K, world, dev)
+    total_q = aggregate_sum(float(wl.N * wl.q_len) * K, world, dev)
     value = total_bytes / t_max / 1e9
     ms_per_step = t_max / K * 1e3
 

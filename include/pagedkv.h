@@ -77,6 +77,7 @@ enum {
 #define PKV_DEVERR_WAIT_TIMEOUT  0x1u  /* a pipeline wait gave up after ~2 s      */
 #define PKV_DEVERR_SEQ_CLAMPED   0x2u  /* seq_lens[r] < 0 or > MB*BS was clamped  */
 #define PKV_DEVERR_BLOCK_RANGE   0x4u  /* a block id outside [0, NB) was read     */
+#define PKV_DEVERR_QLEN_CLAMPED  0x8u  /* a request's query count exceeded max_q_len */
 
 /* Human-readable name of a pkv_status value (static string). */
 PKV_API const char *pkv_status_string(int status);
@@ -162,6 +163,35 @@ PKV_API int pkv_paged_decode_attn(const void *q, const void *k_cache, const void
                           int num_kv_heads, int head_dim, int block_size, int num_blocks,
                           int cache_dtype, float scale, void *out, void *workspace,
                           size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * Multi-query paged attention: q_len >= 1 new query tokens per request, as when a
+ * speculative draft of several tokens is verified in one pass ([P1] "投机解码：打破
+ * 每步一token的假设"; [P2] "投机解码").  Request r owns query rows
+ * q_offsets[r] .. q_offsets[r+1]-1 of q (bf16 [T][Hq][D]; out has the same
+ * layout).  Its query i is the token at position seq_lens[r] - q_len + i, whose
+ * K/V are already in the cache, and it attends causally ([P1] "KV Cache：
+ * Transformer的循环状态") to the cached positions 0 .. seq_lens[r] - q_len + i.
+ * A query that sees no token gets a zero row.  Each KV page is read once for all
+ * of a request's queries and heads of a group.
+ * Supported: 1 <= max_q_len <= 4 with bf16 pages, <= 2 with FP8 pages; every
+ * request must have q_offsets[r+1] - q_offsets[r] <= max_q_len (a larger count
+ * is clamped and sets PKV_DEVERR_QLEN_CLAMPED; the rows past the clamp are not
+ * written).  Everything else as pkv_paged_decode_attn; q_offsets is a device
+ * int32 [N + 1] array.  The workspace comes from pkv_multiquery_workspace_size.
+ */
+PKV_API size_t pkv_multiquery_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                             int head_dim, int block_size, int cache_dtype,
+                                             int max_q_len, int num_sms);
+PKV_API int pkv_paged_multiquery_attn(const void *q, const int32_t *q_offsets, int max_q_len,
+                                      const void *k_cache, const void *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_table, int max_blocks_per_seq,
+                                      const int32_t *seq_lens, int batch, int num_q_heads,
+                                      int num_kv_heads, int head_dim, int block_size,
+                                      int num_blocks, int cache_dtype, float scale, void *out,
+                                      void *workspace, size_t workspace_bytes,
+                                      pkv_stream_t stream);
 
 /*
  * Paged decode attention that allocates nothing.  The sources describe no such

@@ -15,7 +15,8 @@ __all__ = [
     "PkvError", "lib", "library_path", "BF16", "FP8_E4M3", "DEVERR_WAIT_TIMEOUT",
     "DEVERR_SEQ_CLAMPED", "DEVERR_BLOCK_RANGE", "compute_slot_mapping", "kv_cache_write",
     "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn",
-    "paged_decode_attn_noalloc", "prefix_block_hash",
+    "paged_decode_attn_noalloc", "prefix_block_hash", "multiquery_workspace_size",
+    "paged_multiquery_attn", "DEVERR_QLEN_CLAMPED",
     "device_num_sms", "read_device_error",
 ]
 
@@ -24,6 +25,7 @@ FP8_E4M3 = 1
 DEVERR_WAIT_TIMEOUT = 0x1
 DEVERR_SEQ_CLAMPED = 0x2
 DEVERR_BLOCK_RANGE = 0x4
+DEVERR_QLEN_CLAMPED = 0x8
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "lib", "libpagedkv.so")
@@ -65,6 +67,11 @@ def lib():
             L.pkv_paged_decode_attn.restype = i
             L.pkv_paged_decode_attn.argtypes = [p, p, p, p, p, p, i, p, i, i, i, i, i, i, i, f,
                                                 p, p, sz, p]
+            L.pkv_multiquery_workspace_size.restype = sz
+            L.pkv_multiquery_workspace_size.argtypes = [i, i, i, i, i, i, i, i]
+            L.pkv_paged_multiquery_attn.restype = i
+            L.pkv_paged_multiquery_attn.argtypes = [p, p, i, p, p, p, p, p, i, p, i, i, i, i, i,
+                                                    i, i, f, p, p, sz, p]
             L.pkv_paged_decode_attn_noalloc.restype = i
             L.pkv_paged_decode_attn_noalloc.argtypes = [p, p, p, p, p, p, i, p, i, i, i, i, i, i,
                                                         i, f, p, p]
@@ -184,6 +191,44 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, scale, out=Non
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
         block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D, BS, NB, dt, float(scale), _ptr(out),
         _ptr(workspace), workspace.numel(), _stream(stream)))
+    return out
+
+
+def multiquery_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                              cache_dtype, max_q_len, num_sms=0) -> int:
+    return int(lib().pkv_multiquery_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                   block_size, cache_dtype, max_q_len, num_sms))
+
+
+def paged_multiquery_attn(q, q_offsets, max_q_len, k_cache, v_cache, block_table, seq_lens,
+                          scale, out=None, k_scale=None, v_scale=None, workspace=None,
+                          stream=None):
+    """Several new query tokens per request (speculative verify): query rows
+    q_offsets[r]..q_offsets[r+1]-1 of q [T, Hq, D] are request r's newest tokens and
+    attend causally.  Returns out [T, Hq, D] bf16."""
+    import torch
+    _need(q, "q", (torch.bfloat16,))
+    _need(q_offsets, "q_offsets", (torch.int32,))
+    _need(k_cache, "k_cache", None)
+    _need(v_cache, "v_cache", None)
+    _need(block_table, "block_table", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    T, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_cache.shape
+    N = seq_lens.shape[0]
+    dt = _cache_dtype(k_cache)
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        n = multiquery_workspace_size(N, Hq, Hkv, D, BS, dt, max_q_len)
+        if n == 0:
+            raise PkvError("pkv_multiquery_workspace_size", -2)
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    _check("pkv_paged_multiquery_attn", lib().pkv_paged_multiquery_attn(
+        _ptr(q), _ptr(q_offsets), int(max_q_len), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+        _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D,
+        BS, NB, dt, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
+        _stream(stream)))
     return out
 
 

@@ -85,30 +85,40 @@ int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
-                                 int block_size, int cache_dtype, int num_sms) {
-    if (batch < 0 || batch > pkv::kMaxBatch) return 0;
+size_t pkv_multiquery_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int cache_dtype, int max_q_len,
+                                     int num_sms) {
+    if (batch < 0 || batch > pkv::kMaxBatch || max_q_len < 1) return 0;
     if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype)) return 0;
     if (num_sms <= 0 && current_num_sms(&num_sms) != PKV_OK) return 0;
     return pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
-                                       cache_dtype == PKV_FP8_E4M3, num_sms);
+                                       cache_dtype == PKV_FP8_E4M3, num_sms, max_q_len);
 }
 
-int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
-                          const float* k_scale, const float* v_scale,
-                          const int32_t* block_table, int max_blocks_per_seq,
-                          const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
-                          int head_dim, int block_size, int num_blocks, int cache_dtype,
-                          float scale, void* out, void* workspace, size_t workspace_bytes,
-                          pkv_stream_t stream) {
-    if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int cache_dtype, int num_sms) {
+    return pkv_multiquery_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                         cache_dtype, 1, num_sms);
+}
+
+int pkv_paged_multiquery_attn(const void* q, const int32_t* q_offsets, int max_q_len,
+                              const void* k_cache, const void* v_cache, const float* k_scale,
+                              const float* v_scale, const int32_t* block_table,
+                              int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                              int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                              int num_blocks, int cache_dtype, float scale, void* out,
+                              void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+    if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_q_len < 1)
+        return PKV_ERR_INVALID_ARG;
     if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
     if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype))
         return PKV_ERR_UNSUPPORTED;
+    if (pkv::query_tile(cache_dtype == PKV_FP8_E4M3, max_q_len) == 0) return PKV_ERR_UNSUPPORTED;
     if (batch > pkv::kMaxBatch) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
         return PKV_ERR_INVALID_ARG;
+    if (max_q_len > 1 && !q_offsets) return PKV_ERR_INVALID_ARG;
     if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PKV_ERR_INVALID_ARG;
@@ -116,16 +126,19 @@ int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cach
     const int64_t rows = ((int64_t)num_blocks + 1) * num_kv_heads * block_size;
     const int64_t max_pages = (int64_t)batch * num_kv_heads * max_blocks_per_seq;
     if (rows >= (int64_t)1 << 31 || max_pages >= (int64_t)1 << 31 ||
-        (int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 31)
+        (int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 22)
         return PKV_ERR_UNSUPPORTED;
     int num_sms = 0;
     if (current_num_sms(&num_sms) != PKV_OK) return PKV_ERR_CUDA;
     const size_t need = pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
-                                                    cache_dtype == PKV_FP8_E4M3, num_sms);
+                                                    cache_dtype == PKV_FP8_E4M3, num_sms,
+                                                    max_q_len);
     if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
     pkv::DecodeLaunch L;
     L.q = q;
+    L.q_offsets = q_offsets;
+    L.max_q_len = max_q_len;
     L.k_cache = k_cache;
     L.v_cache = v_cache;
     L.k_scale = k_scale;
@@ -145,6 +158,19 @@ int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cach
     L.scale = scale;
     L.num_sms = num_sms;
     return pkv::decode_launch(L, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int pkv_paged_decode_attn(const void* q, const void* k_cache, const void* v_cache,
+                          const float* k_scale, const float* v_scale,
+                          const int32_t* block_table, int max_blocks_per_seq,
+                          const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                          int head_dim, int block_size, int num_blocks, int cache_dtype,
+                          float scale, void* out, void* workspace, size_t workspace_bytes,
+                          pkv_stream_t stream) {
+    return pkv_paged_multiquery_attn(q, nullptr, 1, k_cache, v_cache, k_scale, v_scale,
+                                     block_table, max_blocks_per_seq, seq_lens, batch,
+                                     num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                     cache_dtype, scale, out, workspace, workspace_bytes, stream);
 }
 
 int pkv_prefix_block_hash(const int32_t* tokens, const int64_t* offsets, int num_seqs,

@@ -1,4 +1,5 @@
-// pkv_decode.cu -- paged GQA decode attention for sm_103a.
+// pkv_decode.cu -- paged GQA decode attention for sm_103a, one or several query
+// tokens per request.
 //
 // Computes, for every request r and query head hq (kv head h = hq / G),
 //     out[r][hq] = softmax(scale * q K_r^T) V_r
@@ -7,6 +8,9 @@
 // 的循环状态" and "PagedAttention与Cache管理"), with an online (running max / sum)
 // softmax ("GPU推理深度拆解：KV Cache视角", 算子优化要点) and the KV length split
 // across warps when the batch is small (same note: batch-1 decode leaves SMs idle).
+// With several query tokens per request (verifying speculative drafts, [P1]
+// "投机解码：打破每步一token的假设"), query i of the request's q_len newest tokens
+// attends causally to positions 0 .. seq_len - q_len + i.
 //
 // Work decomposition.  Unit u = (request r, kv head h) owns np_r = ceil(seq_r / BS)
 // pages.  All units' pages form one flat list of P items (request-major, then
@@ -20,18 +24,19 @@
 // arrive merges the partials with log-sum-exp weights; wider units are merged by a
 // small follow-up kernel.  Nobody waits for anybody.
 //
-// Per-warp pipeline.  Each warp owns `stages` shared-memory stages of one
-// (block, head) K page + V page.  Lane 0 issues 2-D bulk tensor copies (TMA,
-// 128-byte swizzle, box = 128 bytes x BS rows) that complete on the stage's
-// mbarrier; all lanes wait on it (bounded), compute, and the stage is refilled
-// with the page `stages` ahead.  Block ids for the next 32 pages are looked up
-// one batch ahead (one lane per page), so the issue path never waits on the
+// Per-warp pipeline.  Each warp owns `stages` shared-memory stages, each holding
+// the K and V tile (TT tokens) of one (block, head) page.  Lane 0 issues 2-D bulk
+// tensor copies (TMA, 128-byte swizzle, box = 128 bytes x TT rows) that complete on
+// the stage's mbarrier; all lanes wait on it (bounded), compute, and the stage is
+// refilled with the tile `stages` ahead.  Block ids for the next 32 pages are looked
+// up one batch ahead (one lane per page), so the issue path never waits on the
 // block table.
 //
-// Math per page (tensor cores, mma.sync m16n8k16, fp32 accumulators):
-//   S^T[t][g] = K[t][:] . Q[g][:]     A = K page tile (16 tokens x 16 d, ldmatrix),
+// Math per tile (tensor cores, mma.sync m16n8k16, fp32 accumulators); one mma
+// n-tile of 8 columns per query position, a column per query head of the group:
+//   S^T[t][g] = K[t][:] . Q[g][:]     A = K tile (16 tokens x 16 d, ldmatrix),
 //                                     B = Q^T of the GQA group (8 heads, registers)
-//   O^T[d][g] += V^T[d][t] P^T[t][g]  A = V page tile (ldmatrix.trans), B = P^T from
+//   O^T[d][g] += V^T[d][t] P^T[t][g]  A = V tile (ldmatrix.trans), B = P^T from
 //                                     the S^T accumulators via movmatrix.trans
 // FP8 (E4M3) pages are widened to fp16 in registers (cvt e4m3x2 -> f16x2); the
 // per-(block, head) K scale multiplies S, the V scale multiplies the page's P.V
@@ -48,6 +53,7 @@ namespace pkv {
 
 struct DecodeArgs {
     const uint16_t* q;
+    const int32_t* q_offsets;       // [N + 1] query rows of each request; null: row r
     uint16_t* out;
     const int32_t* block_table;
     const int32_t* seq_lens;
@@ -103,7 +109,7 @@ __device__ __forceinline__ uint32_t swz(int t, int kc) {
 struct PageBatch {
     int id;        // physical block (NB = out of range sentinel)
     int r, h;      // unit
-    uint32_t fl;   // valid tokens | first << 8 | last << 9
+    uint32_t fl;   // valid tokens | first << 8 | last << 9 | page index j << 10
     float ks, vs;  // FP8 scales
 };
 
@@ -134,10 +140,28 @@ __device__ __forceinline__ void load_batch(PageBatch& b, int xbeg, int x1,
     b.id = id;
     b.r = r;
     b.h = h;
-    b.fl = (uint32_t)ntok | ((j == 0) ? 0x100u : 0u) | ((j == np - 1) ? 0x200u : 0u);
+    b.fl = (uint32_t)ntok | ((j == 0) ? 0x100u : 0u) | ((j == np - 1) ? 0x200u : 0u) |
+           ((uint32_t)j << 10);
     if (FP8 && id < a.NB) {
         b.ks = __ldg(a.k_scale + (int64_t)id * a.Hkv + h);
         b.vs = __ldg(a.v_scale + (int64_t)id * a.Hkv + h);
+    }
+}
+
+// The query rows of request r: first row and count (clamped to QT).
+template <int QT>
+__device__ __forceinline__ void query_rows(const DecodeArgs& a, int r, int& qb, int& qlen,
+                                           uint32_t& errbits) {
+    if (a.q_offsets == nullptr) {
+        qb = r;
+        qlen = 1;
+        return;
+    }
+    qb = __ldg(a.q_offsets + r);
+    qlen = __ldg(a.q_offsets + r + 1) - qb;
+    if (qlen < 0 || qlen > QT) {
+        errbits |= PKV_DEVERR_QLEN_CLAMPED;
+        qlen = min(max(qlen, 0), QT);
     }
 }
 
@@ -163,67 +187,77 @@ __device__ __forceinline__ uint32_t counter_arrive(unsigned long long* p, uint32
 // Log-sum-exp merge of unit u's partials written by warps wf..wl (slots u + w):
 //   M = max_w m_w,  out = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w
 // ("GPU推理深度拆解：KV Cache视角", 系统层：Context Parallel: the online-softmax merge
-// that ring attention also uses).  Lanes 0..7 reduce (m, l) per head; then every lane
-// accumulates D/32 output columns of all heads.  Partials are read through L2 (.cg):
-// they were written by other SMs during this launch.
-template <int D>
+// that ring attention also uses), for each of the request's qlen query positions.
+// Lanes 0..7 reduce (m, l) per head; then every lane accumulates D/32 output
+// columns of all heads.  Partials are read through L2 (.cg): they were written by
+// other SMs during this launch.  A query that saw no token anywhere (M = -inf) gets
+// a zero row.
+template <int D, int QT>
 __device__ __noinline__ void merge_unit(const float* partials, uint16_t* out, int Hq, int G,
-                                        int64_t u, int wf, int wl, int r, int h) {
+                                        int64_t u, int wf, int wl, int qb, int qlen, int h) {
     constexpr int PER = D / 32;
-    constexpr int SLOT = kGroupPad * (D + 4);
+    constexpr int QS = kGroupPad * (D + 4);   // one query position of a slot
+    constexpr int SLOT = QT * QS;
     const int lane = threadIdx.x & 31;
-    const float* base = partials + (u + wf) * SLOT;
     const int n = wl - wf + 1;
-    float M = -INFINITY, L = 0.f;
-    if (lane < kGroupPad) {
-        for (int k = 0; k < n; ++k) M = fmaxf(M, __ldcg(base + (int64_t)k * SLOT + lane * (D + 4) + D));
-        for (int k = 0; k < n; ++k) {
-            const float2 ml = __ldcg(reinterpret_cast<const float2*>(
-                base + (int64_t)k * SLOT + lane * (D + 4) + D));
-            L = fmaf(exp2f(ml.x - M), ml.y, L);
-        }
-    }
-    float Mh[kGroupPad];
-#pragma unroll
-    for (int gg = 0; gg < kGroupPad; ++gg) Mh[gg] = __shfl_sync(0xffffffffu, M, gg);
-    float acc[kGroupPad][PER];
-#pragma unroll
-    for (int gg = 0; gg < kGroupPad; ++gg)
-#pragma unroll
-        for (int k = 0; k < PER; ++k) acc[gg][k] = 0.f;
-    for (int k = 0; k < n; ++k) {
-        const float* ps = base + (int64_t)k * SLOT;
-#pragma unroll
-        for (int gg = 0; gg < kGroupPad; ++gg) {
-            if (gg >= G) break;
-            const float wt = exp2f(__ldcg(ps + gg * (D + 4) + D) - Mh[gg]);
-            if constexpr (PER == 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + gg * (D + 4) + lane * 4));
-                acc[gg][0] = fmaf(wt, v.x, acc[gg][0]);
-                acc[gg][1] = fmaf(wt, v.y, acc[gg][1]);
-                acc[gg][2] = fmaf(wt, v.z, acc[gg][2]);
-                acc[gg][3] = fmaf(wt, v.w, acc[gg][3]);
-            } else {
-                const float2 v = __ldcg(reinterpret_cast<const float2*>(ps + gg * (D + 4) + lane * 2));
-                acc[gg][0] = fmaf(wt, v.x, acc[gg][0]);
-                acc[gg][1] = fmaf(wt, v.y, acc[gg][1]);
+    for (int qi = 0; qi < qlen; ++qi) {
+        const float* base = partials + (u + wf) * SLOT + qi * QS;
+        float M = -INFINITY, L = 0.f;
+        if (lane < kGroupPad) {
+            for (int k = 0; k < n; ++k)
+                M = fmaxf(M, __ldcg(base + (int64_t)k * SLOT + lane * (D + 4) + D));
+            if (M != -INFINITY) {
+                for (int k = 0; k < n; ++k) {
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(
+                        base + (int64_t)k * SLOT + lane * (D + 4) + D));
+                    L = fmaf(exp2f(ml.x - M), ml.y, L);
+                }
             }
         }
-    }
-    uint16_t* ob = out + ((int64_t)r * Hq + (int64_t)h * G) * D;
+        float Mh[kGroupPad];
 #pragma unroll
-    for (int gg = 0; gg < kGroupPad; ++gg) {
-        const float inv = 1.f / __shfl_sync(0xffffffffu, L, gg);
-        if (gg >= G) continue;
+        for (int gg = 0; gg < kGroupPad; ++gg) Mh[gg] = __shfl_sync(0xffffffffu, M, gg);
+        float acc[kGroupPad][PER];
 #pragma unroll
-        for (int k = 0; k < PER; k += 2)
-            *reinterpret_cast<uint32_t*>(ob + gg * D + lane * PER + k) =
-                pack_bf16x2(acc[gg][k] * inv, acc[gg][k + 1] * inv);
+        for (int gg = 0; gg < kGroupPad; ++gg)
+#pragma unroll
+            for (int k = 0; k < PER; ++k) acc[gg][k] = 0.f;
+        for (int k = 0; k < n; ++k) {
+            const float* ps = base + (int64_t)k * SLOT;
+#pragma unroll
+            for (int gg = 0; gg < kGroupPad; ++gg) {
+                if (gg >= G) break;
+                if (Mh[gg] == -INFINITY) continue;
+                const float wt = exp2f(__ldcg(ps + gg * (D + 4) + D) - Mh[gg]);
+                if constexpr (PER == 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(ps + gg * (D + 4) + lane * 4));
+                    acc[gg][0] = fmaf(wt, v.x, acc[gg][0]);
+                    acc[gg][1] = fmaf(wt, v.y, acc[gg][1]);
+                    acc[gg][2] = fmaf(wt, v.z, acc[gg][2]);
+                    acc[gg][3] = fmaf(wt, v.w, acc[gg][3]);
+                } else {
+                    const float2 v = __ldcg(reinterpret_cast<const float2*>(ps + gg * (D + 4) + lane * 2));
+                    acc[gg][0] = fmaf(wt, v.x, acc[gg][0]);
+                    acc[gg][1] = fmaf(wt, v.y, acc[gg][1]);
+                }
+            }
+        }
+        uint16_t* ob = out + ((int64_t)(qb + qi) * Hq + (int64_t)h * G) * D;
+#pragma unroll
+        for (int gg = 0; gg < kGroupPad; ++gg) {
+            const float Lg = __shfl_sync(0xffffffffu, L, gg);
+            const float inv = Lg > 0.f ? 1.f / Lg : 0.f;
+            if (gg >= G) continue;
+#pragma unroll
+            for (int k = 0; k < PER; k += 2)
+                *reinterpret_cast<uint32_t*>(ob + gg * D + lane * PER + k) =
+                    pack_bf16x2(acc[gg][k] * inv, acc[gg][k + 1] * inv);
+        }
     }
 }
 
-template <int D, int BS, bool FP8>
-__global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
+template <int D, int BS, bool FP8, int QT>
+__global__ void __launch_bounds__((FP8 || QT > 1) ? 256 : 384, 1)
     pkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
     using C = Cfg<D, BS, FP8>;
@@ -287,8 +321,11 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
     // requests with no cached tokens get zero output rows (grid-strided over requests)
     for (int r = blockIdx.x; r < a.N; r += gridDim.x) {
         if (s_seq[r] != 0) continue;
-        uint4* ob = reinterpret_cast<uint4*>(a.out + (int64_t)r * a.Hq * D);
-        for (int k = threadIdx.x; k < a.Hq * D / 8; k += blockDim.x) ob[k] = make_uint4(0u, 0u, 0u, 0u);
+        int qb, qlen;
+        query_rows<QT>(a, r, qb, qlen, errbits);
+        uint4* ob = reinterpret_cast<uint4*>(a.out + (int64_t)qb * a.Hq * D);
+        for (int k = threadIdx.x; k < qlen * a.Hq * D / 8; k += blockDim.x)
+            ob[k] = make_uint4(0u, 0u, 0u, 0u);
     }
 
     const int P = s_prefix[a.N];
@@ -342,13 +379,14 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
     const int g = lane >> 2;   // mma row group: head column of B / token row of A
     const int c = lane & 3;
 
-    float o[C::DT][4];
-    float ot[FP8 ? C::DT : 1][4];
-    uint32_t qf[C::KS][2];
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o[C::DT][QT][4];
+    float ot[FP8 ? C::DT : 1][QT][4];
+    uint32_t qf[C::KS][QT][2];
+    float m0[QT], m1[QT], l0[QT], l1[QT];   // heads 2c, 2c+1 of this lane, per query
     float qscale = a.scale_log2;
     bool seg_full = false;
     int seg_r = 0, seg_h = 0;
+    int seg_qb = 0, seg_qlen = 1, seg_vis = 0;   // query rows; query qi sees positions <= seg_vis + qi
 
     for (int i = 0; i < total; ++i) {
         const int pi = (C::SUB == 2) ? (i >> 1) : i;
@@ -371,40 +409,56 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
         const int ntok = (int)(fl & 0xFFu) - sub * C::TT;
         const bool first = ((fl >> 8) & 1u) && sub == 0;
         const bool last = ((fl >> 9) & 1u) && sub == C::SUB - 1;
+        const int tpos0 = (int)(fl >> 10) * BS + sub * C::TT;   // position of tile row 0
 
         // ---- segment start: load the GQA group's queries as mma B fragments ----
         if (i == 0 || first) {
             seg_full = first;
             seg_r = r;
             seg_h = h;
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
+            query_rows<QT>(a, r, seg_qb, seg_qlen, errbits);
+            seg_vis = s_seq[r] - seg_qlen;
 #pragma unroll
-            for (int dt = 0; dt < C::DT; ++dt)
+            for (int qi = 0; qi < QT; ++qi) {
+                m0[qi] = m1[qi] = -INFINITY;
+                l0[qi] = l1[qi] = 0.f;
 #pragma unroll
-                for (int e = 0; e < 4; ++e) o[dt][e] = 0.f;
-            const uint16_t* qrow = a.q + ((int64_t)r * a.Hq + (int64_t)h * a.G + g) * D;
-            const bool gv = g < a.G;
+                for (int dt = 0; dt < C::DT; ++dt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[dt][qi][e] = 0.f;
+            }
             if (!FP8) {
 #pragma unroll
-                for (int ks2 = 0; ks2 < C::KS; ++ks2) {
-                    qf[ks2][0] = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 2 * c)) : 0u;
-                    qf[ks2][1] = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 8 + 2 * c)) : 0u;
+                for (int qi = 0; qi < QT; ++qi) {
+                    const bool gv = g < a.G && qi < seg_qlen;
+                    const uint16_t* qrow =
+                        a.q + ((int64_t)(seg_qb + qi) * a.Hq + (int64_t)h * a.G + g) * D;
+#pragma unroll
+                    for (int ks2 = 0; ks2 < C::KS; ++ks2) {
+                        qf[ks2][qi][0] = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 2 * c)) : 0u;
+                        qf[ks2][qi][1] = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 8 + 2 * c)) : 0u;
+                    }
                 }
                 qscale = a.scale_log2;
             } else {
                 // k-slot mapping for E4M3 A fragments: slots 2c,2c+1 <-> d = 4c,4c+1 and
                 // slots 8+2c,9+2c <-> d = 4c+2,4c+3 of each 16-d step.
-                uint2 raw_q[C::KS];
+                uint2 raw_q[C::KS][QT];
                 float amax = 0.f;
 #pragma unroll
-                for (int ks2 = 0; ks2 < C::KS; ++ks2) {
-                    raw_q[ks2] = gv ? __ldg(reinterpret_cast<const uint2*>(qrow + ks2 * 16 + 4 * c))
-                                    : make_uint2(0u, 0u);
-                    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo_to_f32(raw_q[ks2].x)),
-                                                   fabsf(bf16_hi_to_f32(raw_q[ks2].x))),
-                                             fmaxf(fabsf(bf16_lo_to_f32(raw_q[ks2].y)),
-                                                   fabsf(bf16_hi_to_f32(raw_q[ks2].y)))));
+                for (int qi = 0; qi < QT; ++qi) {
+                    const bool gv = g < a.G && qi < seg_qlen;
+                    const uint16_t* qrow =
+                        a.q + ((int64_t)(seg_qb + qi) * a.Hq + (int64_t)h * a.G + g) * D;
+#pragma unroll
+                    for (int ks2 = 0; ks2 < C::KS; ++ks2) {
+                        raw_q[ks2][qi] = gv ? __ldg(reinterpret_cast<const uint2*>(qrow + ks2 * 16 + 4 * c))
+                                            : make_uint2(0u, 0u);
+                        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(bf16_lo_to_f32(raw_q[ks2][qi].x)),
+                                                       fabsf(bf16_hi_to_f32(raw_q[ks2][qi].x))),
+                                                 fmaxf(fabsf(bf16_lo_to_f32(raw_q[ks2][qi].y)),
+                                                       fabsf(bf16_hi_to_f32(raw_q[ks2][qi].y)))));
+                    }
                 }
 #pragma unroll
                 for (int o2 = 16; o2 > 0; o2 >>= 1)
@@ -416,17 +470,19 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
                 const float sc = __uint_as_float((uint32_t)(268 - E) << 23);
                 const float inv_sc = __uint_as_float((uint32_t)(E - 14) << 23);
 #pragma unroll
-                for (int ks2 = 0; ks2 < C::KS; ++ks2) {
-                    qf[ks2][0] = pack_f16x2(bf16_lo_to_f32(raw_q[ks2].x) * sc,
-                                            bf16_hi_to_f32(raw_q[ks2].x) * sc);
-                    qf[ks2][1] = pack_f16x2(bf16_lo_to_f32(raw_q[ks2].y) * sc,
-                                            bf16_hi_to_f32(raw_q[ks2].y) * sc);
-                }
+                for (int qi = 0; qi < QT; ++qi)
+#pragma unroll
+                    for (int ks2 = 0; ks2 < C::KS; ++ks2) {
+                        qf[ks2][qi][0] = pack_f16x2(bf16_lo_to_f32(raw_q[ks2][qi].x) * sc,
+                                                    bf16_hi_to_f32(raw_q[ks2][qi].x) * sc);
+                        qf[ks2][qi][1] = pack_f16x2(bf16_lo_to_f32(raw_q[ks2][qi].y) * sc,
+                                                    bf16_hi_to_f32(raw_q[ks2][qi].y) * sc);
+                    }
                 qscale = a.scale_log2 * inv_sc;
             }
         }
 
-        // ---- wait for the page ----
+        // ---- wait for the tile ----
         const int s = i % S;
         const uint32_t par = (uint32_t)((i / S) & 1);
         bool ok = mbar_wait_bounded(bars + 8u * s, par, kWaitLimitNs);
@@ -458,92 +514,127 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
             __syncwarp();
         }
 
-        // ---- S^T = K Q^T (tokens x heads) ----
-        float sacc[C::MT][4];
+        // ---- S^T = K Q^T (tokens x heads), one n-tile per query position ----
+        float sacc[C::MT][QT][4];
 #pragma unroll
         for (int mt = 0; mt < C::MT; ++mt) {
-            float e0[4] = {0.f, 0.f, 0.f, 0.f}, e1[4] = {0.f, 0.f, 0.f, 0.f};
+            float e0[QT][4], e1[QT][4];
+#pragma unroll
+            for (int qi = 0; qi < QT; ++qi)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) e0[qi][e] = e1[qi][e] = 0.f;
             const int t = mt * 16 + (lane & 15);
             if (!FP8) {
 #pragma unroll
                 for (int ks2 = 0; ks2 < C::KS; ++ks2) {
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4(kpg + swz<C::TT>(t, 2 * ks2 + (lane >> 4)), a0, a1, a2, a3);
-                    if (ks2 & 1) mma_bf16(e1, a0, a1, a2, a3, qf[ks2][0], qf[ks2][1]);
-                    else         mma_bf16(e0, a0, a1, a2, a3, qf[ks2][0], qf[ks2][1]);
+#pragma unroll
+                    for (int qi = 0; qi < QT; ++qi) {
+                        if (ks2 & 1) mma_bf16(e1[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
+                        else         mma_bf16(e0[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
+                    }
                 }
             } else {
 #pragma unroll
                 for (int kp = 0; kp < C::KS / 2; ++kp) {
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4(kpg + swz<C::TT>(t, 2 * kp + (lane >> 4)), r0, r1, r2, r3);
-                    mma_f16(e0, e4m3x2_to_f16x2(r0), e4m3x2_to_f16x2(r1),
-                            e4m3x2_to_f16x2(r0 >> 16), e4m3x2_to_f16x2(r1 >> 16),
-                            qf[2 * kp][0], qf[2 * kp][1]);
-                    mma_f16(e1, e4m3x2_to_f16x2(r2), e4m3x2_to_f16x2(r3),
-                            e4m3x2_to_f16x2(r2 >> 16), e4m3x2_to_f16x2(r3 >> 16),
-                            qf[2 * kp + 1][0], qf[2 * kp + 1][1]);
+                    const uint32_t k00 = e4m3x2_to_f16x2(r0), k01 = e4m3x2_to_f16x2(r1);
+                    const uint32_t k02 = e4m3x2_to_f16x2(r0 >> 16), k03 = e4m3x2_to_f16x2(r1 >> 16);
+                    const uint32_t k10 = e4m3x2_to_f16x2(r2), k11 = e4m3x2_to_f16x2(r3);
+                    const uint32_t k12 = e4m3x2_to_f16x2(r2 >> 16), k13 = e4m3x2_to_f16x2(r3 >> 16);
+#pragma unroll
+                    for (int qi = 0; qi < QT; ++qi) {
+                        mma_f16(e0[qi], k00, k01, k02, k03, qf[2 * kp][qi][0], qf[2 * kp][qi][1]);
+                        mma_f16(e1[qi], k10, k11, k12, k13, qf[2 * kp + 1][qi][0], qf[2 * kp + 1][qi][1]);
+                    }
                 }
             }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) sacc[mt][e] = e0[e] + e1[e];
+            for (int qi = 0; qi < QT; ++qi)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[mt][qi][e] = e0[qi][e] + e1[qi][e];
         }
 
         // ---- online softmax (log2 domain), heads 2c and 2c+1 of this lane ----
         const float sc_page = FP8 ? qscale * ks : qscale;
-        float mx0 = -INFINITY, mx1 = -INFINITY;
+        float mx0[QT], mx1[QT];
+        bool need = false;
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
+        for (int qi = 0; qi < QT; ++qi) {
+            mx0[qi] = mx1[qi] = -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tok = mt * 16 + g + ((e & 2) ? 8 : 0);
-                const float v = sacc[mt][e] * sc_page;
-                sacc[mt][e] = (tok < ntok) ? v : -INFINITY;
+            for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = mt * 16 + g + ((e & 2) ? 8 : 0);
+                    bool valid = tok < ntok;
+                    if constexpr (QT > 1) valid = valid && (tpos0 + tok <= seg_vis + qi);
+                    const float v = sacc[mt][qi][e] * sc_page;
+                    sacc[mt][qi][e] = valid ? v : -INFINITY;
+                }
+                mx0[qi] = fmaxf(mx0[qi], fmaxf(sacc[mt][qi][0], sacc[mt][qi][2]));
+                mx1[qi] = fmaxf(mx1[qi], fmaxf(sacc[mt][qi][1], sacc[mt][qi][3]));
             }
-            mx0 = fmaxf(mx0, fmaxf(sacc[mt][0], sacc[mt][2]));
-            mx1 = fmaxf(mx1, fmaxf(sacc[mt][1], sacc[mt][3]));
+            // raise the running max (and rescale O and l) only when some lane's score
+            // exceeds it by more than the slack; P <= 2^kRescaleSlack otherwise
+            need = need || (mx0[qi] > m0[qi] + kRescaleSlack) || (mx1[qi] > m1[qi] + kRescaleSlack);
         }
-        // raise the running max (and rescale O and l) only when some lane's score
-        // exceeds it by more than the slack; P <= 2^kRescaleSlack otherwise
-        const bool need = (mx0 > m0 + kRescaleSlack) || (mx1 > m1 + kRescaleSlack);
         if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-            for (int o2 = 4; o2 < 32; o2 <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o2));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            l0 *= al0;
-            l1 *= al1;
+            for (int qi = 0; qi < QT; ++qi) {
 #pragma unroll
-            for (int dt = 0; dt < C::DT; ++dt) {
-                o[dt][0] *= al0;
-                o[dt][2] *= al0;
-                o[dt][1] *= al1;
-                o[dt][3] *= al1;
+                for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                    mx0[qi] = fmaxf(mx0[qi], __shfl_xor_sync(0xffffffffu, mx0[qi], o2));
+                    mx1[qi] = fmaxf(mx1[qi], __shfl_xor_sync(0xffffffffu, mx1[qi], o2));
+                }
+                const float mn0 = fmaxf(m0[qi], mx0[qi]), mn1 = fmaxf(m1[qi], mx1[qi]);
+                float al0 = exp2f(m0[qi] - mn0), al1 = exp2f(m1[qi] - mn1);
+                if constexpr (QT > 1) {
+                    // a query that has seen no token yet keeps -inf without a NaN
+                    if (mn0 == -INFINITY) al0 = 1.f;
+                    if (mn1 == -INFINITY) al1 = 1.f;
+                }
+                m0[qi] = mn0;
+                m1[qi] = mn1;
+                l0[qi] *= al0;
+                l1[qi] *= al1;
+#pragma unroll
+                for (int dt = 0; dt < C::DT; ++dt) {
+                    o[dt][qi][0] *= al0;
+                    o[dt][qi][2] *= al0;
+                    o[dt][qi][1] *= al1;
+                    o[dt][qi][3] *= al1;
+                }
             }
         }
-        float ps0 = 0.f, ps1 = 0.f;
-        uint32_t pb[C::MT][2];
+        uint32_t pb[C::MT][QT][2];
 #pragma unroll
-        for (int mt = 0; mt < C::MT; ++mt) {
-            const float p0 = exp2f(sacc[mt][0] - m0), p1 = exp2f(sacc[mt][1] - m1);
-            const float p2 = exp2f(sacc[mt][2] - m0), p3 = exp2f(sacc[mt][3] - m1);
-            ps0 += p0 + p2;
-            ps1 += p1 + p3;
-            if (!FP8) {
-                pb[mt][0] = movmatrix_trans(pack_bf16x2(p0, p1));
-                pb[mt][1] = movmatrix_trans(pack_bf16x2(p2, p3));
-            } else {
-                pb[mt][0] = movmatrix_trans(pack_f16x2(p0, p1));
-                pb[mt][1] = movmatrix_trans(pack_f16x2(p2, p3));
+        for (int qi = 0; qi < QT; ++qi) {
+            float r0m = m0[qi], r1m = m1[qi];
+            if constexpr (QT > 1) {
+                if (r0m == -INFINITY) r0m = 0.f;   // every score of that head is -inf here
+                if (r1m == -INFINITY) r1m = 0.f;
             }
+            float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+            for (int mt = 0; mt < C::MT; ++mt) {
+                const float p0 = exp2f(sacc[mt][qi][0] - r0m), p1 = exp2f(sacc[mt][qi][1] - r1m);
+                const float p2 = exp2f(sacc[mt][qi][2] - r0m), p3 = exp2f(sacc[mt][qi][3] - r1m);
+                ps0 += p0 + p2;
+                ps1 += p1 + p3;
+                if (!FP8) {
+                    pb[mt][qi][0] = movmatrix_trans(pack_bf16x2(p0, p1));
+                    pb[mt][qi][1] = movmatrix_trans(pack_bf16x2(p2, p3));
+                } else {
+                    pb[mt][qi][0] = movmatrix_trans(pack_f16x2(p0, p1));
+                    pb[mt][qi][1] = movmatrix_trans(pack_f16x2(p2, p3));
+                }
+            }
+            l0[qi] += ps0;
+            l1[qi] += ps1;
         }
-        l0 += ps0;
-        l1 += ps1;
 
         // ---- O^T += V^T P^T ----
         if (!FP8) {
@@ -554,14 +645,18 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
                     const int t = mt * 16 + (lane & 7) + ((lane >> 4) << 3);
                     uint32_t a0, a1, a2, a3;
                     ldsm_x4_trans(vpg + swz<C::TT>(t, 2 * dt + ((lane >> 3) & 1)), a0, a1, a2, a3);
-                    mma_bf16(o[dt], a0, a1, a2, a3, pb[mt][0], pb[mt][1]);
+#pragma unroll
+                    for (int qi = 0; qi < QT; ++qi)
+                        mma_bf16(o[dt][qi], a0, a1, a2, a3, pb[mt][qi][0], pb[mt][qi][1]);
                 }
             }
         } else {
 #pragma unroll
             for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) ot[dt][e] = 0.f;
+                for (int qi = 0; qi < QT; ++qi)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) ot[dt][qi][e] = 0.f;
 #pragma unroll
             for (int dp = 0; dp < C::DT / 2; ++dp) {
 #pragma unroll
@@ -573,78 +668,92 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
                     for (int half = 0; half < 2; ++half) {
                         const uint32_t x = movmatrix_trans(half ? r2 : r0);   // tokens 0-7
                         const uint32_t y = movmatrix_trans(half ? r3 : r1);   // tokens 8-15
-                        mma_f16(ot[2 * dp + half],
-                                e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0020)),
-                                e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0031)),
-                                e4m3x2_to_f16x2(__byte_perm(y, 0u, 0x0020)),
-                                e4m3x2_to_f16x2(__byte_perm(y, 0u, 0x0031)),
-                                pb[mt][0], pb[mt][1]);
+                        const uint32_t v0 = e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0020));
+                        const uint32_t v1 = e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0031));
+                        const uint32_t v2 = e4m3x2_to_f16x2(__byte_perm(y, 0u, 0x0020));
+                        const uint32_t v3 = e4m3x2_to_f16x2(__byte_perm(y, 0u, 0x0031));
+#pragma unroll
+                        for (int qi = 0; qi < QT; ++qi)
+                            mma_f16(ot[2 * dp + half][qi], v0, v1, v2, v3, pb[mt][qi][0],
+                                    pb[mt][qi][1]);
                     }
                 }
             }
 #pragma unroll
             for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) o[dt][e] = fmaf(vs, ot[dt][e], o[dt][e]);
+                for (int qi = 0; qi < QT; ++qi)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[dt][qi][e] = fmaf(vs, ot[dt][qi][e], o[dt][qi][e]);
         }
 
         // ---- segment end ----
         if (last || i == total - 1) {
-            float L0 = l0, L1 = l1;
-#pragma unroll
-            for (int o2 = 4; o2 < 32; o2 <<= 1) {
-                L0 += __shfl_xor_sync(0xffffffffu, L0, o2);
-                L1 += __shfl_xor_sync(0xffffffffu, L1, o2);
-            }
             const int g0 = 2 * c, g1 = 2 * c + 1;
-            if (seg_full && last) {
-                const float inv0 = 1.f / L0, inv1 = 1.f / L1;
-                uint16_t* ob = a.out + ((int64_t)seg_r * a.Hq + (int64_t)seg_h * a.G) * D;
+            const bool complete = seg_full && last;
+            const int64_t u = (int64_t)seg_r * a.Hkv + seg_h;
+            const int64_t slot = u + gw;
 #pragma unroll
-                for (int dt = 0; dt < C::DT; ++dt) {
-                    if (!FP8) {
-                        const int d = dt * 16 + g;
-                        if (g0 < a.G) {
-                            ob[g0 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][0] * inv0));
-                            ob[g0 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][2] * inv0));
+            for (int qi = 0; qi < QT; ++qi) {
+                if (qi >= seg_qlen) break;
+                float L0 = l0[qi], L1 = l1[qi];
+#pragma unroll
+                for (int o2 = 4; o2 < 32; o2 <<= 1) {
+                    L0 += __shfl_xor_sync(0xffffffffu, L0, o2);
+                    L1 += __shfl_xor_sync(0xffffffffu, L1, o2);
+                }
+                if (complete) {
+                    const float inv0 = L0 > 0.f ? 1.f / L0 : 0.f;
+                    const float inv1 = L1 > 0.f ? 1.f / L1 : 0.f;
+                    uint16_t* ob =
+                        a.out + ((int64_t)(seg_qb + qi) * a.Hq + (int64_t)seg_h * a.G) * D;
+#pragma unroll
+                    for (int dt = 0; dt < C::DT; ++dt) {
+                        if (!FP8) {
+                            const int d = dt * 16 + g;
+                            if (g0 < a.G) {
+                                ob[g0 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][0] * inv0));
+                                ob[g0 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][2] * inv0));
+                            }
+                            if (g1 < a.G) {
+                                ob[g1 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][1] * inv1));
+                                ob[g1 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][3] * inv1));
+                            }
+                        } else {
+                            const int d = dt * 16 + 2 * g;
+                            if (g0 < a.G)
+                                *reinterpret_cast<uint32_t*>(ob + g0 * D + d) =
+                                    pack_bf16x2(o[dt][qi][0] * inv0, o[dt][qi][2] * inv0);
+                            if (g1 < a.G)
+                                *reinterpret_cast<uint32_t*>(ob + g1 * D + d) =
+                                    pack_bf16x2(o[dt][qi][1] * inv1, o[dt][qi][3] * inv1);
                         }
-                        if (g1 < a.G) {
-                            ob[g1 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][1] * inv1));
-                            ob[g1 * D + d + 8] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][3] * inv1));
+                    }
+                } else {
+                    float* ps = a.partials + slot * (QT * kGroupPad * (D + 4)) +
+                                qi * (kGroupPad * (D + 4));
+#pragma unroll
+                    for (int dt = 0; dt < C::DT; ++dt) {
+                        if (!FP8) {
+                            const int d = dt * 16 + g;
+                            ps[g0 * (D + 4) + d] = o[dt][qi][0];
+                            ps[g0 * (D + 4) + d + 8] = o[dt][qi][2];
+                            ps[g1 * (D + 4) + d] = o[dt][qi][1];
+                            ps[g1 * (D + 4) + d + 8] = o[dt][qi][3];
+                        } else {
+                            const int d = dt * 16 + 2 * g;
+                            *reinterpret_cast<float2*>(ps + g0 * (D + 4) + d) = make_float2(o[dt][qi][0], o[dt][qi][2]);
+                            *reinterpret_cast<float2*>(ps + g1 * (D + 4) + d) = make_float2(o[dt][qi][1], o[dt][qi][3]);
                         }
-                    } else {
-                        const int d = dt * 16 + 2 * g;
-                        if (g0 < a.G)
-                            *reinterpret_cast<uint32_t*>(ob + g0 * D + d) =
-                                pack_bf16x2(o[dt][0] * inv0, o[dt][2] * inv0);
-                        if (g1 < a.G)
-                            *reinterpret_cast<uint32_t*>(ob + g1 * D + d) =
-                                pack_bf16x2(o[dt][1] * inv1, o[dt][3] * inv1);
+                    }
+                    if (g == 0) {
+                        *reinterpret_cast<float2*>(ps + g0 * (D + 4) + D) = make_float2(m0[qi], L0);
+                        *reinterpret_cast<float2*>(ps + g1 * (D + 4) + D) = make_float2(m1[qi], L1);
                     }
                 }
-            } else {
-                const int64_t slot = (int64_t)seg_r * a.Hkv + seg_h + gw;
-                float* ps = a.partials + slot * (kGroupPad * (D + 4));
-#pragma unroll
-                for (int dt = 0; dt < C::DT; ++dt) {
-                    if (!FP8) {
-                        const int d = dt * 16 + g;
-                        ps[g0 * (D + 4) + d] = o[dt][0];
-                        ps[g0 * (D + 4) + d + 8] = o[dt][2];
-                        ps[g1 * (D + 4) + d] = o[dt][1];
-                        ps[g1 * (D + 4) + d + 8] = o[dt][3];
-                    } else {
-                        const int d = dt * 16 + 2 * g;
-                        *reinterpret_cast<float2*>(ps + g0 * (D + 4) + d) = make_float2(o[dt][0], o[dt][2]);
-                        *reinterpret_cast<float2*>(ps + g1 * (D + 4) + d) = make_float2(o[dt][1], o[dt][3]);
-                    }
-                }
-                if (g == 0) {
-                    *reinterpret_cast<float2*>(ps + g0 * (D + 4) + D) = make_float2(m0, L0);
-                    *reinterpret_cast<float2*>(ps + g1 * (D + 4) + D) = make_float2(m1, L1);
-                }
+            }
+            if (!complete) {
                 // arrive on the unit's counter; the last of its warps merges
-                const int64_t u = (int64_t)seg_r * a.Hkv + seg_h;
                 const int np_u = (s_prefix[seg_r + 1] - s_prefix[seg_r]) / a.Hkv;
                 const int64_t U = (int64_t)s_prefix[seg_r] + (int64_t)seg_h * np_u;
                 const int64_t E = U + np_u - 1;
@@ -661,7 +770,8 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
                 }
                 if (arrived == (uint32_t)(wl - wf + 1)) {
                     __threadfence();
-                    merge_unit<D>(a.partials, a.out, a.Hq, a.G, u, wf, wl, seg_r, seg_h);
+                    merge_unit<D, QT>(a.partials, a.out, a.Hq, a.G, u, wf, wl, seg_qb, seg_qlen,
+                                      seg_h);
                     if (lane == 0) atomicExch(a.counters + u, (unsigned long long)a.epoch << 32);
                 }
             }
@@ -677,15 +787,16 @@ __global__ void __launch_bounds__(FP8 ? 256 : 384, 1)
 }
 
 // Log-sum-exp merge of the units split over more than kInKernelMerge warps: one
-// CTA per unit, one warp per query head of the group, each lane D/32 columns.  The
-// loop over partials keeps several independent loads in flight.  Runs after the
-// decode kernel (programmatic dependent launch: it waits for the decode grid to
-// complete before reading).
-template <int D>
+// CTA per unit, one warp per query head of the group, each lane D/32 columns, for
+// each of the request's query positions.  The loop over partials keeps several
+// independent loads in flight.  Runs after the decode kernel (programmatic
+// dependent launch: it waits for the decode grid to complete before reading).
+template <int D, int QT>
 __global__ void __launch_bounds__(kGroupPad * 32)
     pkv_decode_merge_kernel(const DecodeArgs a) {
     constexpr int PER = D / 32;
-    constexpr int SLOT = kGroupPad * (D + 4);
+    constexpr int QS = kGroupPad * (D + 4);
+    constexpr int SLOT = QT * QS;
     pdl_wait();
     const int u = blockIdx.x;
     const int gg = threadIdx.x >> 5;
@@ -703,42 +814,50 @@ __global__ void __launch_bounds__(kGroupPad * 32)
     const int wl = (int)(((E + 1) * W - 1) / P);
     const int n = wl - wf + 1;
     if (n <= kInKernelMerge) return;   // merged inside the decode kernel
-    const float* base = a.partials + ((int64_t)u + wf) * SLOT + gg * (D + 4);
-    float M = -INFINITY;
-    for (int k = lane; k < n; k += 32) M = fmaxf(M, base[(int64_t)k * SLOT + D]);
+    int qb, qlen;
+    uint32_t errbits = 0;
+    query_rows<QT>(a, r, qb, qlen, errbits);
+    for (int qi = 0; qi < qlen; ++qi) {
+        const float* base = a.partials + ((int64_t)u + wf) * SLOT + qi * QS + gg * (D + 4);
+        float M = -INFINITY;
+        for (int k = lane; k < n; k += 32) M = fmaxf(M, base[(int64_t)k * SLOT + D]);
 #pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-    float L = 0.f;
-    for (int k = lane; k < n; k += 32) {
-        const float2 ml = *reinterpret_cast<const float2*>(base + (int64_t)k * SLOT + D);
-        L = fmaf(exp2f(ml.x - M), ml.y, L);
-    }
+        for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+        float acc[PER];
 #pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
-    float acc[PER];
+        for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+        float L = 0.f;
+        if (M != -INFINITY) {   // else: the query saw no token: zero row
+            for (int k = lane; k < n; k += 32) {
+                const float2 ml = *reinterpret_cast<const float2*>(base + (int64_t)k * SLOT + D);
+                L = fmaf(exp2f(ml.x - M), ml.y, L);
+            }
 #pragma unroll
-    for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+            for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
 #pragma unroll 8
-    for (int k = 0; k < n; ++k) {
-        const float* ps = base + (int64_t)k * SLOT;
-        const float wt = exp2f(ps[D] - M);
-        if constexpr (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(ps + lane * 4);
-            acc[0] = fmaf(wt, v.x, acc[0]);
-            acc[1] = fmaf(wt, v.y, acc[1]);
-            acc[2] = fmaf(wt, v.z, acc[2]);
-            acc[3] = fmaf(wt, v.w, acc[3]);
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(ps + lane * 2);
-            acc[0] = fmaf(wt, v.x, acc[0]);
-            acc[1] = fmaf(wt, v.y, acc[1]);
+            for (int k = 0; k < n; ++k) {
+                const float* ps = base + (int64_t)k * SLOT;
+                const float wt = exp2f(ps[D] - M);
+                if constexpr (PER == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(ps + lane * 4);
+                    acc[0] = fmaf(wt, v.x, acc[0]);
+                    acc[1] = fmaf(wt, v.y, acc[1]);
+                    acc[2] = fmaf(wt, v.z, acc[2]);
+                    acc[3] = fmaf(wt, v.w, acc[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(ps + lane * 2);
+                    acc[0] = fmaf(wt, v.x, acc[0]);
+                    acc[1] = fmaf(wt, v.y, acc[1]);
+                }
+            }
         }
-    }
-    const float inv = 1.f / L;
-    uint16_t* ob = a.out + ((int64_t)r * a.Hq + (int64_t)h * a.G + gg) * D;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        uint16_t* ob = a.out + ((int64_t)(qb + qi) * a.Hq + (int64_t)h * a.G + gg) * D;
 #pragma unroll
-    for (int k = 0; k < PER; k += 2)
-        *reinterpret_cast<uint32_t*>(ob + lane * PER + k) = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+        for (int k = 0; k < PER; k += 2)
+            *reinterpret_cast<uint32_t*>(ob + lane * PER + k) =
+                pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+    }
 }
 
 // ------------------------------------------------------------------ host side
@@ -776,9 +895,18 @@ int env_int(const char* name, int dflt) {
 
 }  // namespace
 
-// The CTA shape for a (dtype, D, BS): `warps` independent pipelines of `stages`
-// pages each, sized to keep about 192 KB of pages in flight per SM.
-DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch) {
+// Compile-time query positions per request for a call with at most `max_q_len`
+// queries per request (0 if unsupported).
+int query_tile(int fp8, int max_q_len) {
+    if (max_q_len <= 1) return 1;
+    if (max_q_len <= 2) return 2;
+    if (max_q_len <= 4 && !fp8) return 4;
+    return 0;
+}
+
+// The CTA shape for a (dtype, D, BS, QT): `warps` independent pipelines of
+// `stages` tiles each.
+DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch, int qt) {
     DecodePlan p;
     const int elt = fp8 ? 1 : 2;
     const int tile_tokens = fp8 ? block_size : 16;
@@ -787,7 +915,7 @@ DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int b
     // instruction chain of a warp, not the bytes in flight, limits the rate, so the
     // CTA runs several warps per SM sub-partition.  Measured on GB300: 6 warps for
     // bf16 pages, 8 for FP8 pages (whose tiles carry twice the tokens).
-    const int max_warps = fp8 ? 8 : 12;            // register budget of the launch bounds
+    const int max_warps = (fp8 || qt > 1) ? 8 : 12;   // register budget of the launch bounds
     p.warps = env_int("PKV_DECODE_WARPS", fp8 ? 8 : 6);
     if (p.warps < 1) p.warps = 1;
     if (p.warps > max_warps) p.warps = max_warps;
@@ -806,10 +934,10 @@ DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int b
     return p;
 }
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, bool FP8, int QT>
 static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const CUtensorMap& tk,
                             const CUtensorMap& tv, const DecodeArgs& args, cudaStream_t st) {
-    auto kern = pkv_decode_kernel<D, BS, FP8>;
+    auto kern = pkv_decode_kernel<D, BS, FP8, QT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          plan.smem_bytes);
     if (e != cudaSuccess) return e;
@@ -818,8 +946,20 @@ static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const
                    args);
     if (e != cudaSuccess) return e;
     // the wide-split merge, a programmatic dependent of the decode grid
-    return launch_pdl(pkv_decode_merge_kernel<D>, dim3((unsigned)(L.N * L.Hkv)),
+    return launch_pdl(pkv_decode_merge_kernel<D, QT>, dim3((unsigned)(L.N * L.Hkv)),
                       dim3(kGroupPad * 32), 0, st, args);
+}
+
+template <int D, int BS, bool FP8>
+static cudaError_t launch_q(int qt, const DecodeLaunch& L, const DecodePlan& plan,
+                            const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& args,
+                            cudaStream_t st) {
+    if (qt == 1) return launch_t<D, BS, FP8, 1>(L, plan, tk, tv, args, st);
+    if (qt == 2) return launch_t<D, BS, FP8, 2>(L, plan, tk, tv, args, st);
+    if constexpr (!FP8) {
+        if (qt == 4) return launch_t<D, BS, FP8, 4>(L, plan, tk, tv, args, st);
+    }
+    return cudaErrorInvalidValue;
 }
 
 static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, int BS,
@@ -840,8 +980,10 @@ static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, i
 
 // Returns a pkv_status.  Arguments are validated by the caller.
 int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
-    const DecodePlan plan = decode_plan(L.fp8, L.D, L.BS, L.num_sms, L.N);
-    const WorkspaceLayout WL = workspace_layout(L.N, L.Hkv, L.D, plan.total_warps);
+    const int qt = query_tile(L.fp8, L.max_q_len);
+    if (qt == 0) return PKV_ERR_UNSUPPORTED;
+    const DecodePlan plan = decode_plan(L.fp8, L.D, L.BS, L.num_sms, L.N, qt);
+    const WorkspaceLayout WL = workspace_layout(L.N, L.Hkv, L.D, plan.total_warps, qt);
     const int64_t rows = (int64_t)L.NB * L.Hkv * L.BS;
     alignas(64) CUtensorMap tk, tv;
     if (!encode_cache_map(&tk, L.k_cache, L.fp8, L.D, L.BS, rows) ||
@@ -850,6 +992,7 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     DecodeArgs a;
     uint8_t* ws = static_cast<uint8_t*>(L.workspace);
     a.q = static_cast<const uint16_t*>(L.q);
+    a.q_offsets = L.q_offsets;
     a.out = static_cast<uint16_t*>(L.out);
     a.block_table = L.block_table;
     a.seq_lens = L.seq_lens;
@@ -871,23 +1014,25 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     a.epoch = next_epoch();
     cudaError_t e = cudaErrorInvalidValue;
     if (!L.fp8) {
-        if (L.D == 128 && L.BS == 16) e = launch_t<128, 16, false>(L, plan, tk, tv, a, st);
-        else if (L.D == 128 && L.BS == 32) e = launch_t<128, 32, false>(L, plan, tk, tv, a, st);
-        else if (L.D == 64 && L.BS == 16) e = launch_t<64, 16, false>(L, plan, tk, tv, a, st);
-        else if (L.D == 64 && L.BS == 32) e = launch_t<64, 32, false>(L, plan, tk, tv, a, st);
+        if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, false>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, false>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 64 && L.BS == 16) e = launch_q<64, 16, false>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 64 && L.BS == 32) e = launch_q<64, 32, false>(qt, L, plan, tk, tv, a, st);
         else return PKV_ERR_UNSUPPORTED;
     } else {
-        if (L.D == 128 && L.BS == 16) e = launch_t<128, 16, true>(L, plan, tk, tv, a, st);
-        else if (L.D == 128 && L.BS == 32) e = launch_t<128, 32, true>(L, plan, tk, tv, a, st);
+        if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, true>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, true>(qt, L, plan, tk, tv, a, st);
         else return PKV_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 size_t decode_workspace_bytes(int batch, int num_kv_heads, int head_dim, int block_size, int fp8,
-                              int num_sms) {
-    const DecodePlan plan = decode_plan(fp8, head_dim, block_size, num_sms, batch);
-    return (size_t)workspace_layout(batch, num_kv_heads, head_dim, plan.total_warps).total;
+                              int num_sms, int max_q_len) {
+    const int qt = query_tile(fp8, max_q_len);
+    if (qt == 0) return 0;
+    const DecodePlan plan = decode_plan(fp8, head_dim, block_size, num_sms, batch, qt);
+    return (size_t)workspace_layout(batch, num_kv_heads, head_dim, plan.total_warps, qt).total;
 }
 
 }  // namespace pkv

@@ -37,25 +37,28 @@ __host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + 
 struct WorkspaceLayout {
     int64_t counter_off;   // u64 [N * Hkv] arrival counters of split units (epoch << 32 | count)
     int64_t prefix_off;    // int32 [N + 1] page prefix over requests (times Hkv)
-    int64_t partial_off;   // fp32 [slots][kGroupPad][D + 4]: o[D], m, l, pad
+    int64_t partial_off;   // fp32 [slots][QT][kGroupPad][D + 4]: o[D], m, l, pad
     int64_t slots;         // N * Hkv + W
     int64_t total;
 };
 
 __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int num_kv_heads,
-                                                            int head_dim, int total_warps) {
+                                                            int head_dim, int total_warps,
+                                                            int qt) {
     WorkspaceLayout L;
     L.counter_off = kWorkspaceHeader;
     L.prefix_off = align_up(L.counter_off + 8 * (int64_t)batch * num_kv_heads, 256);
     L.partial_off = align_up(L.prefix_off + 4 * (int64_t)(batch + 1), 256);
     L.slots = (int64_t)batch * num_kv_heads + total_warps;
-    L.total = L.partial_off + L.slots * kGroupPad * (head_dim + 4) * 4;
+    L.total = L.partial_off + L.slots * qt * kGroupPad * (head_dim + 4) * 4;
     return L;
 }
 
 // ---------------------------------------------------------------- host launchers
 struct DecodeLaunch {
     const void* q;
+    const int32_t* q_offsets;   // null: one query per request
+    int max_q_len;
     const void* k_cache;
     const void* v_cache;
     const float* k_scale;
@@ -69,10 +72,11 @@ struct DecodeLaunch {
     int num_sms;
 };
 
-DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch);
+int query_tile(int fp8, int max_q_len);
+DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch, int qt);
 int decode_launch(const DecodeLaunch& L, cudaStream_t st);
 size_t decode_workspace_bytes(int batch, int num_kv_heads, int head_dim, int block_size, int fp8,
-                              int num_sms);
+                              int num_sms, int max_q_len);
 cudaError_t slot_mapping_launch(const int32_t* block_table, int MB, const int32_t* req_idx,
                                 const int32_t* positions, int T, int BS, int64_t* out,
                                 cudaStream_t st);

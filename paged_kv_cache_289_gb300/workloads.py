@@ -51,6 +51,7 @@ class Workload:
     tokens: np.ndarray            # int32 [sum seq_lens] (CSR by request)
     token_offsets: np.ndarray     # int64 [N + 1]
     hash_block: int = 16
+    q_len: int = 1                # new query tokens per request (speculative verify: > 1)
     notes: dict = field(default_factory=dict)
 
     @property
@@ -76,6 +77,18 @@ class Workload:
     def new_token_positions(self) -> np.ndarray:
         """Decode step: each request's newest token sits at position seq_len - 1."""
         return (self.seq_lens.astype(np.int64) - 1).astype(np.int32)
+
+    def q_offsets(self) -> np.ndarray:
+        """Query rows of each request: q_len rows per request, request-major."""
+        return (np.arange(self.N + 1, dtype=np.int64) * self.q_len).astype(np.int32)
+
+    def new_token_rows(self):
+        """(req_idx, positions) of the step's new tokens: the last q_len tokens of
+        every request (positions seq_len - q_len .. seq_len - 1)."""
+        req = np.repeat(np.arange(self.N, dtype=np.int32), self.q_len)
+        pos = (np.repeat(self.seq_lens.astype(np.int64), self.q_len) - self.q_len +
+               np.tile(np.arange(self.q_len), self.N)).astype(np.int32)
+        return req, pos
 
     def kv_read_bytes(self) -> int:
         """Logical K+V bytes one decode step reads: sum_r seq_len_r * Hkv * D * 2 * elt."""
@@ -122,7 +135,9 @@ def make(cfg: int, seed: int | None = None, small: bool = False,
          batch: int | None = None) -> Workload:
     """Workload `cfg` (1..5).  `small=True` keeps the head/dim/block shape but
     shrinks batch and lengths so the fp64 oracle finishes in seconds.  `batch`
-    overrides the number of requests of workloads 2, 4 and 5 (same length law)."""
+    overrides the number of requests of workloads 2, 4, 5 and 6 (same length law).
+    Workload 6 is workload 2 with four new query tokens per request (speculative
+    verify)."""
     seed = cfg if seed is None else seed
     rng = np.random.default_rng(seed)
     if cfg == 1:
@@ -208,17 +223,27 @@ def make(cfg: int, seed: int | None = None, small: bool = False,
         toks, offs = _tokens(rng, seq, VOCAB)
         return Workload("fp8_at_scale" + ("_small" if small else ""), 5, seed, N, Hq, Hkv, D, BS,
                         NB, True, 1.0 / math.sqrt(D), seq, bt, toks, offs)
+    if cfg == 6:
+        # speculative verify on the 70B-shaped layer: 4 new tokens per request
+        # (3 drafted + 1), all checked in one attention pass
+        wl = make(2, seed=seed, small=small, batch=batch)
+        wl.name = "spec_verify_q4" + ("_small" if small else "")
+        wl.cfg = 6
+        wl.q_len = 4
+        return wl
     raise ValueError(f"unknown workload {cfg}")
 
 
-def custom(N, Hq, Hkv, D, BS, seq_lens, fp8=False, seed=0, slack=1.1, scale=None, name="custom"):
+def custom(N, Hq, Hkv, D, BS, seq_lens, fp8=False, seed=0, slack=1.1, scale=None, name="custom",
+           q_len=1):
     """A workload with explicit lengths (edge cases: empty, ragged, one-token requests)."""
     rng = np.random.default_rng(seed)
     seq = np.asarray(seq_lens, dtype=np.int32)
     bt, NB = _assign_blocks(rng, seq, BS, slack=slack)
     toks, offs = _tokens(rng, seq, VOCAB)
     sc = 1.0 / math.sqrt(D) if scale is None else scale
-    return Workload(name, 0, seed, N, Hq, Hkv, D, BS, NB, fp8, sc, seq, bt, toks, offs)
+    return Workload(name, 0, seed, N, Hq, Hkv, D, BS, NB, fp8, sc, seq, bt, toks, offs,
+                    q_len=q_len)
 
 
 # ----------------------------------------------------------------------------
@@ -278,7 +303,7 @@ def host_data(wl: Workload, seed_offset: int = 1000) -> dict:
     Both: `q` uint16 [N, Hq, D]; `k_new`, `v_new` uint16 [N, Hkv, D] (the decode
     step's new token of each request, written at position seq_len - 1)."""
     rng = np.random.default_rng(wl.seed + seed_offset)
-    d = {"q": _randn_bf16(rng, (wl.N, wl.Hq, wl.D))}
+    d = {"q": _randn_bf16(rng, (wl.N * wl.q_len, wl.Hq, wl.D))}
     if not wl.fp8:
         d["k_cache"] = _randn_bf16(rng, (wl.NB, wl.Hkv, wl.BS, wl.D))
         d["v_cache"] = _randn_bf16(rng, (wl.NB, wl.Hkv, wl.BS, wl.D))
@@ -287,8 +312,8 @@ def host_data(wl: Workload, seed_offset: int = 1000) -> dict:
         d["k_rows"] = _randn_bf16(rng, (T, wl.Hkv, wl.D))
         d["v_rows"] = _randn_bf16(rng, (T, wl.Hkv, wl.D))
         d["k_scale"], d["v_scale"] = fp8_scales_from_rows(wl, d["k_rows"], d["v_rows"])
-    d["k_new"] = _randn_bf16(rng, (wl.N, wl.Hkv, wl.D))
-    d["v_new"] = _randn_bf16(rng, (wl.N, wl.Hkv, wl.D))
+    d["k_new"] = _randn_bf16(rng, (wl.N * wl.q_len, wl.Hkv, wl.D))
+    d["v_new"] = _randn_bf16(rng, (wl.N * wl.q_len, wl.Hkv, wl.D))
     return d
 
 
@@ -302,7 +327,7 @@ def device_data(wl: Workload, device, seed_offset: int = 2000) -> dict:
     g = torch.Generator(device=device)
     g.manual_seed(wl.seed + seed_offset)
     bf = torch.bfloat16
-    d = {"q": torch.randn((wl.N, wl.Hq, wl.D), generator=g, device=device, dtype=bf)}
+    d = {"q": torch.randn((wl.N * wl.q_len, wl.Hq, wl.D), generator=g, device=device, dtype=bf)}
     if not wl.fp8:
         d["k_cache"] = torch.randn((wl.NB, wl.Hkv, wl.BS, wl.D), generator=g, device=device,
                                    dtype=bf)
@@ -336,6 +361,6 @@ def device_data(wl: Workload, device, seed_offset: int = 2000) -> dict:
             full = torch.ones((wl.NB, wl.Hkv), dtype=torch.float32, device=device)
             full[phys_t] = sc
             d[skey] = full
-    d["k_new"] = torch.randn((wl.N, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
-    d["v_new"] = torch.randn((wl.N, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
+    d["k_new"] = torch.randn((wl.N * wl.q_len, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
+    d["v_new"] = torch.randn((wl.N * wl.q_len, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
     return d

@@ -82,13 +82,18 @@ class HostCase:
             self.vc = self.d["v_cache"].copy()
 
     def oracle_step(self):
-        """Oracle decode step: write each request's new token at seq_len-1, attend."""
+        """Oracle step: write each request's new tokens (its last q_len positions), then
+        attend (single-query decode, or causal multi-query for q_len > 1)."""
         wl = self.wl
-        req = np.arange(wl.N, dtype=np.int32)
-        slots = oracle.slot_mapping(wl.block_table, req, wl.new_token_positions(), wl.BS)
+        req, pos = wl.new_token_rows()
+        slots = oracle.slot_mapping(wl.block_table, req, pos, wl.BS)
         ks = self.d.get("k_scale")
         vs = self.d.get("v_scale")
         oracle.kv_cache_write(self.d["k_new"], self.d["v_new"], slots, self.kc, self.vc, ks, vs)
-        out = oracle.decode_attn(self.d["q"], self.kc, self.vc, wl.block_table, wl.seq_lens,
-                                 wl.scale, ks, vs)
+        if wl.q_len == 1:
+            out = oracle.decode_attn(self.d["q"], self.kc, self.vc, wl.block_table, wl.seq_lens,
+                                     wl.scale, ks, vs)
+        else:
+            out = oracle.multiquery_attn(self.d["q"], wl.q_offsets(), self.kc, self.vc,
+                                         wl.block_table, wl.seq_lens, wl.scale, ks, vs)
         return slots, out

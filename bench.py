@@ -49,6 +49,9 @@ def parse():
     p.add_argument("--seed", type=int, default=None)
     p.add_argument("--batch", type=int, default=None,
                    help="fewer requests of the same shapes (profiling captures only)")
+    p.add_argument("--op", choices=["step", "copy_blocks"], default="step",
+                   help="copy_blocks: time the copy-on-write block copy alone")
+    p.add_argument("--pairs", type=int, default=4096, help="block pairs per copy_blocks launch")
     return p.parse_args()
 
 
@@ -178,8 +181,9 @@ def aggregate_sum(value, world, device=None):
 
 def workload_config(wl):
     return {"workload": wl.name, "batch": wl.N, "num_q_heads": wl.Hq, "num_kv_heads": wl.Hkv,
-            "head_dim": wl.D, "block_size": wl.BS, "kv_dtype": "fp8_e4m3" if wl.fp8 else "bf16",
-            "seq_lens": "log-uniform [128, 16384]" if wl.cfg == 5 else
+            "head_dim": wl.D, "block_size": wl.BS,
+            "kv_dtype": ["bf16", "fp8_e4m3", "int8"][wl.kv_kind],
+            "seq_lens": "log-uniform [128, 16384]" if wl.cfg in (5, 7) else
             ("uniform [1024, 8192]" if wl.cfg in (2, 6) else "see workload"),
             "query_tokens_per_request": wl.q_len,
             "mean_seq_len": round(float(wl.seq_lens.mean()), 1), "num_blocks": wl.NB,
@@ -194,7 +198,7 @@ def decode_algorithmic_bytes(wl):
     nblk = sum(len(wl.blocks_of(r)) for r in range(wl.N))
     b = wl.kv_read_bytes()
     b += nblk * 4                                        # block table entries read
-    if wl.fp8:
+    if wl.quant:
         b += nblk * wl.Hkv * 2 * 4                       # K and V scales
     b += 2 * wl.N * wl.q_len * wl.Hq * wl.D * 2          # q in, out
     return b
@@ -223,7 +227,7 @@ def oracle_sample(wl, dd, reqs):
     vc = bits(dd["v_cache"].index_select(0, idx))
     q = bits(dd["q"][torch.tensor(reqs, device=idx.device)])
     ks = vs = None
-    if wl.fp8:
+    if wl.quant:
         ks = dd["k_scale"].index_select(0, idx).cpu().numpy()
         vs = dd["v_scale"].index_select(0, idx).cpu().numpy()
     return q, kc, vc, bt, wl.seq_lens[reqs].copy(), ks, vs
@@ -280,16 +284,17 @@ def run_ours(args):
     wl = W.make(args.workload, seed=(args.seed if args.seed is not None else args.workload) + rank,
                 batch=args.batch)
     dd = W.device_data(wl, dev)
-    fp8 = wl.fp8
-    dt_code = pkv.FP8_E4M3 if fp8 else pkv.BF16
+    quant = wl.quant                      # 8-bit pages (E4M3 or int8) with scales
+    dt_code = wl.kv_kind
     bt = torch.from_numpy(wl.block_table).to(dev)
     sl = torch.from_numpy(wl.seq_lens).to(dev)
     req_new, pos_new = wl.new_token_rows()      # the step's new tokens (q_len per request)
     pos = torch.from_numpy(pos_new).to(dev)
     req = torch.from_numpy(req_new).to(dev)
     qoffs = torch.from_numpy(wl.q_offsets()).to(dev)
-    if fp8:
-        kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch.uint8, device=dev)
+    if quant:
+        kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D),
+                         dtype=torch.int8 if wl.int8 else torch.uint8, device=dev)
         vc = torch.zeros_like(kc)
         req_all, pos_all = W.token_rows_order(wl)
         sm_all = pkv.compute_slot_mapping(bt, torch.from_numpy(pos_all).to(dev), wl.BS,
@@ -472,7 +477,8 @@ def run_ours(args):
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
                 "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "fp8_e4m3 KV, bf16 q/out, fp32 accumulate" if fp8 else "bf16",
+                "dtype": ("bf16" if not quant else
+                          ["", "fp8_e4m3", "int8"][wl.kv_kind] + " KV, bf16 q/out, fp32 accumulate"),
                 "data": "synthetic (seeded N(0,1) q/K/V, uniform token ids)",
                 "config": dict(workload_config(wl),
                                parallelism=f"{world} independent replicas (no collective)"),
@@ -484,6 +490,85 @@ def run_ours(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ block copy alone
+def run_copy_blocks(args):
+    """pkv_copy_blocks on the 70B-layer pool (8 KV heads x 16 tokens x 128 bf16: 32 KB per
+    block and cache, 20,480 blocks, 1.34 GB for K and V): `--pairs` (source, destination)
+    pairs per launch, a fresh random mapping per launch so no launch re-reads the previous
+    one's destinations from L2."""
+    import torch
+    import paged_kv_cache_289_gb300 as pkv
+    from oracle.block_manager import copy_blocks as oracle_copy
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    NB, Hkv, BS, D = 20480, 8, 16, 128
+    P = min(args.pairs, NB // 2)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    kc = torch.randn((NB, Hkv, BS, D), generator=g, device=dev, dtype=torch.bfloat16)
+    vc = torch.randn((NB, Hkv, BS, D), generator=g, device=dev, dtype=torch.bfloat16)
+    rng = np.random.default_rng(6)
+    K, Wm = args.steps, max(args.warmup, 3)
+    maps = []
+    for _ in range(min(K + Wm, 64)):
+        ids = rng.permutation(NB)
+        maps.append(torch.from_numpy(np.stack([ids[:P], ids[P:2 * P]], 1).astype(np.int32))
+                    .to(dev))
+    main = torch.cuda.current_stream(dev)
+    for i in range(Wm):
+        pkv.copy_blocks(kc, vc, maps[i % len(maps)], stream=main)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = ClockSampler(0)
+    sampler.start()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for k in range(K):
+        ev[k][0].record(main)
+        pkv.copy_blocks(kc, vc, maps[(Wm + k) % len(maps)], stream=main)
+        ev[k][1].record(main)
+    e1.record(main)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    t = e0.elapsed_time(e1) / 1e3
+    avg = sum(a.elapsed_time(b) for a, b in ev) / K / 1e3
+    block_bytes = Hkv * BS * D * 2
+    alg = P * (2 * 2 * block_bytes + 2 * 4)      # K and V blocks read + written, one pair entry
+    peak, peak_kind = peak_hbm()
+    # oracle: the same copy on host memory, a bounded sample of pairs
+    kh = np.zeros((2048, Hkv, BS, D), np.uint16)
+    vh = np.zeros_like(kh)
+    mp = np.stack([np.arange(0, 1024), np.arange(1024, 2048)], 1)
+    t0 = time.perf_counter()
+    reps = 0
+    while time.perf_counter() - t0 < 10.0:
+        oracle_copy(kh, vh, mp)
+        reps += 1
+    tc = time.perf_counter() - t0
+    cpu = {"value": round(reps * 1024 * 4 * block_bytes / tc / 1e9, 3), "unit": "GB/s",
+           "cores": 1, "kind": "oracle",
+           "sample": f"{reps} x 1024 pairs of 32 KB blocks in host memory (numpy, {tc:.1f} s)"}
+    line = {"metric": "copy-on-write block copy: HBM GB/s (read + write)",
+            "value": round(alg * K / t / 1e9, 2), "unit": "GB/s", "n_gpus": 1, "steps": K,
+            "warmup": Wm, "ms_per_step": round(t / K * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16 bytes (copy)",
+            "data": "synthetic", "config": {"workload": "copy_blocks_llama70b_pool",
+                                            "num_blocks": NB, "pairs_per_launch": P,
+                                            "block_bytes_per_cache": block_bytes,
+                                            "l2": "fresh random mapping per launch; "
+                                                  f"{alg / 1e6:.0f} MB moved per launch"},
+            "roofline": {"bound": "hbm", "achieved": round(alg / avg / 1e9, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(alg / avg / 1e9 / peak, 4),
+                         "traffic": None, "peak_source": f"{peak_kind} hbm_gbs",
+                         "kernel": "pkv_copy_blocks_kernel", "algorithmic_bytes_per_launch": alg,
+                         "avg_launch_ms": round(avg * 1e3, 4)},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": K, "clocks": clocks}
+    print(json.dumps(line), flush=True)
 
 
 # ------------------------------------------------------------------ reference arm
@@ -498,12 +583,12 @@ def run_reference(args):
     # host copies of a bounded sample (the first 4 requests) drawn on the host generator
     reqs = list(range(min(4, wl.N)))
     sub = W.custom(len(reqs), wl.Hq, wl.Hkv, wl.D, wl.BS, wl.seq_lens[reqs], fp8=wl.fp8,
-                   seed=wl.seed, scale=wl.scale, name=wl.name + "_sample")
+                   int8=wl.int8, seed=wl.seed, scale=wl.scale, name=wl.name + "_sample")
     hd = W.host_data(sub)
-    if sub.fp8:
+    if sub.quant:
         req_all, pos_all = W.token_rows_order(sub)
         sm = oracle.slot_mapping(sub.block_table, req_all, pos_all, sub.BS)
-        kc = np.zeros((sub.NB, sub.Hkv, sub.BS, sub.D), np.uint8)
+        kc = np.zeros((sub.NB, sub.Hkv, sub.BS, sub.D), sub.cache_np_dtype)
         vc = np.zeros_like(kc)
         oracle.kv_cache_write(hd["k_rows"], hd["v_rows"], sm, kc, vc, hd["k_scale"], hd["v_scale"])
         ks, vs = hd["k_scale"], hd["v_scale"]
@@ -541,6 +626,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "copy_blocks":
+        run_copy_blocks(args)
     else:
         run_ours(args)
 

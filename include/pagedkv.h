@@ -33,9 +33,9 @@
  *   - Layouts are row-major and contiguous:
  *       q, out          bf16 [N][Hq][D]
  *       k, v (new rows) bf16 [T][Hkv][D]
- *       k_cache,v_cache [NB][Hkv][BS][D]  bf16 or E4M3 bytes; one (block, head)
- *                       page of BS*D elements is contiguous
- *       k_scale,v_scale fp32 [NB][Hkv]    FP8 caches only
+ *       k_cache,v_cache [NB][Hkv][BS][D]  bf16, E4M3 bytes or int8 codes; one
+ *                       (block, head) page of BS*D elements is contiguous
+ *       k_scale,v_scale fp32 [NB][Hkv]    8-bit caches only
  *       block_table     int32 [N][MB]     physical block of logical block j of request r
  *       seq_lens        int32 [N]         tokens cached for request r, including the
  *                                         one written this step
@@ -60,8 +60,9 @@ extern "C" {
 /* Same object as cudaStream_t. */
 typedef struct CUstream_st *pkv_stream_t;
 
-/* Cache element type. */
-enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1 };
+/* Cache element type.  The 8-bit kinds carry one fp32 scale per (block, kv head):
+ * element value = code * scale. */
+enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1, PKV_INT8 = 2 };
 
 /* Return codes. */
 enum {
@@ -69,7 +70,8 @@ enum {
     PKV_ERR_INVALID_ARG = -1,   /* null pointer, bad size, misaligned buffer */
     PKV_ERR_UNSUPPORTED = -2,   /* a shape this build has no kernel for */
     PKV_ERR_WORKSPACE = -3,     /* workspace missing or smaller than required */
-    PKV_ERR_CUDA = -4           /* a CUDA runtime call or launch failed */
+    PKV_ERR_CUDA = -4,          /* a CUDA runtime call or launch failed */
+    PKV_ERR_NO_BLOCKS = -5      /* block manager: not enough free blocks; nothing changed */
 };
 
 /* Bits of the device error word (first 4 bytes of the decode workspace).  The
@@ -111,6 +113,9 @@ PKV_API int pkv_compute_slot_mapping(const int32_t *block_table, int max_blocks_
  *                 round to nearest even, saturating to +-448 (k_scale/v_scale
  *                 fp32 [NB][Hkv], required).  A later token of a block reuses
  *                 the block's scale.
+ *   PKV_INT8:     byte = clamp(round_half_even(float(x) / scale[blk][h]), -127, 127)
+ *                 as int8, same division and scales ([P3] "优化五：KV 本体压缩":
+ *                 FP16 -> FP8/INT8/INT4).  NaN inputs give 0.
  * Bytes not addressed by a slot are untouched.  Two tokens with the same slot
  * race (last writer wins, undefined which).
  * Requirements: head_dim % 8 == 0; k, v, caches 16-byte aligned.
@@ -119,6 +124,29 @@ PKV_API int pkv_kv_cache_write(const void *k, const void *v, const int64_t *slot
                        int num_tokens, int num_kv_heads, int head_dim, int block_size,
                        int num_blocks, int cache_dtype, void *k_cache, void *v_cache,
                        const float *k_scale, const float *v_scale, pkv_stream_t stream);
+
+/*
+ * KV write that also sets the block scales ([P3] "优化五：KV 本体压缩" and 传输量化:
+ * 8-bit KV with a scale; here the scale is derived from the data being written).
+ * For every (block, kv head) that receives at least one row in this call, its scale
+ * becomes amax / QMAX over the |values| of the rows written to it by this call
+ * (QMAX = 448 for PKV_FP8_E4M3, 127 for PKV_INT8; binary32 divide; NaN values
+ * ignored; an all-zero block gets 1); the rows are then coded exactly as
+ * pkv_kv_cache_write does with those scales.  Scales of blocks receiving no row are
+ * unchanged; bytes written to a touched block by earlier calls are not re-coded, so
+ * use it for whole blocks (prefill) and pkv_kv_cache_write for later tokens.
+ * k_scale / v_scale are read and written.  workspace: device, >=
+ * pkv_rescale_workspace_size(num_blocks, num_kv_heads) bytes, 4-byte aligned, no
+ * clearing needed.  Three launches, no host synchronisation.
+ */
+PKV_API size_t pkv_rescale_workspace_size(int num_blocks, int num_kv_heads);
+PKV_API int pkv_kv_cache_write_rescale(const void *k, const void *v,
+                                       const int64_t *slot_mapping, int num_tokens,
+                                       int num_kv_heads, int head_dim, int block_size,
+                                       int num_blocks, int cache_dtype, void *k_cache,
+                                       void *v_cache, float *k_scale, float *v_scale,
+                                       void *workspace, size_t workspace_bytes,
+                                       pkv_stream_t stream);
 
 /*
  * Bytes of device workspace pkv_paged_decode_attn needs for this shape on a
@@ -141,7 +169,7 @@ PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_
  * (likewise V), dequantised with k_scale/v_scale[block][h] for FP8 pages.
  * Accumulation is fp32; out is bf16.  seq_lens[r] == 0 gives out[r] = 0.
  * Supported: Hq % Hkv == 0, G = Hq / Hkv <= 8; block_size 16 or 32;
- *   PKV_BF16 with head_dim 64 or 128; PKV_FP8_E4M3 with head_dim 128
+ *   PKV_BF16 with head_dim 64 or 128; PKV_FP8_E4M3 and PKV_INT8 with head_dim 128
  *   (FP8: the group's bf16 q values are rescaled by a power of two so the
  *   largest lands in [2^14, 2^15) and converted to fp16; this is exact except
  *   for nonzero elements more than 2^31 times smaller than the group's
@@ -174,7 +202,7 @@ PKV_API int pkv_paged_decode_attn(const void *q, const void *k_cache, const void
  * Transformer的循环状态") to the cached positions 0 .. seq_lens[r] - q_len + i.
  * A query that sees no token gets a zero row.  Each KV page is read once for all
  * of a request's queries and heads of a group.
- * Supported: 1 <= max_q_len <= 4 with bf16 pages, <= 2 with FP8 pages; every
+ * Supported: 1 <= max_q_len <= 4 with bf16 pages, <= 2 with 8-bit pages; every
  * request must have q_offsets[r+1] - q_offsets[r] <= max_q_len (a larger count
  * is clamped and sets PKV_DEVERR_QLEN_CLAMPED; the rows past the clamp are not
  * written).  Everything else as pkv_paged_decode_attn; q_offsets is a device
@@ -235,6 +263,92 @@ PKV_API int pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache,
 PKV_API int pkv_prefix_block_hash(const int32_t *tokens, const int64_t *offsets, int num_seqs,
                           int block_size, uint64_t seed, uint64_t *hashes,
                           const int64_t *hash_offsets, pkv_stream_t stream);
+
+/*
+ * Copy whole blocks inside the cache pool, for copy-on-write of a shared block
+ * ([P1] "PagedAttention与Cache管理": physical blocks are shared between
+ * sequences, and a sequence that must change a shared block gets its own copy
+ * first -- beam search).  For each pair i, block block_mapping[2i] (source) is
+ * copied to block block_mapping[2i+1] (destination): all num_kv_heads pages of K
+ * and of V, BS*D elements each, and for 8-bit caches the 2*num_kv_heads fp32
+ * scales of the block.  block_mapping is a DEVICE int32 array [num_pairs][2].
+ *   - Destinations must be distinct and must not be the source of another pair
+ *     (the block manager below only ever names a fresh block as destination);
+ *     overlapping pairs give an unspecified result, never an out-of-bounds access.
+ *   - A pair with an id outside [0, num_blocks) or with source == destination is
+ *     skipped.
+ *   - num_pairs == 0 launches nothing.  k_scale/v_scale are required for the
+ *     8-bit kinds and ignored for bf16.
+ */
+PKV_API int pkv_copy_blocks(void *k_cache, void *v_cache, float *k_scale, float *v_scale,
+                            const int32_t *block_mapping, int num_pairs, int num_kv_heads,
+                            int head_dim, int block_size, int num_blocks, int cache_dtype,
+                            pkv_stream_t stream);
+
+/*
+ * Host block manager: owns the ids of the physical blocks of one cache pool and
+ * builds the block tables the kernels above read ([P1] "PagedAttention与Cache管理":
+ * on-demand blocks, waste under one block per sequence, sharing and copy-on-write;
+ * [P3] "优化一：Prefix Cache": full blocks found again by their chained hash;
+ * [P2] "缓存命中与复用": block-granular hits that must be a prefix, LRU eviction,
+ * blocks in use are never evicted).  Pure host code, touches no device memory and
+ * no CUDA context; every call is thread-safe (one mutex per manager).
+ *
+ * States of a block: FREE (refcount 0, no hash), USED (refcount >= 1, hash or
+ * not), CACHED (refcount 0, still registered under its hash, reusable by a hit,
+ * evictable).  Deterministic policy:
+ *   - a fresh block is the lowest-numbered FREE block; with none FREE, the least
+ *     recently released CACHED block is evicted (its hash forgotten) and reused;
+ *   - pkv_bm_add_sequence takes the leading blocks whose hashes are registered
+ *     (stopping at the first miss), then fresh blocks for the rest; the first
+ *     num_hashes fresh blocks are registered under their hashes;
+ *   - pkv_bm_free_sequence releases the blocks last to first, so the tail of a
+ *     prefix becomes CACHED before its head and is evicted first;
+ *   - a hash is registered to at most one block: the first registration wins;
+ *   - calls that need blocks are all-or-nothing and return PKV_ERR_NO_BLOCKS with
+ *     no change when too few FREE + CACHED blocks remain.
+ * Sequence ids are any int64 chosen by the caller; an unknown id, or adding an id
+ * that exists, returns PKV_ERR_INVALID_ARG.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* A manager of blocks 0 .. num_blocks-1, all FREE, of block_size tokens each. */
+PKV_API int pkv_bm_create(int num_blocks, int block_size, pkv_block_manager **out);
+PKV_API void pkv_bm_destroy(pkv_block_manager *m);
+/* FREE + CACHED blocks (what a call may still take), or a negative status. */
+PKV_API int pkv_bm_num_available(pkv_block_manager *m);
+/* Register a sequence of num_tokens tokens whose first num_hashes full blocks have
+ * the given chained hashes (num_hashes <= num_tokens / block_size; pass the
+ * output of pkv_prefix_block_hash).  Writes ceil(num_tokens / block_size) block
+ * ids to block_ids (host int32) and the number of leading blocks reused from the
+ * cache to *cached_blocks (may be NULL). */
+PKV_API int pkv_bm_add_sequence(pkv_block_manager *m, int64_t seq_id, int64_t num_tokens,
+                                const uint64_t *block_hashes, int num_hashes,
+                                int32_t *block_ids, int *cached_blocks);
+/* The sequence now holds num_tokens tokens (>= before): appends fresh blocks as
+ * needed; *new_block (may be NULL) gets the last block appended, or -1 if none. */
+PKV_API int pkv_bm_grow(pkv_block_manager *m, int64_t seq_id, int64_t num_tokens,
+                        int32_t *new_block);
+/* Register the sequence's full logical block under hash (after it was filled). */
+PKV_API int pkv_bm_commit_block_hash(pkv_block_manager *m, int64_t seq_id, int logical_block,
+                                     uint64_t hash);
+/* child_id gets the parent's blocks and token count; every block's refcount + 1. */
+PKV_API int pkv_bm_fork(pkv_block_manager *m, int64_t parent_id, int64_t child_id);
+/* Before writing into logical_block of seq_id: if its block is shared (refcount
+ * > 1) or registered under a hash, the sequence gets a fresh block in its place
+ * and *copy_src / *copy_dst name the copy to make first (pkv_copy_blocks);
+ * otherwise both are -1 and the block may be written in place. */
+PKV_API int pkv_bm_prepare_write(pkv_block_manager *m, int64_t seq_id, int logical_block,
+                                 int32_t *copy_src, int32_t *copy_dst);
+/* Release every block of the sequence and forget the id. */
+PKV_API int pkv_bm_free_sequence(pkv_block_manager *m, int64_t seq_id);
+/* Copies the sequence's block ids to block_ids (capacity entries available);
+ * returns their number, or a negative status.  block_ids == NULL returns the
+ * number only. */
+PKV_API int pkv_bm_block_table(pkv_block_manager *m, int64_t seq_id, int32_t *block_ids,
+                               int capacity);
+/* Refcount of a block (0 for FREE and CACHED), or a negative status. */
+PKV_API int pkv_bm_refcount(pkv_block_manager *m, int block);
 
 #ifdef __cplusplus
 }

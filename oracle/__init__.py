@@ -13,6 +13,9 @@ Sources, by page title and section:
 
 Parity status per function (what pins it, see tests/test_oracle_pins.py):
   bf16_to_double, e4m3_to_double, e4m3_from_float  -- library codecs (torch CPU) + OCP spec values
+  int8_from_float                                  -- torch round-half-even + clamp, brute force
+  kv_cache_write_rescale                           -- the generator's amax/QMAX recipe, written
+                                                      independently
   kv_bytes                                         -- the printed 327,680 B/token and ~10 GB at 32K
   slot_mapping, kv_cache_write                     -- worked example + write/gather round trip
   multiquery_attn                                  -- dense causal brute force, q_len = 1 case
@@ -20,6 +23,8 @@ Parity status per function (what pins it, see tests/test_oracle_pins.py):
                                                       GQA == replicated MHA, closed-form cases, LSE merge
   fnv1a64, fmix64                                  -- published FNV-1a and SplitMix64 test vectors
   prefix_block_hash                                -- token-exact prefix equality properties
+  block_manager.BlockManagerModel, copy_blocks     -- hand-worked call sequences and invariants
+                                                      (tests/test_block_manager.py)
 """
 from __future__ import annotations
 
@@ -69,12 +74,17 @@ def lib():
             L.orc_e4m3_to_double.argtypes = [ctypes.c_uint8]
             L.orc_e4m3_from_float.restype = ctypes.c_uint8
             L.orc_e4m3_from_float.argtypes = [ctypes.c_float]
+            L.orc_int8_from_float.restype = ctypes.c_int8
+            L.orc_int8_from_float.argtypes = [ctypes.c_float]
             L.orc_kv_bytes.restype = _i64
             L.orc_kv_bytes.argtypes = [_i64] * 5
             L.orc_slot_mapping.restype = None
             L.orc_slot_mapping.argtypes = [_p, _i, _p, _p, _i, _i, _p]
             L.orc_kv_cache_write.restype = None
             L.orc_kv_cache_write.argtypes = [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p, _p]
+            L.orc_kv_cache_write_rescale.restype = None
+            L.orc_kv_cache_write_rescale.argtypes = [_p, _p, _p, _i, _i, _i, _i, _i, _p, _p, _p,
+                                                     _p]
             L.orc_decode_row.restype = None
             L.orc_decode_row.argtypes = [_p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i, _i, _i,
                                          _d, _i, _i, _p, _p, _p]
@@ -120,6 +130,21 @@ def e4m3_from_float(x: float) -> int:
     return int(lib().orc_e4m3_from_float(float(x)))
 
 
+def int8_from_float(x: float) -> int:
+    return int(lib().orc_int8_from_float(float(x)))
+
+
+def _kind(cache):
+    """0: bf16 bit patterns (uint16), 1: E4M3 bytes (uint8), 2: int8."""
+    if cache.dtype == np.uint16:
+        return 0
+    if cache.dtype == np.uint8:
+        return 1
+    if cache.dtype == np.int8:
+        return 2
+    raise TypeError(f"cache dtype {cache.dtype}")
+
+
 def kv_bytes(L: int, Hkv: int, d: int, S: int, b: int) -> int:
     return int(lib().orc_kv_bytes(L, Hkv, d, S, b))
 
@@ -140,42 +165,55 @@ def slot_mapping(block_table, req_idx, positions, block_size):
 
 
 def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=None):
-    """In-place write into numpy caches (uint16 bf16 bits or uint8 e4m3 bytes).
+    """In-place write into numpy caches (uint16 bf16 bits, uint8 E4M3 bytes or int8).
 
     k, v: uint16 [T, Hkv, D] bf16 bit patterns.  Caches [NB, Hkv, BS, D]."""
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     sm = _c(slot_mapping, np.int64)
-    fp8 = k_cache.dtype == np.uint8
+    kind = _kind(k_cache)
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
-    ks = _c(k_scale, np.float32) if fp8 else None
-    vs = _c(v_scale, np.float32) if fp8 else None
+    ks = _c(k_scale, np.float32) if kind else None
+    vs = _c(v_scale, np.float32) if kind else None
     T, Hkv, D = k.shape
-    lib().orc_kv_cache_write(_ptr(k), _ptr(v), _ptr(sm), T, Hkv, D, k_cache.shape[2], int(fp8),
+    lib().orc_kv_cache_write(_ptr(k), _ptr(v), _ptr(sm), T, Hkv, D, k_cache.shape[2], kind,
                              _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs))
+
+
+def kv_cache_write_rescale(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+    """In-place: set the scale of every (block, head) written by this call to
+    amax/QMAX of its rows here, then write the rows (8-bit caches only)."""
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    sm = _c(slot_mapping, np.int64)
+    kind = _kind(k_cache)
+    assert kind in (1, 2) and k_scale.dtype == np.float32 and k_scale.flags.c_contiguous
+    T, Hkv, D = k.shape
+    lib().orc_kv_cache_write_rescale(_ptr(k), _ptr(v), _ptr(sm), T, Hkv, D, k_cache.shape[2], kind,
+                                     _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale))
 
 
 def _decode_args(q, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale):
     q = _c(q, np.uint16)
-    fp8 = k_cache.dtype == np.uint8
+    kind = _kind(k_cache)
     kc = np.ascontiguousarray(k_cache)
     vc = np.ascontiguousarray(v_cache)
-    ks = _c(k_scale, np.float32) if fp8 else None
-    vs = _c(v_scale, np.float32) if fp8 else None
+    ks = _c(k_scale, np.float32) if kind else None
+    vs = _c(v_scale, np.float32) if kind else None
     bt = _c(block_table, np.int32)
     sl = _c(seq_lens, np.int32)
-    return q, kc, vc, ks, vs, bt, sl, fp8
+    return q, kc, vc, ks, vs, bt, sl, kind
 
 
 def decode_attn(q, k_cache, v_cache, block_table, seq_lens, scale, k_scale=None, v_scale=None):
     """fp64 output [N, Hq, D] for every (request, query head)."""
-    q, kc, vc, ks, vs, bt, sl, fp8 = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
+    q, kc, vc, ks, vs, bt, sl, kind = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
                                                   k_scale, v_scale)
     N, Hq, D = q.shape
     Hkv, BS = kc.shape[1], kc.shape[2]
     out = np.empty((N, Hq, D), dtype=np.float64)
     lib().orc_paged_decode_attn(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
-                                bt.shape[1], _ptr(sl), N, Hq, Hkv, D, BS, int(fp8),
+                                bt.shape[1], _ptr(sl), N, Hq, Hkv, D, BS, int(kind),
                                 float(scale), _ptr(out))
     return out
 
@@ -184,14 +222,14 @@ def multiquery_attn(q, q_offsets, k_cache, v_cache, block_table, seq_lens, scale
                     v_scale=None):
     """fp64 output [T, Hq, D]: query rows q_offsets[r]..q_offsets[r+1]-1 of request r are
     its newest tokens and attend causally (position seq_len - q_len + i and before)."""
-    q, kc, vc, ks, vs, bt, sl, fp8 = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
+    q, kc, vc, ks, vs, bt, sl, kind = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
                                                   k_scale, v_scale)
     qo = _c(q_offsets, np.int32)
     T, Hq, D = q.shape
     Hkv, BS = kc.shape[1], kc.shape[2]
     out = np.empty((T, Hq, D), dtype=np.float64)
     lib().orc_multiquery_attn(_ptr(q), _ptr(qo), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
-                              bt.shape[1], _ptr(sl), qo.shape[0] - 1, Hq, Hkv, D, BS, int(fp8),
+                              bt.shape[1], _ptr(sl), qo.shape[0] - 1, Hq, Hkv, D, BS, int(kind),
                               float(scale), _ptr(out))
     return out
 
@@ -199,14 +237,14 @@ def multiquery_attn(q, q_offsets, k_cache, v_cache, block_table, seq_lens, scale
 def decode_rows(q, k_cache, v_cache, block_table, seq_lens, scale, rows, k_scale=None,
                 v_scale=None):
     """fp64 output [len(rows), D] for selected rows (row = r * Hq + hq)."""
-    q, kc, vc, ks, vs, bt, sl, fp8 = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
+    q, kc, vc, ks, vs, bt, sl, kind = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
                                                   k_scale, v_scale)
     N, Hq, D = q.shape
     Hkv, BS = kc.shape[1], kc.shape[2]
     rows = _c(rows, np.int64)
     out = np.empty((rows.shape[0], D), dtype=np.float64)
     lib().orc_decode_rows(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
-                          bt.shape[1], _ptr(sl), Hq, Hkv, D, BS, int(fp8), float(scale),
+                          bt.shape[1], _ptr(sl), Hq, Hkv, D, BS, int(kind), float(scale),
                           _ptr(rows), rows.shape[0], _ptr(out))
     return out
 
@@ -214,7 +252,7 @@ def decode_rows(q, k_cache, v_cache, block_table, seq_lens, scale, rows, k_scale
 def decode_row_detail(q, k_cache, v_cache, block_table, seq_lens, scale, r, hq, k_scale=None,
                       v_scale=None):
     """(o [D], p [seq_len], lse) for one (request, query head)."""
-    q, kc, vc, ks, vs, bt, sl, fp8 = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
+    q, kc, vc, ks, vs, bt, sl, kind = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
                                                   k_scale, v_scale)
     N, Hq, D = q.shape
     Hkv, BS = kc.shape[1], kc.shape[2]
@@ -222,7 +260,7 @@ def decode_row_detail(q, k_cache, v_cache, block_table, seq_lens, scale, r, hq, 
     p = np.empty(max(int(sl[r]), 1), dtype=np.float64)
     lse = ctypes.c_double(0.0)
     lib().orc_decode_row(_ptr(q), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), bt.shape[1],
-                         _ptr(sl), Hq, Hkv, D, BS, int(fp8), float(scale), int(r), int(hq),
+                         _ptr(sl), Hq, Hkv, D, BS, int(kind), float(scale), int(r), int(hq),
                          _ptr(o), _ptr(p), ctypes.byref(lse))
     return o, p[: max(int(sl[r]), 0)], lse.value
 

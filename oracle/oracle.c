@@ -20,8 +20,9 @@
  * Layout conventions (shared *as a specification* with the library, not as
  * code):
  *   q        bf16  [N][Hq][D]
- *   caches   [NB][Hkv][BS][D]   (bf16 = uint16 bit patterns, fp8 = e4m3 bytes)
- *   scales   fp32  [NB][Hkv]    (fp8 only; one per (block, kv head), K and V separate)
+ *   caches   [NB][Hkv][BS][D]   cache_kind 0: bf16 (uint16 bit patterns),
+ *                               1: E4M3 bytes, 2: int8
+ *   scales   fp32  [NB][Hkv]    (8-bit kinds; one per (block, kv head), K and V separate)
  *   block_table int32 [N][MB], seq_lens int32 [N]
  *
  * Build: gcc -O2 -fopenmp -shared -fPIC (no -ffast-math: the fp32 divide in
@@ -107,6 +108,21 @@ uint8_t orc_e4m3_from_float(float xf)
     }
 }
 
+/* Symmetric int8 code of a binary32 value: round to nearest, ties to even, then
+ * clamp to [-127, 127] (the KV quantisation to INT8 of [P3] "优化五：KV 本体压缩",
+ * FP16 -> FP8/INT8/INT4; per-(block, head) scale, symmetric so that 0 maps to 0). */
+int8_t orc_int8_from_float(float x)
+{
+    double r = rint((double)x);   /* x is a binary32 value: exact in double */
+    if (isnan(x))
+        return 0;
+    if (r > 127.0)
+        r = 127.0;
+    if (r < -127.0)
+        r = -127.0;
+    return (int8_t)r;
+}
+
 /* ------------------------------------------------------------------------ */
 /* KV size formula  ([P3] "KV Cache 到底有多大？", KV Size equation)          */
 /* ------------------------------------------------------------------------ */
@@ -152,13 +168,14 @@ void orc_slot_mapping(const int32_t *block_table, int max_blocks_per_seq,
 
 /* Writes row (t, h) of k and v (bf16 [T][Hkv][D]) to cache row
  * [slot / BS][h][slot % BS][:].  bf16 caches receive the bytes unchanged.
- * fp8 caches receive e4m3_RNE_satfinite(float(x) / scale[blk][h]) where the
- * division is the IEEE binary32 divide.  Tokens with slot < 0 are skipped;
- * every other byte of the caches is left as it was. */
+ * 8-bit caches receive code(float(x) / scale[blk][h]) where the division is the
+ * IEEE binary32 divide and code is E4M3 (RNE, saturating) or int8 (RNE, clamp to
+ * +-127).  Tokens with slot < 0 are skipped; every other byte of the caches is
+ * left as it was. */
 void orc_kv_cache_write(const uint16_t *k, const uint16_t *v,
                         const int64_t *slot_mapping, int num_tokens,
                         int num_kv_heads, int head_dim, int block_size,
-                        int cache_is_fp8, void *k_cache, void *v_cache,
+                        int cache_kind, void *k_cache, void *v_cache,
                         const float *k_scale, const float *v_scale)
 {
     for (int t = 0; t < num_tokens; ++t) {
@@ -171,7 +188,7 @@ void orc_kv_cache_write(const uint16_t *k, const uint16_t *v,
             int64_t src = ((int64_t)t * num_kv_heads + h) * head_dim;
             int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * head_dim;
             for (int d = 0; d < head_dim; ++d) {
-                if (!cache_is_fp8) {
+                if (!cache_kind) {
                     ((uint16_t *)k_cache)[dst + d] = k[src + d];
                     ((uint16_t *)v_cache)[dst + d] = v[src + d];
                 } else {
@@ -181,12 +198,70 @@ void orc_kv_cache_write(const uint16_t *k, const uint16_t *v,
                     float vx = (float)orc_bf16_to_double(v[src + d]);
                     volatile float kq = kx / ks;  /* binary32 divide, RN */
                     volatile float vq = vx / vs;
-                    ((uint8_t *)k_cache)[dst + d] = orc_e4m3_from_float(kq);
-                    ((uint8_t *)v_cache)[dst + d] = orc_e4m3_from_float(vq);
+                    if (cache_kind == 1) {
+                        ((uint8_t *)k_cache)[dst + d] = orc_e4m3_from_float(kq);
+                        ((uint8_t *)v_cache)[dst + d] = orc_e4m3_from_float(vq);
+                    } else {
+                        ((int8_t *)k_cache)[dst + d] = orc_int8_from_float(kq);
+                        ((int8_t *)v_cache)[dst + d] = orc_int8_from_float(vq);
+                    }
                 }
             }
         }
     }
+}
+
+/* KV write that first sets the scale of every (block, head) receiving rows in
+ * this call: scale = amax / QMAX over the |values| of those rows (QMAX = 448 for
+ * E4M3, 127 for int8; binary32 divide; NaN values ignored; amax = 0 gives 1), then
+ * writes the rows as orc_kv_cache_write does.  Scales of blocks receiving no row
+ * are unchanged, and bytes written to a touched block by earlier calls are not
+ * re-coded.  cache_kind 1 or 2. */
+void orc_kv_cache_write_rescale(const uint16_t *k, const uint16_t *v,
+                                const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
+                                int head_dim, int block_size, int cache_kind, void *k_cache,
+                                void *v_cache, float *k_scale, float *v_scale)
+{
+    int64_t nblk = 0;
+    for (int t = 0; t < num_tokens; ++t)
+        if (slot_mapping[t] >= 0 && slot_mapping[t] / block_size + 1 > nblk)
+            nblk = slot_mapping[t] / block_size + 1;
+    float *kmax = (float *)malloc(sizeof(float) * (size_t)(nblk * num_kv_heads + 1));
+    float *vmax = (float *)malloc(sizeof(float) * (size_t)(nblk * num_kv_heads + 1));
+    for (int64_t i = 0; i < nblk * num_kv_heads; ++i)
+        kmax[i] = vmax[i] = -1.0f;              /* -1: not touched by this call */
+    for (int t = 0; t < num_tokens; ++t) {
+        int64_t slot = slot_mapping[t];
+        if (slot < 0)
+            continue;
+        int64_t blk = slot / block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t i = blk * num_kv_heads + h;
+            if (kmax[i] < 0.0f)
+                kmax[i] = vmax[i] = 0.0f;
+            for (int d = 0; d < head_dim; ++d) {
+                float kx = fabsf((float)orc_bf16_to_double(k[((int64_t)t * num_kv_heads + h) * head_dim + d]));
+                float vx = fabsf((float)orc_bf16_to_double(v[((int64_t)t * num_kv_heads + h) * head_dim + d]));
+                if (!isnan(kx) && kx > kmax[i])
+                    kmax[i] = kx;
+                if (!isnan(vx) && vx > vmax[i])
+                    vmax[i] = vx;
+            }
+        }
+    }
+    volatile float qmax = cache_kind == 1 ? 448.0f : 127.0f;
+    for (int64_t i = 0; i < nblk * num_kv_heads; ++i) {
+        if (kmax[i] < 0.0f)
+            continue;
+        volatile float ks = kmax[i] > 0.0f ? kmax[i] / qmax : 1.0f;   /* binary32 divide */
+        volatile float vs = vmax[i] > 0.0f ? vmax[i] / qmax : 1.0f;
+        k_scale[i] = ks;
+        v_scale[i] = vs;
+    }
+    free(kmax);
+    free(vmax);
+    orc_kv_cache_write(k, v, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size,
+                       cache_kind, k_cache, v_cache, k_scale, v_scale);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -196,15 +271,17 @@ void orc_kv_cache_write(const uint16_t *k, const uint16_t *v,
 /* ------------------------------------------------------------------------ */
 
 /* Value of cache element (blk, h, off, d) in fp64, dequantised for fp8. */
-static double cache_elem(const void *cache, int cache_is_fp8, const float *scale,
+static double cache_elem(const void *cache, int cache_kind, const float *scale,
                          int64_t blk, int h, int64_t off, int d,
                          int num_kv_heads, int block_size, int head_dim)
 {
     int64_t idx = ((blk * num_kv_heads + h) * block_size + off) * head_dim + d;
-    if (!cache_is_fp8)
+    if (!cache_kind)
         return orc_bf16_to_double(((const uint16_t *)cache)[idx]);
-    return orc_e4m3_to_double(((const uint8_t *)cache)[idx]) *
-           (double)scale[blk * num_kv_heads + h];
+    if (cache_kind == 1)
+        return orc_e4m3_to_double(((const uint8_t *)cache)[idx]) *
+               (double)scale[blk * num_kv_heads + h];
+    return (double)((const int8_t *)cache)[idx] * (double)scale[blk * num_kv_heads + h];
 }
 
 /* One (request r, query head hq) output row.  Query head hq reads KV head
@@ -221,7 +298,7 @@ void orc_decode_row(const uint16_t *q, const void *k_cache, const void *v_cache,
                     const float *k_scale, const float *v_scale,
                     const int32_t *block_table, int max_blocks_per_seq,
                     const int32_t *seq_lens, int num_q_heads, int num_kv_heads,
-                    int head_dim, int block_size, int cache_is_fp8, double scale,
+                    int head_dim, int block_size, int cache_kind, double scale,
                     int r, int hq, double *out_row, double *probs, double *lse)
 {
     int G = num_q_heads / num_kv_heads;
@@ -243,7 +320,7 @@ void orc_decode_row(const uint16_t *q, const void *k_cache, const void *v_cache,
         double acc = 0.0;
         for (int d = 0; d < head_dim; ++d)
             acc += orc_bf16_to_double(qrow[d]) *
-                   cache_elem(k_cache, cache_is_fp8, k_scale, blk, h, off, d,
+                   cache_elem(k_cache, cache_kind, k_scale, blk, h, off, d,
                               num_kv_heads, block_size, head_dim);
         s[t] = scale * acc;
         if (s[t] > smax)
@@ -259,7 +336,7 @@ void orc_decode_row(const uint16_t *q, const void *k_cache, const void *v_cache,
         int64_t blk = block_table[(int64_t)r * max_blocks_per_seq + t / block_size];
         int64_t off = t % block_size;
         for (int d = 0; d < head_dim; ++d)
-            out_row[d] += p * cache_elem(v_cache, cache_is_fp8, v_scale, blk, h, off,
+            out_row[d] += p * cache_elem(v_cache, cache_kind, v_scale, blk, h, off,
                                          d, num_kv_heads, block_size, head_dim);
         if (probs)
             probs[t] = p;
@@ -284,7 +361,7 @@ void orc_multiquery_attn(const uint16_t *q, const int32_t *q_offsets, const void
                          const void *v_cache, const float *k_scale, const float *v_scale,
                          const int32_t *block_table, int max_blocks_per_seq,
                          const int32_t *seq_lens, int batch, int num_q_heads, int num_kv_heads,
-                         int head_dim, int block_size, int cache_is_fp8, double scale,
+                         int head_dim, int block_size, int cache_kind, double scale,
                          double *out)
 {
     int64_t T = q_offsets[batch];
@@ -309,7 +386,7 @@ void orc_multiquery_attn(const uint16_t *q, const int32_t *q_offsets, const void
         const int32_t *bt_row = block_table + (int64_t)r * max_blocks_per_seq;
         orc_decode_row(q + tq * num_q_heads * head_dim, k_cache, v_cache, k_scale, v_scale,
                        bt_row, max_blocks_per_seq, &len1, num_q_heads, num_kv_heads, head_dim,
-                       block_size, cache_is_fp8, scale, 0, hq, out + row * head_dim, NULL,
+                       block_size, cache_kind, scale, 0, hq, out + row * head_dim, NULL,
                        NULL);
     }
 }
@@ -321,7 +398,7 @@ void orc_paged_decode_attn(const uint16_t *q, const void *k_cache, const void *v
                            const int32_t *block_table, int max_blocks_per_seq,
                            const int32_t *seq_lens, int batch, int num_q_heads,
                            int num_kv_heads, int head_dim, int block_size,
-                           int cache_is_fp8, double scale, double *out)
+                           int cache_kind, double scale, double *out)
 {
     int64_t rows = (int64_t)batch * num_q_heads;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -330,7 +407,7 @@ void orc_paged_decode_attn(const uint16_t *q, const void *k_cache, const void *v
         int hq = (int)(i % num_q_heads);
         orc_decode_row(q, k_cache, v_cache, k_scale, v_scale, block_table,
                        max_blocks_per_seq, seq_lens, num_q_heads, num_kv_heads,
-                       head_dim, block_size, cache_is_fp8, scale, r, hq,
+                       head_dim, block_size, cache_kind, scale, r, hq,
                        out + i * head_dim, NULL, NULL);
     }
 }
@@ -340,7 +417,7 @@ void orc_decode_rows(const uint16_t *q, const void *k_cache, const void *v_cache
                      const float *k_scale, const float *v_scale,
                      const int32_t *block_table, int max_blocks_per_seq,
                      const int32_t *seq_lens, int num_q_heads, int num_kv_heads,
-                     int head_dim, int block_size, int cache_is_fp8, double scale,
+                     int head_dim, int block_size, int cache_kind, double scale,
                      const int64_t *rows, int64_t count, double *out)
 {
 #pragma omp parallel for schedule(dynamic, 1)
@@ -349,7 +426,7 @@ void orc_decode_rows(const uint16_t *q, const void *k_cache, const void *v_cache
         int hq = (int)(rows[i] % num_q_heads);
         orc_decode_row(q, k_cache, v_cache, k_scale, v_scale, block_table,
                        max_blocks_per_seq, seq_lens, num_q_heads, num_kv_heads,
-                       head_dim, block_size, cache_is_fp8, scale, r, hq,
+                       head_dim, block_size, cache_kind, scale, r, hq,
                        out + i * head_dim, NULL, NULL);
     }
 }

@@ -12,20 +12,22 @@ import os
 import threading
 
 __all__ = [
-    "PkvError", "lib", "library_path", "BF16", "FP8_E4M3", "DEVERR_WAIT_TIMEOUT",
+    "PkvError", "lib", "library_path", "BF16", "FP8_E4M3", "INT8", "DEVERR_WAIT_TIMEOUT",
     "DEVERR_SEQ_CLAMPED", "DEVERR_BLOCK_RANGE", "compute_slot_mapping", "kv_cache_write",
     "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn",
     "paged_decode_attn_noalloc", "prefix_block_hash", "multiquery_workspace_size",
-    "paged_multiquery_attn", "DEVERR_QLEN_CLAMPED",
-    "device_num_sms", "read_device_error",
+    "paged_multiquery_attn", "DEVERR_QLEN_CLAMPED", "kv_cache_write_rescale",
+    "device_num_sms", "read_device_error", "copy_blocks", "BlockManager", "ERR_NO_BLOCKS",
 ]
 
 BF16 = 0
 FP8_E4M3 = 1
+INT8 = 2
 DEVERR_WAIT_TIMEOUT = 0x1
 DEVERR_SEQ_CLAMPED = 0x2
 DEVERR_BLOCK_RANGE = 0x4
 DEVERR_QLEN_CLAMPED = 0x8
+ERR_NO_BLOCKS = -5
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "lib", "libpagedkv.so")
@@ -72,11 +74,40 @@ def lib():
             L.pkv_paged_multiquery_attn.restype = i
             L.pkv_paged_multiquery_attn.argtypes = [p, p, i, p, p, p, p, p, i, p, i, i, i, i, i,
                                                     i, i, f, p, p, sz, p]
+            L.pkv_rescale_workspace_size.restype = sz
+            L.pkv_rescale_workspace_size.argtypes = [i, i]
+            L.pkv_kv_cache_write_rescale.restype = i
+            L.pkv_kv_cache_write_rescale.argtypes = [p, p, p, i, i, i, i, i, i, p, p, p, p, p, sz,
+                                                     p]
             L.pkv_paged_decode_attn_noalloc.restype = i
             L.pkv_paged_decode_attn_noalloc.argtypes = [p, p, p, p, p, p, i, p, i, i, i, i, i, i,
                                                         i, f, p, p]
             L.pkv_prefix_block_hash.restype = i
             L.pkv_prefix_block_hash.argtypes = [p, p, i, i, u64, p, p, p]
+            L.pkv_copy_blocks.restype = i
+            L.pkv_copy_blocks.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p]
+            L.pkv_bm_create.restype = i
+            L.pkv_bm_create.argtypes = [i, i, p]
+            L.pkv_bm_destroy.restype = None
+            L.pkv_bm_destroy.argtypes = [p]
+            L.pkv_bm_num_available.restype = i
+            L.pkv_bm_num_available.argtypes = [p]
+            L.pkv_bm_add_sequence.restype = i
+            L.pkv_bm_add_sequence.argtypes = [p, i64, i64, p, i, p, p]
+            L.pkv_bm_grow.restype = i
+            L.pkv_bm_grow.argtypes = [p, i64, i64, p]
+            L.pkv_bm_commit_block_hash.restype = i
+            L.pkv_bm_commit_block_hash.argtypes = [p, i64, i, u64]
+            L.pkv_bm_fork.restype = i
+            L.pkv_bm_fork.argtypes = [p, i64, i64]
+            L.pkv_bm_prepare_write.restype = i
+            L.pkv_bm_prepare_write.argtypes = [p, i64, i, p, p]
+            L.pkv_bm_free_sequence.restype = i
+            L.pkv_bm_free_sequence.argtypes = [p, i64]
+            L.pkv_bm_block_table.restype = i
+            L.pkv_bm_block_table.argtypes = [p, i64, p, i]
+            L.pkv_bm_refcount.restype = i
+            L.pkv_bm_refcount.argtypes = [p, i]
             _lib = L
     return _lib
 
@@ -109,6 +140,9 @@ def _need(t, name, dtypes, contiguous=True):
 
 
 def _cache_dtype(t):
+    import torch
+    if t.dtype == torch.int8:
+        return INT8
     return FP8_E4M3 if t.element_size() == 1 else BF16
 
 
@@ -147,6 +181,27 @@ def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=N
     _check("pkv_kv_cache_write", lib().pkv_kv_cache_write(
         _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, BS, NB, _cache_dtype(k_cache),
         _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _stream(stream)))
+
+
+def kv_cache_write_rescale(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                           workspace=None, stream=None):
+    """Write rows into 8-bit caches after setting each touched (block, head)'s scale to
+    amax/QMAX of the rows written to it here (k_scale / v_scale are updated)."""
+    import torch
+    _need(k, "k", (torch.bfloat16,))
+    _need(v, "v", (torch.bfloat16,))
+    _need(slot_mapping, "slot_mapping", (torch.int64,))
+    _need(k_scale, "k_scale", (torch.float32,))
+    _need(v_scale, "v_scale", (torch.float32,))
+    T, Hkv, D = k.shape
+    NB, _, BS, _ = k_cache.shape
+    n = int(lib().pkv_rescale_workspace_size(NB, Hkv))
+    if workspace is None:
+        workspace = torch.empty(n, dtype=torch.uint8, device=k.device)
+    _check("pkv_kv_cache_write_rescale", lib().pkv_kv_cache_write_rescale(
+        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, BS, NB, _cache_dtype(k_cache),
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(workspace),
+        workspace.numel(), _stream(stream)))
 
 
 def decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype,
@@ -267,3 +322,85 @@ def prefix_block_hash(tokens, offsets, block_size, hash_offsets, num_hashes, see
         _ptr(tokens), _ptr(offsets), offsets.shape[0] - 1, block_size,
         int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out), _ptr(hash_offsets), _stream(stream)))
     return out[:num_hashes]
+
+
+def copy_blocks(k_cache, v_cache, block_mapping, k_scale=None, v_scale=None, stream=None):
+    """Copy block block_mapping[i, 0] to block block_mapping[i, 1] in both caches (and their
+    scales for 8-bit caches); block_mapping is an int32 CUDA tensor [pairs, 2]."""
+    import torch
+    _need(k_cache, "k_cache", None)
+    _need(v_cache, "v_cache", None)
+    _need(block_mapping, "block_mapping", (torch.int32,))
+    NB, Hkv, BS, D = k_cache.shape
+    _check("pkv_copy_blocks", lib().pkv_copy_blocks(
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_mapping),
+        block_mapping.numel() // 2, Hkv, D, BS, NB, _cache_dtype(k_cache), _stream(stream)))
+
+
+class BlockManager:
+    """Host block manager of one cache pool (the pkv_bm_* calls): block tables built on
+    demand, prefix reuse by chained block hash, LRU eviction, copy-on-write.  Pure host
+    code; a failed call raises PkvError (status ERR_NO_BLOCKS when the pool is full)."""
+
+    def __init__(self, num_blocks: int, block_size: int):
+        self._h = ctypes.c_void_p()
+        self.block_size = block_size
+        _check("pkv_bm_create", lib().pkv_bm_create(num_blocks, block_size,
+                                                     ctypes.byref(self._h)))
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.pkv_bm_destroy(h)
+            self._h = None
+
+    def num_available(self) -> int:
+        n = lib().pkv_bm_num_available(self._h)
+        _check("pkv_bm_num_available", min(n, 0))
+        return n
+
+    def add_sequence(self, seq_id: int, num_tokens: int, block_hashes=()):
+        """Returns (block ids, number of leading blocks reused from the cache)."""
+        hs = [int(h) & 0xFFFFFFFFFFFFFFFF for h in block_hashes]
+        harr = (ctypes.c_uint64 * max(len(hs), 1))(*hs)
+        nb = -(-num_tokens // self.block_size) if num_tokens > 0 else 0
+        ids = (ctypes.c_int32 * max(nb, 1))()
+        hits = ctypes.c_int(0)
+        _check("pkv_bm_add_sequence", lib().pkv_bm_add_sequence(
+            self._h, seq_id, num_tokens, harr, len(hs), ids, ctypes.byref(hits)))
+        return list(ids[:nb]), hits.value
+
+    def grow(self, seq_id: int, num_tokens: int) -> int:
+        nb = ctypes.c_int32(-1)
+        _check("pkv_bm_grow", lib().pkv_bm_grow(self._h, seq_id, num_tokens, ctypes.byref(nb)))
+        return nb.value
+
+    def commit_block_hash(self, seq_id: int, logical_block: int, block_hash: int) -> None:
+        _check("pkv_bm_commit_block_hash", lib().pkv_bm_commit_block_hash(
+            self._h, seq_id, logical_block, int(block_hash) & 0xFFFFFFFFFFFFFFFF))
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        _check("pkv_bm_fork", lib().pkv_bm_fork(self._h, parent_id, child_id))
+
+    def prepare_write(self, seq_id: int, logical_block: int):
+        """(source, destination) of the copy to make before writing, or (-1, -1)."""
+        src, dst = ctypes.c_int32(-1), ctypes.c_int32(-1)
+        _check("pkv_bm_prepare_write", lib().pkv_bm_prepare_write(
+            self._h, seq_id, logical_block, ctypes.byref(src), ctypes.byref(dst)))
+        return src.value, dst.value
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check("pkv_bm_free_sequence", lib().pkv_bm_free_sequence(self._h, seq_id))
+
+    def block_table(self, seq_id: int):
+        n = lib().pkv_bm_block_table(self._h, seq_id, None, 0)
+        _check("pkv_bm_block_table", min(n, 0))
+        ids = (ctypes.c_int32 * max(n, 1))()
+        n = lib().pkv_bm_block_table(self._h, seq_id, ids, n)
+        _check("pkv_bm_block_table", min(n, 0))
+        return list(ids[:n])
+
+    def refcount(self, block: int) -> int:
+        n = lib().pkv_bm_refcount(self._h, block)
+        _check("pkv_bm_refcount", min(n, 0))
+        return n

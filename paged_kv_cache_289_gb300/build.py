@@ -1,6 +1,7 @@
 """Build libpagedkv.so in-tree with nvcc for sm_103a (GB300).
 
-Each .cu under csrc/ is compiled to an object in parallel, then linked into
+Each .cu (device code) and .cpp (host-only code) under csrc/ is compiled to an
+object in parallel by nvcc, then linked into
 paged_kv_cache_289_gb300/lib/libpagedkv.so (CUDA runtime linked statically).
 Objects are rebuilt when their source or any header is newer.
 """
@@ -37,12 +38,12 @@ def _headers():
 
 def build(force: bool = False, verbose_ptxas: bool = False, jobs: int | None = None) -> str:
     os.makedirs(LIBDIR, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     hdr_mtime = max([os.path.getmtime(h) for h in _headers()] + [0])
     objs = []
     todo = []
     for s in srcs:
-        o = os.path.join(LIBDIR, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(LIBDIR, os.path.splitext(os.path.basename(s))[0] + ".o")
         objs.append(o)
         if force or verbose_ptxas or not os.path.exists(o) or \
                 os.path.getmtime(o) < max(os.path.getmtime(s), hdr_mtime):

@@ -16,7 +16,7 @@ bool shape_supported(int Hq, int Hkv, int D, int BS, int dtype) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > pkv::kGroupPad) return false;
     if (BS != 16 && BS != 32) return false;
     if (dtype == PKV_BF16) return D == 64 || D == 128;
-    if (dtype == PKV_FP8_E4M3) return D == 128;
+    if (dtype == PKV_FP8_E4M3 || dtype == PKV_INT8) return D == 128;
     return false;
 }
 
@@ -41,6 +41,7 @@ const char* pkv_status_string(int status) {
         case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED";
         case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
         case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+        case PKV_ERR_NO_BLOCKS: return "PKV_ERR_NO_BLOCKS";
         default: return "PKV_UNKNOWN_STATUS";
     }
 }
@@ -71,16 +72,47 @@ int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
-    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8)
+        return PKV_ERR_UNSUPPORTED;
     if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PKV_OK;
     if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PKV_ERR_INVALID_ARG;
-    if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+    if (cache_dtype != PKV_BF16 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
     if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PKV_ERR_INVALID_ARG;
     cudaError_t e = pkv::cache_write_launch(
         k, v, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, num_blocks,
-        cache_dtype == PKV_FP8_E4M3, k_cache, v_cache, k_scale, v_scale,
+        cache_dtype, k_cache, v_cache, k_scale, v_scale,
+        reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_rescale_workspace_size(int num_blocks, int num_kv_heads) {
+    if (num_blocks <= 0 || num_kv_heads <= 0) return 0;
+    return (size_t)2 * num_blocks * num_kv_heads * 4;
+}
+
+int pkv_kv_cache_write_rescale(const void* k, const void* v, const int64_t* slot_mapping,
+                               int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                               int num_blocks, int cache_dtype, void* k_cache, void* v_cache,
+                               float* k_scale, float* v_scale, void* workspace,
+                               size_t workspace_bytes, pkv_stream_t stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
+    if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PKV_OK;
+    if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PKV_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < pkv_rescale_workspace_size(num_blocks, num_kv_heads))
+        return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 4)) return PKV_ERR_INVALID_ARG;
+    cudaError_t e = pkv::cache_write_rescale_launch(
+        k, v, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, num_blocks,
+        cache_dtype, k_cache, v_cache, k_scale, v_scale, workspace,
         reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
@@ -92,7 +124,7 @@ size_t pkv_multiquery_workspace_size(int batch, int num_q_heads, int num_kv_head
     if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype)) return 0;
     if (num_sms <= 0 && current_num_sms(&num_sms) != PKV_OK) return 0;
     return pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
-                                       cache_dtype == PKV_FP8_E4M3, num_sms, max_q_len);
+                                       cache_dtype != PKV_BF16, num_sms, max_q_len);
 }
 
 size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
@@ -110,16 +142,17 @@ int pkv_paged_multiquery_attn(const void* q, const int32_t* q_offsets, int max_q
                               void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
     if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_q_len < 1)
         return PKV_ERR_INVALID_ARG;
-    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3) return PKV_ERR_UNSUPPORTED;
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8)
+        return PKV_ERR_UNSUPPORTED;
     if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype))
         return PKV_ERR_UNSUPPORTED;
-    if (pkv::query_tile(cache_dtype == PKV_FP8_E4M3, max_q_len) == 0) return PKV_ERR_UNSUPPORTED;
+    if (pkv::query_tile(cache_dtype != PKV_BF16, max_q_len) == 0) return PKV_ERR_UNSUPPORTED;
     if (batch > pkv::kMaxBatch) return PKV_ERR_UNSUPPORTED;
     if (batch == 0) return PKV_OK;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
         return PKV_ERR_INVALID_ARG;
     if (max_q_len > 1 && !q_offsets) return PKV_ERR_INVALID_ARG;
-    if (cache_dtype == PKV_FP8_E4M3 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+    if (cache_dtype != PKV_BF16 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
         return PKV_ERR_INVALID_ARG;
     // flat page index and TMA row coordinates are int32
@@ -131,7 +164,7 @@ int pkv_paged_multiquery_attn(const void* q, const int32_t* q_offsets, int max_q
     int num_sms = 0;
     if (current_num_sms(&num_sms) != PKV_OK) return PKV_ERR_CUDA;
     const size_t need = pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
-                                                    cache_dtype == PKV_FP8_E4M3, num_sms,
+                                                    cache_dtype != PKV_BF16, num_sms,
                                                     max_q_len);
     if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
@@ -154,7 +187,8 @@ int pkv_paged_multiquery_attn(const void* q, const int32_t* q_offsets, int max_q
     L.BS = block_size;
     L.MB = max_blocks_per_seq;
     L.NB = num_blocks;
-    L.fp8 = cache_dtype == PKV_FP8_E4M3;
+    L.fp8 = cache_dtype != PKV_BF16;
+    L.kt = cache_dtype;
     L.scale = scale;
     L.num_sms = num_sms;
     return pkv::decode_launch(L, reinterpret_cast<cudaStream_t>(stream));
@@ -181,6 +215,33 @@ int pkv_prefix_block_hash(const int32_t* tokens, const int64_t* offsets, int num
     if (!tokens || !offsets || !hashes || !hash_offsets) return PKV_ERR_INVALID_ARG;
     cudaError_t e = pkv::prefix_hash_launch(tokens, offsets, num_seqs, block_size, seed, hashes,
                                             hash_offsets, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                    const int32_t* block_mapping, int num_pairs, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int cache_dtype, pkv_stream_t stream) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
+        num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8)
+        return PKV_ERR_UNSUPPORTED;
+    const int64_t elt = cache_dtype == PKV_BF16 ? 2 : 1;
+    const int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_dim * elt;
+    if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
+    if (num_pairs == 0) return PKV_OK;
+    if (!k_cache || !v_cache || !block_mapping) return PKV_ERR_INVALID_ARG;
+    if (cache_dtype != PKV_BF16 && (!k_scale || !v_scale)) return PKV_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(block_mapping, 4))
+        return PKV_ERR_INVALID_ARG;
+    int sms = 0;
+    const int st = current_num_sms(&sms);
+    if (st != PKV_OK) return st;
+    const bool q8 = cache_dtype != PKV_BF16;
+    cudaError_t e = pkv::copy_blocks_launch(k_cache, v_cache, q8 ? k_scale : nullptr,
+                                            q8 ? v_scale : nullptr, block_mapping, num_pairs,
+                                            block_bytes, num_blocks, num_kv_heads, sms,
+                                            reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

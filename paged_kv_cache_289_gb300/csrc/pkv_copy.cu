@@ -1,0 +1,73 @@
+// pkv_copy.cu -- copy whole blocks inside the cache pool (copy-on-write).
+//
+// "深入LLM推理：从KV Cache到PD分离的Serving全景解析", PagedAttention与Cache管理:
+// physical blocks are shared between sequences; the sequence about to change a
+// shared block first gets a private copy of it.
+//
+// A block of the pool is Hkv pages of BS*D elements, contiguous in [NB][Hkv][BS][D],
+// so one block of one cache is a single contiguous run of Hkv*BS*D*elt bytes (32 KB
+// for 8 KV heads x 16 tokens x 128 bf16).  The copy is HBM-bound: every byte is read
+// once and written once.  Work item = (pair, cache, 16 KB chunk); each thread keeps
+// four 16-byte loads in flight before it stores them, the grid holds up to eight
+// 256-thread CTAs per SM and strides over the items.
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+namespace {
+constexpr int kCopyThreads = 256;
+constexpr int kCopyUnroll = 4;
+constexpr int kChunkVec = kCopyThreads * kCopyUnroll;   // 16-byte vectors per item (16 KB)
+}  // namespace
+
+__global__ void __launch_bounds__(kCopyThreads)
+    pkv_copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                           float* __restrict__ k_scale, float* __restrict__ v_scale,
+                           const int32_t* __restrict__ mapping, int64_t vec_per_block,
+                           int chunks, int64_t items, int NB, int Hkv) {
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t pair = it / (2 * chunks);
+        const int rem = (int)(it - pair * 2 * chunks);
+        const int part = rem / chunks;            // 0 = K, 1 = V
+        const int chunk = rem - part * chunks;
+        const int src = mapping[2 * pair];
+        const int dst = mapping[2 * pair + 1];
+        if (src < 0 || src >= NB || dst < 0 || dst >= NB || src == dst) continue;
+        uint4* base = part ? v_cache : k_cache;
+        const int64_t off = (int64_t)chunk * kChunkVec;
+        const uint4* s = base + (int64_t)src * vec_per_block + off;
+        uint4* d = base + (int64_t)dst * vec_per_block + off;
+        const int n = (int)min((int64_t)kChunkVec, vec_per_block - off);
+        if (n == kChunkVec) {
+            uint4 r[kCopyUnroll];
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) r[u] = __ldcs(s + threadIdx.x + u * kCopyThreads);
+#pragma unroll
+            for (int u = 0; u < kCopyUnroll; ++u) __stcs(d + threadIdx.x + u * kCopyThreads, r[u]);
+        } else {
+            for (int i = threadIdx.x; i < n; i += kCopyThreads) __stcs(d + i, __ldcs(s + i));
+        }
+        if (k_scale != nullptr && chunk == 0) {
+            float* sc = part ? v_scale : k_scale;
+            for (int h = threadIdx.x; h < Hkv; h += kCopyThreads)
+                sc[(int64_t)dst * Hkv + h] = sc[(int64_t)src * Hkv + h];
+        }
+    }
+}
+
+cudaError_t copy_blocks_launch(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                               const int32_t* mapping, int pairs, int64_t block_bytes, int NB,
+                               int Hkv, int num_sms, cudaStream_t st) {
+    const int64_t vec = block_bytes / 16;
+    const int chunks = (int)((vec + kChunkVec - 1) / kChunkVec);
+    const int64_t items = (int64_t)pairs * 2 * chunks;
+    const int64_t cap = (int64_t)num_sms * 8;
+    const unsigned grid = (unsigned)(items < cap ? items : cap);
+    return launch_pdl(pkv_copy_blocks_kernel, dim3(grid), dim3(kCopyThreads), 0, st,
+                      reinterpret_cast<uint4*>(k_cache), reinterpret_cast<uint4*>(v_cache),
+                      k_scale, v_scale, mapping, vec, chunks, items, NB, Hkv);
+}
+
+}  // namespace pkv

@@ -38,9 +38,10 @@
 //                                     B = Q^T of the GQA group (8 heads, registers)
 //   O^T[d][g] += V^T[d][t] P^T[t][g]  A = V tile (ldmatrix.trans), B = P^T from
 //                                     the S^T accumulators via movmatrix.trans
-// FP8 (E4M3) pages are widened to fp16 in registers (cvt e4m3x2 -> f16x2); the
-// per-(block, head) K scale multiplies S, the V scale multiplies the page's P.V
-// contribution, so neither scale is rounded into an fp16 operand.
+// 8-bit pages (E4M3 or int8) are widened exactly to fp16 in registers (cvt
+// e4m3x2 -> f16x2, or an exact int8 -> fp16 construction); the per-(block, head)
+// K scale multiplies S, the V scale multiplies the page's P.V contribution, so
+// neither scale is rounded into an fp16 operand.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -256,10 +257,11 @@ __device__ __noinline__ void merge_unit(const float* partials, uint16_t* out, in
     }
 }
 
-template <int D, int BS, bool FP8, int QT>
-__global__ void __launch_bounds__((FP8 || QT > 1) ? 256 : 384, 1)
+template <int D, int BS, int KT, int QT>
+__global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
     pkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
+    constexpr bool FP8 = KT != 0;   // 8-bit pages (E4M3 or int8) with per-(block, head) scales
     using C = Cfg<D, BS, FP8>;
     extern __shared__ uint8_t smem_raw[];
     const int NW = blockDim.x >> 5;
@@ -531,8 +533,10 @@ __global__ void __launch_bounds__((FP8 || QT > 1) ? 256 : 384, 1)
                     ldsm_x4(kpg + swz<C::TT>(t, 2 * ks2 + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
                     for (int qi = 0; qi < QT; ++qi) {
-                        if (ks2 & 1) mma_bf16(e1[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
-                        else         mma_bf16(e0[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
+                        // two accumulator chains give the single-query case its ILP; with
+                        // several query tiles the tiles themselves are independent
+                        if (QT == 1 && (ks2 & 1)) mma_bf16(e1[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
+                        else                      mma_bf16(e0[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
                     }
                 }
             } else {
@@ -540,14 +544,26 @@ __global__ void __launch_bounds__((FP8 || QT > 1) ? 256 : 384, 1)
                 for (int kp = 0; kp < C::KS / 2; ++kp) {
                     uint32_t r0, r1, r2, r3;
                     ldsm_x4(kpg + swz<C::TT>(t, 2 * kp + (lane >> 4)), r0, r1, r2, r3);
-                    const uint32_t k00 = e4m3x2_to_f16x2(r0), k01 = e4m3x2_to_f16x2(r1);
-                    const uint32_t k02 = e4m3x2_to_f16x2(r0 >> 16), k03 = e4m3x2_to_f16x2(r1 >> 16);
-                    const uint32_t k10 = e4m3x2_to_f16x2(r2), k11 = e4m3x2_to_f16x2(r3);
-                    const uint32_t k12 = e4m3x2_to_f16x2(r2 >> 16), k13 = e4m3x2_to_f16x2(r3 >> 16);
+                    uint32_t k00, k01, k02, k03, k10, k11, k12, k13;
+                    if constexpr (KT == 2) {
+                        // int8: one sign flip per register, then gather + widen per pair
+                        const uint32_t s0 = r0 ^ 0x80808080u, s1 = r1 ^ 0x80808080u;
+                        const uint32_t s2 = r2 ^ 0x80808080u, s3 = r3 ^ 0x80808080u;
+                        k00 = i8pick_to_f16x2<0x5140>(s0); k02 = i8pick_to_f16x2<0x7362>(s0);
+                        k01 = i8pick_to_f16x2<0x5140>(s1); k03 = i8pick_to_f16x2<0x7362>(s1);
+                        k10 = i8pick_to_f16x2<0x5140>(s2); k12 = i8pick_to_f16x2<0x7362>(s2);
+                        k11 = i8pick_to_f16x2<0x5140>(s3); k13 = i8pick_to_f16x2<0x7362>(s3);
+                    } else {
+                        k00 = b8x2_to_f16x2<KT>(r0); k01 = b8x2_to_f16x2<KT>(r1);
+                        k02 = b8x2_to_f16x2<KT>(r0 >> 16); k03 = b8x2_to_f16x2<KT>(r1 >> 16);
+                        k10 = b8x2_to_f16x2<KT>(r2); k11 = b8x2_to_f16x2<KT>(r3);
+                        k12 = b8x2_to_f16x2<KT>(r2 >> 16); k13 = b8x2_to_f16x2<KT>(r3 >> 16);
+                    }
 #pragma unroll
                     for (int qi = 0; qi < QT; ++qi) {
                         mma_f16(e0[qi], k00, k01, k02, k03, qf[2 * kp][qi][0], qf[2 * kp][qi][1]);
-                        mma_f16(e1[qi], k10, k11, k12, k13, qf[2 * kp + 1][qi][0], qf[2 * kp + 1][qi][1]);
+                        mma_f16(QT == 1 ? e1[qi] : e0[qi], k10, k11, k12, k13, qf[2 * kp + 1][qi][0],
+                                qf[2 * kp + 1][qi][1]);
                     }
                 }
             }
@@ -668,10 +684,20 @@ __global__ void __launch_bounds__((FP8 || QT > 1) ? 256 : 384, 1)
                     for (int half = 0; half < 2; ++half) {
                         const uint32_t x = movmatrix_trans(half ? r2 : r0);   // tokens 0-7
                         const uint32_t y = movmatrix_trans(half ? r3 : r1);   // tokens 8-15
-                        const uint32_t v0 = e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0020));
-                        const uint32_t v1 = e4m3x2_to_f16x2(__byte_perm(x, 0u, 0x0031));
-                        const uint32_t v2 = e4m3x2_to_f16x2(__byte_perm(y, 0u, 0x0020));
-                        const uint32_t v3 = e4m3x2_to_f16x2(__byte_perm(y, 0u, 0x0031));
+                        uint32_t v0, v1, v2, v3;
+                        if constexpr (KT == 2) {
+                            // int8: the token regroup and the widening are one permute
+                            const uint32_t xs = x ^ 0x80808080u, ys = y ^ 0x80808080u;
+                            v0 = i8pick_to_f16x2<0x5240>(xs);
+                            v1 = i8pick_to_f16x2<0x5341>(xs);
+                            v2 = i8pick_to_f16x2<0x5240>(ys);
+                            v3 = i8pick_to_f16x2<0x5341>(ys);
+                        } else {
+                            v0 = b8x2_to_f16x2<KT>(__byte_perm(x, 0u, 0x0020));
+                            v1 = b8x2_to_f16x2<KT>(__byte_perm(x, 0u, 0x0031));
+                            v2 = b8x2_to_f16x2<KT>(__byte_perm(y, 0u, 0x0020));
+                            v3 = b8x2_to_f16x2<KT>(__byte_perm(y, 0u, 0x0031));
+                        }
 #pragma unroll
                         for (int qi = 0; qi < QT; ++qi)
                             mma_f16(ot[2 * dp + half][qi], v0, v1, v2, v3, pb[mt][qi][0],
@@ -934,10 +960,10 @@ DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int b
     return p;
 }
 
-template <int D, int BS, bool FP8, int QT>
+template <int D, int BS, int KT, int QT>
 static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const CUtensorMap& tk,
                             const CUtensorMap& tv, const DecodeArgs& args, cudaStream_t st) {
-    auto kern = pkv_decode_kernel<D, BS, FP8, QT>;
+    auto kern = pkv_decode_kernel<D, BS, KT, QT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          plan.smem_bytes);
     if (e != cudaSuccess) return e;
@@ -950,14 +976,14 @@ static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const
                       dim3(kGroupPad * 32), 0, st, args);
 }
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, int KT>
 static cudaError_t launch_q(int qt, const DecodeLaunch& L, const DecodePlan& plan,
                             const CUtensorMap& tk, const CUtensorMap& tv, const DecodeArgs& args,
                             cudaStream_t st) {
-    if (qt == 1) return launch_t<D, BS, FP8, 1>(L, plan, tk, tv, args, st);
-    if (qt == 2) return launch_t<D, BS, FP8, 2>(L, plan, tk, tv, args, st);
-    if constexpr (!FP8) {
-        if (qt == 4) return launch_t<D, BS, FP8, 4>(L, plan, tk, tv, args, st);
+    if (qt == 1) return launch_t<D, BS, KT, 1>(L, plan, tk, tv, args, st);
+    if (qt == 2) return launch_t<D, BS, KT, 2>(L, plan, tk, tv, args, st);
+    if constexpr (KT == 0) {
+        if (qt == 4) return launch_t<D, BS, KT, 4>(L, plan, tk, tv, args, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -1013,15 +1039,19 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     a.total_warps = plan.total_warps;
     a.epoch = next_epoch();
     cudaError_t e = cudaErrorInvalidValue;
-    if (!L.fp8) {
-        if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, false>(qt, L, plan, tk, tv, a, st);
-        else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, false>(qt, L, plan, tk, tv, a, st);
-        else if (L.D == 64 && L.BS == 16) e = launch_q<64, 16, false>(qt, L, plan, tk, tv, a, st);
-        else if (L.D == 64 && L.BS == 32) e = launch_q<64, 32, false>(qt, L, plan, tk, tv, a, st);
+    if (L.kt == 0) {
+        if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, 0>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, 0>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 64 && L.BS == 16) e = launch_q<64, 16, 0>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 64 && L.BS == 32) e = launch_q<64, 32, 0>(qt, L, plan, tk, tv, a, st);
+        else return PKV_ERR_UNSUPPORTED;
+    } else if (L.kt == 1) {
+        if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, 1>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, 1>(qt, L, plan, tk, tv, a, st);
         else return PKV_ERR_UNSUPPORTED;
     } else {
-        if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, true>(qt, L, plan, tk, tv, a, st);
-        else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, true>(qt, L, plan, tk, tv, a, st);
+        if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, 2>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, 2>(qt, L, plan, tk, tv, a, st);
         else return PKV_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

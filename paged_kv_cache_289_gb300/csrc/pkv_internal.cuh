@@ -67,7 +67,8 @@ struct DecodeLaunch {
     const int32_t* seq_lens;
     void* out;
     void* workspace;
-    int N, Hq, Hkv, D, BS, MB, NB, fp8;
+    int N, Hq, Hkv, D, BS, MB, NB, fp8;   // fp8: any 8-bit page kind (E4M3 or int8)
+    int kt;                               // page kind: 0 bf16, 1 E4M3, 2 int8
     float scale;
     int num_sms;
 };
@@ -81,12 +82,19 @@ cudaError_t slot_mapping_launch(const int32_t* block_table, int MB, const int32_
                                 const int32_t* positions, int T, int BS, int64_t* out,
                                 cudaStream_t st);
 cudaError_t cache_write_launch(const void* k, const void* v, const int64_t* slots, int T,
-                               int Hkv, int D, int BS, int NB, int fp8, void* k_cache,
+                               int Hkv, int D, int BS, int NB, int kt, void* k_cache,
                                void* v_cache, const float* k_scale, const float* v_scale,
                                cudaStream_t st);
+cudaError_t cache_write_rescale_launch(const void* k, const void* v, const int64_t* slots, int T,
+                                       int Hkv, int D, int BS, int NB, int kt, void* k_cache,
+                                       void* v_cache, float* k_scale, float* v_scale,
+                                       void* workspace, cudaStream_t st);
 cudaError_t prefix_hash_launch(const int32_t* tokens, const int64_t* offsets, int num_seqs, int B,
                                uint64_t seed, uint64_t* hashes, const int64_t* hash_offsets,
                                cudaStream_t st);
+cudaError_t copy_blocks_launch(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                               const int32_t* mapping, int pairs, int64_t block_bytes, int NB,
+                               int Hkv, int num_sms, cudaStream_t st);
 
 // Launch `kern` as a programmatic dependent of the previous kernel in `st`: its CTAs
 // may be dispatched while that kernel finishes, and the kernel itself calls
@@ -256,6 +264,34 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
         : "=r"(y)
         : "r"(x));
     return y;
+}
+
+// Two int8 (low 16 bits of x, low byte first) -> fp16x2, exactly.  fp16 holds
+// 1024 + k exactly for integers 0 <= k < 1024 (exponent of 1024, k in the
+// mantissa), so q + 128 is placed under that exponent and 1152 subtracted.
+__device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t x) {
+    const uint32_t y = __byte_perm(x ^ 0x8080u, 0x64646464u, 0x5140);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(0x64806480u));
+    return r;
+}
+
+// Two int8 codes picked from the 4 bytes of x by a byte-permute selector `sel`
+// (low pair first) -> fp16x2; `xs` is x with its sign bits already flipped
+// (x ^ 0x80808080), so the permute both gathers and widens.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t i8pick_to_f16x2(uint32_t xs) {
+    const uint32_t y = __byte_perm(xs, 0x64646464u, SEL);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(0x64806480u));
+    return r;
+}
+
+// Two 8-bit cache codes -> fp16x2 for page kind KT (1 = E4M3, 2 = int8).
+template <int KT>
+__device__ __forceinline__ uint32_t b8x2_to_f16x2(uint32_t x) {
+    if constexpr (KT == 2) return i8x2_to_f16x2(x);
+    else return e4m3x2_to_f16x2(x);
 }
 
 // Two fp32 -> E4M3x2 with round-to-nearest-even and saturation to +-448;

@@ -31,6 +31,7 @@ import numpy as np
 VOCAB_SMALL = 32000
 VOCAB = 128000
 E4M3_MAX = 448.0
+INT8_MAX = 127.0
 
 
 @dataclass
@@ -52,7 +53,27 @@ class Workload:
     token_offsets: np.ndarray     # int64 [N + 1]
     hash_block: int = 16
     q_len: int = 1                # new query tokens per request (speculative verify: > 1)
+    int8: bool = False            # int8 pages (symmetric, scale = amax/127)
     notes: dict = field(default_factory=dict)
+
+    @property
+    def quant(self) -> bool:
+        """8-bit pages with one fp32 scale per (block, kv head) (E4M3 or int8)."""
+        return self.fp8 or self.int8
+
+    @property
+    def kv_kind(self) -> int:
+        """0: bf16 pages, 1: E4M3, 2: int8."""
+        return 2 if self.int8 else (1 if self.fp8 else 0)
+
+    @property
+    def qmax(self) -> float:
+        """Largest code magnitude of the 8-bit kind (the scale recipe divides amax by it)."""
+        return INT8_MAX if self.int8 else E4M3_MAX
+
+    @property
+    def cache_np_dtype(self):
+        return np.int8 if self.int8 else (np.uint8 if self.fp8 else np.uint16)
 
     @property
     def G(self) -> int:
@@ -68,7 +89,7 @@ class Workload:
 
     @property
     def elt(self) -> int:
-        return 1 if self.fp8 else 2
+        return 1 if self.quant else 2
 
     def blocks_of(self, r: int) -> np.ndarray:
         nb = -(-int(self.seq_lens[r]) // self.BS)
@@ -223,6 +244,14 @@ def make(cfg: int, seed: int | None = None, small: bool = False,
         toks, offs = _tokens(rng, seq, VOCAB)
         return Workload("fp8_at_scale" + ("_small" if small else ""), 5, seed, N, Hq, Hkv, D, BS,
                         NB, True, 1.0 / math.sqrt(D), seq, bt, toks, offs)
+    if cfg == 7:
+        # int8 pages at scale: workload 5's requests with symmetric int8 codes
+        wl = make(5, seed=seed, small=small, batch=batch)
+        wl.name = "int8_at_scale" + ("_small" if small else "")
+        wl.cfg = 7
+        wl.fp8 = False
+        wl.int8 = True
+        return wl
     if cfg == 6:
         # speculative verify on the 70B-shaped layer: 4 new tokens per request
         # (3 drafted + 1), all checked in one attention pass
@@ -235,7 +264,7 @@ def make(cfg: int, seed: int | None = None, small: bool = False,
 
 
 def custom(N, Hq, Hkv, D, BS, seq_lens, fp8=False, seed=0, slack=1.1, scale=None, name="custom",
-           q_len=1):
+           q_len=1, int8=False):
     """A workload with explicit lengths (edge cases: empty, ragged, one-token requests)."""
     rng = np.random.default_rng(seed)
     seq = np.asarray(seq_lens, dtype=np.int32)
@@ -243,7 +272,7 @@ def custom(N, Hq, Hkv, D, BS, seq_lens, fp8=False, seed=0, slack=1.1, scale=None
     toks, offs = _tokens(rng, seq, VOCAB)
     sc = 1.0 / math.sqrt(D) if scale is None else scale
     return Workload(name, 0, seed, N, Hq, Hkv, D, BS, NB, fp8, sc, seq, bt, toks, offs,
-                    q_len=q_len)
+                    q_len=q_len, int8=int8)
 
 
 # ----------------------------------------------------------------------------
@@ -273,8 +302,9 @@ def token_rows_order(wl: Workload):
 
 
 def fp8_scales_from_rows(wl: Workload, k_rows_bits: np.ndarray, v_rows_bits: np.ndarray):
-    """Workload-5 recipe: one fp32 scale per (physical block, kv head) = amax/448 of the
-    source values of the block's tokens (1.0 for an all-zero or unused block)."""
+    """Workloads 5 and 7: one fp32 scale per (physical block, kv head) = amax/448 (E4M3) or
+    amax/127 (int8) of the source values of the block's tokens (1.0 for an all-zero or
+    unused block)."""
     ks = np.ones((wl.NB, wl.Hkv), dtype=np.float32)
     vs = np.ones((wl.NB, wl.Hkv), dtype=np.float32)
     kf = np.abs(bf16_bits_to_f32(k_rows_bits)).max(axis=2)  # [T, Hkv]
@@ -286,8 +316,8 @@ def fp8_scales_from_rows(wl: Workload, k_rows_bits: np.ndarray, v_rows_bits: np.
             lo, hi = o + j * wl.BS, o + min(S, (j + 1) * wl.BS)
             ka = np.float32(kf[lo:hi].max(axis=0)) if hi > lo else np.zeros(wl.Hkv, np.float32)
             va = np.float32(vf[lo:hi].max(axis=0)) if hi > lo else np.zeros(wl.Hkv, np.float32)
-            ks[b] = np.where(ka > 0, ka / np.float32(E4M3_MAX), np.float32(1.0))
-            vs[b] = np.where(va > 0, va / np.float32(E4M3_MAX), np.float32(1.0))
+            ks[b] = np.where(ka > 0, ka / np.float32(wl.qmax), np.float32(1.0))
+            vs[b] = np.where(va > 0, va / np.float32(wl.qmax), np.float32(1.0))
         o += S
     return ks, vs
 
@@ -304,7 +334,7 @@ def host_data(wl: Workload, seed_offset: int = 1000) -> dict:
     step's new token of each request, written at position seq_len - 1)."""
     rng = np.random.default_rng(wl.seed + seed_offset)
     d = {"q": _randn_bf16(rng, (wl.N * wl.q_len, wl.Hq, wl.D))}
-    if not wl.fp8:
+    if not wl.quant:
         d["k_cache"] = _randn_bf16(rng, (wl.NB, wl.Hkv, wl.BS, wl.D))
         d["v_cache"] = _randn_bf16(rng, (wl.NB, wl.Hkv, wl.BS, wl.D))
     else:
@@ -328,7 +358,7 @@ def device_data(wl: Workload, device, seed_offset: int = 2000) -> dict:
     g.manual_seed(wl.seed + seed_offset)
     bf = torch.bfloat16
     d = {"q": torch.randn((wl.N * wl.q_len, wl.Hq, wl.D), generator=g, device=device, dtype=bf)}
-    if not wl.fp8:
+    if not wl.quant:
         d["k_cache"] = torch.randn((wl.NB, wl.Hkv, wl.BS, wl.D), generator=g, device=device,
                                    dtype=bf)
         d["v_cache"] = torch.randn((wl.NB, wl.Hkv, wl.BS, wl.D), generator=g, device=device,
@@ -357,10 +387,44 @@ def device_data(wl: Workload, device, seed_offset: int = 2000) -> dict:
             amax_rows = d[key].abs().amax(dim=2).float()            # [T, Hkv]
             amax = torch.zeros((s_id, wl.Hkv), dtype=torch.float32, device=device)
             amax.scatter_reduce_(0, seg_t[:, None].expand(T, wl.Hkv), amax_rows, "amax")
-            sc = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+            sc = torch.where(amax > 0, amax / wl.qmax, torch.ones_like(amax))
             full = torch.ones((wl.NB, wl.Hkv), dtype=torch.float32, device=device)
             full[phys_t] = sc
             d[skey] = full
     d["k_new"] = torch.randn((wl.N * wl.q_len, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
     d["v_new"] = torch.randn((wl.N * wl.q_len, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
     return d
+
+
+def beam_case(seed: int = 31, BS: int = 16, Hq: int = 32, Hkv: int = 8, D: int = 128,
+              families: int = 2, prefix_blocks: int = 4, requests: int = 6, NB: int = 128,
+              vocab: int = 32000) -> dict:
+    """Inputs of a block-sharing scenario: `requests` prompts, request r opening with the
+    system prompt of family r % families (prefix_blocks full blocks, identical tokens and
+    identical K/V rows across the family) followed by a private tail; requests 0 and 1
+    each fork two beams (sequence ids 100 + 2r and 101 + 2r); then every live sequence
+    appends one new token.  Tails of requests 0 and 1 end inside a block, so their beams
+    share a partial block.  Everything is drawn from one seeded generator; bf16 values
+    are N(0, 1) bit patterns (uint16)."""
+    rng = np.random.default_rng(seed)
+    P = prefix_blocks * BS
+    fam_tok = rng.integers(0, vocab, size=(families, P), dtype=np.int32)
+    fam_k = _randn_bf16(rng, (families, P, Hkv, D))
+    fam_v = _randn_bf16(rng, (families, P, Hkv, D))
+    tails = rng.integers(5, 40, size=requests)
+    tails[0], tails[1] = 7, BS + 3
+    prompts, k_rows, v_rows = [], [], []
+    for r in range(requests):
+        f = r % families
+        t = int(tails[r])
+        prompts.append(np.concatenate([fam_tok[f], rng.integers(0, vocab, size=t,
+                                                                dtype=np.int32)]))
+        k_rows.append(np.concatenate([fam_k[f], _randn_bf16(rng, (t, Hkv, D))]))
+        v_rows.append(np.concatenate([fam_v[f], _randn_bf16(rng, (t, Hkv, D))]))
+    forks = [(0, 100), (0, 101), (1, 102), (1, 103)]
+    live = list(range(requests)) + [c for _, c in forks]
+    n = len(live)
+    return {"BS": BS, "Hq": Hq, "Hkv": Hkv, "D": D, "NB": NB, "prompts": prompts,
+            "k_rows": k_rows, "v_rows": v_rows, "forks": forks, "live": live,
+            "q": _randn_bf16(rng, (n, Hq, D)), "k_new": _randn_bf16(rng, (n, Hkv, D)),
+            "v_new": _randn_bf16(rng, (n, Hkv, D)), "scale": 1.0 / float(np.sqrt(D))}

@@ -13,6 +13,15 @@ BF16_REL_L2 = 5e-3
 FP8_MAX_ABS = 5e-2
 
 
+def torch_cache_dtype(wl):
+    torch = torch_mod()
+    return torch.int8 if wl.int8 else (torch.uint8 if wl.fp8 else torch.bfloat16)
+
+
+def pkv_kind(wl):
+    return wl.kv_kind
+
+
 def torch_mod():
     import torch
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
@@ -33,8 +42,11 @@ def bf16_dev(bits):
 
 
 def dev_bits(t):
-    """Device tensor -> numpy bit patterns (uint16 for 2-byte, uint8 for 1-byte)."""
+    """Device tensor -> numpy bit patterns (uint16 for 2-byte, int8 for int8, uint8 for
+    other 1-byte tensors)."""
     torch = torch_mod()
+    if t.dtype == torch.int8:
+        return t.contiguous().cpu().numpy()
     if t.element_size() == 2:
         return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
     return t.contiguous().view(torch.uint8).cpu().numpy()
@@ -68,12 +80,12 @@ class HostCase:
     def __init__(self, wl, seed_offset=1000):
         self.wl = wl
         self.d = W.host_data(wl, seed_offset)
-        if wl.fp8:
+        if wl.quant:
             # each side quantises the source rows with its own write
             req, pos = W.token_rows_order(wl)
             self.req_all, self.pos_all = req, pos
             slots = oracle.slot_mapping(wl.block_table, req, pos, wl.BS)
-            self.kc = np.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), np.uint8)
+            self.kc = np.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), wl.cache_np_dtype)
             self.vc = np.zeros_like(self.kc)
             oracle.kv_cache_write(self.d["k_rows"], self.d["v_rows"], slots, self.kc, self.vc,
                                   self.d["k_scale"], self.d["v_scale"])

@@ -7,7 +7,7 @@ import pytest
 import oracle
 import paged_kv_cache_289_gb300 as pkv
 from paged_kv_cache_289_gb300 import workloads as W
-from helpers import compare, dev_bits, out_to_f64, torch_mod
+from helpers import compare, dev_bits, out_to_f64, torch_cache_dtype, torch_mod
 
 pytestmark = pytest.mark.gpu
 
@@ -45,15 +45,15 @@ def _compact(wl, reqs):
     return bt, np.array(old, np.int64)
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5, 7])
 def test_fullsize_decode_step_sampled(cfg):
     torch = torch_mod()
     wl = W.make(cfg)
     dd = W.device_data(wl, "cuda")
     bt = torch.from_numpy(wl.block_table).cuda()
     sl = torch.from_numpy(wl.seq_lens).cuda()
-    if wl.fp8:
-        kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch.uint8, device="cuda")
+    if wl.quant:
+        kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch_cache_dtype(wl), device="cuda")
         vc = torch.zeros_like(kc)
         req, pos = W.token_rows_order(wl)
         slots_all = pkv.compute_slot_mapping(bt, torch.from_numpy(pos).cuda(), wl.BS,
@@ -77,7 +77,7 @@ def test_fullsize_decode_step_sampled(cfg):
     slots = pkv.compute_slot_mapping(bt, pos_new, wl.BS)
     pkv.kv_cache_write(dd["k_new"], dd["v_new"], slots, kc, vc, ks, vs)
     ws = pkv.alloc_decode_workspace(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS,
-                                    pkv.FP8_E4M3 if wl.fp8 else pkv.BF16)
+                                    wl.kv_kind)
     out = pkv.paged_decode_attn(dd["q"], kc, vc, bt, sl, wl.scale, k_scale=ks, v_scale=vs,
                                 workspace=ws)
     torch.cuda.synchronize()
@@ -91,7 +91,7 @@ def test_fullsize_decode_step_sampled(cfg):
     newpos = (sl_s.astype(np.int64) - 1).astype(np.int32)
     k_new_s = dev_bits(dd["k_new"][torch.tensor(reqs).cuda()])
     v_new_s = dev_bits(dd["v_new"][torch.tensor(reqs).cuda()])
-    if not wl.fp8:
+    if not wl.quant:
         # the oracle applies the step's write to the pre-step pages itself
         kc_o, vc_o = kc_pre.copy(), vc_pre.copy()
         sm = oracle.slot_mapping(cbt, np.arange(len(reqs), dtype=np.int32), newpos, wl.BS)
@@ -125,4 +125,4 @@ def test_fullsize_decode_step_sampled(cfg):
                           np.int64)
     ref = oracle.decode_rows(q_s, kc_o, vc_o, cbt, sl_s, wl.scale, local_rows, ks_s, vs_s)
     got = out_to_f64(out).reshape(wl.N * wl.Hq, wl.D)[rows]
-    compare(got, ref, wl.fp8)
+    compare(got, ref, wl.quant)

@@ -7,7 +7,8 @@ import pytest
 import oracle
 import paged_kv_cache_289_gb300 as pkv
 from paged_kv_cache_289_gb300 import workloads as W
-from helpers import HostCase, bf16_dev, compare, dev_bits, out_to_f64, to_dev, torch_mod
+from helpers import (HostCase, bf16_dev, compare, dev_bits, out_to_f64, to_dev, torch_mod,
+                     torch_cache_dtype)
 
 pytestmark = pytest.mark.gpu
 
@@ -22,9 +23,9 @@ def _built():
 def _device_caches(case):
     torch = torch_mod()
     wl = case.wl
-    if not wl.fp8:
+    if not wl.quant:
         return bf16_dev(case.d["k_cache"]), bf16_dev(case.d["v_cache"]), None, None
-    kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch.uint8, device="cuda")
+    kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch_cache_dtype(wl), device="cuda")
     vc = torch.zeros_like(kc)
     ks, vs = to_dev(case.d["k_scale"]), to_dev(case.d["v_scale"])
     slots = pkv.compute_slot_mapping(to_dev(wl.block_table), to_dev(case.pos_all), wl.BS,
@@ -42,7 +43,7 @@ def _gpu_step(case, kc, vc, ks, vs, q_offsets=None, max_q_len=None):
     pkv.kv_cache_write(bf16_dev(case.d["k_new"]), bf16_dev(case.d["v_new"]), slots, kc, vc, ks, vs)
     qo = wl.q_offsets() if q_offsets is None else q_offsets
     mq = wl.q_len if max_q_len is None else max_q_len
-    dt = pkv.FP8_E4M3 if wl.fp8 else pkv.BF16
+    dt = wl.kv_kind
     torch = torch_mod()
     ws = torch.zeros(pkv.multiquery_workspace_size(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, dt, mq),
                      dtype=torch.uint8, device="cuda")
@@ -64,11 +65,11 @@ def test_spec_verify_step_small():
     assert pkv.read_device_error(ws) == 0
 
 
-@pytest.mark.parametrize("G,D,BS,fp8,qmax", [(8, 128, 16, False, 4), (8, 128, 32, False, 2),
-                                             (4, 64, 16, False, 4), (1, 64, 32, False, 4),
-                                             (8, 128, 32, True, 2), (4, 128, 16, True, 2),
-                                             (3, 128, 16, False, 3)])
-def test_multiquery_shapes_variable_qlen(G, D, BS, fp8, qmax):
+@pytest.mark.parametrize("G,D,BS,kind,qmax", [(8, 128, 16, "bf16", 4), (8, 128, 32, "bf16", 2),
+                                              (4, 64, 16, "bf16", 4), (1, 64, 32, "bf16", 4),
+                                              (8, 128, 32, "fp8", 2), (4, 128, 16, "fp8", 2),
+                                              (8, 128, 32, "int8", 2), (3, 128, 16, "bf16", 3)])
+def test_multiquery_shapes_variable_qlen(G, D, BS, kind, qmax):
     """Every supported shape; each request has its own q_len in 1..qmax; short requests
     have fewer tokens than queries (their first queries see nothing: zero rows)."""
     rng = np.random.default_rng(G * 1000 + D + BS + qmax)
@@ -76,14 +77,16 @@ def test_multiquery_shapes_variable_qlen(G, D, BS, fp8, qmax):
     lens = [1, 2, BS - 1, BS, BS + 1, 3 * BS + 5, 700, 37]
     qlens = [int(rng.integers(1, qmax + 1)) for _ in lens]
     qlens[0], qlens[1] = qmax, qmax          # q_len > seq_len for the 1- and 2-token requests
-    wl = W.custom(len(lens), G * Hkv, Hkv, D, BS, lens, fp8=fp8, seed=G + D + BS)
+    fp8 = kind != "bf16"
+    wl = W.custom(len(lens), G * Hkv, Hkv, D, BS, lens, fp8=kind == "fp8", int8=kind == "int8",
+                  seed=G + D + BS)
     qoffs = np.zeros(len(lens) + 1, np.int32)
     np.cumsum(qlens, out=qoffs[1:])
     case = HostCase(wl)
     q = W.f32_to_bf16_bits(rng.standard_normal((int(qoffs[-1]), wl.Hq, D)).astype(np.float32))
     kc, vc, ks, vs = _device_caches(case)
     torch = torch_mod()
-    dt = pkv.FP8_E4M3 if fp8 else pkv.BF16
+    dt = wl.kv_kind
     ws = torch.zeros(pkv.multiquery_workspace_size(wl.N, wl.Hq, Hkv, D, BS, dt, qmax),
                      dtype=torch.uint8, device="cuda")
     out = pkv.paged_multiquery_attn(bf16_dev(q), to_dev(qoffs), qmax, kc, vc,

@@ -9,7 +9,8 @@ import pytest
 import oracle
 import paged_kv_cache_289_gb300 as pkv
 from paged_kv_cache_289_gb300 import workloads as W
-from helpers import (HostCase, bf16_dev, compare, dev_bits, out_to_f64, to_dev, torch_mod)
+from helpers import (HostCase, bf16_dev, compare, dev_bits, out_to_f64, to_dev, torch_mod,
+                     torch_cache_dtype)
 
 pytestmark = pytest.mark.gpu
 
@@ -24,9 +25,9 @@ def _built():
 def _device_caches(case):
     torch = torch_mod()
     wl = case.wl
-    if not wl.fp8:
+    if not wl.quant:
         return bf16_dev(case.d["k_cache"]), bf16_dev(case.d["v_cache"]), None, None
-    kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch.uint8, device="cuda")
+    kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch_cache_dtype(wl), device="cuda")
     vc = torch.zeros_like(kc)
     ks = to_dev(case.d["k_scale"])
     vs = to_dev(case.d["v_scale"])
@@ -47,13 +48,13 @@ def _gpu_step(case, kc, vc, ks, vs):
     slots = pkv.compute_slot_mapping(bt, to_dev(wl.new_token_positions()), wl.BS)
     pkv.kv_cache_write(bf16_dev(case.d["k_new"]), bf16_dev(case.d["v_new"]), slots, kc, vc, ks, vs)
     ws = pkv.alloc_decode_workspace(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS,
-                                    pkv.FP8_E4M3 if wl.fp8 else pkv.BF16)
+                                    wl.kv_kind)
     out = pkv.paged_decode_attn(bf16_dev(case.d["q"]), kc, vc, bt, sl, wl.scale, k_scale=ks,
                                 v_scale=vs, workspace=ws)
     return slots, out, ws
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 7])
 def test_decode_step_small(cfg):
     """Workloads 1..5 at oracle-friendly sizes: slots and cache bytes bit-exact,
     attention within tolerance, device error word clear."""
@@ -65,19 +66,22 @@ def test_decode_step_small(cfg):
     assert np.array_equal(slots_d.cpu().numpy(), slots_o)
     assert np.array_equal(dev_bits(kc), case.kc)
     assert np.array_equal(dev_bits(vc), case.vc)
-    compare(out_to_f64(out_d), out_o, wl.fp8)
+    compare(out_to_f64(out_d), out_o, wl.quant)
     assert pkv.read_device_error(ws) == 0
 
 
-@pytest.mark.parametrize("G,D,BS,fp8", [(1, 64, 16, False), (2, 128, 32, False),
-                                        (4, 128, 16, False), (8, 64, 32, False),
-                                        (3, 128, 16, False), (1, 128, 32, True),
-                                        (4, 128, 16, True), (8, 128, 32, True)])
-def test_decode_shapes_ragged(G, D, BS, fp8):
+@pytest.mark.parametrize("G,D,BS,kind", [(1, 64, 16, "bf16"), (2, 128, 32, "bf16"),
+                                         (4, 128, 16, "bf16"), (8, 64, 32, "bf16"),
+                                         (3, 128, 16, "bf16"), (1, 128, 32, "fp8"),
+                                         (4, 128, 16, "fp8"), (8, 128, 32, "fp8"),
+                                         (8, 128, 32, "int8"), (2, 128, 16, "int8")])
+def test_decode_shapes_ragged(G, D, BS, kind):
     """Every supported shape on ragged lengths: 1 token, BS-1, BS, BS+1, long tails."""
     Hkv = 2
     lens = [1, BS - 1, BS, BS + 1, 7 * BS + 3, 1000, 37]
-    wl = W.custom(len(lens), G * Hkv, Hkv, D, BS, lens, fp8=fp8, seed=G * 100 + D + BS)
+    fp8 = kind != "bf16"
+    wl = W.custom(len(lens), G * Hkv, Hkv, D, BS, lens, fp8=kind == "fp8", int8=kind == "int8",
+                  seed=G * 100 + D + BS)
     case = HostCase(wl)
     kc, vc, ks, vs = _device_caches(case)
     _, out_d, ws = _gpu_step(case, kc, vc, ks, vs)
@@ -221,6 +225,27 @@ def test_fp8_write_exhaustive_bf16_patterns():
             nan_got = (got & 0x7F) == 0x7F
             assert np.array_equal(nan_ref, nan_got)
             assert np.array_equal(got[~nan_ref], ref[~nan_ref])
+
+
+def test_int8_write_exhaustive_bf16_patterns():
+    """Every bf16 bit pattern through the int8 write with scale 1 and random scales:
+    the library's bytes equal the oracle's."""
+    torch = torch_mod()
+    bits = np.arange(65536, dtype=np.uint16).reshape(512, 1, 128)
+    T, BS, NB = 512, 16, 32
+    slots = np.arange(T, dtype=np.int64)
+    rng = np.random.default_rng(3)
+    for scales in (np.ones((NB, 1), np.float32),
+                   rng.uniform(0.001, 3.0, (NB, 1)).astype(np.float32)):
+        kc_o = np.zeros((NB, 1, BS, 128), np.int8)
+        vc_o = np.zeros_like(kc_o)
+        oracle.kv_cache_write(bits, bits[::-1].copy(), slots, kc_o, vc_o, scales, scales)
+        kc = torch.zeros((NB, 1, BS, 128), dtype=torch.int8, device="cuda")
+        vc = torch.zeros_like(kc)
+        pkv.kv_cache_write(bf16_dev(bits), bf16_dev(bits[::-1].copy()), to_dev(slots), kc, vc,
+                           to_dev(scales), to_dev(scales))
+        assert np.array_equal(dev_bits(kc), kc_o)
+        assert np.array_equal(dev_bits(vc), vc_o)
 
 
 def test_slot_mapping_padding_and_req_idx():

@@ -478,3 +478,69 @@ def test_multiquery_single_query_is_decode_and_empty_rows_are_zero():
     got = oracle.multiquery_attn(q, np.array([0, 5], np.int32), d["k_cache"], d["v_cache"],
                                  wl.block_table[:1], lens, wl.scale)
     assert np.all(got[:2] == 0) and np.all(np.any(got[2:] != 0, axis=-1))
+
+
+# ---------------------------------------------------------------- int8 pages
+def test_int8_encode_matches_torch_round_half_even_and_clamp():
+    rng = np.random.default_rng(5)
+    xs = np.concatenate([rng.standard_normal(4000).astype(np.float32) * 60,
+                         np.float32([k + 0.5 for k in range(-130, 130)]),   # exact ties
+                         np.float32([126.5, 127.5, -127.5, -128.0, 1e9, -1e9, 0.0, -0.0])])
+    ref = torch.clamp(torch.round(torch.from_numpy(xs)), -127, 127).to(torch.int8).numpy()
+    got = np.array([oracle.int8_from_float(float(x)) for x in xs], np.int8)
+    assert np.array_equal(got, ref)
+    assert oracle.int8_from_float(float("nan")) == 0
+
+
+def test_int8_write_and_decode_use_code_times_scale():
+    wl = W.make(7, small=True)
+    d = W.host_data(wl)
+    req, pos = W.token_rows_order(wl)
+    slots = oracle.slot_mapping(wl.block_table, req, pos, wl.BS)
+    kc = np.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), np.int8)
+    vc = np.zeros_like(kc)
+    oracle.kv_cache_write(d["k_rows"], d["v_rows"], slots, kc, vc, d["k_scale"], d["v_scale"])
+    x = W.bf16_bits_to_f32(d["k_rows"]).astype(np.float64)
+    b, o = slots // wl.BS, slots % wl.BS
+    codes = kc[b, :, o].astype(np.float64)
+    s = d["k_scale"][b].astype(np.float64)[:, :, None]
+    # half a step, plus the one binary32 rounding of the quotient x / s
+    assert np.all(np.abs(codes * s - x) <= 0.5 * s * (1 + 1e-6) + np.abs(x) * 2.0 ** -23)
+    assert np.abs(codes).max() == 127                                 # amax/127 scaling
+    rows = np.array([0, 3 * wl.Hq + 10], np.int64)
+    got = oracle.decode_rows(d["q"], kc, vc, wl.block_table, wl.seq_lens, wl.scale, rows,
+                             d["k_scale"], d["v_scale"])
+    for i, row in enumerate(rows):
+        r, hq = divmod(int(row), wl.Hq)
+        h = hq // wl.G
+        blocks = wl.blocks_of(r)
+        S = int(wl.seq_lens[r])
+        Kd = np.concatenate([kc[bb, h].astype(np.float64) * float(d["k_scale"][bb, h]) for bb in blocks])[:S]
+        Vd = np.concatenate([vc[bb, h].astype(np.float64) * float(d["v_scale"][bb, h]) for bb in blocks])[:S]
+        qv = W.bf16_bits_to_f32(d["q"][r, hq]).astype(np.float64)
+        p = scipy.special.softmax(wl.scale * (Kd @ qv))
+        np.testing.assert_allclose(got[i], p @ Vd, atol=1e-12)
+
+
+@pytest.mark.parametrize("cfg", [5, 7])
+def test_rescale_write_scales_equal_the_amax_recipe(cfg):
+    """Writing every token of a workload in one rescaling call gives each used block the
+    scale amax/QMAX of its rows: the same numbers as the generator's independent numpy
+    recipe; blocks nobody writes keep their scale."""
+    wl = W.make(cfg, small=True)
+    d = W.host_data(wl)
+    req, pos = W.token_rows_order(wl)
+    slots = oracle.slot_mapping(wl.block_table, req, pos, wl.BS)
+    kc = np.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), wl.cache_np_dtype)
+    vc = np.zeros_like(kc)
+    ks = np.full((wl.NB, wl.Hkv), 123.0, np.float32)
+    vs = np.full((wl.NB, wl.Hkv), 123.0, np.float32)
+    oracle.kv_cache_write_rescale(d["k_rows"], d["v_rows"], slots, kc, vc, ks, vs)
+    used = np.zeros(wl.NB, bool)
+    used[np.unique(slots // wl.BS)] = True
+    assert np.array_equal(ks[used], d["k_scale"][used])
+    assert np.array_equal(vs[used], d["v_scale"][used])
+    assert np.all(ks[~used] == 123.0) and np.all(vs[~used] == 123.0)
+    kc2, vc2 = np.zeros_like(kc), np.zeros_like(vc)
+    oracle.kv_cache_write(d["k_rows"], d["v_rows"], slots, kc2, vc2, d["k_scale"], d["v_scale"])
+    assert np.array_equal(kc, kc2) and np.array_equal(vc, vc2)

@@ -33,7 +33,7 @@ def _inputs(cfg):
     wl = W.make(cfg, small=True)
     d = W.host_data(wl)
     bt, sl = to_dev(wl.block_table), to_dev(wl.seq_lens)
-    if wl.fp8:
+    if wl.quant:
         kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch.uint8, device="cuda")
         vc = torch.zeros_like(kc)
         ks, vs = to_dev(d["k_scale"]), to_dev(d["v_scale"])
@@ -56,7 +56,7 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(cfg):
         pkv.paged_decode_attn_noalloc(q, kc, vc, bt, sl, wl.scale, out=out, k_scale=ks,
                                       v_scale=vs)
         torch.cuda.synchronize()
-        compare(out_to_f64(out), ref64, wl.fp8)
+        compare(out_to_f64(out), ref64, wl.quant)
         # same kernels, same launch plan: the bits agree as well
         assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
 

@@ -49,8 +49,9 @@ def parse():
     p.add_argument("--seed", type=int, default=None)
     p.add_argument("--batch", type=int, default=None,
                    help="fewer requests of the same shapes (profiling captures only)")
-    p.add_argument("--op", choices=["step", "copy_blocks"], default="step",
-                   help="copy_blocks: time the copy-on-write block copy alone")
+    p.add_argument("--op", choices=["step", "copy_blocks", "prefill"], default="step",
+                   help="copy_blocks: the copy-on-write block copy alone; prefill: paged "
+                        "prefill attention on workload 8")
     p.add_argument("--pairs", type=int, default=4096, help="block pairs per copy_blocks launch")
     return p.parse_args()
 
@@ -571,6 +572,103 @@ def run_copy_blocks(args):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ prefill attention
+def run_prefill(args):
+    """pkv_paged_prefill_attn on workload 8: 8 requests, each a 2048-token prompt chunk
+    after a cached context of U[0, 6144] tokens, Llama-3.3-70B layer shape (64/8 heads,
+    head_dim 128, bf16, 16-token blocks).  Metric: causal-effective attention TFLOP/s."""
+    import torch
+    import oracle
+    import paged_kv_cache_289_gb300 as pkv
+    from paged_kv_cache_289_gb300 import workloads as W
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = W.make(8, batch=args.batch)
+    dd = W.device_data(wl, dev)
+    qo = torch.from_numpy(wl.q_offsets()).to(dev)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    sl = torch.from_numpy(wl.seq_lens).to(dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty_like(dd["q"])
+    main = torch.cuda.current_stream(dev)
+
+    def launch():
+        pkv.paged_prefill_attn(dd["q"], qo, wl.max_q_len, dd["k_cache"], dd["v_cache"], bt, sl,
+                               wl.scale, out=out, error_word=err, stream=main)
+
+    K, Wm = args.steps, max(args.warmup, 3)
+    for _ in range(Wm):
+        launch()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    sampler = ClockSampler(0)
+    sampler.start()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(main)
+    for k in range(K):
+        ev[k][0].record(main)
+        launch()
+        ev[k][1].record(main)
+    e1.record(main)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    assert int(err.item()) == 0, "device error word set during the benchmark"
+    t = e0.elapsed_time(e1) / 1e3
+    avg = sum(a.elapsed_time(b) for a, b in ev) / K / 1e3
+    flops = wl.prefill_flops()
+    peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        peak, peak_kind = float(pk["bf16_tflops"]), "measured bf16_tflops (cuBLAS burst)"
+    except Exception:
+        peak, peak_kind = 1900.0, "fallback bf16 burst"
+    achieved = flops / avg / 1e12
+    # oracle: sampled rows of the same workload on the host cores, about 10 s
+    q = dd["q"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    kc = dd["k_cache"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    vc = dd["v_cache"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    rng = np.random.default_rng(1)
+    qo_np = wl.q_offsets()
+    ql = wl.query_lens
+    tot_t, tot_f, n_rows = 0.0, 0, 0
+    while tot_t < 10.0:
+        rows = rng.integers(0, wl.total_q * wl.Hq, size=64).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.multiquery_rows(q, qo_np, kc, vc, wl.block_table, wl.seq_lens, wl.scale, rows)
+        tot_t += time.perf_counter() - t0
+        for row in rows:
+            tq_ = int(row) // wl.Hq
+            r = int(np.searchsorted(qo_np, tq_, side="right")) - 1
+            vis = int(wl.seq_lens[r]) - int(ql[r]) + (tq_ - int(qo_np[r])) + 1
+            tot_f += max(0, min(vis, int(wl.seq_lens[r]))) * 4 * wl.D
+        n_rows += rows.shape[0]
+    cpu = {"value": round(tot_f / tot_t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+           "kind": "oracle", "sample": f"{n_rows} random (token, head) rows of {wl.name} "
+                                       f"({tot_f/1e9:.1f} GFLOP in {tot_t:.1f} s), fp64 C + OpenMP"}
+    line = {"metric": "paged prefill attention: causal-effective TFLOP/s (bf16 tensor cores)",
+            "value": round(flops * K / t / 1e12, 2), "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": K, "warmup": Wm, "ms_per_step": round(t / K * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) q/K/V)",
+            "config": {"workload": wl.name, "batch": wl.N, "num_q_heads": wl.Hq,
+                       "num_kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.BS,
+                       "chunk_tokens": int(ql.max()), "context": "U[0, 6144] cached tokens",
+                       "flops_per_launch": flops,
+                       "l2": "pages %.0f MB + q/out %.0f MB; no flush (compute-bound)" % (
+                           2 * wl.NB * wl.Hkv * wl.BS * wl.D * 2 / 1e6,
+                           2 * wl.total_q * wl.Hq * wl.D * 2 / 1e6)},
+            "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_source": peak_kind, "kernel": "pkv_prefill_kernel",
+                         "flops_per_launch": flops, "avg_launch_ms": round(avg * 1e3, 4)},
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": K, "clocks": clocks}
+    print(json.dumps(line), flush=True)
+
+
 # ------------------------------------------------------------------ reference arm
 def run_reference(args):
     rank, world, local = dist_setup(args.gpus)
@@ -628,6 +726,8 @@ def main():
         run_reference(args)
     elif args.op == "copy_blocks":
         run_copy_blocks(args)
+    elif args.op == "prefill":
+        run_prefill(args)
     else:
         run_ours(args)
 

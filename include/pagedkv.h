@@ -265,6 +265,32 @@ PKV_API int pkv_prefix_block_hash(const int32_t *tokens, const int64_t *offsets,
                           const int64_t *hash_offsets, pkv_stream_t stream);
 
 /*
+ * Paged prefill attention ([P1] "推理的两阶段计算形态": prefill processes every prompt
+ * token at once and is compute-bound; "KV Cache：Transformer的循环状态": causal
+ * attention; "PagedAttention与Cache管理": the block table).  A chunk of new tokens per
+ * request, their K/V already written to the pages (pkv_kv_cache_write): request r's
+ * query rows are q[q_offsets[r] .. q_offsets[r+1]) (q_len_r rows, int32 q_offsets
+ * [batch + 1], q_offsets[batch] <= total_q); row i is the token at position
+ * seq_lens[r] - q_len_r + i and attends to positions 0 .. seq_lens[r] - q_len_r + i.
+ * A row that sees no token is zero.  Same result as pkv_paged_multiquery_attn, any
+ * q_len.  max_q_len bounds every q_len_r: rows past it are not computed and
+ * PKV_DEVERR_QLEN_CLAMPED is set; a request whose rows run past total_q is skipped
+ * and flagged the same way.  Runs on the tcgen05 tensor cores: one CTA per 128 query rows
+ * (128/G tokens x the G heads of a KV head).
+ *   q, out          bf16 [total_q][Hq][D], 16-byte aligned; rows of no request untouched
+ *   k/v_cache       bf16 pages [NB][Hkv][BS][D]
+ *   error_word      device uint32 collecting PKV_DEVERR_* bits (sticky), or NULL
+ * Supported: bf16 pages, head_dim 64 or 128, block_size 16 or 32, G in {1, 2, 4, 8};
+ * other shapes return PKV_ERR_UNSUPPORTED.  No workspace. */
+PKV_API int pkv_paged_prefill_attn(const void *q, const int32_t *q_offsets, int total_q,
+                                   int max_q_len, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_table, int max_blocks_per_seq,
+                                   const int32_t *seq_lens, int batch, int num_q_heads,
+                                   int num_kv_heads, int head_dim, int block_size,
+                                   int num_blocks, int cache_dtype, float scale, void *out,
+                                   uint32_t *error_word, pkv_stream_t stream);
+
+/*
  * Copy whole blocks inside the cache pool, for copy-on-write of a shared block
  * ([P1] "PagedAttention与Cache管理": physical blocks are shared between
  * sequences, and a sequence that must change a shared block gets its own copy

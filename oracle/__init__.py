@@ -97,6 +97,9 @@ def lib():
             L.orc_multiquery_attn.restype = None
             L.orc_multiquery_attn.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i,
                                               _i, _i, _i, _d, _p]
+            L.orc_multiquery_rows.restype = None
+            L.orc_multiquery_rows.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i,
+                                              _i, _i, _i, _d, _p, _i64, _p]
             L.orc_num_threads.restype = _i
             L.orc_num_threads.argtypes = []
             L.orc_fnv1a64.restype = _u64
@@ -231,6 +234,22 @@ def multiquery_attn(q, q_offsets, k_cache, v_cache, block_table, seq_lens, scale
     lib().orc_multiquery_attn(_ptr(q), _ptr(qo), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt),
                               bt.shape[1], _ptr(sl), qo.shape[0] - 1, Hq, Hkv, D, BS, int(kind),
                               float(scale), _ptr(out))
+    return out
+
+
+def multiquery_rows(q, q_offsets, k_cache, v_cache, block_table, seq_lens, scale, rows,
+                    k_scale=None, v_scale=None):
+    """fp64 rows of multiquery_attn for selected rows (row = query token * Hq + hq)."""
+    q, kc, vc, ks, vs, bt, sl, kind = _decode_args(q, k_cache, v_cache, block_table, seq_lens,
+                                                  k_scale, v_scale)
+    qo = _c(q_offsets, np.int32)
+    T, Hq, D = q.shape
+    Hkv, BS = kc.shape[1], kc.shape[2]
+    rows = _c(rows, np.int64)
+    out = np.empty((rows.shape[0], D), dtype=np.float64)
+    lib().orc_multiquery_rows(_ptr(q), _ptr(qo), _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs),
+                              _ptr(bt), bt.shape[1], _ptr(sl), qo.shape[0] - 1, Hq, Hkv, D, BS,
+                              int(kind), float(scale), _ptr(rows), rows.shape[0], _ptr(out))
     return out
 
 

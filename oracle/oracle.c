@@ -391,6 +391,40 @@ void orc_multiquery_attn(const uint16_t *q, const int32_t *q_offsets, const void
     }
 }
 
+/* Selected rows of orc_multiquery_attn: rows[i] = tq * Hq + hq for query token tq
+ * (an index into q's T rows) and query head hq; out [count][D] doubles.  Each row
+ * is computed exactly as in orc_multiquery_attn (the same visible prefix and the
+ * same single-row attention); used where the whole output is too large to compute
+ * on the host (long prefill chunks). */
+void orc_multiquery_rows(const uint16_t *q, const int32_t *q_offsets, const void *k_cache,
+                         const void *v_cache, const float *k_scale, const float *v_scale,
+                         const int32_t *block_table, int max_blocks_per_seq,
+                         const int32_t *seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                         int head_dim, int block_size, int cache_kind, double scale,
+                         const int64_t *rows, int64_t count, double *out)
+{
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t i = 0; i < count; ++i) {
+        int64_t tq = rows[i] / num_q_heads;
+        int hq = (int)(rows[i] % num_q_heads);
+        int r = 0;
+        while (r < batch - 1 && q_offsets[r + 1] <= tq)
+            ++r;
+        int q_len = q_offsets[r + 1] - q_offsets[r];
+        int qi = (int)(tq - q_offsets[r]);
+        int visible = seq_lens[r] - q_len + qi + 1;
+        if (visible < 0)
+            visible = 0;
+        if (visible > seq_lens[r])
+            visible = seq_lens[r];
+        int32_t len1 = visible;
+        orc_decode_row(q + tq * num_q_heads * head_dim, k_cache, v_cache, k_scale, v_scale,
+                       block_table + (int64_t)r * max_blocks_per_seq, max_blocks_per_seq, &len1,
+                       num_q_heads, num_kv_heads, head_dim, block_size, cache_kind, scale, 0, hq,
+                       out + i * head_dim, NULL, NULL);
+    }
+}
+
 /* All rows of a batch: out [N][Hq][D] doubles.  Rows are independent, so they
  * are spread over threads; each row is computed exactly as above. */
 void orc_paged_decode_attn(const uint16_t *q, const void *k_cache, const void *v_cache,

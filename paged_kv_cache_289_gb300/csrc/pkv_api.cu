@@ -218,6 +218,47 @@ int pkv_prefix_block_hash(const int32_t* tokens, const int64_t* offsets, int num
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+int pkv_paged_prefill_attn(const void* q, const int32_t* q_offsets, int total_q, int max_q_len,
+                           const void* k_cache, const void* v_cache,
+                           const int32_t* block_table, int max_blocks_per_seq,
+                           const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                           int head_dim, int block_size, int num_blocks, int cache_dtype,
+                           float scale, void* out, uint32_t* error_word, pkv_stream_t stream) {
+    if (batch < 0 || total_q < 0 || max_q_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
+        return PKV_ERR_INVALID_ARG;
+    if (!pkv::prefill_shape_supported(num_q_heads, num_kv_heads, head_dim, block_size,
+                                      cache_dtype))
+        return PKV_ERR_UNSUPPORTED;
+    if (batch == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
+    if ((int64_t)(num_blocks + 1) * num_kv_heads * block_size >= ((int64_t)1 << 31))
+        return PKV_ERR_UNSUPPORTED;
+    if (!q || !q_offsets || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(error_word, 4))
+        return PKV_ERR_INVALID_ARG;
+    pkv::PrefillLaunch L;
+    L.q = q;
+    L.q_offsets = q_offsets;
+    L.k_cache = k_cache;
+    L.v_cache = v_cache;
+    L.block_table = block_table;
+    L.seq_lens = seq_lens;
+    L.out = out;
+    L.err = error_word;
+    L.total_q = total_q;
+    L.max_q_len = max_q_len;
+    L.N = batch;
+    L.Hq = num_q_heads;
+    L.Hkv = num_kv_heads;
+    L.D = head_dim;
+    L.BS = block_size;
+    L.MB = max_blocks_per_seq;
+    L.NB = num_blocks;
+    L.scale = scale;
+    return pkv::prefill_launch(L, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int pkv_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                     const int32_t* block_mapping, int num_pairs, int num_kv_heads, int head_dim,
                     int block_size, int num_blocks, int cache_dtype, pkv_stream_t stream) {

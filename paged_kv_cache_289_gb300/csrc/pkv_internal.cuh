@@ -92,6 +92,20 @@ cudaError_t cache_write_rescale_launch(const void* k, const void* v, const int64
 cudaError_t prefix_hash_launch(const int32_t* tokens, const int64_t* offsets, int num_seqs, int B,
                                uint64_t seed, uint64_t* hashes, const int64_t* hash_offsets,
                                cudaStream_t st);
+struct PrefillLaunch {
+    const void* q;
+    const int32_t* q_offsets;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    void* out;
+    uint32_t* err;                     // device error word, may be null
+    int total_q, max_q_len, N, Hq, Hkv, D, BS, MB, NB;
+    float scale;
+};
+bool prefill_shape_supported(int Hq, int Hkv, int D, int BS, int dtype);
+int prefill_launch(const PrefillLaunch& L, cudaStream_t st);
 cudaError_t copy_blocks_launch(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                                const int32_t* mapping, int pairs, int64_t block_bytes, int NB,
                                int Hkv, int num_sms, cudaStream_t st);

@@ -1,0 +1,611 @@
+// pkv_prefill.cu -- paged prefill attention on the 5th-generation tensor cores.
+//
+// Prefill is the compute-bound phase: every prompt token is a query
+// ("深入LLM推理：从KV Cache到PD分离的Serving全景解析", 推理的两阶段计算形态).  A chunk of
+// q_len new tokens of request r (positions ctx .. ctx + q_len - 1, ctx = seq_len - q_len,
+// their K/V already written to the pages) attends causally to the request's paged
+// cache: query i sees positions 0 .. ctx + i ("KV Cache：Transformer的循环状态",
+// causal mask; "PagedAttention与Cache管理", block table).
+//
+// One CTA = one 128-row query tile of one (request, KV head): 128 / G query tokens x
+// the G query heads of the group, so every K/V tile staged in shared memory serves
+// the whole GQA group.  Per 128-token KV tile:
+//   S = Q K^T      tcgen05.mma, M = 128, N = 128, K = D; A and B K-major in shared
+//                  memory (128-byte swizzle, TMA), D in tensor memory (two S buffers)
+//   softmax        4 warps, one TMEM lane (= one query row) per thread: online max and
+//                  sum in the log2 domain, P rounded to bf16 into tensor memory
+//   O += P V       tcgen05.mma with A = P read from tensor memory and B = V, MN-major
+//                  (the page rows are tokens, d contiguous)
+// Warp roles: warps 0-3 softmax + epilogue, warp 4 TMA producer (and TMEM owner),
+// warp 5 MMA issuer.  K/V tiles are double-buffered; S is double-buffered so the
+// next tile's Q K^T runs while this tile's softmax does.  Every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "pkv_internal.cuh"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kRows = 128;        // query rows per tile (TMEM lanes)
+constexpr int kKvTile = 128;      // tokens per K/V tile
+constexpr int kThreads = 192;     // 6 warps
+constexpr uint64_t kWaitNs = 2000000000ull;
+constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384, kTmemCols = 512;
+
+// ------------------------------------------------------------ tcgen05 wrappers
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: start, leading / stride byte offsets (16-byte
+// units), descriptor version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B, A K-major,
+// B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                       uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's lane.  The load and its wait sit in
+// one asm statement, so no use of the outputs can be scheduled before the wait.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
+        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
+        "r"(w[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+        "f"(v[15]), "f"(v[16]), "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]),
+        "f"(v[22]), "f"(v[23]), "f"(v[24]), "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]),
+        "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void flag_err(uint32_t* err, uint32_t bits) {
+    if (err != nullptr) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+}  // namespace
+
+struct PrefillArgs {
+    const int32_t* q_offsets;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    uint16_t* out;
+    uint32_t* err;
+    int N, Hq, Hkv, MB, NB, total_q, max_q_len, tiles;
+    float scale_log2;
+};
+
+// Shared memory: Q [KB][128 rows][128 B] | K stages [2][KB][128][128 B] |
+// V stages [2][KB][128][128 B]; 1024-byte aligned (128-byte swizzle atoms).
+template <int D>
+struct PrefillSmem {
+    static constexpr int KB = D / 64;
+    static constexpr int TILE = KB * kRows * 128;   // bytes of one 128-row operand tile
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = TILE;
+    static constexpr int V_OFF = 3 * TILE;
+    static constexpr int BYTES = 5 * TILE;
+    static constexpr int ALLOC = BYTES + 1024;
+};
+
+template <int D, int BS, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    pkv_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, const PrefillArgs a) {
+    using SM = PrefillSmem<D>;
+    constexpr int KB = SM::KB;
+    constexpr int TQ = kRows / G;            // query tokens per tile
+    constexpr int PAGES = kKvTile / BS;      // pages per K/V tile
+    constexpr uint32_t ID_S = idesc_bf16(kRows, kKvTile, 0);
+    constexpr uint32_t ID_O = idesc_bf16(kRows, D, 1);
+
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bars[10];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ int abort_s;
+
+    pdl_launch_dependents();
+    pdl_wait();
+
+    const int tile = a.tiles - 1 - (int)blockIdx.x;   // heavy (late) tiles first
+    const int h = blockIdx.y;
+    const int r = blockIdx.z;
+    const int q0 = a.q_offsets[r];
+    int q_len = a.q_offsets[r + 1] - q0;
+    const int seq = a.seq_lens[r];
+    if (q_len < 0) q_len = 0;
+    if (q0 < 0 || q0 + q_len > a.total_q) {
+        if (threadIdx.x == 0 && tile == 0 && h == 0 && a.err) flag_err(a.err, PKV_DEVERR_QLEN_CLAMPED);
+        return;
+    }
+    const int ctx = seq - q_len;             // tokens before the chunk
+    if (q_len > a.max_q_len) {               // rows past max_q_len are not computed
+        if (threadIdx.x == 0 && h == 0 && (int)blockIdx.x == 0)
+            flag_err(a.err, PKV_DEVERR_QLEN_CLAMPED);
+        q_len = a.max_q_len;
+    }
+    if (tile * TQ >= q_len) return;          // past this request's queries: no work
+    const int qi_last = min(tile * TQ + TQ, q_len) - 1;
+    int kv_end = ctx + qi_last + 1;          // tokens the tile's last query sees
+    if (kv_end > seq) kv_end = seq;
+    if (kv_end > a.MB * BS) kv_end = a.MB * BS;
+    if (kv_end < 0) kv_end = 0;
+    const int n_tiles = (kv_end + kKvTile - 1) / kKvTile;
+
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+    const uint32_t sQ = smem_u32(sm + SM::Q_OFF);
+    const uint32_t sK = smem_u32(sm + SM::K_OFF);
+    const uint32_t sV = smem_u32(sm + SM::V_OFF);
+    const uint32_t bar_q = smem_u32(&bars[0]);
+    const uint32_t bar_kv_full = smem_u32(&bars[1]);    // [2]
+    const uint32_t bar_kv_empty = smem_u32(&bars[3]);   // [2]
+    const uint32_t bar_s_full = smem_u32(&bars[5]);     // [2]
+    const uint32_t bar_s_free = smem_u32(&bars[7]);     // [2]
+    const uint32_t bar_p_ready = smem_u32(&bars[9]);
+    __shared__ __align__(8) uint64_t bar_pv_s;
+    const uint32_t bar_pv = smem_u32(&bar_pv_s);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) {
+        mbar_init(bar_q, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_kv_full + 8 * i, 1);
+            mbar_init(bar_kv_empty + 8 * i, 1);
+            mbar_init(bar_s_full + 8 * i, 1);
+            mbar_init(bar_s_free + 8 * i, 4);
+        }
+        mbar_init(bar_p_ready, 4);
+        mbar_init(bar_pv, 1);
+        abort_s = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(&tmem_base_s)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+    volatile int* abort_v = &abort_s;
+
+    if (warp == 4) {
+        // ---------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            prefetch_tensormap(&tq);
+            prefetch_tensormap(&tk);
+            prefetch_tensormap(&tv);
+            mbar_arrive_expect_tx(bar_q, KB * kRows * 128);
+            for (int kb = 0; kb < KB; ++kb)
+                tma_load_3d(sQ + kb * kRows * 128, &tq, kb * 64, h * G, q0 + tile * TQ, bar_q);
+        }
+        const int64_t row_end = (int64_t)a.NB * a.Hkv * BS;   // first row past the pool
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j & 1;
+            if (j >= 2) {
+                bool ok = true;
+                if (lane == 0) ok = mbar_wait_bounded(bar_kv_empty + 8 * st, ((j - 2) >> 1) & 1, kWaitNs);
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) {
+                    if (lane == 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
+                    break;
+                }
+            }
+            if (*abort_v) break;
+            const int lb0 = j * PAGES;
+            int npages = (kv_end - lb0 * BS + BS - 1) / BS;
+            if (npages > PAGES) npages = PAGES;
+            if (lane == 0)
+                mbar_arrive_expect_tx(bar_kv_full + 8 * st, (uint32_t)(npages * 2 * KB * BS * 128));
+            __syncwarp();
+            if (lane < npages) {
+                int blk = a.block_table[(int64_t)r * a.MB + lb0 + lane];
+                int64_t row;
+                if (blk < 0 || blk >= a.NB) {
+                    flag_err(a.err, PKV_DEVERR_BLOCK_RANGE);
+                    row = row_end;                 // past the end: TMA fills zeros
+                } else {
+                    row = ((int64_t)blk * a.Hkv + h) * BS;
+                }
+                const uint32_t off = (uint32_t)(lane * BS * 128);
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb) {
+                    tma_load_2d(sK + st * SM::TILE + kb * kRows * 128 + off, &tk, kb * 64, (int)row,
+                                bar_kv_full + 8 * st);
+                    tma_load_2d(sV + st * SM::TILE + kb * kRows * 128 + off, &tv, kb * 64, (int)row,
+                                bar_kv_full + 8 * st);
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------------------------------------------------- MMA issuer
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(bar_q, 0, kWaitNs);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok && lane == 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
+        auto issue_pv = [&](int t) -> bool {
+            bool w = true;
+            if (lane == 0) w = mbar_wait_bounded(bar_p_ready, t & 1, kWaitNs);
+            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+            if (!w) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t vbase = sV + (t & 1) * SM::TILE;
+#pragma unroll
+                for (int k = 0; k < kKvTile / 16; ++k) {
+                    const uint64_t b = smem_desc_sw128(vbase + k * 2048, kRows * 128, 1024);
+                    mma_ts(tmem + kColO, tmem + kColP + k * 8, b, ID_O, (t > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(bar_pv);
+                mma_commit(bar_kv_empty + 8 * (t & 1));
+            }
+            __syncwarp();
+            return true;
+        };
+        int issued_pv = 0;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            const int st = j & 1;
+            bool w = true;
+            if (lane == 0) {
+                w = mbar_wait_bounded(bar_kv_full + 8 * st, (j >> 1) & 1, kWaitNs);
+                if (w && j >= 2) w = mbar_wait_bounded(bar_s_free + 8 * st, ((j - 2) >> 1) & 1, kWaitNs);
+            }
+            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+            if (!w || *abort_v) { ok = false; break; }
+            // the last tile: zero V rows at or past kv_end (partial page, missing pages),
+            // so P = 0 never meets stale or NaN values
+            const int valid = kv_end - j * kKvTile;
+            if (valid < kKvTile) {
+                uint8_t* vst = sm + SM::V_OFF + st * SM::TILE;
+                for (int kb = 0; kb < KB; ++kb)
+                    for (int rr = valid + (lane >> 3); rr < kKvTile; rr += 4)
+                        *reinterpret_cast<uint4*>(vst + kb * kRows * 128 + rr * 128 + (lane & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t kbase = sK + st * SM::TILE;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const int kb = k >> 2;
+                    const uint32_t off = (uint32_t)(kb * kRows * 128 + (k & 3) * 32);
+                    mma_ss(tmem + (st ? kColS1 : kColS0), smem_desc_sw128(sQ + off, 16, 1024),
+                           smem_desc_sw128(kbase + off, 16, 1024), ID_S, k > 0 ? 1u : 0u);
+                }
+                mma_commit(bar_s_full + 8 * st);
+            }
+            __syncwarp();
+            if (j >= 1) {
+                if (!issue_pv(j - 1)) { ok = false; break; }
+                issued_pv = j;
+            }
+        }
+        if (ok && n_tiles > 0) {
+            if (!issue_pv(n_tiles - 1)) ok = false;
+            else issued_pv = n_tiles;
+        }
+        if (!ok && lane == 0 && n_tiles > 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
+        (void)issued_pv;
+    } else {
+        // ---------------------------------------------------------- softmax warps 0-3
+        const int m = tid;                       // query row = TMEM lane
+        const int tq_i = m / G, g = m - (m / G) * G;
+        const int qi = tile * TQ + tq_i;
+        const bool row_valid = qi < q_len;
+        int vis = row_valid ? ctx + qi + 1 : 0;  // tokens this row sees
+        if (vis > kv_end) vis = kv_end;
+        if (vis < 0) vis = 0;
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        float m_ref = -INFINITY;                 // reference max (log2 domain) of O and l
+        float l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int sb = j & 1;
+            bool w = true;
+            if (lane == 0) w = mbar_wait_bounded(bar_s_full + 8 * sb, (j >> 1) & 1, kWaitNs);
+            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+            if (!w || *abort_v) { ok = false; break; }
+            tc_fence_after();
+            float s[kKvTile];
+#pragma unroll
+            for (int c = 0; c < kKvTile / 32; ++c) {
+                float t[32];
+                tmem_ld32(lane_base + (sb ? kColS1 : kColS0) + c * 32, t);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[c * 32 + i] = t[i];
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_s_free + 8 * sb);
+            // scale, mask, tile max
+            const int lim = vis - j * kKvTile;   // columns >= lim are masked
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kKvTile; ++c) {
+                const float x = c < lim ? s[c] * a.scale_log2 : -INFINITY;
+                s[c] = x;
+                mx = fmaxf(mx, x);
+            }
+            // raise the reference max only when a score passes it by more than 2^8
+            float alpha = 1.f;
+            bool rescale = false;
+            if (mx > m_ref + 8.f) {
+                alpha = m_ref == -INFINITY ? 0.f : exp2f(m_ref - mx);
+                m_ref = mx;
+                rescale = j > 0;
+                l *= alpha;
+            }
+            const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+            uint32_t p[kKvTile / 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < kKvTile; c += 2) {
+                const uint32_t w2 = pack_bf16x2(exp2f(s[c] - mu), exp2f(s[c + 1] - mu));
+                p[c / 2] = w2;
+                lsum += bf16_lo_to_f32(w2) + bf16_hi_to_f32(w2);
+            }
+            l += lsum;
+            // P buffer and O are free once the previous P V has completed
+            if (j >= 1) {
+                if (lane == 0) w = mbar_wait_bounded(bar_pv, (j - 1) & 1, kWaitNs);
+                w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+                if (!w || *abort_v) { ok = false; break; }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                const float f = rescale ? alpha : 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(lane_base + kColO + c * 32, o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= f;
+                    tmem_st32f(lane_base + kColO + c * 32, o);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < kKvTile / 32; ++c) tmem_st16(lane_base + kColP + c * 16, p + c * 16);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_p_ready);
+        }
+        // ------------------------------------------------------------ epilogue
+        if (ok && n_tiles > 0) {
+            bool w = true;
+            if (lane == 0) w = mbar_wait_bounded(bar_pv, (n_tiles - 1) & 1, kWaitNs);
+            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+            if (!w) ok = false;
+            tc_fence_after();
+        }
+        if (!ok && n_tiles > 0 && lane == 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
+        const float inv = (l > 0.f && ok) ? 1.f / l : 0.f;
+        uint16_t* orow = a.out + ((int64_t)(q0 + qi) * a.Hq + (int64_t)h * G + g) * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            if (n_tiles > 0 && ok) {
+                tmem_ld32(lane_base + kColO + c * 32, o);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] = 0.f;
+            }
+            if (row_valid) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 8) {
+                    uint4 u;
+                    u.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+                    u.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
+                    u.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
+                    u.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
+                    *reinterpret_cast<uint4*>(orow + c * 32 + i) = u;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 4) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ------------------------------------------------------------------ host side
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 prefill_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        cudaDriverEntryPointQueryResult qr;
+        void* p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+template <int D, int BS, int G>
+cudaError_t prefill_launch_t(const PrefillLaunch& L, const PrefillArgs& a, const CUtensorMap& tq,
+                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+    auto kern = pkv_prefill_kernel<D, BS, G>;
+    // one CTA per SM (it holds all 512 TMEM columns); ask for enough shared memory
+    // that no second CTA can be co-resident
+    int smem = PrefillSmem<D>::ALLOC;
+    if (smem < 120 * 1024) smem = 120 * 1024;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3((unsigned)a.tiles, (unsigned)L.Hkv, (unsigned)L.N),
+                      dim3(kThreads), (size_t)smem, st, tq, tk, tv, a);
+}
+
+template <int D, int BS>
+cudaError_t prefill_launch_g(int G, const PrefillLaunch& L, const PrefillArgs& a,
+                             const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             cudaStream_t st) {
+    switch (G) {
+        case 1: return prefill_launch_t<D, BS, 1>(L, a, tq, tk, tv, st);
+        case 2: return prefill_launch_t<D, BS, 2>(L, a, tq, tk, tv, st);
+        case 4: return prefill_launch_t<D, BS, 4>(L, a, tq, tk, tv, st);
+        case 8: return prefill_launch_t<D, BS, 8>(L, a, tq, tk, tv, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool prefill_shape_supported(int Hq, int Hkv, int D, int BS, int dtype) {
+    if (dtype != PKV_BF16) return false;
+    if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0) return false;
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return false;
+    return (D == 64 || D == 128) && (BS == 16 || BS == 32);
+}
+
+int prefill_launch(const PrefillLaunch& L, cudaStream_t st) {
+    auto fn = prefill_encode_fn();
+    if (!fn) return PKV_ERR_CUDA;
+    const int G = L.Hq / L.Hkv;
+    const int TQ = kRows / G;
+    alignas(64) CUtensorMap tq, tk, tv;
+    {
+        cuuint64_t dims[3] = {(cuuint64_t)L.D, (cuuint64_t)L.Hq, (cuuint64_t)L.total_q};
+        cuuint64_t strides[2] = {(cuuint64_t)L.D * 2, (cuuint64_t)L.Hq * L.D * 2};
+        cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(L.q), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PKV_ERR_CUDA;
+    }
+    const int64_t rows = (int64_t)L.NB * L.Hkv * L.BS;
+    for (int i = 0; i < 2; ++i) {
+        cuuint64_t dims[2] = {(cuuint64_t)L.D, (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)L.D * 2};
+        cuuint32_t box[2] = {64, (cuuint32_t)L.BS};
+        cuuint32_t es[2] = {1, 1};
+        if (fn(i ? &tv : &tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+               const_cast<void*>(i ? L.v_cache : L.k_cache), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PKV_ERR_CUDA;
+    }
+    PrefillArgs a;
+    a.q_offsets = L.q_offsets;
+    a.block_table = L.block_table;
+    a.seq_lens = L.seq_lens;
+    a.out = static_cast<uint16_t*>(L.out);
+    a.err = L.err;
+    a.N = L.N;
+    a.Hq = L.Hq;
+    a.Hkv = L.Hkv;
+    a.MB = L.MB;
+    a.NB = L.NB;
+    a.total_q = L.total_q;
+    a.max_q_len = L.max_q_len;
+    a.tiles = (L.max_q_len + TQ - 1) / TQ;
+    a.scale_log2 = L.scale * 1.4426950408889634f;
+    if (a.tiles <= 0) return PKV_OK;
+    cudaError_t e = cudaErrorInvalidValue;
+    if (L.D == 128 && L.BS == 16) e = prefill_launch_g<128, 16>(G, L, a, tq, tk, tv, st);
+    else if (L.D == 128 && L.BS == 32) e = prefill_launch_g<128, 32>(G, L, a, tq, tk, tv, st);
+    else if (L.D == 64 && L.BS == 16) e = prefill_launch_g<64, 16>(G, L, a, tq, tk, tv, st);
+    else if (L.D == 64 && L.BS == 32) e = prefill_launch_g<64, 32>(G, L, a, tq, tk, tv, st);
+    else return PKV_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // namespace pkv

@@ -54,7 +54,24 @@ class Workload:
     hash_block: int = 16
     q_len: int = 1                # new query tokens per request (speculative verify: > 1)
     int8: bool = False            # int8 pages (symmetric, scale = amax/127)
+    q_lens: np.ndarray | None = None   # int32 [N] per-request query counts (prefill chunks);
+                                       # None: q_len for every request
     notes: dict = field(default_factory=dict)
+
+    @property
+    def query_lens(self) -> np.ndarray:
+        """New query tokens of each request (int64 [N])."""
+        if self.q_lens is not None:
+            return np.asarray(self.q_lens, dtype=np.int64)
+        return np.full(self.N, self.q_len, dtype=np.int64)
+
+    @property
+    def total_q(self) -> int:
+        return int(self.query_lens.sum())
+
+    @property
+    def max_q_len(self) -> int:
+        return int(self.query_lens.max()) if self.N else 0
 
     @property
     def quant(self) -> bool:
@@ -100,16 +117,30 @@ class Workload:
         return (self.seq_lens.astype(np.int64) - 1).astype(np.int32)
 
     def q_offsets(self) -> np.ndarray:
-        """Query rows of each request: q_len rows per request, request-major."""
-        return (np.arange(self.N + 1, dtype=np.int64) * self.q_len).astype(np.int32)
+        """Query rows of each request, request-major (int32 [N + 1])."""
+        o = np.zeros(self.N + 1, dtype=np.int64)
+        np.cumsum(self.query_lens, out=o[1:])
+        return o.astype(np.int32)
 
     def new_token_rows(self):
         """(req_idx, positions) of the step's new tokens: the last q_len tokens of
         every request (positions seq_len - q_len .. seq_len - 1)."""
-        req = np.repeat(np.arange(self.N, dtype=np.int32), self.q_len)
-        pos = (np.repeat(self.seq_lens.astype(np.int64), self.q_len) - self.q_len +
-               np.tile(np.arange(self.q_len), self.N)).astype(np.int32)
-        return req, pos
+        ql = self.query_lens
+        req = np.repeat(np.arange(self.N, dtype=np.int32), ql)
+        pos = np.concatenate([np.arange(int(s) - int(n), int(s)) for s, n in
+                              zip(self.seq_lens, ql)]) if self.N else np.zeros(0)
+        return req, pos.astype(np.int32)
+
+    def prefill_flops(self) -> int:
+        """Causal-effective flops of attention over the new queries: every (query head,
+        visible key) pair costs 2 D for Q K^T and 2 D for P V."""
+        tot = 0
+        for s, n in zip(self.seq_lens.astype(np.int64), self.query_lens):
+            ctx = int(s) - int(n)
+            i = np.arange(int(n), dtype=np.int64)
+            vis = np.clip(ctx + i + 1, 0, int(s))
+            tot += int(vis.sum())
+        return tot * self.Hq * 4 * self.D
 
     def kv_read_bytes(self) -> int:
         """Logical K+V bytes one decode step reads: sum_r seq_len_r * Hkv * D * 2 * elt."""
@@ -252,6 +283,24 @@ def make(cfg: int, seed: int | None = None, small: bool = False,
         wl.fp8 = False
         wl.int8 = True
         return wl
+    if cfg == 8:
+        # chunked prefill on the 70B-shaped layer: a chunk of new prompt tokens per
+        # request after a cached context; small: ragged chunks spanning several tiles
+        Hq, Hkv, D, BS = 64, 8, 128, 16
+        if small:
+            qls = np.array([130, 257, 1, 64, 300], dtype=np.int32)
+            ctx = rng.integers(0, 700, size=qls.shape[0]).astype(np.int32)
+            ctx[2] = 0
+        else:
+            N = batch or 8
+            qls = np.full(N, 2048, dtype=np.int32)
+            ctx = rng.integers(0, 6144 + 1, size=N).astype(np.int32)
+        seq = (ctx + qls).astype(np.int32)
+        bt, NB = _assign_blocks(rng, seq, BS)
+        toks, offs = _tokens(rng, seq, VOCAB)
+        return Workload("prefill_chunk" + ("_small" if small else ""), 8, seed, int(seq.shape[0]),
+                        Hq, Hkv, D, BS, NB, False, 1.0 / math.sqrt(D), seq, bt, toks, offs,
+                        q_lens=qls)
     if cfg == 6:
         # speculative verify on the 70B-shaped layer: 4 new tokens per request
         # (3 drafted + 1), all checked in one attention pass
@@ -333,7 +382,7 @@ def host_data(wl: Workload, seed_offset: int = 1000) -> dict:
     Both: `q` uint16 [N, Hq, D]; `k_new`, `v_new` uint16 [N, Hkv, D] (the decode
     step's new token of each request, written at position seq_len - 1)."""
     rng = np.random.default_rng(wl.seed + seed_offset)
-    d = {"q": _randn_bf16(rng, (wl.N * wl.q_len, wl.Hq, wl.D))}
+    d = {"q": _randn_bf16(rng, (wl.total_q, wl.Hq, wl.D))}
     if not wl.quant:
         d["k_cache"] = _randn_bf16(rng, (wl.NB, wl.Hkv, wl.BS, wl.D))
         d["v_cache"] = _randn_bf16(rng, (wl.NB, wl.Hkv, wl.BS, wl.D))
@@ -342,8 +391,8 @@ def host_data(wl: Workload, seed_offset: int = 1000) -> dict:
         d["k_rows"] = _randn_bf16(rng, (T, wl.Hkv, wl.D))
         d["v_rows"] = _randn_bf16(rng, (T, wl.Hkv, wl.D))
         d["k_scale"], d["v_scale"] = fp8_scales_from_rows(wl, d["k_rows"], d["v_rows"])
-    d["k_new"] = _randn_bf16(rng, (wl.N * wl.q_len, wl.Hkv, wl.D))
-    d["v_new"] = _randn_bf16(rng, (wl.N * wl.q_len, wl.Hkv, wl.D))
+    d["k_new"] = _randn_bf16(rng, (wl.total_q, wl.Hkv, wl.D))
+    d["v_new"] = _randn_bf16(rng, (wl.total_q, wl.Hkv, wl.D))
     return d
 
 
@@ -357,7 +406,7 @@ def device_data(wl: Workload, device, seed_offset: int = 2000) -> dict:
     g = torch.Generator(device=device)
     g.manual_seed(wl.seed + seed_offset)
     bf = torch.bfloat16
-    d = {"q": torch.randn((wl.N * wl.q_len, wl.Hq, wl.D), generator=g, device=device, dtype=bf)}
+    d = {"q": torch.randn((wl.total_q, wl.Hq, wl.D), generator=g, device=device, dtype=bf)}
     if not wl.quant:
         d["k_cache"] = torch.randn((wl.NB, wl.Hkv, wl.BS, wl.D), generator=g, device=device,
                                    dtype=bf)
@@ -391,8 +440,8 @@ def device_data(wl: Workload, device, seed_offset: int = 2000) -> dict:
             full = torch.ones((wl.NB, wl.Hkv), dtype=torch.float32, device=device)
             full[phys_t] = sc
             d[skey] = full
-    d["k_new"] = torch.randn((wl.N * wl.q_len, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
-    d["v_new"] = torch.randn((wl.N * wl.q_len, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
+    d["k_new"] = torch.randn((wl.total_q, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
+    d["v_new"] = torch.randn((wl.total_q, wl.Hkv, wl.D), generator=g, device=device, dtype=bf)
     return d
 
 

@@ -635,7 +635,7 @@ def run_prefill(args):
     qo_np = wl.q_offsets()
     ql = wl.query_lens
     tot_t, tot_f, n_rows = 0.0, 0, 0
-    while tot_t < 10.0:
+    while tot_t < (0.0 if args.skip_cpu else 10.0):
         rows = rng.integers(0, wl.total_q * wl.Hq, size=64).astype(np.int64)
         t0 = time.perf_counter()
         oracle.multiquery_rows(q, qo_np, kc, vc, wl.block_table, wl.seq_lens, wl.scale, rows)
@@ -646,7 +646,8 @@ def run_prefill(args):
             vis = int(wl.seq_lens[r]) - int(ql[r]) + (tq_ - int(qo_np[r])) + 1
             tot_f += max(0, min(vis, int(wl.seq_lens[r]))) * 4 * wl.D
         n_rows += rows.shape[0]
-    cpu = {"value": round(tot_f / tot_t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+    cpu = None if args.skip_cpu else {
+           "value": round(tot_f / tot_t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
            "kind": "oracle", "sample": f"{n_rows} random (token, head) rows of {wl.name} "
                                        f"({tot_f/1e9:.1f} GFLOP in {tot_t:.1f} s), fp64 C + OpenMP"}
     line = {"metric": "paged prefill attention: causal-effective TFLOP/s (bf16 tensor cores)",

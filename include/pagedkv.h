@@ -280,6 +280,7 @@ PKV_API int pkv_prefix_block_hash(const int32_t *tokens, const int64_t *offsets,
  *   q, out          bf16 [total_q][Hq][D], 16-byte aligned; rows of no request untouched
  *   k/v_cache       bf16 pages [NB][Hkv][BS][D]
  *   error_word      device uint32 collecting PKV_DEVERR_* bits (sticky), or NULL
+ * scale must be finite and > 0 (else PKV_ERR_INVALID_ARG).
  * Supported: bf16 pages, head_dim 64 or 128, block_size 16 or 32, G in {1, 2, 4, 8};
  * other shapes return PKV_ERR_UNSUPPORTED.  No workspace. */
 PKV_API int pkv_paged_prefill_attn(const void *q, const int32_t *q_offsets, int total_q,

@@ -229,6 +229,7 @@ int pkv_paged_prefill_attn(const void* q, const int32_t* q_offsets, int total_q,
     if (!pkv::prefill_shape_supported(num_q_heads, num_kv_heads, head_dim, block_size,
                                       cache_dtype))
         return PKV_ERR_UNSUPPORTED;
+    if (!(scale > 0.f) || scale > 3.0e38f) return PKV_ERR_INVALID_ARG;   // finite, > 0
     if (batch == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
     if ((int64_t)(num_blocks + 1) * num_kv_heads * block_size >= ((int64_t)1 << 31))
         return PKV_ERR_UNSUPPORTED;

@@ -30,7 +30,8 @@ namespace {
 
 constexpr int kRows = 128;        // query rows per tile (TMEM lanes)
 constexpr int kKvTile = 128;      // tokens per K/V tile
-constexpr int kThreads = 192;     // 6 warps
+constexpr int kThreads = 224;     // 7 warps: 4 softmax, K producer, V producer, MMA
+constexpr int kStages = 3;        // K tiles and V tiles in flight (separate rings)
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384, kTmemCols = 512;
 
@@ -100,14 +101,33 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* w) {
+// All 128 fp32 columns of this thread's lane in one load (+ its wait).
+__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
+    uint32_t r[128];
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7]),
-        "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]), "r"(w[14]),
-        "r"(w[15])
+        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),"=r"(r[32]),"=r"(r[33]),"=r"(r[34]),"=r"(r[35]),"=r"(r[36]),"=r"(r[37]),"=r"(r[38]),"=r"(r[39]),"=r"(r[40]),"=r"(r[41]),"=r"(r[42]),"=r"(r[43]),"=r"(r[44]),"=r"(r[45]),"=r"(r[46]),"=r"(r[47]),"=r"(r[48]),"=r"(r[49]),"=r"(r[50]),"=r"(r[51]),"=r"(r[52]),"=r"(r[53]),"=r"(r[54]),"=r"(r[55]),"=r"(r[56]),"=r"(r[57]),"=r"(r[58]),"=r"(r[59]),"=r"(r[60]),"=r"(r[61]),"=r"(r[62]),"=r"(r[63]),"=r"(r[64]),"=r"(r[65]),"=r"(r[66]),"=r"(r[67]),"=r"(r[68]),"=r"(r[69]),"=r"(r[70]),"=r"(r[71]),"=r"(r[72]),"=r"(r[73]),"=r"(r[74]),"=r"(r[75]),"=r"(r[76]),"=r"(r[77]),"=r"(r[78]),"=r"(r[79]),"=r"(r[80]),"=r"(r[81]),"=r"(r[82]),"=r"(r[83]),"=r"(r[84]),"=r"(r[85]),"=r"(r[86]),"=r"(r[87]),"=r"(r[88]),"=r"(r[89]),"=r"(r[90]),"=r"(r[91]),"=r"(r[92]),"=r"(r[93]),"=r"(r[94]),"=r"(r[95]),"=r"(r[96]),"=r"(r[97]),"=r"(r[98]),"=r"(r[99]),"=r"(r[100]),"=r"(r[101]),"=r"(r[102]),"=r"(r[103]),"=r"(r[104]),"=r"(r[105]),"=r"(r[106]),"=r"(r[107]),"=r"(r[108]),"=r"(r[109]),"=r"(r[110]),"=r"(r[111]),"=r"(r[112]),"=r"(r[113]),"=r"(r[114]),"=r"(r[115]),"=r"(r[116]),"=r"(r[117]),"=r"(r[118]),"=r"(r[119]),"=r"(r[120]),"=r"(r[121]),"=r"(r[122]),"=r"(r[123]),"=r"(r[124]),"=r"(r[125]),"=r"(r[126]),"=r"(r[127])
+        : "r"(taddr)
         : "memory");
+#pragma unroll
+    for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 64 32-bit columns (bf16 pairs) of this thread's lane.
+__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&w)[64]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};"
+        ::"r"(taddr), "r"(w[0]),"r"(w[1]),"r"(w[2]),"r"(w[3]),"r"(w[4]),"r"(w[5]),"r"(w[6]),"r"(w[7]),"r"(w[8]),"r"(w[9]),"r"(w[10]),"r"(w[11]),"r"(w[12]),"r"(w[13]),"r"(w[14]),"r"(w[15]),"r"(w[16]),"r"(w[17]),"r"(w[18]),"r"(w[19]),"r"(w[20]),"r"(w[21]),"r"(w[22]),"r"(w[23]),"r"(w[24]),"r"(w[25]),"r"(w[26]),"r"(w[27]),"r"(w[28]),"r"(w[29]),"r"(w[30]),"r"(w[31]),"r"(w[32]),"r"(w[33]),"r"(w[34]),"r"(w[35]),"r"(w[36]),"r"(w[37]),"r"(w[38]),"r"(w[39]),"r"(w[40]),"r"(w[41]),"r"(w[42]),"r"(w[43]),"r"(w[44]),"r"(w[45]),"r"(w[46]),"r"(w[47]),"r"(w[48]),"r"(w[49]),"r"(w[50]),"r"(w[51]),"r"(w[52]),"r"(w[53]),"r"(w[54]),"r"(w[55]),"r"(w[56]),"r"(w[57]),"r"(w[58]),"r"(w[59]),"r"(w[60]),"r"(w[61]),"r"(w[62]),"r"(w[63])
+        : "memory");
+}
+
+// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero): one MUFU op;
+// -inf gives +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32]) {
@@ -156,16 +176,16 @@ struct PrefillArgs {
     float scale_log2;
 };
 
-// Shared memory: Q [KB][128 rows][128 B] | K stages [2][KB][128][128 B] |
-// V stages [2][KB][128][128 B]; 1024-byte aligned (128-byte swizzle atoms).
+// Shared memory: Q [KB][128 rows][128 B] | K ring [kStages][KB][128][128 B] |
+// V ring [kStages][KB][128][128 B]; 1024-byte aligned (128-byte swizzle atoms).
 template <int D>
 struct PrefillSmem {
     static constexpr int KB = D / 64;
     static constexpr int TILE = KB * kRows * 128;   // bytes of one 128-row operand tile
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = TILE;
-    static constexpr int V_OFF = 3 * TILE;
-    static constexpr int BYTES = 5 * TILE;
+    static constexpr int V_OFF = (1 + kStages) * TILE;
+    static constexpr int BYTES = (1 + 2 * kStages) * TILE;
     static constexpr int ALLOC = BYTES + 1024;
 };
 
@@ -181,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t ID_O = idesc_bf16(kRows, D, 1);
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[10];
+    __shared__ __align__(8) uint64_t bars[8 + 4 * kStages];
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
 
@@ -219,22 +239,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t sK = smem_u32(sm + SM::K_OFF);
     const uint32_t sV = smem_u32(sm + SM::V_OFF);
     const uint32_t bar_q = smem_u32(&bars[0]);
-    const uint32_t bar_kv_full = smem_u32(&bars[1]);    // [2]
-    const uint32_t bar_kv_empty = smem_u32(&bars[3]);   // [2]
-    const uint32_t bar_s_full = smem_u32(&bars[5]);     // [2]
-    const uint32_t bar_s_free = smem_u32(&bars[7]);     // [2]
-    const uint32_t bar_p_ready = smem_u32(&bars[9]);
-    __shared__ __align__(8) uint64_t bar_pv_s;
-    const uint32_t bar_pv = smem_u32(&bar_pv_s);
+    const uint32_t bar_s_full = smem_u32(&bars[1]);     // [2]
+    const uint32_t bar_s_free = smem_u32(&bars[3]);     // [2]
+    const uint32_t bar_p_ready = smem_u32(&bars[5]);
+    const uint32_t bar_pv = smem_u32(&bars[6]);
+    const uint32_t bar_k_full = smem_u32(&bars[8]);                 // [kStages]
+    const uint32_t bar_k_empty = smem_u32(&bars[8 + kStages]);      // [kStages]
+    const uint32_t bar_v_full = smem_u32(&bars[8 + 2 * kStages]);   // [kStages]
+    const uint32_t bar_v_empty = smem_u32(&bars[8 + 3 * kStages]);  // [kStages]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         mbar_init(bar_q, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_kv_full + 8 * i, 1);
-            mbar_init(bar_kv_empty + 8 * i, 1);
             mbar_init(bar_s_full + 8 * i, 1);
             mbar_init(bar_s_free + 8 * i, 4);
+        }
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(bar_k_full + 8 * i, 1);
+            mbar_init(bar_k_empty + 8 * i, 1);
+            mbar_init(bar_v_full + 8 * i, 1);
+            mbar_init(bar_v_empty + 8 * i, 1);
         }
         mbar_init(bar_p_ready, 4);
         mbar_init(bar_pv, 1);
@@ -254,22 +279,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_base_s;
     volatile int* abort_v = &abort_s;
 
-    if (warp == 4) {
-        // ---------------------------------------------------------- TMA producer
-        if (lane == 0) {
+    if (warp == 4 || warp == 5) {
+        // ---------------------------------------------------------- TMA producers
+        // warp 4 feeds the K ring (and loads Q), warp 5 the V ring; a K slot frees when
+        // its Q K^T completes, a V slot when its P V completes, so K runs further ahead
+        const bool is_k = warp == 4;
+        if (is_k && lane == 0) {
             prefetch_tensormap(&tq);
             prefetch_tensormap(&tk);
-            prefetch_tensormap(&tv);
             mbar_arrive_expect_tx(bar_q, KB * kRows * 128);
             for (int kb = 0; kb < KB; ++kb)
                 tma_load_3d(sQ + kb * kRows * 128, &tq, kb * 64, h * G, q0 + tile * TQ, bar_q);
         }
+        if (!is_k && lane == 0) prefetch_tensormap(&tv);
+        const CUtensorMap* map = is_k ? &tk : &tv;
+        const uint32_t ring = is_k ? sK : sV;
+        const uint32_t full = is_k ? bar_k_full : bar_v_full;
+        const uint32_t empty = is_k ? bar_k_empty : bar_v_empty;
         const int64_t row_end = (int64_t)a.NB * a.Hkv * BS;   // first row past the pool
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j & 1;
-            if (j >= 2) {
+            const int st = j % kStages;
+            if (j >= kStages) {
                 bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(bar_kv_empty + 8 * st, ((j - 2) >> 1) & 1, kWaitNs);
+                if (lane == 0) ok = mbar_wait_bounded(empty + 8 * st, ((j / kStages) - 1) & 1, kWaitNs);
                 ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (!ok) {
                     if (lane == 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
@@ -281,67 +313,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             int npages = (kv_end - lb0 * BS + BS - 1) / BS;
             if (npages > PAGES) npages = PAGES;
             if (lane == 0)
-                mbar_arrive_expect_tx(bar_kv_full + 8 * st, (uint32_t)(npages * 2 * KB * BS * 128));
+                mbar_arrive_expect_tx(full + 8 * st, (uint32_t)(npages * KB * BS * 128));
             __syncwarp();
             if (lane < npages) {
                 int blk = a.block_table[(int64_t)r * a.MB + lb0 + lane];
                 int64_t row;
                 if (blk < 0 || blk >= a.NB) {
-                    flag_err(a.err, PKV_DEVERR_BLOCK_RANGE);
+                    if (is_k) flag_err(a.err, PKV_DEVERR_BLOCK_RANGE);
                     row = row_end;                 // past the end: TMA fills zeros
                 } else {
                     row = ((int64_t)blk * a.Hkv + h) * BS;
                 }
                 const uint32_t off = (uint32_t)(lane * BS * 128);
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb) {
-                    tma_load_2d(sK + st * SM::TILE + kb * kRows * 128 + off, &tk, kb * 64, (int)row,
-                                bar_kv_full + 8 * st);
-                    tma_load_2d(sV + st * SM::TILE + kb * kRows * 128 + off, &tv, kb * 64, (int)row,
-                                bar_kv_full + 8 * st);
-                }
+                for (int kb = 0; kb < KB; ++kb)
+                    tma_load_2d(ring + st * SM::TILE + kb * kRows * 128 + off, map, kb * 64,
+                                (int)row, full + 8 * st);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 6) {
         // ---------------------------------------------------------- MMA issuer
         bool ok = true;
         if (lane == 0) ok = mbar_wait_bounded(bar_q, 0, kWaitNs);
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok && lane == 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
         auto issue_pv = [&](int t) -> bool {
+            const int vs = t % kStages;
             bool w = true;
-            if (lane == 0) w = mbar_wait_bounded(bar_p_ready, t & 1, kWaitNs);
+            if (lane == 0) {
+                w = mbar_wait_bounded(bar_v_full + 8 * vs, (t / kStages) & 1, kWaitNs);
+                if (w) w = mbar_wait_bounded(bar_p_ready, t & 1, kWaitNs);
+            }
             w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
             if (!w) return false;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t vbase = sV + (t & 1) * SM::TILE;
-#pragma unroll
-                for (int k = 0; k < kKvTile / 16; ++k) {
-                    const uint64_t b = smem_desc_sw128(vbase + k * 2048, kRows * 128, 1024);
-                    mma_ts(tmem + kColO, tmem + kColP + k * 8, b, ID_O, (t > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit(bar_pv);
-                mma_commit(bar_kv_empty + 8 * (t & 1));
-            }
-            __syncwarp();
-            return true;
-        };
-        int issued_pv = 0;
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            const int st = j & 1;
-            bool w = true;
-            if (lane == 0) {
-                w = mbar_wait_bounded(bar_kv_full + 8 * st, (j >> 1) & 1, kWaitNs);
-                if (w && j >= 2) w = mbar_wait_bounded(bar_s_free + 8 * st, ((j - 2) >> 1) & 1, kWaitNs);
-            }
-            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-            if (!w || *abort_v) { ok = false; break; }
             // the last tile: zero V rows at or past kv_end (partial page, missing pages),
             // so P = 0 never meets stale or NaN values
-            const int valid = kv_end - j * kKvTile;
+            const int valid = kv_end - t * kKvTile;
             if (valid < kKvTile) {
-                uint8_t* vst = sm + SM::V_OFF + st * SM::TILE;
+                uint8_t* vst = sm + SM::V_OFF + vs * SM::TILE;
                 for (int kb = 0; kb < KB; ++kb)
                     for (int rr = valid + (lane >> 3); rr < kKvTile; rr += 4)
                         *reinterpret_cast<uint4*>(vst + kb * kRows * 128 + rr * 128 + (lane & 7) * 16) =
@@ -351,15 +360,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             if (lane == 0) {
-                const uint32_t kbase = sK + st * SM::TILE;
+                const uint32_t vbase = sV + vs * SM::TILE;
+#pragma unroll
+                for (int k = 0; k < kKvTile / 16; ++k) {
+                    const uint64_t b = smem_desc_sw128(vbase + k * 2048, kRows * 128, 1024);
+                    mma_ts(tmem + kColO, tmem + kColP + k * 8, b, ID_O, (t > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit(bar_pv);
+                mma_commit(bar_v_empty + 8 * vs);
+            }
+            __syncwarp();
+            return true;
+        };
+        int issued_pv = 0;
+        for (int j = 0; ok && j < n_tiles; ++j) {
+            const int sb = j & 1, ks = j % kStages;
+            bool w = true;
+            if (lane == 0) {
+                w = mbar_wait_bounded(bar_k_full + 8 * ks, (j / kStages) & 1, kWaitNs);
+                if (w && j >= 2) w = mbar_wait_bounded(bar_s_free + 8 * sb, ((j - 2) >> 1) & 1, kWaitNs);
+            }
+            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+            if (!w || *abort_v) { ok = false; break; }
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t kbase = sK + ks * SM::TILE;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const int kb = k >> 2;
                     const uint32_t off = (uint32_t)(kb * kRows * 128 + (k & 3) * 32);
-                    mma_ss(tmem + (st ? kColS1 : kColS0), smem_desc_sw128(sQ + off, 16, 1024),
+                    mma_ss(tmem + (sb ? kColS1 : kColS0), smem_desc_sw128(sQ + off, 16, 1024),
                            smem_desc_sw128(kbase + off, 16, 1024), ID_S, k > 0 ? 1u : 0u);
                 }
-                mma_commit(bar_s_full + 8 * st);
+                mma_commit(bar_s_full + 8 * sb);
+                mma_commit(bar_k_empty + 8 * ks);
             }
             __syncwarp();
             if (j >= 1) {
@@ -394,25 +428,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!w || *abort_v) { ok = false; break; }
             tc_fence_after();
             float s[kKvTile];
-#pragma unroll
-            for (int c = 0; c < kKvTile / 32; ++c) {
-                float t[32];
-                tmem_ld32(lane_base + (sb ? kColS1 : kColS0) + c * 32, t);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = t[i];
-            }
+            tmem_ld128(lane_base + (sb ? kColS1 : kColS0), s);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_s_free + 8 * sb);
-            // scale, mask, tile max
+            // mask (diagonal and tail tiles only), tile max on raw scores (scale > 0)
             const int lim = vis - j * kKvTile;   // columns >= lim are masked
-            float mx = -INFINITY;
+            if (lim < kKvTile) {
 #pragma unroll
-            for (int c = 0; c < kKvTile; ++c) {
-                const float x = c < lim ? s[c] * a.scale_log2 : -INFINITY;
-                s[c] = x;
-                mx = fmaxf(mx, x);
+                for (int c = 0; c < kKvTile; ++c) s[c] = c < lim ? s[c] : -INFINITY;
             }
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+            for (int c = 8; c < kKvTile; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) *
+                             a.scale_log2;
             // raise the reference max only when a score passes it by more than 2^8
             float alpha = 1.f;
             bool rescale = false;
@@ -422,16 +455,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 rescale = j > 0;
                 l *= alpha;
             }
-            const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+            const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
             uint32_t p[kKvTile / 2];
-            float lsum = 0.f;
+            float l8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) l8[i] = 0.f;
 #pragma unroll
             for (int c = 0; c < kKvTile; c += 2) {
-                const uint32_t w2 = pack_bf16x2(exp2f(s[c] - mu), exp2f(s[c + 1] - mu));
-                p[c / 2] = w2;
-                lsum += bf16_lo_to_f32(w2) + bf16_hi_to_f32(w2);
+                const float e0 = ex2_approx(fmaf(s[c], a.scale_log2, nmu));
+                const float e1 = ex2_approx(fmaf(s[c + 1], a.scale_log2, nmu));
+                p[c / 2] = pack_bf16x2(e0, e1);
+                l8[(c >> 1) & 7] += e0 + e1;
             }
-            l += lsum;
+            l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             // P buffer and O are free once the previous P V has completed
             if (j >= 1) {
                 if (lane == 0) w = mbar_wait_bounded(bar_pv, (j - 1) & 1, kWaitNs);
@@ -450,8 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32f(lane_base + kColO + c * 32, o);
                 }
             }
-#pragma unroll
-            for (int c = 0; c < kKvTile / 32; ++c) tmem_st16(lane_base + kColP + c * 16, p + c * 16);
+            tmem_st64(lane_base + kColP, p);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();

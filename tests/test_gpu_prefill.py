@@ -158,6 +158,9 @@ def test_prefill_rejects():
                                     p, None, None) == -1
     assert L.pkv_paged_prefill_attn(p, p, 0, 0, p, p, p, 1, p, 1, 8, 8, 128, 16, 4, 0, 1.0, p,
                                     None, None) == 0
+    for bad in (0.0, -1.0, float("nan"), float("inf")):    # scale must be finite and > 0
+        assert L.pkv_paged_prefill_attn(p, p, 1, 1, p, p, p, 1, p, 1, 8, 8, 128, 16, 4, 0, bad,
+                                        p, None, None) == -1
 
 
 def test_prefill_full_size_sampled():

@@ -30,10 +30,9 @@ namespace {
 
 constexpr int kRows = 128;        // query rows per tile (TMEM lanes)
 constexpr int kKvTile = 128;      // tokens per K/V tile
-constexpr int kThreads = 224;     // 7 warps: 4 softmax, K producer, V producer, MMA
-constexpr int kStages = 3;        // K tiles and V tiles in flight (separate rings)
+constexpr int kThreads = 352;     // 11 warps: 2 x 4 softmax, K producer, V producer, MMA
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 384, kTmemCols = 512;
+constexpr uint32_t kColO = 256, kColP = 384, kColQ = 448, kTmemCols = 512;
 
 // ------------------------------------------------------------ tcgen05 wrappers
 __device__ __forceinline__ void tc_fence_before() {
@@ -101,24 +100,24 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// All 128 fp32 columns of this thread's lane in one load (+ its wait).
-__device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
-    uint32_t r[128];
+// 64 fp32 columns of this thread's lane in one load (+ its wait).
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+    uint32_t r[64];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x128.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64,%65,%66,%67,%68,%69,%70,%71,%72,%73,%74,%75,%76,%77,%78,%79,%80,%81,%82,%83,%84,%85,%86,%87,%88,%89,%90,%91,%92,%93,%94,%95,%96,%97,%98,%99,%100,%101,%102,%103,%104,%105,%106,%107,%108,%109,%110,%111,%112,%113,%114,%115,%116,%117,%118,%119,%120,%121,%122,%123,%124,%125,%126,%127}, [%128];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
         "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),"=r"(r[32]),"=r"(r[33]),"=r"(r[34]),"=r"(r[35]),"=r"(r[36]),"=r"(r[37]),"=r"(r[38]),"=r"(r[39]),"=r"(r[40]),"=r"(r[41]),"=r"(r[42]),"=r"(r[43]),"=r"(r[44]),"=r"(r[45]),"=r"(r[46]),"=r"(r[47]),"=r"(r[48]),"=r"(r[49]),"=r"(r[50]),"=r"(r[51]),"=r"(r[52]),"=r"(r[53]),"=r"(r[54]),"=r"(r[55]),"=r"(r[56]),"=r"(r[57]),"=r"(r[58]),"=r"(r[59]),"=r"(r[60]),"=r"(r[61]),"=r"(r[62]),"=r"(r[63]),"=r"(r[64]),"=r"(r[65]),"=r"(r[66]),"=r"(r[67]),"=r"(r[68]),"=r"(r[69]),"=r"(r[70]),"=r"(r[71]),"=r"(r[72]),"=r"(r[73]),"=r"(r[74]),"=r"(r[75]),"=r"(r[76]),"=r"(r[77]),"=r"(r[78]),"=r"(r[79]),"=r"(r[80]),"=r"(r[81]),"=r"(r[82]),"=r"(r[83]),"=r"(r[84]),"=r"(r[85]),"=r"(r[86]),"=r"(r[87]),"=r"(r[88]),"=r"(r[89]),"=r"(r[90]),"=r"(r[91]),"=r"(r[92]),"=r"(r[93]),"=r"(r[94]),"=r"(r[95]),"=r"(r[96]),"=r"(r[97]),"=r"(r[98]),"=r"(r[99]),"=r"(r[100]),"=r"(r[101]),"=r"(r[102]),"=r"(r[103]),"=r"(r[104]),"=r"(r[105]),"=r"(r[106]),"=r"(r[107]),"=r"(r[108]),"=r"(r[109]),"=r"(r[110]),"=r"(r[111]),"=r"(r[112]),"=r"(r[113]),"=r"(r[114]),"=r"(r[115]),"=r"(r[116]),"=r"(r[117]),"=r"(r[118]),"=r"(r[119]),"=r"(r[120]),"=r"(r[121]),"=r"(r[122]),"=r"(r[123]),"=r"(r[124]),"=r"(r[125]),"=r"(r[126]),"=r"(r[127])
+        : "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]),"=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]),"=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]),"=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31]),"=r"(r[32]),"=r"(r[33]),"=r"(r[34]),"=r"(r[35]),"=r"(r[36]),"=r"(r[37]),"=r"(r[38]),"=r"(r[39]),"=r"(r[40]),"=r"(r[41]),"=r"(r[42]),"=r"(r[43]),"=r"(r[44]),"=r"(r[45]),"=r"(r[46]),"=r"(r[47]),"=r"(r[48]),"=r"(r[49]),"=r"(r[50]),"=r"(r[51]),"=r"(r[52]),"=r"(r[53]),"=r"(r[54]),"=r"(r[55]),"=r"(r[56]),"=r"(r[57]),"=r"(r[58]),"=r"(r[59]),"=r"(r[60]),"=r"(r[61]),"=r"(r[62]),"=r"(r[63])
         : "r"(taddr)
         : "memory");
 #pragma unroll
-    for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 64 32-bit columns (bf16 pairs) of this thread's lane.
-__device__ __forceinline__ void tmem_st64(uint32_t taddr, const uint32_t (&w)[64]) {
+// 32 32-bit columns (bf16 pairs) of this thread's lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&w)[32]) {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x64.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};"
-        ::"r"(taddr), "r"(w[0]),"r"(w[1]),"r"(w[2]),"r"(w[3]),"r"(w[4]),"r"(w[5]),"r"(w[6]),"r"(w[7]),"r"(w[8]),"r"(w[9]),"r"(w[10]),"r"(w[11]),"r"(w[12]),"r"(w[13]),"r"(w[14]),"r"(w[15]),"r"(w[16]),"r"(w[17]),"r"(w[18]),"r"(w[19]),"r"(w[20]),"r"(w[21]),"r"(w[22]),"r"(w[23]),"r"(w[24]),"r"(w[25]),"r"(w[26]),"r"(w[27]),"r"(w[28]),"r"(w[29]),"r"(w[30]),"r"(w[31]),"r"(w[32]),"r"(w[33]),"r"(w[34]),"r"(w[35]),"r"(w[36]),"r"(w[37]),"r"(w[38]),"r"(w[39]),"r"(w[40]),"r"(w[41]),"r"(w[42]),"r"(w[43]),"r"(w[44]),"r"(w[45]),"r"(w[46]),"r"(w[47]),"r"(w[48]),"r"(w[49]),"r"(w[50]),"r"(w[51]),"r"(w[52]),"r"(w[53]),"r"(w[54]),"r"(w[55]),"r"(w[56]),"r"(w[57]),"r"(w[58]),"r"(w[59]),"r"(w[60]),"r"(w[61]),"r"(w[62]),"r"(w[63])
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        ::"r"(taddr), "r"(w[0]),"r"(w[1]),"r"(w[2]),"r"(w[3]),"r"(w[4]),"r"(w[5]),"r"(w[6]),"r"(w[7]),"r"(w[8]),"r"(w[9]),"r"(w[10]),"r"(w[11]),"r"(w[12]),"r"(w[13]),"r"(w[14]),"r"(w[15]),"r"(w[16]),"r"(w[17]),"r"(w[18]),"r"(w[19]),"r"(w[20]),"r"(w[21]),"r"(w[22]),"r"(w[23]),"r"(w[24]),"r"(w[25]),"r"(w[26]),"r"(w[27]),"r"(w[28]),"r"(w[29]),"r"(w[30]),"r"(w[31])
         : "memory");
 }
 
@@ -147,17 +146,30 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
-
 __device__ __forceinline__ void flag_err(uint32_t* err, uint32_t bits) {
     if (err != nullptr) atomicOr(err, bits);
+}
+
+// Barrier among `count` threads (whole warps) under hardware barrier `id` (not 0).
+__device__ __forceinline__ void named_barrier_sync(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// N (16 or 32) 32-bit columns of this thread's lane.
+template <int N>
+__device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&w)[N]) {
+    static_assert(N == 16 || N == 32, "16 or 32 columns");
+    if constexpr (N == 32) {
+        tmem_st32(taddr, w);
+    } else {
+        asm volatile(
+            "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,"
+            "%12,%13,%14,%15,%16};" ::"r"(taddr),
+            "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
+            "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
+            "r"(w[14]), "r"(w[15])
+            : "memory");
+    }
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -167,6 +179,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }  // namespace
 
 struct PrefillArgs {
+    const uint16_t* q;
     const int32_t* q_offsets;
     const int32_t* block_table;
     const int32_t* seq_lens;
@@ -176,34 +189,48 @@ struct PrefillArgs {
     float scale_log2;
 };
 
-// Shared memory: Q [KB][128 rows][128 B] | K ring [kStages][KB][128][128 B] |
-// V ring [kStages][KB][128][128 B]; 1024-byte aligned (128-byte swizzle atoms).
+// Shared memory: K ring [NS][KB][128 rows][128 B] | V ring [NS][KB][128][128 B];
+// 1024-byte aligned (128-byte swizzle atoms).  Q lives in tensor memory.
 template <int D>
 struct PrefillSmem {
     static constexpr int KB = D / 64;
+    static constexpr int NS = 3;                    // ring depth
     static constexpr int TILE = KB * kRows * 128;   // bytes of one 128-row operand tile
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = TILE;
-    static constexpr int V_OFF = (1 + kStages) * TILE;
-    static constexpr int BYTES = (1 + 2 * kStages) * TILE;
+    static constexpr int K_OFF = 0;
+    static constexpr int V_OFF = NS * TILE;
+    static constexpr int BYTES = 2 * NS * TILE;
     static constexpr int ALLOC = BYTES + 1024;
 };
 
+// TMEM columns: S buffers 0 and 128 (fp32 scores of one K/V tile), O at 256 (fp32),
+// P at 384 (bf16 pairs, 64 columns), Q at 448 (bf16 pairs, D/2 columns).  Q K^T reads
+// its A operand (Q) and P V its A operand (P) from tensor memory, so each MMA streams
+// only its B operand (a K or V tile) from shared memory.
+//
+// Softmax: two warpgroups split every score row: warps 0-3 take columns 0-63 of the
+// tile, warps 4-7 columns 64-127 (the same TMEM lanes, i.e. the same query rows).  The
+// partners exchange their row max through shared memory once per tile; each keeps its
+// own partial row sum, the halves are added at the end.
 template <int D, int BS, int G>
 __global__ void __launch_bounds__(kThreads, 1)
-    pkv_prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                       const __grid_constant__ CUtensorMap tv, const PrefillArgs a) {
+    pkv_prefill_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                       const PrefillArgs a) {
     using SM = PrefillSmem<D>;
     constexpr int KB = SM::KB;
+    constexpr int NS = SM::NS;
     constexpr int TQ = kRows / G;            // query tokens per tile
     constexpr int PAGES = kKvTile / BS;      // pages per K/V tile
+    constexpr int HALF = kKvTile / 2;        // score columns per softmax warpgroup
+    constexpr int DH = D / 2;                // O / Q columns per warpgroup (d values)
     constexpr uint32_t ID_S = idesc_bf16(kRows, kKvTile, 0);
     constexpr uint32_t ID_O = idesc_bf16(kRows, D, 1);
 
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[8 + 4 * kStages];
+    __shared__ __align__(8) uint64_t bars[8 + 4 * NS];
     __shared__ uint32_t tmem_base_s;
     __shared__ int abort_s;
+    __shared__ float xch[2][2][kRows];       // [tile parity][half][row]: partial row maxima
+    __shared__ float xl[2][kRows];           // [half][row]: partial row sums
 
     pdl_launch_dependents();
     pdl_wait();
@@ -216,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int seq = a.seq_lens[r];
     if (q_len < 0) q_len = 0;
     if (q0 < 0 || q0 + q_len > a.total_q) {
-        if (threadIdx.x == 0 && tile == 0 && h == 0 && a.err) flag_err(a.err, PKV_DEVERR_QLEN_CLAMPED);
+        if (threadIdx.x == 0 && tile == 0 && h == 0) flag_err(a.err, PKV_DEVERR_QLEN_CLAMPED);
         return;
     }
     const int ctx = seq - q_len;             // tokens before the chunk
@@ -226,8 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         q_len = a.max_q_len;
     }
     if (tile * TQ >= q_len) return;          // past this request's queries: no work
-    const int qi_last = min(tile * TQ + TQ, q_len) - 1;
-    int kv_end = ctx + qi_last + 1;          // tokens the tile's last query sees
+    int kv_end = ctx + min(tile * TQ + TQ, q_len);   // tokens the tile's last query sees
     if (kv_end > seq) kv_end = seq;
     if (kv_end > a.MB * BS) kv_end = a.MB * BS;
     if (kv_end < 0) kv_end = 0;
@@ -235,38 +261,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-    const uint32_t sQ = smem_u32(sm + SM::Q_OFF);
     const uint32_t sK = smem_u32(sm + SM::K_OFF);
     const uint32_t sV = smem_u32(sm + SM::V_OFF);
-    const uint32_t bar_q = smem_u32(&bars[0]);
-    const uint32_t bar_s_full = smem_u32(&bars[1]);     // [2]
-    const uint32_t bar_s_free = smem_u32(&bars[3]);     // [2]
-    const uint32_t bar_p_ready = smem_u32(&bars[5]);
-    const uint32_t bar_pv = smem_u32(&bars[6]);
-    const uint32_t bar_k_full = smem_u32(&bars[8]);                 // [kStages]
-    const uint32_t bar_k_empty = smem_u32(&bars[8 + kStages]);      // [kStages]
-    const uint32_t bar_v_full = smem_u32(&bars[8 + 2 * kStages]);   // [kStages]
-    const uint32_t bar_v_empty = smem_u32(&bars[8 + 3 * kStages]);  // [kStages]
+    const uint32_t bar_q = smem_u32(&bars[0]);          // Q stored to TMEM (8 warps)
+    const uint32_t bar_p_ready = smem_u32(&bars[1]);    // P stored (8 warps)
+    const uint32_t bar_pv = smem_u32(&bars[2]);
+    const uint32_t bar_s_full = smem_u32(&bars[3]);     // [2]
+    const uint32_t bar_s_free = smem_u32(&bars[5]);     // [2] (8 warps)
+    const uint32_t bar_v_tail = smem_u32(&bars[7]);     // last V tile's tail zeroed
+    const uint32_t bar_k_full = smem_u32(&bars[8]);            // [NS]
+    const uint32_t bar_k_empty = smem_u32(&bars[8 + NS]);      // [NS]
+    const uint32_t bar_v_full = smem_u32(&bars[8 + 2 * NS]);   // [NS]
+    const uint32_t bar_v_empty = smem_u32(&bars[8 + 3 * NS]);  // [NS]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
-        mbar_init(bar_q, 1);
+        mbar_init(bar_q, 8);
+        mbar_init(bar_p_ready, 8);
+        mbar_init(bar_pv, 1);
+        mbar_init(bar_v_tail, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(bar_s_full + 8 * i, 1);
-            mbar_init(bar_s_free + 8 * i, 4);
+            mbar_init(bar_s_free + 8 * i, 8);
         }
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(bar_k_full + 8 * i, 1);
             mbar_init(bar_k_empty + 8 * i, 1);
             mbar_init(bar_v_full + 8 * i, 1);
             mbar_init(bar_v_empty + 8 * i, 1);
         }
-        mbar_init(bar_p_ready, 4);
-        mbar_init(bar_pv, 1);
         abort_s = 0;
         fence_mbar_init();
     }
-    if (warp == 4) {
+    if (warp == 8) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(&tmem_base_s)),
                      "r"(kTmemCols)
@@ -279,35 +306,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_base_s;
     volatile int* abort_v = &abort_s;
 
-    if (warp == 4 || warp == 5) {
-        // ---------------------------------------------------------- TMA producers
-        // warp 4 feeds the K ring (and loads Q), warp 5 the V ring; a K slot frees when
-        // its Q K^T completes, a V slot when its P V completes, so K runs further ahead
-        const bool is_k = warp == 4;
-        if (is_k && lane == 0) {
-            prefetch_tensormap(&tq);
-            prefetch_tensormap(&tk);
-            mbar_arrive_expect_tx(bar_q, KB * kRows * 128);
-            for (int kb = 0; kb < KB; ++kb)
-                tma_load_3d(sQ + kb * kRows * 128, &tq, kb * 64, h * G, q0 + tile * TQ, bar_q);
+    // a bounded wait by lane 0, its outcome broadcast to the warp (a time-out also
+    // raises the abort flag, which the other roles see at their next failed wait)
+    auto warp_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait_bounded(bar, parity, kWaitNs);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok && lane == 0) {
+            flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT);
+            *abort_v = 1;
         }
-        if (!is_k && lane == 0) prefetch_tensormap(&tv);
+        return ok;
+    };
+    // the same for a single thread
+    auto thread_wait = [&](uint32_t bar, uint32_t parity) -> bool {
+        if (mbar_wait_bounded(bar, parity, kWaitNs)) return true;
+        flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT);
+        *abort_v = 1;
+        return false;
+    };
+
+    if (warp == 8 || warp == 9) {
+        // ---------------------------------------------------------- TMA producers
+        // warp 8 feeds the K ring, warp 9 the V ring; a K slot frees when its Q K^T
+        // completes, a V slot when its P V completes
+        const bool is_k = warp == 8;
+        if (lane == 0) prefetch_tensormap(is_k ? &tk : &tv);
         const CUtensorMap* map = is_k ? &tk : &tv;
         const uint32_t ring = is_k ? sK : sV;
         const uint32_t full = is_k ? bar_k_full : bar_v_full;
         const uint32_t empty = is_k ? bar_k_empty : bar_v_empty;
         const int64_t row_end = (int64_t)a.NB * a.Hkv * BS;   // first row past the pool
         for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % kStages;
-            if (j >= kStages) {
-                bool ok = true;
-                if (lane == 0) ok = mbar_wait_bounded(empty + 8 * st, ((j / kStages) - 1) & 1, kWaitNs);
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-                if (!ok) {
-                    if (lane == 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
-                    break;
-                }
-            }
+            const int st = j % NS;
+            if (j >= NS && !warp_wait(empty + 8 * st, ((j / NS) - 1) & 1)) break;
             if (*abort_v) break;
             const int lb0 = j * PAGES;
             int npages = (kv_end - lb0 * BS + BS - 1) / BS;
@@ -331,35 +363,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (int)row, full + 8 * st);
             }
         }
-    } else if (warp == 6) {
-        // ---------------------------------------------------------- MMA issuer
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait_bounded(bar_q, 0, kWaitNs);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok && lane == 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
-        auto issue_pv = [&](int t) -> bool {
-            const int vs = t % kStages;
-            bool w = true;
-            if (lane == 0) {
-                w = mbar_wait_bounded(bar_v_full + 8 * vs, (t / kStages) & 1, kWaitNs);
-                if (w) w = mbar_wait_bounded(bar_p_ready, t & 1, kWaitNs);
-            }
-            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-            if (!w) return false;
-            // the last tile: zero V rows at or past kv_end (partial page, missing pages),
-            // so P = 0 never meets stale or NaN values
-            const int valid = kv_end - t * kKvTile;
-            if (valid < kKvTile) {
-                uint8_t* vst = sm + SM::V_OFF + vs * SM::TILE;
+        // V of the last tile: once it has landed, zero its rows at or past kv_end (the
+        // partial page, pages past the request), so P = 0 never meets stale or NaN bytes
+        const int tail = n_tiles - 1;
+        const int valid = kv_end - tail * kKvTile;
+        if (!is_k && n_tiles > 0 && valid < kKvTile && !*abort_v) {
+            if (warp_wait(bar_v_full + 8 * (tail % NS), (tail / NS) & 1)) {
+                uint8_t* vst = sm + SM::V_OFF + (tail % NS) * SM::TILE;
                 for (int kb = 0; kb < KB; ++kb)
                     for (int rr = valid + (lane >> 3); rr < kKvTile; rr += 4)
-                        *reinterpret_cast<uint4*>(vst + kb * kRows * 128 + rr * 128 + (lane & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(vst + kb * kRows * 128 + rr * 128 +
+                                                  (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 fence_proxy_async_smem();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(bar_v_tail);
             }
-            tc_fence_after();
-            if (lane == 0) {
+        }
+    } else if (warp == 10) {
+        // ---------------------------------------------------------- MMA issuer (lane 0)
+        if (lane == 0) {
+            auto issue_pv = [&](int t) -> bool {
+                const int vs = t % NS;
+                if (!thread_wait(bar_v_full + 8 * vs, (t / NS) & 1)) return false;
+                if (t == n_tiles - 1 && kv_end - t * kKvTile < kKvTile &&
+                    !thread_wait(bar_v_tail, 0))
+                    return false;
+                if (!thread_wait(bar_p_ready, t & 1)) return false;
+                tc_fence_after();
                 const uint32_t vbase = sV + vs * SM::TILE;
 #pragma unroll
                 for (int k = 0; k < kKvTile / 16; ++k) {
@@ -368,85 +398,98 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mma_commit(bar_pv);
                 mma_commit(bar_v_empty + 8 * vs);
-            }
-            __syncwarp();
-            return true;
-        };
-        int issued_pv = 0;
-        for (int j = 0; ok && j < n_tiles; ++j) {
-            const int sb = j & 1, ks = j % kStages;
-            bool w = true;
-            if (lane == 0) {
-                w = mbar_wait_bounded(bar_k_full + 8 * ks, (j / kStages) & 1, kWaitNs);
-                if (w && j >= 2) w = mbar_wait_bounded(bar_s_free + 8 * sb, ((j - 2) >> 1) & 1, kWaitNs);
-            }
-            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-            if (!w || *abort_v) { ok = false; break; }
+                return true;
+            };
+            bool ok = thread_wait(bar_q, 0);
             tc_fence_after();
-            if (lane == 0) {
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                const int sb = j & 1, ks = j % NS;
+                if (!thread_wait(bar_k_full + 8 * ks, (j / NS) & 1)) { ok = false; break; }
+                if (j >= 2 && !thread_wait(bar_s_free + 8 * sb, ((j - 2) >> 1) & 1)) { ok = false; break; }
+                tc_fence_after();
                 const uint32_t kbase = sK + ks * SM::TILE;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const int kb = k >> 2;
-                    const uint32_t off = (uint32_t)(kb * kRows * 128 + (k & 3) * 32);
-                    mma_ss(tmem + (sb ? kColS1 : kColS0), smem_desc_sw128(sQ + off, 16, 1024),
+                    const uint32_t off = (uint32_t)((k >> 2) * kRows * 128 + (k & 3) * 32);
+                    mma_ts(tmem + sb * 128, tmem + kColQ + k * 8,
                            smem_desc_sw128(kbase + off, 16, 1024), ID_S, k > 0 ? 1u : 0u);
                 }
                 mma_commit(bar_s_full + 8 * sb);
                 mma_commit(bar_k_empty + 8 * ks);
+                // the previous tile's P V runs after this tile's scores are queued
+                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
-            __syncwarp();
-            if (j >= 1) {
-                if (!issue_pv(j - 1)) { ok = false; break; }
-                issued_pv = j;
-            }
+            if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
         }
-        if (ok && n_tiles > 0) {
-            if (!issue_pv(n_tiles - 1)) ok = false;
-            else issued_pv = n_tiles;
-        }
-        if (!ok && lane == 0 && n_tiles > 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
-        (void)issued_pv;
+        __syncwarp();
     } else {
-        // ---------------------------------------------------------- softmax warps 0-3
-        const int m = tid;                       // query row = TMEM lane
+        // ---------------------------------------------------------- softmax, 2 x 4 warps
+        const int hf = warp >> 2;                // column half of every score row
+        const int m = tid & 127;                 // query row = TMEM lane
         const int tq_i = m / G, g = m - (m / G) * G;
         const int qi = tile * TQ + tq_i;
         const bool row_valid = qi < q_len;
         int vis = row_valid ? ctx + qi + 1 : 0;  // tokens this row sees
         if (vis > kv_end) vis = kv_end;
         if (vis < 0) vis = 0;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const int nbar = 1 + (warp & 3);         // named barrier of this warp pair
+        // Q row (this half's D/2 values) into tensor memory
+        {
+            uint32_t w[DH / 2];
+            if (row_valid) {
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    a.q + ((int64_t)(q0 + qi) * a.Hq + (int64_t)h * G + g) * D + hf * DH);
+#pragma unroll
+                for (int i = 0; i < DH / 8; ++i) {
+                    const uint4 v4 = src[i];
+                    w[4 * i] = v4.x;
+                    w[4 * i + 1] = v4.y;
+                    w[4 * i + 2] = v4.z;
+                    w[4 * i + 3] = v4.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < DH / 2; ++i) w[i] = 0u;
+            }
+            tmem_st_words<DH / 2>(lane_base + kColQ + hf * (DH / 2), w);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_q);
+        }
         float m_ref = -INFINITY;                 // reference max (log2 domain) of O and l
-        float l = 0.f;
+        float l = 0.f;                           // this half's partial row sum
+        // A failed wait marks the rows bad (zero output, flagged) but never leaves the
+        // loop: the partner warp must meet every named barrier below.
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             const int sb = j & 1;
-            bool w = true;
-            if (lane == 0) w = mbar_wait_bounded(bar_s_full + 8 * sb, (j >> 1) & 1, kWaitNs);
-            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-            if (!w || *abort_v) { ok = false; break; }
+            if (ok && !warp_wait(bar_s_full + 8 * sb, (j >> 1) & 1)) ok = false;
             tc_fence_after();
-            float s[kKvTile];
-            tmem_ld128(lane_base + (sb ? kColS1 : kColS0), s);
+            float s[HALF];
+            tmem_ld64(lane_base + sb * 128 + hf * HALF, s);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_s_free + 8 * sb);
-            // mask (diagonal and tail tiles only), tile max on raw scores (scale > 0)
-            const int lim = vis - j * kKvTile;   // columns >= lim are masked
-            if (lim < kKvTile) {
+            // mask (diagonal and tail tiles only), partial max on raw scores (scale > 0)
+            const int lim = vis - j * kKvTile - hf * HALF;   // columns >= lim are masked
+            if (lim < HALF) {
 #pragma unroll
-                for (int c = 0; c < kKvTile; ++c) s[c] = c < lim ? s[c] : -INFINITY;
+                for (int c = 0; c < HALF; ++c) s[c] = c < lim ? s[c] : -INFINITY;
             }
             float m8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) m8[i] = s[i];
 #pragma unroll
-            for (int c = 8; c < kKvTile; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
-            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) *
-                             a.scale_log2;
+            for (int c = 8; c < HALF; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
+            const float pmx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                    fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            xch[sb][hf][m] = pmx;
+            named_barrier_sync(nbar, 64);
+            const float mx = fmaxf(pmx, xch[sb][hf ^ 1][m]) * a.scale_log2;
             // raise the reference max only when a score passes it by more than 2^8
+            // (both halves take the same decision from the same numbers)
             float alpha = 1.f;
             bool rescale = false;
             if (mx > m_ref + 8.f) {
@@ -456,12 +499,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
             }
             const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-            uint32_t p[kKvTile / 2];
+            uint32_t p[HALF / 2];
             float l8[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) l8[i] = 0.f;
 #pragma unroll
-            for (int c = 0; c < kKvTile; c += 2) {
+            for (int c = 0; c < HALF; c += 2) {
                 const float e0 = ex2_approx(fmaf(s[c], a.scale_log2, nmu));
                 const float e1 = ex2_approx(fmaf(s[c + 1], a.scale_log2, nmu));
                 p[c / 2] = pack_bf16x2(e0, e1);
@@ -470,23 +513,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             // P buffer and O are free once the previous P V has completed
             if (j >= 1) {
-                if (lane == 0) w = mbar_wait_bounded(bar_pv, (j - 1) & 1, kWaitNs);
-                w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-                if (!w || *abort_v) { ok = false; break; }
+                if (ok && !warp_wait(bar_pv, (j - 1) & 1)) ok = false;
                 tc_fence_after();
             }
             if (__any_sync(0xffffffffu, rescale)) {
                 const float f = rescale ? alpha : 1.f;
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                for (int c = 0; c < DH / 32; ++c) {
                     float o[32];
-                    tmem_ld32(lane_base + kColO + c * 32, o);
+                    tmem_ld32(lane_base + kColO + hf * DH + c * 32, o);
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= f;
-                    tmem_st32f(lane_base + kColO + c * 32, o);
+                    tmem_st32f(lane_base + kColO + hf * DH + c * 32, o);
                 }
             }
-            tmem_st64(lane_base + kColP, p);
+            tmem_st32(lane_base + kColP + hf * (HALF / 2), p);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -494,20 +535,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // ------------------------------------------------------------ epilogue
         if (ok && n_tiles > 0) {
-            bool w = true;
-            if (lane == 0) w = mbar_wait_bounded(bar_pv, (n_tiles - 1) & 1, kWaitNs);
-            w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-            if (!w) ok = false;
+            ok = warp_wait(bar_pv, (n_tiles - 1) & 1);
             tc_fence_after();
         }
-        if (!ok && n_tiles > 0 && lane == 0) { flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT); *abort_v = 1; }
-        const float inv = (l > 0.f && ok) ? 1.f / l : 0.f;
-        uint16_t* orow = a.out + ((int64_t)(q0 + qi) * a.Hq + (int64_t)h * G + g) * D;
+        xl[hf][m] = l;                           // the halves' partial sums
+        named_barrier_sync(nbar, 64);
+        const float lt = l + xl[hf ^ 1][m];
+        const float inv = (lt > 0.f && ok) ? 1.f / lt : 0.f;
+        uint16_t* orow = a.out + ((int64_t)(q0 + qi) * a.Hq + (int64_t)h * G + g) * D + hf * DH;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < DH / 32; ++c) {
             float o[32];
             if (n_tiles > 0 && ok) {
-                tmem_ld32(lane_base + kColO + c * 32, o);
+                tmem_ld32(lane_base + kColO + hf * DH + c * 32, o);
             } else {
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = 0.f;
@@ -515,19 +555,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_valid) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 8) {
-                    uint4 u;
-                    u.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
-                    u.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
-                    u.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
-                    u.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
-                    *reinterpret_cast<uint4*>(orow + c * 32 + i) = u;
+                    uint4 u4;
+                    u4.x = pack_bf16x2(o[i] * inv, o[i + 1] * inv);
+                    u4.y = pack_bf16x2(o[i + 2] * inv, o[i + 3] * inv);
+                    u4.z = pack_bf16x2(o[i + 4] * inv, o[i + 5] * inv);
+                    u4.w = pack_bf16x2(o[i + 6] * inv, o[i + 7] * inv);
+                    *reinterpret_cast<uint4*>(orow + c * 32 + i) = u4;
                 }
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 4) {
+    if (warp == 8) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(kTmemCols)
@@ -554,8 +594,8 @@ PFN_cuTensorMapEncodeTiled_v12000 prefill_encode_fn() {
 }
 
 template <int D, int BS, int G>
-cudaError_t prefill_launch_t(const PrefillLaunch& L, const PrefillArgs& a, const CUtensorMap& tq,
-                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
+cudaError_t prefill_launch_t(const PrefillLaunch& L, const PrefillArgs& a, const CUtensorMap& tk,
+                             const CUtensorMap& tv, cudaStream_t st) {
     auto kern = pkv_prefill_kernel<D, BS, G>;
     // one CTA per SM (it holds all 512 TMEM columns); ask for enough shared memory
     // that no second CTA can be co-resident
@@ -564,18 +604,17 @@ cudaError_t prefill_launch_t(const PrefillLaunch& L, const PrefillArgs& a, const
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3((unsigned)a.tiles, (unsigned)L.Hkv, (unsigned)L.N),
-                      dim3(kThreads), (size_t)smem, st, tq, tk, tv, a);
+                      dim3(kThreads), (size_t)smem, st, tk, tv, a);
 }
 
 template <int D, int BS>
 cudaError_t prefill_launch_g(int G, const PrefillLaunch& L, const PrefillArgs& a,
-                             const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                             cudaStream_t st) {
+                             const CUtensorMap& tk, const CUtensorMap& tv, cudaStream_t st) {
     switch (G) {
-        case 1: return prefill_launch_t<D, BS, 1>(L, a, tq, tk, tv, st);
-        case 2: return prefill_launch_t<D, BS, 2>(L, a, tq, tk, tv, st);
-        case 4: return prefill_launch_t<D, BS, 4>(L, a, tq, tk, tv, st);
-        case 8: return prefill_launch_t<D, BS, 8>(L, a, tq, tk, tv, st);
+        case 1: return prefill_launch_t<D, BS, 1>(L, a, tk, tv, st);
+        case 2: return prefill_launch_t<D, BS, 2>(L, a, tk, tv, st);
+        case 4: return prefill_launch_t<D, BS, 4>(L, a, tk, tv, st);
+        case 8: return prefill_launch_t<D, BS, 8>(L, a, tk, tv, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -595,17 +634,7 @@ int prefill_launch(const PrefillLaunch& L, cudaStream_t st) {
     if (!fn) return PKV_ERR_CUDA;
     const int G = L.Hq / L.Hkv;
     const int TQ = kRows / G;
-    alignas(64) CUtensorMap tq, tk, tv;
-    {
-        cuuint64_t dims[3] = {(cuuint64_t)L.D, (cuuint64_t)L.Hq, (cuuint64_t)L.total_q};
-        cuuint64_t strides[2] = {(cuuint64_t)L.D * 2, (cuuint64_t)L.Hq * L.D * 2};
-        cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)TQ};
-        cuuint32_t es[3] = {1, 1, 1};
-        if (fn(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(L.q), dims, strides, box,
-               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-            return PKV_ERR_CUDA;
-    }
+    alignas(64) CUtensorMap tk, tv;
     const int64_t rows = (int64_t)L.NB * L.Hkv * L.BS;
     for (int i = 0; i < 2; ++i) {
         cuuint64_t dims[2] = {(cuuint64_t)L.D, (cuuint64_t)rows};
@@ -619,6 +648,7 @@ int prefill_launch(const PrefillLaunch& L, cudaStream_t st) {
             return PKV_ERR_CUDA;
     }
     PrefillArgs a;
+    a.q = static_cast<const uint16_t*>(L.q);
     a.q_offsets = L.q_offsets;
     a.block_table = L.block_table;
     a.seq_lens = L.seq_lens;
@@ -631,14 +661,14 @@ int prefill_launch(const PrefillLaunch& L, cudaStream_t st) {
     a.NB = L.NB;
     a.total_q = L.total_q;
     a.max_q_len = L.max_q_len;
-    a.tiles = (L.max_q_len + TQ - 1) / TQ;
+    a.tiles = (L.max_q_len + TQ - 1) / TQ;   // query tiles per request
     a.scale_log2 = L.scale * 1.4426950408889634f;
     if (a.tiles <= 0) return PKV_OK;
     cudaError_t e = cudaErrorInvalidValue;
-    if (L.D == 128 && L.BS == 16) e = prefill_launch_g<128, 16>(G, L, a, tq, tk, tv, st);
-    else if (L.D == 128 && L.BS == 32) e = prefill_launch_g<128, 32>(G, L, a, tq, tk, tv, st);
-    else if (L.D == 64 && L.BS == 16) e = prefill_launch_g<64, 16>(G, L, a, tq, tk, tv, st);
-    else if (L.D == 64 && L.BS == 32) e = prefill_launch_g<64, 32>(G, L, a, tq, tk, tv, st);
+    if (L.D == 128 && L.BS == 16) e = prefill_launch_g<128, 16>(G, L, a, tk, tv, st);
+    else if (L.D == 128 && L.BS == 32) e = prefill_launch_g<128, 32>(G, L, a, tk, tv, st);
+    else if (L.D == 64 && L.BS == 16) e = prefill_launch_g<64, 16>(G, L, a, tk, tv, st);
+    else if (L.D == 64 && L.BS == 32) e = prefill_launch_g<64, 32>(G, L, a, tk, tv, st);
     else return PKV_ERR_UNSUPPORTED;
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }

@@ -183,8 +183,8 @@ def aggregate_sum(value, world, device=None):
 def workload_config(wl):
     return {"workload": wl.name, "batch": wl.N, "num_q_heads": wl.Hq, "num_kv_heads": wl.Hkv,
             "head_dim": wl.D, "block_size": wl.BS,
-            "kv_dtype": ["bf16", "fp8_e4m3", "int8"][wl.kv_kind],
-            "seq_lens": "log-uniform [128, 16384]" if wl.cfg in (5, 7) else
+            "kv_dtype": ["bf16", "fp8_e4m3", "int8", "int4"][wl.kv_kind],
+            "seq_lens": "log-uniform [128, 16384]" if wl.cfg in (5, 7, 9) else
             ("uniform [1024, 8192]" if wl.cfg in (2, 6) else "see workload"),
             "query_tokens_per_request": wl.q_len,
             "mean_seq_len": round(float(wl.seq_lens.mean()), 1), "num_blocks": wl.NB,
@@ -243,7 +243,7 @@ def time_oracle(wl, sample, units):
     t0 = time.perf_counter()
     oracle.decode_rows(q, kc, vc, bt, sl, wl.scale, rows, ks, vs)
     dt = time.perf_counter() - t0
-    nbytes = sum(int(sl[r]) for (r, h) in units) * wl.D * 2 * wl.elt
+    nbytes = int(sum(int(sl[r]) for (r, h) in units) * wl.D * 2 * wl.elt)
     return dt, nbytes
 
 
@@ -294,8 +294,7 @@ def run_ours(args):
     req = torch.from_numpy(req_new).to(dev)
     qoffs = torch.from_numpy(wl.q_offsets()).to(dev)
     if quant:
-        kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D),
-                         dtype=torch.int8 if wl.int8 else torch.uint8, device=dev)
+        kc = torch.zeros(wl.cache_shape, dtype=torch.int8 if wl.int8 else torch.uint8, device=dev)
         vc = torch.zeros_like(kc)
         req_all, pos_all = W.token_rows_order(wl)
         sm_all = pkv.compute_slot_mapping(bt, torch.from_numpy(pos_all).to(dev), wl.BS,
@@ -479,7 +478,7 @@ def run_ours(args):
                 "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
                 "dtype": ("bf16" if not quant else
-                          ["", "fp8_e4m3", "int8"][wl.kv_kind] + " KV, bf16 q/out, fp32 accumulate"),
+                          ["", "fp8_e4m3", "int8", "int4"][wl.kv_kind] + " KV, bf16 q/out, fp32 accumulate"),
                 "data": "synthetic (seeded N(0,1) q/K/V, uniform token ids)",
                 "config": dict(workload_config(wl),
                                parallelism=f"{world} independent replicas (no collective)"),
@@ -682,12 +681,13 @@ def run_reference(args):
     # host copies of a bounded sample (the first 4 requests) drawn on the host generator
     reqs = list(range(min(4, wl.N)))
     sub = W.custom(len(reqs), wl.Hq, wl.Hkv, wl.D, wl.BS, wl.seq_lens[reqs], fp8=wl.fp8,
-                   int8=wl.int8, seed=wl.seed, scale=wl.scale, name=wl.name + "_sample")
+                   int8=wl.int8, int4=wl.int4, seed=wl.seed, scale=wl.scale,
+                   name=wl.name + "_sample")
     hd = W.host_data(sub)
     if sub.quant:
         req_all, pos_all = W.token_rows_order(sub)
         sm = oracle.slot_mapping(sub.block_table, req_all, pos_all, sub.BS)
-        kc = np.zeros((sub.NB, sub.Hkv, sub.BS, sub.D), sub.cache_np_dtype)
+        kc = np.zeros(sub.cache_shape, sub.cache_np_dtype)
         vc = np.zeros_like(kc)
         oracle.kv_cache_write(hd["k_rows"], hd["v_rows"], sm, kc, vc, hd["k_scale"], hd["v_scale"])
         ks, vs = hd["k_scale"], hd["v_scale"]

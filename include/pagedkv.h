@@ -33,9 +33,10 @@
  *   - Layouts are row-major and contiguous:
  *       q, out          bf16 [N][Hq][D]
  *       k, v (new rows) bf16 [T][Hkv][D]
- *       k_cache,v_cache [NB][Hkv][BS][D]  bf16, E4M3 bytes or int8 codes; one
- *                       (block, head) page of BS*D elements is contiguous
- *       k_scale,v_scale fp32 [NB][Hkv]    8-bit caches only
+ *       k_cache,v_cache [NB][Hkv][BS][D]  bf16, E4M3 bytes or int8 codes, or
+ *                       [NB][Hkv][BS][D/2] bytes of int4 codes; one (block, head)
+ *                       page is contiguous
+ *       k_scale,v_scale fp32 [NB][Hkv]    quantised caches only
  *       block_table     int32 [N][MB]     physical block of logical block j of request r
  *       seq_lens        int32 [N]         tokens cached for request r, including the
  *                                         one written this step
@@ -60,9 +61,12 @@ extern "C" {
 /* Same object as cudaStream_t. */
 typedef struct CUstream_st *pkv_stream_t;
 
-/* Cache element type.  The 8-bit kinds carry one fp32 scale per (block, kv head):
- * element value = code * scale. */
-enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1, PKV_INT8 = 2 };
+/* Cache element type.  The quantised kinds carry one fp32 scale per (block, kv
+ * head): element value = code * scale.  PKV_INT4 pages hold two codes per byte,
+ * offset-binary (code = q + 8, q in [-7, 7]): value 2b of a row in the low nibble of
+ * byte b, value 2b+1 in the high nibble; a row of D values is D/2 bytes
+ * ([P3] "优化五：KV 本体压缩": FP16 -> FP8/INT8/INT4). */
+enum { PKV_BF16 = 0, PKV_FP8_E4M3 = 1, PKV_INT8 = 2, PKV_INT4 = 3 };
 
 /* Return codes. */
 enum {

@@ -14,6 +14,7 @@ Sources, by page title and section:
 Parity status per function (what pins it, see tests/test_oracle_pins.py):
   bf16_to_double, e4m3_to_double, e4m3_from_float  -- library codecs (torch CPU) + OCP spec values
   int8_from_float                                  -- torch round-half-even + clamp, brute force
+  int4_code_from_float                             -- nearest-integer brute force, the nibble layout
   kv_cache_write_rescale                           -- the generator's amax/QMAX recipe, written
                                                       independently
   kv_bytes                                         -- the printed 327,680 B/token and ~10 GB at 32K
@@ -76,6 +77,8 @@ def lib():
             L.orc_e4m3_from_float.argtypes = [ctypes.c_float]
             L.orc_int8_from_float.restype = ctypes.c_int8
             L.orc_int8_from_float.argtypes = [ctypes.c_float]
+            L.orc_int4_code_from_float.restype = ctypes.c_uint8
+            L.orc_int4_code_from_float.argtypes = [ctypes.c_float]
             L.orc_kv_bytes.restype = _i64
             L.orc_kv_bytes.argtypes = [_i64] * 5
             L.orc_slot_mapping.restype = None
@@ -133,16 +136,21 @@ def e4m3_from_float(x: float) -> int:
     return int(lib().orc_e4m3_from_float(float(x)))
 
 
+def int4_code_from_float(x: float) -> int:
+    return int(lib().orc_int4_code_from_float(float(x)))
+
+
 def int8_from_float(x: float) -> int:
     return int(lib().orc_int8_from_float(float(x)))
 
 
-def _kind(cache):
-    """0: bf16 bit patterns (uint16), 1: E4M3 bytes (uint8), 2: int8."""
+def _kind(cache, head_dim):
+    """0: bf16 bit patterns (uint16), 1: E4M3 bytes (uint8), 2: int8, 3: int4 (uint8
+    bytes holding two offset-binary codes each, so the last axis is head_dim / 2)."""
     if cache.dtype == np.uint16:
         return 0
     if cache.dtype == np.uint8:
-        return 1
+        return 3 if cache.shape[-1] * 2 == head_dim else 1
     if cache.dtype == np.int8:
         return 2
     raise TypeError(f"cache dtype {cache.dtype}")
@@ -174,11 +182,11 @@ def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=N
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     sm = _c(slot_mapping, np.int64)
-    kind = _kind(k_cache)
+    T, Hkv, D = k.shape
+    kind = _kind(k_cache, D)
     assert k_cache.flags.c_contiguous and v_cache.flags.c_contiguous
     ks = _c(k_scale, np.float32) if kind else None
     vs = _c(v_scale, np.float32) if kind else None
-    T, Hkv, D = k.shape
     lib().orc_kv_cache_write(_ptr(k), _ptr(v), _ptr(sm), T, Hkv, D, k_cache.shape[2], kind,
                              _ptr(k_cache), _ptr(v_cache), _ptr(ks), _ptr(vs))
 
@@ -189,16 +197,16 @@ def kv_cache_write_rescale(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scal
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
     sm = _c(slot_mapping, np.int64)
-    kind = _kind(k_cache)
-    assert kind in (1, 2) and k_scale.dtype == np.float32 and k_scale.flags.c_contiguous
     T, Hkv, D = k.shape
+    kind = _kind(k_cache, D)
+    assert kind in (1, 2, 3) and k_scale.dtype == np.float32 and k_scale.flags.c_contiguous
     lib().orc_kv_cache_write_rescale(_ptr(k), _ptr(v), _ptr(sm), T, Hkv, D, k_cache.shape[2], kind,
                                      _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale))
 
 
 def _decode_args(q, k_cache, v_cache, block_table, seq_lens, k_scale, v_scale):
     q = _c(q, np.uint16)
-    kind = _kind(k_cache)
+    kind = _kind(k_cache, q.shape[-1])
     kc = np.ascontiguousarray(k_cache)
     vc = np.ascontiguousarray(v_cache)
     ks = _c(k_scale, np.float32) if kind else None

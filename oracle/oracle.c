@@ -123,6 +123,23 @@ int8_t orc_int8_from_float(float x)
     return (int8_t)r;
 }
 
+/* Symmetric int4 code of a binary32 value, stored offset-binary in a nibble: the
+ * value q = round-to-nearest-even(x) clamped to [-7, 7] (NaN -> 0) is kept as the
+ * unsigned nibble q + 8 (the INT4 KV of [P3] "优化五：KV 本体压缩"; symmetric, one
+ * scale per (block, head)).  A cache row of D values is D/2 bytes: value 2b sits
+ * in the low nibble of byte b, value 2b+1 in its high nibble. */
+uint8_t orc_int4_code_from_float(float x)
+{
+    double r = rint((double)x);
+    if (isnan(x))
+        r = 0.0;
+    if (r > 7.0)
+        r = 7.0;
+    if (r < -7.0)
+        r = -7.0;
+    return (uint8_t)((int)r + 8);
+}
+
 /* ------------------------------------------------------------------------ */
 /* KV size formula  ([P3] "KV Cache 到底有多大？", KV Size equation)          */
 /* ------------------------------------------------------------------------ */
@@ -168,10 +185,10 @@ void orc_slot_mapping(const int32_t *block_table, int max_blocks_per_seq,
 
 /* Writes row (t, h) of k and v (bf16 [T][Hkv][D]) to cache row
  * [slot / BS][h][slot % BS][:].  bf16 caches receive the bytes unchanged.
- * 8-bit caches receive code(float(x) / scale[blk][h]) where the division is the
- * IEEE binary32 divide and code is E4M3 (RNE, saturating) or int8 (RNE, clamp to
- * +-127).  Tokens with slot < 0 are skipped; every other byte of the caches is
- * left as it was. */
+ * Quantised caches receive code(float(x) / scale[blk][h]) where the division is the
+ * IEEE binary32 divide and code is E4M3 (RNE, saturating), int8 (RNE, clamp to
+ * +-127) or int4 (RNE, clamp to +-7, two codes per byte).  Tokens with slot < 0
+ * are skipped; every other byte of the caches is left as it was. */
 void orc_kv_cache_write(const uint16_t *k, const uint16_t *v,
                         const int64_t *slot_mapping, int num_tokens,
                         int num_kv_heads, int head_dim, int block_size,
@@ -201,6 +218,13 @@ void orc_kv_cache_write(const uint16_t *k, const uint16_t *v,
                     if (cache_kind == 1) {
                         ((uint8_t *)k_cache)[dst + d] = orc_e4m3_from_float(kq);
                         ((uint8_t *)v_cache)[dst + d] = orc_e4m3_from_float(vq);
+                    } else if (cache_kind == 3) {
+                        int64_t byte = (dst + d) >> 1;
+                        int shift = (d & 1) ? 4 : 0;
+                        uint8_t keep = (uint8_t)(0xF0u >> shift);
+                        uint8_t *kb = (uint8_t *)k_cache + byte, *vb = (uint8_t *)v_cache + byte;
+                        *kb = (uint8_t)((*kb & keep) | (orc_int4_code_from_float(kq) << shift));
+                        *vb = (uint8_t)((*vb & keep) | (orc_int4_code_from_float(vq) << shift));
                     } else {
                         ((int8_t *)k_cache)[dst + d] = orc_int8_from_float(kq);
                         ((int8_t *)v_cache)[dst + d] = orc_int8_from_float(vq);
@@ -213,10 +237,10 @@ void orc_kv_cache_write(const uint16_t *k, const uint16_t *v,
 
 /* KV write that first sets the scale of every (block, head) receiving rows in
  * this call: scale = amax / QMAX over the |values| of those rows (QMAX = 448 for
- * E4M3, 127 for int8; binary32 divide; NaN values ignored; amax = 0 gives 1), then
- * writes the rows as orc_kv_cache_write does.  Scales of blocks receiving no row
- * are unchanged, and bytes written to a touched block by earlier calls are not
- * re-coded.  cache_kind 1 or 2. */
+ * E4M3, 127 for int8, 7 for int4; binary32 divide; NaN values ignored; amax = 0
+ * gives 1), then writes the rows as orc_kv_cache_write does.  Scales of blocks
+ * receiving no row are unchanged, and bytes written to a touched block by earlier
+ * calls are not re-coded.  cache_kind 1, 2 or 3. */
 void orc_kv_cache_write_rescale(const uint16_t *k, const uint16_t *v,
                                 const int64_t *slot_mapping, int num_tokens, int num_kv_heads,
                                 int head_dim, int block_size, int cache_kind, void *k_cache,
@@ -249,7 +273,7 @@ void orc_kv_cache_write_rescale(const uint16_t *k, const uint16_t *v,
             }
         }
     }
-    volatile float qmax = cache_kind == 1 ? 448.0f : 127.0f;
+    volatile float qmax = cache_kind == 1 ? 448.0f : (cache_kind == 3 ? 7.0f : 127.0f);
     for (int64_t i = 0; i < nblk * num_kv_heads; ++i) {
         if (kmax[i] < 0.0f)
             continue;
@@ -281,6 +305,11 @@ static double cache_elem(const void *cache, int cache_kind, const float *scale,
     if (cache_kind == 1)
         return orc_e4m3_to_double(((const uint8_t *)cache)[idx]) *
                (double)scale[blk * num_kv_heads + h];
+    if (cache_kind == 3) {   /* int4: nibble d % 2 of byte idx / 2, offset-binary */
+        uint8_t byte = ((const uint8_t *)cache)[idx >> 1];
+        int code = (idx & 1) ? (byte >> 4) : (byte & 0xF);
+        return (double)(code - 8) * (double)scale[blk * num_kv_heads + h];
+    }
     return (double)((const int8_t *)cache)[idx] * (double)scale[blk * num_kv_heads + h];
 }
 

@@ -12,7 +12,7 @@ import os
 import threading
 
 __all__ = [
-    "PkvError", "lib", "library_path", "BF16", "FP8_E4M3", "INT8", "DEVERR_WAIT_TIMEOUT",
+    "PkvError", "lib", "library_path", "BF16", "FP8_E4M3", "INT8", "INT4", "DEVERR_WAIT_TIMEOUT",
     "DEVERR_SEQ_CLAMPED", "DEVERR_BLOCK_RANGE", "compute_slot_mapping", "kv_cache_write",
     "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn",
     "paged_decode_attn_noalloc", "prefix_block_hash", "multiquery_workspace_size",
@@ -24,6 +24,7 @@ __all__ = [
 BF16 = 0
 FP8_E4M3 = 1
 INT8 = 2
+INT4 = 3
 DEVERR_WAIT_TIMEOUT = 0x1
 DEVERR_SEQ_CLAMPED = 0x2
 DEVERR_BLOCK_RANGE = 0x4
@@ -143,11 +144,15 @@ def _need(t, name, dtypes, contiguous=True):
     return t
 
 
-def _cache_dtype(t):
+def _cache_dtype(t, head_dim):
+    """Page kind of a cache tensor: int8 codes, int4 (uint8 bytes holding two codes, last
+    axis head_dim / 2), E4M3 bytes (uint8, last axis head_dim) or bf16."""
     import torch
     if t.dtype == torch.int8:
         return INT8
-    return FP8_E4M3 if t.element_size() == 1 else BF16
+    if t.element_size() == 1:
+        return INT4 if t.shape[-1] * 2 == head_dim else FP8_E4M3
+    return BF16
 
 
 def device_num_sms() -> int:
@@ -183,7 +188,7 @@ def kv_cache_write(k, v, slot_mapping, k_cache, v_cache, k_scale=None, v_scale=N
     T, Hkv, D = k.shape
     NB, _, BS, _ = k_cache.shape
     _check("pkv_kv_cache_write", lib().pkv_kv_cache_write(
-        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, BS, NB, _cache_dtype(k_cache),
+        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, BS, NB, _cache_dtype(k_cache, D),
         _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _stream(stream)))
 
 
@@ -203,7 +208,7 @@ def kv_cache_write_rescale(k, v, slot_mapping, k_cache, v_cache, k_scale, v_scal
     if workspace is None:
         workspace = torch.empty(n, dtype=torch.uint8, device=k.device)
     _check("pkv_kv_cache_write_rescale", lib().pkv_kv_cache_write_rescale(
-        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, BS, NB, _cache_dtype(k_cache),
+        _ptr(k), _ptr(v), _ptr(slot_mapping), T, Hkv, D, BS, NB, _cache_dtype(k_cache, D),
         _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(workspace),
         workspace.numel(), _stream(stream)))
 
@@ -241,7 +246,7 @@ def paged_decode_attn(q, k_cache, v_cache, block_table, seq_lens, scale, out=Non
     _need(seq_lens, "seq_lens", (torch.int32,))
     N, Hq, D = q.shape
     NB, Hkv, BS, _ = k_cache.shape
-    dt = _cache_dtype(k_cache)
+    dt = _cache_dtype(k_cache, D)
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -275,7 +280,7 @@ def paged_multiquery_attn(q, q_offsets, max_q_len, k_cache, v_cache, block_table
     T, Hq, D = q.shape
     NB, Hkv, BS, _ = k_cache.shape
     N = seq_lens.shape[0]
-    dt = _cache_dtype(k_cache)
+    dt = _cache_dtype(k_cache, D)
     if out is None:
         out = torch.empty_like(q)
     if workspace is None:
@@ -307,7 +312,7 @@ def paged_decode_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, scale,
         out = torch.empty_like(q)
     _check("pkv_paged_decode_attn_noalloc", lib().pkv_paged_decode_attn_noalloc(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
-        block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D, BS, NB, _cache_dtype(k_cache),
+        block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D, BS, NB, _cache_dtype(k_cache, D),
         float(scale), _ptr(out), _stream(stream)))
     return out
 
@@ -338,7 +343,7 @@ def copy_blocks(k_cache, v_cache, block_mapping, k_scale=None, v_scale=None, str
     NB, Hkv, BS, D = k_cache.shape
     _check("pkv_copy_blocks", lib().pkv_copy_blocks(
         _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_mapping),
-        block_mapping.numel() // 2, Hkv, D, BS, NB, _cache_dtype(k_cache), _stream(stream)))
+        block_mapping.numel() // 2, Hkv, D, BS, NB, _cache_dtype(k_cache, D), _stream(stream)))
 
 
 class BlockManager:

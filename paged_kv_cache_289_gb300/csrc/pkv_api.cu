@@ -16,7 +16,7 @@ bool shape_supported(int Hq, int Hkv, int D, int BS, int dtype) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || Hq / Hkv > pkv::kGroupPad) return false;
     if (BS != 16 && BS != 32) return false;
     if (dtype == PKV_BF16) return D == 64 || D == 128;
-    if (dtype == PKV_FP8_E4M3 || dtype == PKV_INT8) return D == 128;
+    if (dtype == PKV_FP8_E4M3 || dtype == PKV_INT8 || dtype == PKV_INT4) return D == 128;
     return false;
 }
 
@@ -72,7 +72,8 @@ int pkv_kv_cache_write(const void* k, const void* v, const int64_t* slot_mapping
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
-    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8)
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8 &&
+        cache_dtype != PKV_INT4)
         return PKV_ERR_UNSUPPORTED;
     if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PKV_OK;
@@ -100,7 +101,8 @@ int pkv_kv_cache_write_rescale(const void* k, const void* v, const int64_t* slot
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
-    if (cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8) return PKV_ERR_UNSUPPORTED;
+    if (cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8 && cache_dtype != PKV_INT4)
+        return PKV_ERR_UNSUPPORTED;
     if (head_dim % 8 != 0) return PKV_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PKV_OK;
     if (!k || !v || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
@@ -124,7 +126,7 @@ size_t pkv_multiquery_workspace_size(int batch, int num_q_heads, int num_kv_head
     if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype)) return 0;
     if (num_sms <= 0 && current_num_sms(&num_sms) != PKV_OK) return 0;
     return pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
-                                       cache_dtype != PKV_BF16, num_sms, max_q_len);
+                                       cache_dtype, num_sms, max_q_len);
 }
 
 size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim,
@@ -142,7 +144,8 @@ int pkv_paged_multiquery_attn(const void* q, const int32_t* q_offsets, int max_q
                               void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
     if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || max_q_len < 1)
         return PKV_ERR_INVALID_ARG;
-    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8)
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8 &&
+        cache_dtype != PKV_INT4)
         return PKV_ERR_UNSUPPORTED;
     if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, cache_dtype))
         return PKV_ERR_UNSUPPORTED;
@@ -164,7 +167,7 @@ int pkv_paged_multiquery_attn(const void* q, const int32_t* q_offsets, int max_q
     int num_sms = 0;
     if (current_num_sms(&num_sms) != PKV_OK) return PKV_ERR_CUDA;
     const size_t need = pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
-                                                    cache_dtype != PKV_BF16, num_sms,
+                                                    cache_dtype, num_sms,
                                                     max_q_len);
     if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
     if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
@@ -266,10 +269,12 @@ int pkv_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
         num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
-    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8)
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8 &&
+        cache_dtype != PKV_INT4)
         return PKV_ERR_UNSUPPORTED;
-    const int64_t elt = cache_dtype == PKV_BF16 ? 2 : 1;
-    const int64_t block_bytes = (int64_t)num_kv_heads * block_size * head_dim * elt;
+    const int64_t elems = (int64_t)num_kv_heads * block_size * head_dim;
+    const int64_t block_bytes = cache_dtype == PKV_BF16 ? 2 * elems
+                                : (cache_dtype == PKV_INT4 ? elems / 2 : elems);
     if (block_bytes % 16 != 0) return PKV_ERR_UNSUPPORTED;
     if (num_pairs == 0) return PKV_OK;
     if (!k_cache || !v_cache || !block_mapping) return PKV_ERR_INVALID_ARG;

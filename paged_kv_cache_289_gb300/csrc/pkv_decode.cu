@@ -71,11 +71,13 @@ struct DecodeArgs {
     uint32_t epoch;     // differs between calls (graph replays reuse one; counters reset)
 };
 
-template <int D, int BS, bool FP8>
+template <int D, int BS, int KT>
 struct Cfg {
+    static constexpr bool FP8 = KT != 0;                  // quantised pages (one scale each)
+    static constexpr bool I4 = KT == 3;                   // int4: two codes per byte
     static constexpr int ELT = FP8 ? 1 : 2;
-    static constexpr int ROW_BYTES = D * ELT;
-    static constexpr int CH = ROW_BYTES / 128;            // 128-byte column chunks per row
+    static constexpr int ROW_BYTES = I4 ? D / 2 : D * ELT;
+    static constexpr int CH = I4 ? 1 : ROW_BYTES / 128;   // 128-byte column chunks per row
     static constexpr int CH_ELEMS = 128 / ELT;            // elements per chunk
     static constexpr int TT = FP8 ? BS : 16;              // tokens per pipeline tile
     static constexpr int SUB = BS / TT;                   // tiles per page (1 or 2)
@@ -84,7 +86,9 @@ struct Cfg {
     static constexpr int MT = TT / 16;                    // 16-token mma tiles per tile
     static constexpr int KS = D / 16;                     // QK k-steps
     static constexpr int DT = D / 16;                     // PV d-tiles
-    static_assert(ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle lines");
+    // 8/16-bit rows are whole 128-byte swizzle lines; int4 rows (64 bytes at D = 128)
+    // are stored unswizzled
+    static_assert(I4 || ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle lines");
     static_assert(BS % 16 == 0, "block size must be a multiple of 16");
     static_assert(SUB == 1 || SUB == 2, "one or two tiles per page");
 };
@@ -261,8 +265,8 @@ template <int D, int BS, int KT, int QT>
 __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
     pkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
-    constexpr bool FP8 = KT != 0;   // 8-bit pages (E4M3 or int8) with per-(block, head) scales
-    using C = Cfg<D, BS, FP8>;
+    constexpr bool FP8 = KT != 0;   // quantised pages (E4M3, int8, int4) with per-(block, head) scales
+    using C = Cfg<D, BS, KT>;
     extern __shared__ uint8_t smem_raw[];
     const int NW = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
@@ -364,13 +368,20 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
             const int y = (id * a.Hkv + h) * BS + sub * C::TT;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
+            if constexpr (C::I4) {
+                // one box per tile: TT rows of D/2 bytes, unswizzled
+                tma_load_2d_hint(dst, &tmK, 0, y, bar, policy);
+                tma_load_2d_hint(dst + C::TILE_BYTES, &tmV, 0, y, bar, policy);
+            } else {
 #pragma unroll
-            for (int ch = 0; ch < C::CH; ++ch)
-                tma_load_2d_hint(dst + ch * (C::TT * 128), &tmK, ch * C::CH_ELEMS, y, bar, policy);
+                for (int ch = 0; ch < C::CH; ++ch)
+                    tma_load_2d_hint(dst + ch * (C::TT * 128), &tmK, ch * C::CH_ELEMS, y, bar,
+                                     policy);
 #pragma unroll
-            for (int ch = 0; ch < C::CH; ++ch)
-                tma_load_2d_hint(dst + C::TILE_BYTES + ch * (C::TT * 128), &tmV, ch * C::CH_ELEMS,
-                                 y, bar, policy);
+                for (int ch = 0; ch < C::CH; ++ch)
+                    tma_load_2d_hint(dst + C::TILE_BYTES + ch * (C::TT * 128), &tmV,
+                                     ch * C::CH_ELEMS, y, bar, policy);
+            }
         }
     };
 
@@ -442,6 +453,52 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                     }
                 }
                 qscale = a.scale_log2;
+            } else if constexpr (C::I4) {
+                // k-slot mapping for int4 A fragments (see the K path): for mma (dblk, i),
+                // slots 2c,2c+1 <-> d = 64 dblk + 8c + i, +4 and slots 8+2c,9+2c <->
+                // d = 64 dblk + 32 + 8c + i, +4.  Group gi of this lane: d = 32 gi + 8c + 0..7.
+                uint4 raw4[4][QT];
+                float amax = 0.f;
+#pragma unroll
+                for (int qi = 0; qi < QT; ++qi) {
+                    const bool gv = g < a.G && qi < seg_qlen;
+                    const uint16_t* qrow =
+                        a.q + ((int64_t)(seg_qb + qi) * a.Hq + (int64_t)h * a.G + g) * D;
+#pragma unroll
+                    for (int gi = 0; gi < 4; ++gi) {
+                        raw4[gi][qi] = gv ? __ldg(reinterpret_cast<const uint4*>(qrow + 32 * gi + 8 * c))
+                                          : make_uint4(0u, 0u, 0u, 0u);
+                        const uint32_t w4[4] = {raw4[gi][qi].x, raw4[gi][qi].y, raw4[gi][qi].z,
+                                                raw4[gi][qi].w};
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo_to_f32(w4[k])),
+                                                     fabsf(bf16_hi_to_f32(w4[k]))));
+                    }
+                }
+#pragma unroll
+                for (int o2 = 16; o2 > 0; o2 >>= 1)
+                    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o2));
+                int E = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+                E = max(E, 15);
+                const float sc = __uint_as_float((uint32_t)(268 - E) << 23);
+                const float inv_sc = __uint_as_float((uint32_t)(E - 14) << 23);
+                auto qv = [&](const uint4& u, int j) {   // bf16 value j (0..7) of u, as fp32
+                    const uint32_t w = j < 2 ? u.x : (j < 4 ? u.y : (j < 6 ? u.z : u.w));
+                    return (j & 1) ? bf16_hi_to_f32(w) : bf16_lo_to_f32(w);
+                };
+#pragma unroll
+                for (int qi = 0; qi < QT; ++qi)
+#pragma unroll
+                    for (int dblk = 0; dblk < 2; ++dblk)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const uint4& A = raw4[2 * dblk][qi];
+                            const uint4& B = raw4[2 * dblk + 1][qi];
+                            qf[dblk * 4 + i][qi][0] = pack_f16x2(qv(A, i) * sc, qv(A, i + 4) * sc);
+                            qf[dblk * 4 + i][qi][1] = pack_f16x2(qv(B, i) * sc, qv(B, i + 4) * sc);
+                        }
+                qscale = a.scale_log2 * inv_sc;
             } else {
                 // k-slot mapping for E4M3 A fragments: slots 2c,2c+1 <-> d = 4c,4c+1 and
                 // slots 8+2c,9+2c <-> d = 4c+2,4c+3 of each 16-d step.
@@ -501,7 +558,15 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
 
         // rows past the request's length hold stale data: zero them in V so that
         // P = 0 times them stays 0 even if they hold NaN patterns
-        if (ntok < C::TT) {
+        if (C::I4 && ntok < C::TT) {
+            uint8_t* vp = basep + (vpg - base);
+            const int t0 = max(ntok, 0);
+            constexpr int UPR = C::ROW_BYTES / 16;          // 16-byte units per row
+            for (int u = lane; u < (C::TT - t0) * UPR; u += 32)
+                *reinterpret_cast<uint4*>(vp + (t0 + u / UPR) * C::ROW_BYTES + (u % UPR) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            __syncwarp();
+        } else if (ntok < C::TT) {
             uint8_t* vp = basep + (vpg - base);
             const int t0 = max(ntok, 0);
             const int units = (C::TT - t0) * C::CH * 8;   // 16-byte units
@@ -537,6 +602,34 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                         // several query tiles the tiles themselves are independent
                         if (QT == 1 && (ks2 & 1)) mma_bf16(e1[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
                         else                      mma_bf16(e0[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
+                    }
+                }
+            } else if constexpr (C::I4) {
+                // int4 rows: a 32-byte d-block (64 values) of tokens 0-7 / 8-15, bytes
+                // 0-15 / 16-31 as the four 8x8 b16 matrices; each 32-bit register holds 8
+                // nibbles (d = 64 dblk + 8c + 0..7 of token g, or +32 / token g+8)
+                const int tr = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                for (int dblk = 0; dblk < D / 64; ++dblk) {
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4(kpg + (uint32_t)(tr * C::ROW_BYTES + dblk * 32 + (lane >> 4) * 16), r0,
+                            r1, r2, r3);
+#pragma unroll
+                    for (int qi = 0; qi < QT; ++qi) {
+                        mma_f16(e0[qi], i4pick_to_f16x2<0>(r0), i4pick_to_f16x2<0>(r1),
+                                i4pick_to_f16x2<0>(r2), i4pick_to_f16x2<0>(r3),
+                                qf[dblk * 4][qi][0], qf[dblk * 4][qi][1]);
+                        mma_f16(QT == 1 ? e1[qi] : e0[qi], i4pick_to_f16x2<1>(r0),
+                                i4pick_to_f16x2<1>(r1), i4pick_to_f16x2<1>(r2),
+                                i4pick_to_f16x2<1>(r3), qf[dblk * 4 + 1][qi][0],
+                                qf[dblk * 4 + 1][qi][1]);
+                        mma_f16(e0[qi], i4pick_to_f16x2<2>(r0), i4pick_to_f16x2<2>(r1),
+                                i4pick_to_f16x2<2>(r2), i4pick_to_f16x2<2>(r3),
+                                qf[dblk * 4 + 2][qi][0], qf[dblk * 4 + 2][qi][1]);
+                        mma_f16(QT == 1 ? e1[qi] : e0[qi], i4pick_to_f16x2<3>(r0),
+                                i4pick_to_f16x2<3>(r1), i4pick_to_f16x2<3>(r2),
+                                i4pick_to_f16x2<3>(r3), qf[dblk * 4 + 3][qi][0],
+                                qf[dblk * 4 + 3][qi][1]);
                     }
                 }
             } else {
@@ -673,6 +766,41 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                 for (int qi = 0; qi < QT; ++qi)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) ot[dt][qi][e] = 0.f;
+            if constexpr (C::I4) {
+                // the K-path matrices, transposed per 8x8 b16 block: a lane then holds
+                // tokens 2c, 2c+1 of b16 unit g (d = 64 dblk + 4g + 0..3), and nibble pair
+                // (j, j + 4) is one d for both tokens.  mma (dblk, i): V^T row g <-> d =
+                // 64 dblk + 4g + i, row g + 8 <-> d = 64 dblk + 32 + 4g + i.
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    const int tr = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+                    for (int dblk = 0; dblk < D / 64; ++dblk) {
+                        uint32_t r0, r1, r2, r3;
+                        ldsm_x4(vpg + (uint32_t)(tr * C::ROW_BYTES + dblk * 32 + (lane >> 4) * 16),
+                                r0, r1, r2, r3);
+                        const uint32_t m0 = movmatrix_trans(r0);   // tokens 0-7,  d + 0
+                        const uint32_t m1 = movmatrix_trans(r1);   // tokens 8-15, d + 0
+                        const uint32_t m2 = movmatrix_trans(r2);   // tokens 0-7,  d + 32
+                        const uint32_t m3 = movmatrix_trans(r3);   // tokens 8-15, d + 32
+#pragma unroll
+                        for (int qi = 0; qi < QT; ++qi) {
+                            mma_f16(ot[dblk * 4][qi], i4pick_to_f16x2<0>(m0), i4pick_to_f16x2<0>(m2),
+                                    i4pick_to_f16x2<0>(m1), i4pick_to_f16x2<0>(m3),
+                                    pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(ot[dblk * 4 + 1][qi], i4pick_to_f16x2<1>(m0),
+                                    i4pick_to_f16x2<1>(m2), i4pick_to_f16x2<1>(m1),
+                                    i4pick_to_f16x2<1>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(ot[dblk * 4 + 2][qi], i4pick_to_f16x2<2>(m0),
+                                    i4pick_to_f16x2<2>(m2), i4pick_to_f16x2<2>(m1),
+                                    i4pick_to_f16x2<2>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(ot[dblk * 4 + 3][qi], i4pick_to_f16x2<3>(m0),
+                                    i4pick_to_f16x2<3>(m2), i4pick_to_f16x2<3>(m1),
+                                    i4pick_to_f16x2<3>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                        }
+                    }
+                }
+            } else {
 #pragma unroll
             for (int dp = 0; dp < C::DT / 2; ++dp) {
 #pragma unroll
@@ -705,6 +833,7 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                     }
                 }
             }
+            }
 #pragma unroll
             for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
@@ -735,7 +864,18 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                         a.out + ((int64_t)(seg_qb + qi) * a.Hq + (int64_t)seg_h * a.G) * D;
 #pragma unroll
                     for (int dt = 0; dt < C::DT; ++dt) {
-                        if (!FP8) {
+                        if constexpr (C::I4) {
+                            // accumulator dt = 4 dblk + i: row g <-> d, row g + 8 <-> d + 32
+                            const int d = (dt >> 2) * 64 + 4 * g + (dt & 3);
+                            if (g0 < a.G) {
+                                ob[g0 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][0] * inv0));
+                                ob[g0 * D + d + 32] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][2] * inv0));
+                            }
+                            if (g1 < a.G) {
+                                ob[g1 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][1] * inv1));
+                                ob[g1 * D + d + 32] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][3] * inv1));
+                            }
+                        } else if (!FP8) {
                             const int d = dt * 16 + g;
                             if (g0 < a.G) {
                                 ob[g0 * D + d] = __bfloat16_as_ushort(__float2bfloat16_rn(o[dt][qi][0] * inv0));
@@ -760,7 +900,13 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                                 qi * (kGroupPad * (D + 4));
 #pragma unroll
                     for (int dt = 0; dt < C::DT; ++dt) {
-                        if (!FP8) {
+                        if constexpr (C::I4) {
+                            const int d = (dt >> 2) * 64 + 4 * g + (dt & 3);
+                            ps[g0 * (D + 4) + d] = o[dt][qi][0];
+                            ps[g0 * (D + 4) + d + 32] = o[dt][qi][2];
+                            ps[g1 * (D + 4) + d] = o[dt][qi][1];
+                            ps[g1 * (D + 4) + d + 32] = o[dt][qi][3];
+                        } else if (!FP8) {
                             const int d = dt * 16 + g;
                             ps[g0 * (D + 4) + d] = o[dt][qi][0];
                             ps[g0 * (D + 4) + d + 8] = o[dt][qi][2];
@@ -932,11 +1078,12 @@ int query_tile(int fp8, int max_q_len) {
 
 // The CTA shape for a (dtype, D, BS, QT): `warps` independent pipelines of
 // `stages` tiles each.
-DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch, int qt) {
+DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int batch, int qt) {
     DecodePlan p;
-    const int elt = fp8 ? 1 : 2;
+    const int fp8 = kt != 0;
+    const int row_bytes = kt == 3 ? head_dim / 2 : head_dim * (fp8 ? 1 : 2);
     const int tile_tokens = fp8 ? block_size : 16;
-    p.stage_bytes = 2 * tile_tokens * head_dim * elt;
+    p.stage_bytes = 2 * tile_tokens * row_bytes;
     // Each warp streams its pages through its own 2-stage pipeline; the per-page
     // instruction chain of a warp, not the bytes in flight, limits the rate, so the
     // CTA runs several warps per SM sub-partition.  Measured on GB300: 6 warps for
@@ -989,9 +1136,19 @@ static cudaError_t launch_q(int qt, const DecodeLaunch& L, const DecodePlan& pla
 }
 
 static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, int BS,
-                             int64_t rows) {
+                             int64_t rows, int kt) {
     auto fn = encode_fn();
     if (!fn) return false;
+    if (kt == 3) {   // int4 rows: D/2 bytes, one unswizzled box of BS rows
+        cuuint64_t dims[2] = {(cuuint64_t)(D / 2), (cuuint64_t)rows};
+        cuuint64_t strides[1] = {(cuuint64_t)(D / 2)};
+        cuuint32_t box[2] = {(cuuint32_t)(D / 2), (cuuint32_t)BS};
+        cuuint32_t estr[2] = {1, 1};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
     const int elt = fp8 ? 1 : 2;
     cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)(D * elt)};
@@ -1008,12 +1165,12 @@ static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, i
 int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     const int qt = query_tile(L.fp8, L.max_q_len);
     if (qt == 0) return PKV_ERR_UNSUPPORTED;
-    const DecodePlan plan = decode_plan(L.fp8, L.D, L.BS, L.num_sms, L.N, qt);
+    const DecodePlan plan = decode_plan(L.kt, L.D, L.BS, L.num_sms, L.N, qt);
     const WorkspaceLayout WL = workspace_layout(L.N, L.Hkv, L.D, plan.total_warps, qt);
     const int64_t rows = (int64_t)L.NB * L.Hkv * L.BS;
     alignas(64) CUtensorMap tk, tv;
-    if (!encode_cache_map(&tk, L.k_cache, L.fp8, L.D, L.BS, rows) ||
-        !encode_cache_map(&tv, L.v_cache, L.fp8, L.D, L.BS, rows))
+    if (!encode_cache_map(&tk, L.k_cache, L.fp8, L.D, L.BS, rows, L.kt) ||
+        !encode_cache_map(&tv, L.v_cache, L.fp8, L.D, L.BS, rows, L.kt))
         return PKV_ERR_CUDA;
     DecodeArgs a;
     uint8_t* ws = static_cast<uint8_t*>(L.workspace);
@@ -1049,19 +1206,23 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
         if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, 1>(qt, L, plan, tk, tv, a, st);
         else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, 1>(qt, L, plan, tk, tv, a, st);
         else return PKV_ERR_UNSUPPORTED;
-    } else {
+    } else if (L.kt == 2) {
         if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, 2>(qt, L, plan, tk, tv, a, st);
         else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, 2>(qt, L, plan, tk, tv, a, st);
+        else return PKV_ERR_UNSUPPORTED;
+    } else {
+        if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, 3>(qt, L, plan, tk, tv, a, st);
+        else if (L.D == 128 && L.BS == 32) e = launch_q<128, 32, 3>(qt, L, plan, tk, tv, a, st);
         else return PKV_ERR_UNSUPPORTED;
     }
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-size_t decode_workspace_bytes(int batch, int num_kv_heads, int head_dim, int block_size, int fp8,
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int head_dim, int block_size, int kt,
                               int num_sms, int max_q_len) {
-    const int qt = query_tile(fp8, max_q_len);
+    const int qt = query_tile(kt != 0, max_q_len);
     if (qt == 0) return 0;
-    const DecodePlan plan = decode_plan(fp8, head_dim, block_size, num_sms, batch, qt);
+    const DecodePlan plan = decode_plan(kt, head_dim, block_size, num_sms, batch, qt);
     return (size_t)workspace_layout(batch, num_kv_heads, head_dim, plan.total_warps, qt).total;
 }
 

@@ -74,9 +74,9 @@ struct DecodeLaunch {
 };
 
 int query_tile(int fp8, int max_q_len);
-DecodePlan decode_plan(int fp8, int head_dim, int block_size, int num_sms, int batch, int qt);
+DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int batch, int qt);
 int decode_launch(const DecodeLaunch& L, cudaStream_t st);
-size_t decode_workspace_bytes(int batch, int num_kv_heads, int head_dim, int block_size, int fp8,
+size_t decode_workspace_bytes(int batch, int num_kv_heads, int head_dim, int block_size, int kt,
                               int num_sms, int max_q_len);
 cudaError_t slot_mapping_launch(const int32_t* block_table, int MB, const int32_t* req_idx,
                                 const int32_t* positions, int T, int BS, int64_t* out,
@@ -298,6 +298,25 @@ __device__ __forceinline__ uint32_t i8pick_to_f16x2(uint32_t xs) {
     const uint32_t y = __byte_perm(xs, 0x64646464u, SEL);
     uint32_t r;
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(0x64806480u));
+    return r;
+}
+
+// Two int4 codes picked from the 8 offset-binary nibbles n0..n7 of x (n_j at bits
+// 4j..4j+3) -> fp16x2 (n_I - 8, n_{I+4} - 8), exactly.  fp16 1024 + k (k < 1024)
+// is the exponent of 1024 with k in the mantissa: the mask-or puts a nibble there
+// directly (I even) or 16 times a nibble (I odd, then a multiply by 1/16 is exact).
+template <int I>
+__device__ __forceinline__ uint32_t i4pick_to_f16x2(uint32_t x) {
+    const uint32_t w = (I >= 2) ? (x >> 8) : x;
+    uint32_t r;
+    if constexpr ((I & 1) == 0) {
+        const uint32_t y = (w & 0x000F000Fu) | 0x64006400u;      // (1024 + n, 1024 + n')
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(0x64086408u));   // - 1032
+    } else {
+        const uint32_t y = (w & 0x00F000F0u) | 0x64006400u;      // (1024 + 16 n, ...)
+        // (1024 + 16 n) / 16 - 72 = n - 8
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(y), "r"(0x2C002C00u), "r"(0xD480D480u));
+    }
     return r;
 }
 

@@ -100,7 +100,7 @@ __device__ __forceinline__ void block_scales(int64_t i, int chunk, float* k_scal
         ksc = k_scale[i];
         vsc = v_scale[i];
     } else {
-        constexpr float QMAX = KT == 2 ? 127.f : 448.f;
+        constexpr float QMAX = KT == 3 ? 7.f : (KT == 2 ? 127.f : 448.f);
         const float ka = __uint_as_float(kmax[i]), va = __uint_as_float(vmax[i]);
         ksc = ka > 0.f ? __fdiv_rn(ka, QMAX) : 1.f;
         vsc = va > 0.f ? __fdiv_rn(va, QMAX) : 1.f;
@@ -111,7 +111,9 @@ __device__ __forceinline__ void block_scales(int64_t i, int chunk, float* k_scal
     }
 }
 
-// KT: 0 bf16 copy, 1 E4M3 (RNE, saturate to +-448), 2 int8 (RNE, clamp to +-127).
+// KT: 0 bf16 copy, 1 E4M3 (RNE, saturate to +-448), 2 int8 (RNE, clamp to +-127),
+// 3 int4 (RNE, clamp to +-7, stored offset-binary q + 8: value 2b in the low nibble of
+// byte b of the row, value 2b+1 in its high nibble).
 // RESCALE: the block scales come from the gathered amax (and are stored), else
 // they are read from k_scale / v_scale.
 template <int KT, bool RESCALE = false>
@@ -142,6 +144,24 @@ __global__ void __launch_bounds__(256)
     if constexpr (KT == 0) {
         *reinterpret_cast<uint4*>(k_cache + (dst_row * D + chunk * 8) * 2) = ks;
         *reinterpret_cast<uint4*>(v_cache + (dst_row * D + chunk * 8) * 2) = vs;
+    } else if constexpr (KT == 3) {
+        float ksc, vsc;
+        block_scales<KT, RESCALE>(blk * Hkv + h, chunk, k_scale, v_scale, kmax, vmax, ksc, vsc);
+        const uint32_t kw[4] = {ks.x, ks.y, ks.z, ks.w};
+        const uint32_t vw[4] = {vs.x, vs.y, vs.z, vs.w};
+        uint32_t ko = 0u, vo = 0u;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const uint32_t kb = (e & 1) ? (kw[e >> 1] & 0xFFFF0000u) : (kw[e >> 1] << 16);
+            const uint32_t vb = (e & 1) ? (vw[e >> 1] & 0xFFFF0000u) : (vw[e >> 1] << 16);
+            // IEEE binary32 division, round to nearest even, clamp to +-7 (NaN gives 0)
+            const int kq = min(max(__float2int_rn(__fdiv_rn(__uint_as_float(kb), ksc)), -7), 7);
+            const int vq = min(max(__float2int_rn(__fdiv_rn(__uint_as_float(vb), vsc)), -7), 7);
+            ko |= (uint32_t)(kq + 8) << (4 * e);
+            vo |= (uint32_t)(vq + 8) << (4 * e);
+        }
+        *reinterpret_cast<uint32_t*>(k_cache + (dst_row * D + chunk * 8) / 2) = ko;
+        *reinterpret_cast<uint32_t*>(v_cache + (dst_row * D + chunk * 8) / 2) = vo;
     } else if constexpr (KT == 2) {
         float ksc, vsc;
         block_scales<KT, RESCALE>(blk * Hkv + h, chunk, k_scale, v_scale, kmax, vmax, ksc, vsc);
@@ -213,6 +233,9 @@ cudaError_t cache_write_launch(const void* k, const void* v, const int64_t* slot
     if (kt == 2)
         return launch_pdl(pkv_cache_write_kernel<2, false>, dim3((unsigned)grid), dim3(256), 0, st,
                           kk, vv, slots, chunks, Hkv, D, BS, NB, kc, vc, ks, vs, nz, nz);
+    if (kt == 3)
+        return launch_pdl(pkv_cache_write_kernel<3, false>, dim3((unsigned)grid), dim3(256), 0, st,
+                          kk, vv, slots, chunks, Hkv, D, BS, NB, kc, vc, ks, vs, nz, nz);
     return launch_pdl(pkv_cache_write_kernel<0, false>, dim3((unsigned)grid), dim3(256), 0, st, kk,
                       vv, slots, chunks, Hkv, D, BS, NB, kc, vc, (float*)nullptr, (float*)nullptr,
                       nz, nz);
@@ -242,6 +265,9 @@ cudaError_t cache_write_rescale_launch(const void* k, const void* v, const int64
     const uint32_t* cvm = vmax;
     if (kt == 2)
         return launch_pdl(pkv_cache_write_kernel<2, true>, dim3(grid), dim3(256), 0, st, kk, vv,
+                          slots, chunks, Hkv, D, BS, NB, kc, vc, k_scale, v_scale, ckm, cvm);
+    if (kt == 3)
+        return launch_pdl(pkv_cache_write_kernel<3, true>, dim3(grid), dim3(256), 0, st, kk, vv,
                           slots, chunks, Hkv, D, BS, NB, kc, vc, k_scale, v_scale, ckm, cvm);
     return launch_pdl(pkv_cache_write_kernel<1, true>, dim3(grid), dim3(256), 0, st, kk, vv, slots,
                       chunks, Hkv, D, BS, NB, kc, vc, k_scale, v_scale, ckm, cvm);

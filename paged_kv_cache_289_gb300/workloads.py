@@ -32,6 +32,7 @@ VOCAB_SMALL = 32000
 VOCAB = 128000
 E4M3_MAX = 448.0
 INT8_MAX = 127.0
+INT4_MAX = 7.0
 
 
 @dataclass
@@ -54,6 +55,7 @@ class Workload:
     hash_block: int = 16
     q_len: int = 1                # new query tokens per request (speculative verify: > 1)
     int8: bool = False            # int8 pages (symmetric, scale = amax/127)
+    int4: bool = False            # int4 pages (two offset-binary codes per byte, amax/7)
     q_lens: np.ndarray | None = None   # int32 [N] per-request query counts (prefill chunks);
                                        # None: q_len for every request
     notes: dict = field(default_factory=dict)
@@ -75,22 +77,28 @@ class Workload:
 
     @property
     def quant(self) -> bool:
-        """8-bit pages with one fp32 scale per (block, kv head) (E4M3 or int8)."""
-        return self.fp8 or self.int8
+        """Quantised pages with one fp32 scale per (block, kv head) (E4M3, int8, int4)."""
+        return self.fp8 or self.int8 or self.int4
 
     @property
     def kv_kind(self) -> int:
-        """0: bf16 pages, 1: E4M3, 2: int8."""
-        return 2 if self.int8 else (1 if self.fp8 else 0)
+        """0: bf16 pages, 1: E4M3, 2: int8, 3: int4."""
+        return 3 if self.int4 else (2 if self.int8 else (1 if self.fp8 else 0))
 
     @property
     def qmax(self) -> float:
         """Largest code magnitude of the 8-bit kind (the scale recipe divides amax by it)."""
-        return INT8_MAX if self.int8 else E4M3_MAX
+        return INT4_MAX if self.int4 else (INT8_MAX if self.int8 else E4M3_MAX)
 
     @property
     def cache_np_dtype(self):
-        return np.int8 if self.int8 else (np.uint8 if self.fp8 else np.uint16)
+        return np.int8 if self.int8 else (np.uint8 if (self.fp8 or self.int4) else np.uint16)
+
+    @property
+    def cache_shape(self):
+        """Shape of one cache tensor: [NB, Hkv, BS, D] elements, or [.., D / 2] bytes for
+        int4 pages."""
+        return (self.NB, self.Hkv, self.BS, self.D // 2 if self.int4 else self.D)
 
     @property
     def G(self) -> int:
@@ -105,8 +113,9 @@ class Workload:
         return int(self.seq_lens.astype(np.int64).sum())
 
     @property
-    def elt(self) -> int:
-        return 1 if self.quant else 2
+    def elt(self) -> float:
+        """Bytes per cached element: 2 (bf16), 1 (E4M3, int8), 0.5 (int4)."""
+        return 0.5 if self.int4 else (1 if self.quant else 2)
 
     def blocks_of(self, r: int) -> np.ndarray:
         nb = -(-int(self.seq_lens[r]) // self.BS)
@@ -144,7 +153,7 @@ class Workload:
 
     def kv_read_bytes(self) -> int:
         """Logical K+V bytes one decode step reads: sum_r seq_len_r * Hkv * D * 2 * elt."""
-        return self.total_tokens * self.Hkv * self.D * 2 * self.elt
+        return int(self.total_tokens * self.Hkv * self.D * 2 * self.elt)
 
     def unique_kv_read_bytes(self) -> int:
         """K+V bytes of distinct physical token rows read (shared prefix pages once)."""
@@ -155,7 +164,7 @@ class Workload:
             for j, b in enumerate(blocks):
                 rows.add((int(b), min(self.BS, S - j * self.BS)))
         n = sum(cnt for _, cnt in rows)
-        return n * self.Hkv * self.D * 2 * self.elt
+        return int(n * self.Hkv * self.D * 2 * self.elt)
 
 
 # ----------------------------------------------------------------------------
@@ -283,6 +292,14 @@ def make(cfg: int, seed: int | None = None, small: bool = False,
         wl.fp8 = False
         wl.int8 = True
         return wl
+    if cfg == 9:
+        # int4 pages at scale: workload 5's requests with symmetric int4 codes
+        wl = make(5, seed=seed, small=small, batch=batch)
+        wl.name = "int4_at_scale" + ("_small" if small else "")
+        wl.cfg = 9
+        wl.fp8 = False
+        wl.int4 = True
+        return wl
     if cfg == 8:
         # chunked prefill on the 70B-shaped layer: a chunk of new prompt tokens per
         # request after a cached context; small: ragged chunks spanning several tiles
@@ -313,7 +330,7 @@ def make(cfg: int, seed: int | None = None, small: bool = False,
 
 
 def custom(N, Hq, Hkv, D, BS, seq_lens, fp8=False, seed=0, slack=1.1, scale=None, name="custom",
-           q_len=1, int8=False):
+           q_len=1, int8=False, int4=False):
     """A workload with explicit lengths (edge cases: empty, ragged, one-token requests)."""
     rng = np.random.default_rng(seed)
     seq = np.asarray(seq_lens, dtype=np.int32)
@@ -321,7 +338,7 @@ def custom(N, Hq, Hkv, D, BS, seq_lens, fp8=False, seed=0, slack=1.1, scale=None
     toks, offs = _tokens(rng, seq, VOCAB)
     sc = 1.0 / math.sqrt(D) if scale is None else scale
     return Workload(name, 0, seed, N, Hq, Hkv, D, BS, NB, fp8, sc, seq, bt, toks, offs,
-                    q_len=q_len, int8=int8)
+                    q_len=q_len, int8=int8, int4=int4)
 
 
 # ----------------------------------------------------------------------------

@@ -15,7 +15,7 @@ FP8_MAX_ABS = 5e-2
 
 def torch_cache_dtype(wl):
     torch = torch_mod()
-    return torch.int8 if wl.int8 else (torch.uint8 if wl.fp8 else torch.bfloat16)
+    return torch.int8 if wl.int8 else (torch.uint8 if (wl.fp8 or wl.int4) else torch.bfloat16)
 
 
 def pkv_kind(wl):
@@ -85,7 +85,7 @@ class HostCase:
             req, pos = W.token_rows_order(wl)
             self.req_all, self.pos_all = req, pos
             slots = oracle.slot_mapping(wl.block_table, req, pos, wl.BS)
-            self.kc = np.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), wl.cache_np_dtype)
+            self.kc = np.zeros(wl.cache_shape, wl.cache_np_dtype)
             self.vc = np.zeros_like(self.kc)
             oracle.kv_cache_write(self.d["k_rows"], self.d["v_rows"], slots, self.kc, self.vc,
                                   self.d["k_scale"], self.d["v_scale"])

@@ -74,7 +74,7 @@ def test_decode_rejects_bad_arguments_without_launching(L):
     assert _decode(L, BS=8) == -2
     assert _decode(L, Hq=9) == -2
     assert _decode(L, Hq=72, Hkv=8) == -2
-    assert _decode(L, dt=3) == -2
+    assert _decode(L, dt=7) == -2
     assert _decode(L, dt=1, D=64) == -2
     assert _decode(L, N=-1) == -1
     assert _decode(L, MB=0) == -1

@@ -45,7 +45,7 @@ def _compact(wl, reqs):
     return bt, np.array(old, np.int64)
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5, 7])
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5, 7, 9])
 def test_fullsize_decode_step_sampled(cfg):
     torch = torch_mod()
     wl = W.make(cfg)
@@ -53,7 +53,7 @@ def test_fullsize_decode_step_sampled(cfg):
     bt = torch.from_numpy(wl.block_table).cuda()
     sl = torch.from_numpy(wl.seq_lens).cuda()
     if wl.quant:
-        kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch_cache_dtype(wl), device="cuda")
+        kc = torch.zeros(wl.cache_shape, dtype=torch_cache_dtype(wl), device="cuda")
         vc = torch.zeros_like(kc)
         req, pos = W.token_rows_order(wl)
         slots_all = pkv.compute_slot_mapping(bt, torch.from_numpy(pos).cuda(), wl.BS,

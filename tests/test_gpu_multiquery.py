@@ -25,7 +25,7 @@ def _device_caches(case):
     wl = case.wl
     if not wl.quant:
         return bf16_dev(case.d["k_cache"]), bf16_dev(case.d["v_cache"]), None, None
-    kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch_cache_dtype(wl), device="cuda")
+    kc = torch.zeros(wl.cache_shape, dtype=torch_cache_dtype(wl), device="cuda")
     vc = torch.zeros_like(kc)
     ks, vs = to_dev(case.d["k_scale"]), to_dev(case.d["v_scale"])
     slots = pkv.compute_slot_mapping(to_dev(wl.block_table), to_dev(case.pos_all), wl.BS,
@@ -68,7 +68,8 @@ def test_spec_verify_step_small():
 @pytest.mark.parametrize("G,D,BS,kind,qmax", [(8, 128, 16, "bf16", 4), (8, 128, 32, "bf16", 2),
                                               (4, 64, 16, "bf16", 4), (1, 64, 32, "bf16", 4),
                                               (8, 128, 32, "fp8", 2), (4, 128, 16, "fp8", 2),
-                                              (8, 128, 32, "int8", 2), (3, 128, 16, "bf16", 3)])
+                                              (8, 128, 32, "int8", 2), (3, 128, 16, "bf16", 3),
+                                              (8, 128, 32, "int4", 2), (4, 128, 16, "int4", 2)])
 def test_multiquery_shapes_variable_qlen(G, D, BS, kind, qmax):
     """Every supported shape; each request has its own q_len in 1..qmax; short requests
     have fewer tokens than queries (their first queries see nothing: zero rows)."""
@@ -79,6 +80,7 @@ def test_multiquery_shapes_variable_qlen(G, D, BS, kind, qmax):
     qlens[0], qlens[1] = qmax, qmax          # q_len > seq_len for the 1- and 2-token requests
     fp8 = kind != "bf16"
     wl = W.custom(len(lens), G * Hkv, Hkv, D, BS, lens, fp8=kind == "fp8", int8=kind == "int8",
+                  int4=kind == "int4",
                   seed=G + D + BS)
     qoffs = np.zeros(len(lens) + 1, np.int32)
     np.cumsum(qlens, out=qoffs[1:])

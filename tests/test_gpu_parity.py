@@ -27,7 +27,7 @@ def _device_caches(case):
     wl = case.wl
     if not wl.quant:
         return bf16_dev(case.d["k_cache"]), bf16_dev(case.d["v_cache"]), None, None
-    kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch_cache_dtype(wl), device="cuda")
+    kc = torch.zeros(wl.cache_shape, dtype=torch_cache_dtype(wl), device="cuda")
     vc = torch.zeros_like(kc)
     ks = to_dev(case.d["k_scale"])
     vs = to_dev(case.d["v_scale"])
@@ -54,7 +54,7 @@ def _gpu_step(case, kc, vc, ks, vs):
     return slots, out, ws
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 7])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, 7, 9])
 def test_decode_step_small(cfg):
     """Workloads 1..5 at oracle-friendly sizes: slots and cache bytes bit-exact,
     attention within tolerance, device error word clear."""
@@ -74,14 +74,16 @@ def test_decode_step_small(cfg):
                                          (4, 128, 16, "bf16"), (8, 64, 32, "bf16"),
                                          (3, 128, 16, "bf16"), (1, 128, 32, "fp8"),
                                          (4, 128, 16, "fp8"), (8, 128, 32, "fp8"),
-                                         (8, 128, 32, "int8"), (2, 128, 16, "int8")])
+                                         (8, 128, 32, "int8"), (2, 128, 16, "int8"),
+                                         (8, 128, 32, "int4"), (4, 128, 16, "int4"),
+                                         (1, 128, 32, "int4"), (3, 128, 16, "int4")])
 def test_decode_shapes_ragged(G, D, BS, kind):
     """Every supported shape on ragged lengths: 1 token, BS-1, BS, BS+1, long tails."""
     Hkv = 2
     lens = [1, BS - 1, BS, BS + 1, 7 * BS + 3, 1000, 37]
     fp8 = kind != "bf16"
     wl = W.custom(len(lens), G * Hkv, Hkv, D, BS, lens, fp8=kind == "fp8", int8=kind == "int8",
-                  seed=G * 100 + D + BS)
+                  int4=kind == "int4", seed=G * 100 + D + BS)
     case = HostCase(wl)
     kc, vc, ks, vs = _device_caches(case)
     _, out_d, ws = _gpu_step(case, kc, vc, ks, vs)
@@ -241,6 +243,27 @@ def test_int8_write_exhaustive_bf16_patterns():
         vc_o = np.zeros_like(kc_o)
         oracle.kv_cache_write(bits, bits[::-1].copy(), slots, kc_o, vc_o, scales, scales)
         kc = torch.zeros((NB, 1, BS, 128), dtype=torch.int8, device="cuda")
+        vc = torch.zeros_like(kc)
+        pkv.kv_cache_write(bf16_dev(bits), bf16_dev(bits[::-1].copy()), to_dev(slots), kc, vc,
+                           to_dev(scales), to_dev(scales))
+        assert np.array_equal(dev_bits(kc), kc_o)
+        assert np.array_equal(dev_bits(vc), vc_o)
+
+
+def test_int4_write_exhaustive_bf16_patterns():
+    """Every bf16 bit pattern through the int4 write (two codes per byte) with scale 1 and
+    random scales: the library's bytes equal the oracle's."""
+    torch = torch_mod()
+    bits = np.arange(65536, dtype=np.uint16).reshape(512, 1, 128)
+    T, BS, NB = 512, 16, 32
+    slots = np.arange(T, dtype=np.int64)
+    rng = np.random.default_rng(4)
+    for scales in (np.ones((NB, 1), np.float32),
+                   rng.uniform(0.001, 3.0, (NB, 1)).astype(np.float32)):
+        kc_o = np.zeros((NB, 1, BS, 64), np.uint8)
+        vc_o = np.zeros_like(kc_o)
+        oracle.kv_cache_write(bits, bits[::-1].copy(), slots, kc_o, vc_o, scales, scales)
+        kc = torch.zeros((NB, 1, BS, 64), dtype=torch.uint8, device="cuda")
         vc = torch.zeros_like(kc)
         pkv.kv_cache_write(bf16_dev(bits), bf16_dev(bits[::-1].copy()), to_dev(slots), kc, vc,
                            to_dev(scales), to_dev(scales))

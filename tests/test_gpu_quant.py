@@ -18,7 +18,7 @@ def _built():
     torch_mod()
 
 
-@pytest.mark.parametrize("cfg", [5, 7])
+@pytest.mark.parametrize("cfg", [5, 7, 9])
 def test_rescale_write_bit_exact_then_partial_rewrite(cfg):
     torch = torch_mod()
     wl = W.make(cfg, small=True)
@@ -27,13 +27,13 @@ def test_rescale_write_bit_exact_then_partial_rewrite(cfg):
     bt = to_dev(wl.block_table)
     # oracle
     slots_o = oracle.slot_mapping(wl.block_table, req, pos, wl.BS)
-    kc_o = np.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), wl.cache_np_dtype)
+    kc_o = np.zeros(wl.cache_shape, wl.cache_np_dtype)
     vc_o = np.zeros_like(kc_o)
     ks_o = np.full((wl.NB, wl.Hkv), 123.0, np.float32)
     vs_o = ks_o.copy()
     oracle.kv_cache_write_rescale(d["k_rows"], d["v_rows"], slots_o, kc_o, vc_o, ks_o, vs_o)
     # library (garbage workspace: it needs no clearing)
-    kc = torch.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), dtype=torch_cache_dtype(wl), device="cuda")
+    kc = torch.zeros(wl.cache_shape, dtype=torch_cache_dtype(wl), device="cuda")
     vc = torch.zeros_like(kc)
     ks = torch.full((wl.NB, wl.Hkv), 123.0, dtype=torch.float32, device="cuda")
     vs = ks.clone()

@@ -522,7 +522,72 @@ def test_int8_write_and_decode_use_code_times_scale():
         np.testing.assert_allclose(got[i], p @ Vd, atol=1e-12)
 
 
-@pytest.mark.parametrize("cfg", [5, 7])
+# ---------------------------------------------------------------- int4 pages
+def test_int4_code_is_nearest_integer_clamped_offset_binary():
+    """Code = q + 8 with q the nearest integer to x (ties to even), clamped to [-7, 7]:
+    checked against a brute-force search over the 15 candidate values."""
+    rng = np.random.default_rng(9)
+    xs = np.concatenate([rng.standard_normal(3000).astype(np.float32) * 4,
+                         np.float32([k + 0.5 for k in range(-9, 9)]),       # exact ties
+                         np.float32([6.5, 7.5, -7.5, -8.0, 1e9, -1e9, 0.0, -0.0, 0.49999997])])
+    for x in xs:
+        cands = np.arange(-7, 8, dtype=np.float64)
+        dist = np.abs(cands - float(x))
+        best = cands[dist == dist.min()]
+        q = best[0] if len(best) == 1 else [c for c in best if int(c) % 2 == 0][0]
+        assert oracle.int4_code_from_float(float(x)) == int(q) + 8, x
+    assert oracle.int4_code_from_float(float("nan")) == 8
+
+
+def test_int4_write_packs_two_codes_per_byte_low_nibble_first():
+    """A row of D values becomes D/2 bytes, value 2b in the low nibble of byte b; the
+    attention reads value = (code - 8) * scale and equals a dense brute force."""
+    D, BS, NB = 128, 16, 4
+    vals = np.float32(np.tile(np.arange(-7, 9), D // 16))                 # -7 .. 8 repeated
+    bits = W.f32_to_bf16_bits(vals).reshape(1, 1, D)
+    kc = np.zeros((NB, 1, BS, D // 2), np.uint8)
+    vc = np.zeros_like(kc)
+    sc = np.ones((NB, 1), np.float32)
+    oracle.kv_cache_write(bits, bits, np.array([BS + 3], np.int64), kc, vc, sc, sc)
+    row = kc[1, 0, 3]
+    q = np.clip(np.rint(vals), -7, 7).astype(np.int64) + 8
+    assert np.array_equal(row & 0xF, q[0::2]) and np.array_equal(row >> 4, q[1::2])
+    assert np.all(kc[0] == 0) and np.all(kc[1, 0, :3] == 0)          # nothing else written
+    wl = W.make(9, small=True)
+    d = W.host_data(wl)
+    req, pos = W.token_rows_order(wl)
+    slots = oracle.slot_mapping(wl.block_table, req, pos, wl.BS)
+    kc = np.zeros(wl.cache_shape, np.uint8)
+    vc = np.zeros_like(kc)
+    oracle.kv_cache_write(d["k_rows"], d["v_rows"], slots, kc, vc, d["k_scale"], d["v_scale"])
+    x = W.bf16_bits_to_f32(d["k_rows"]).astype(np.float64)
+    b, o = slots // wl.BS, slots % wl.BS
+    packed = kc[b, :, o]
+    codes = np.stack([packed & 0xF, packed >> 4], axis=-1).reshape(x.shape).astype(np.float64) - 8
+    s = d["k_scale"][b].astype(np.float64)[:, :, None]
+    assert np.all(np.abs(codes * s - x) <= 0.5 * s * (1 + 1e-6) + np.abs(x) * 2.0 ** -23)
+    assert np.abs(codes).max() == 7                                   # amax/7 scaling
+    rows = np.array([0, 2 * wl.Hq + 17], np.int64)
+    got = oracle.decode_rows(d["q"], kc, vc, wl.block_table, wl.seq_lens, wl.scale, rows,
+                             d["k_scale"], d["v_scale"])
+
+    def deq(cache, scale, bb, h):
+        p_ = cache[bb, h]
+        c_ = np.stack([p_ & 0xF, p_ >> 4], axis=-1).reshape(wl.BS, wl.D).astype(np.float64) - 8
+        return c_ * float(scale[bb, h])
+    for i, row_ in enumerate(rows):
+        r, hq = divmod(int(row_), wl.Hq)
+        h = hq // wl.G
+        blocks = wl.blocks_of(r)
+        S = int(wl.seq_lens[r])
+        Kd = np.concatenate([deq(kc, d["k_scale"], bb, h) for bb in blocks])[:S]
+        Vd = np.concatenate([deq(vc, d["v_scale"], bb, h) for bb in blocks])[:S]
+        qv = W.bf16_bits_to_f32(d["q"][r, hq]).astype(np.float64)
+        p = scipy.special.softmax(wl.scale * (Kd @ qv))
+        np.testing.assert_allclose(got[i], p @ Vd, atol=1e-12)
+
+
+@pytest.mark.parametrize("cfg", [5, 7, 9])
 def test_rescale_write_scales_equal_the_amax_recipe(cfg):
     """Writing every token of a workload in one rescaling call gives each used block the
     scale amax/QMAX of its rows: the same numbers as the generator's independent numpy
@@ -531,7 +596,7 @@ def test_rescale_write_scales_equal_the_amax_recipe(cfg):
     d = W.host_data(wl)
     req, pos = W.token_rows_order(wl)
     slots = oracle.slot_mapping(wl.block_table, req, pos, wl.BS)
-    kc = np.zeros((wl.NB, wl.Hkv, wl.BS, wl.D), wl.cache_np_dtype)
+    kc = np.zeros(wl.cache_shape, wl.cache_np_dtype)
     vc = np.zeros_like(kc)
     ks = np.full((wl.NB, wl.Hkv), 123.0, np.float32)
     vs = np.full((wl.NB, wl.Hkv), 123.0, np.float32)

@@ -267,6 +267,10 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                       const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
     constexpr bool FP8 = KT != 0;   // quantised pages (E4M3, int8, int4) with per-(block, head) scales
     using C = Cfg<D, BS, KT>;
+    // four query positions (bf16 pages only) keep the GQA group's q fragments in shared
+    // memory instead of 64 registers per lane, read back per k-step
+    constexpr bool QSMEM = QT == 4;
+    constexpr int QB = QSMEM ? C::KS * QT * 32 * 8 : 0;   // bytes per warp
     extern __shared__ uint8_t smem_raw[];
     const int NW = blockDim.x >> 5;
     const int warp = threadIdx.x >> 5;
@@ -277,8 +281,11 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* basep = smem_raw + (base - raw);
     const uint32_t stage0 = base + (uint32_t)(warp * S * C::STAGE_BYTES);
-    const uint32_t bars = base + (uint32_t)(NW * S * C::STAGE_BYTES) + (uint32_t)(warp * S * 8);
-    int32_t* s_prefix = reinterpret_cast<int32_t*>(basep + NW * S * C::STAGE_BYTES + NW * S * 8);
+    uint2* qs = reinterpret_cast<uint2*>(basep + NW * S * C::STAGE_BYTES + warp * QB);
+    const uint32_t bars =
+        base + (uint32_t)(NW * S * C::STAGE_BYTES + NW * QB) + (uint32_t)(warp * S * 8);
+    int32_t* s_prefix =
+        reinterpret_cast<int32_t*>(basep + NW * S * C::STAGE_BYTES + NW * QB + NW * S * 8);
     int32_t* s_seq = s_prefix + (a.N + 1);
 
     if (lane == 0) {
@@ -394,7 +401,7 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
 
     float o[C::DT][QT][4];
     float ot[FP8 ? C::DT : 1][QT][4];
-    uint32_t qf[C::KS][QT][2];
+    uint32_t qf[QSMEM ? 1 : C::KS][QT][2];
     float m0[QT], m1[QT], l0[QT], l1[QT];   // heads 2c, 2c+1 of this lane, per query
     float qscale = a.scale_log2;
     bool seg_full = false;
@@ -448,8 +455,14 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                         a.q + ((int64_t)(seg_qb + qi) * a.Hq + (int64_t)h * a.G + g) * D;
 #pragma unroll
                     for (int ks2 = 0; ks2 < C::KS; ++ks2) {
-                        qf[ks2][qi][0] = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 2 * c)) : 0u;
-                        qf[ks2][qi][1] = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 8 + 2 * c)) : 0u;
+                        const uint32_t b0 = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 2 * c)) : 0u;
+                        const uint32_t b1 = gv ? __ldg(reinterpret_cast<const uint32_t*>(qrow + ks2 * 16 + 8 + 2 * c)) : 0u;
+                        if constexpr (QSMEM) {
+                            qs[(ks2 * QT + qi) * 32 + lane] = make_uint2(b0, b1);   // own slots
+                        } else {
+                            qf[ks2][qi][0] = b0;
+                            qf[ks2][qi][1] = b1;
+                        }
                     }
                 }
                 qscale = a.scale_log2;
@@ -598,10 +611,19 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
                     ldsm_x4(kpg + swz<C::TT>(t, 2 * ks2 + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
                     for (int qi = 0; qi < QT; ++qi) {
+                        uint32_t b0, b1;
+                        if constexpr (QSMEM) {
+                            const uint2 bq = qs[(ks2 * QT + qi) * 32 + lane];
+                            b0 = bq.x;
+                            b1 = bq.y;
+                        } else {
+                            b0 = qf[ks2][qi][0];
+                            b1 = qf[ks2][qi][1];
+                        }
                         // two accumulator chains give the single-query case its ILP; with
                         // several query tiles the tiles themselves are independent
-                        if (QT == 1 && (ks2 & 1)) mma_bf16(e1[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
-                        else                      mma_bf16(e0[qi], a0, a1, a2, a3, qf[ks2][qi][0], qf[ks2][qi][1]);
+                        if (QT == 1 && (ks2 & 1)) mma_bf16(e1[qi], a0, a1, a2, a3, b0, b1);
+                        else                      mma_bf16(e0[qi], a0, a1, a2, a3, b0, b1);
                     }
                 }
             } else if constexpr (C::I4) {
@@ -1087,9 +1109,10 @@ DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int ba
     // Each warp streams its pages through its own 2-stage pipeline; the per-page
     // instruction chain of a warp, not the bytes in flight, limits the rate, so the
     // CTA runs several warps per SM sub-partition.  Measured on GB300: 6 warps for
-    // bf16 pages, 8 for FP8 pages (whose tiles carry twice the tokens).
+    // single-query bf16 pages, 8 for 8-bit pages (whose tiles carry twice the tokens)
+    // and for several query positions.
     const int max_warps = (fp8 || qt > 1) ? 8 : 12;   // register budget of the launch bounds
-    p.warps = env_int("PKV_DECODE_WARPS", fp8 ? 8 : 6);
+    p.warps = env_int("PKV_DECODE_WARPS", (fp8 || qt > 1) ? 8 : 6);
     if (p.warps < 1) p.warps = 1;
     if (p.warps > max_warps) p.warps = max_warps;
     int stages = env_int("PKV_DECODE_STAGES", 0);
@@ -1097,7 +1120,8 @@ DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int ba
     if (stages > 16) stages = 16;
     if (stages < 2) stages = 2;
     const int fixed = 1024 + (int)align_up(4 * (2 * (int64_t)batch + 1), 16);
-    auto bytes = [&](int w, int st) { return fixed + w * st * (p.stage_bytes + 8); };
+    const int qbytes = qt == 4 ? (head_dim / 16) * 4 * 32 * 8 : 0;   // per-warp q fragments
+    auto bytes = [&](int w, int st) { return fixed + w * (st * (p.stage_bytes + 8) + qbytes); };
     while (stages > 2 && bytes(p.warps, stages) > 232448) --stages;
     while (p.warps > 1 && bytes(p.warps, stages) > 232448) --p.warps;
     p.stages = stages;

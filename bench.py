@@ -544,15 +544,17 @@ def run_copy_blocks(args):
     kh = np.zeros((2048, Hkv, BS, D), np.uint16)
     vh = np.zeros_like(kh)
     mp = np.stack([np.arange(0, 1024), np.arange(1024, 2048)], 1)
-    t0 = time.perf_counter()
-    reps = 0
-    while time.perf_counter() - t0 < 10.0:
-        oracle_copy(kh, vh, mp)
-        reps += 1
-    tc = time.perf_counter() - t0
-    cpu = {"value": round(reps * 1024 * 4 * block_bytes / tc / 1e9, 3), "unit": "GB/s",
-           "cores": 1, "kind": "oracle",
-           "sample": f"{reps} x 1024 pairs of 32 KB blocks in host memory (numpy, {tc:.1f} s)"}
+    cpu = None
+    if not args.skip_cpu:
+        t0 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t0 < 10.0:
+            oracle_copy(kh, vh, mp)
+            reps += 1
+        tc = time.perf_counter() - t0
+        cpu = {"value": round(reps * 1024 * 4 * block_bytes / tc / 1e9, 3), "unit": "GB/s",
+               "cores": 1, "kind": "oracle",
+               "sample": f"{reps} x 1024 pairs of 32 KB blocks in host memory (numpy, {tc:.1f} s)"}
     line = {"metric": "copy-on-write block copy: HBM GB/s (read + write)",
             "value": round(alg * K / t / 1e9, 2), "unit": "GB/s", "n_gpus": 1, "steps": K,
             "warmup": Wm, "ms_per_step": round(t / K * 1e3, 4), "higher_is_better": True,

@@ -1,0 +1,90 @@
+"""The decode step captured once in a CUDA graph and replayed ("GPU推理深度拆解：KV Cache视角",
+算子优化要点: CUDA Graph wants static shapes and addresses).  Every entry point takes
+caller-owned buffers and never synchronises, so slot mapping, cache write, decode (with its
+split-unit merges) and the prefix hash record into one graph.  Each replay, fed new values in
+the same buffers, must equal the eager calls bit for bit.  Split units reuse the arrival
+counters across replays with the same call tag, and must still merge correctly."""
+import numpy as np
+import pytest
+
+import paged_kv_cache_289_gb300 as pkv
+from paged_kv_cache_289_gb300 import workloads as W
+from helpers import bf16_dev, dev_bits, to_dev, torch_mod
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    torch_mod()
+
+
+@pytest.mark.parametrize("cfg", [2, 3])
+def test_decode_step_graph_replay_equals_eager(cfg):
+    torch = torch_mod()
+    wl = W.make(cfg, small=True)
+    d = W.host_data(wl)
+    bt = to_dev(wl.block_table)
+    sl = to_dev(wl.seq_lens)
+    pos = to_dev(wl.new_token_positions())
+    toks = to_dev(wl.tokens)
+    toffs = to_dev(wl.token_offsets)
+    ho = np.zeros(wl.N + 1, np.int64)
+    np.cumsum(np.diff(wl.token_offsets) // wl.hash_block, out=ho[1:])
+    hoffs = to_dev(ho)
+    nh = int(ho[-1])
+    # static buffers the graph reads and writes
+    q = bf16_dev(d["q"])
+    kn, vn = bf16_dev(d["k_new"]), bf16_dev(d["v_new"])
+    kc, vc = bf16_dev(d["k_cache"]), bf16_dev(d["v_cache"])
+    slots = torch.empty(wl.N, dtype=torch.int64, device="cuda")
+    out = torch.empty_like(q)
+    hashes = torch.empty(max(nh, 1), dtype=torch.int64, device="cuda")
+    ws = pkv.alloc_decode_workspace(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, pkv.BF16)
+    stream = torch.cuda.Stream()
+
+    def step(st):
+        pkv.compute_slot_mapping(bt, pos, wl.BS, out=slots, stream=st)
+        pkv.kv_cache_write(kn, vn, slots, kc, vc, stream=st)
+        pkv.paged_decode_attn(q, kc, vc, bt, sl, wl.scale, out=out, workspace=ws, stream=st)
+        pkv.prefix_block_hash(toks, toffs, wl.hash_block, hoffs, nh, seed=7, out=hashes,
+                              stream=st)
+
+    # warm up on the side stream (first calls may set kernel attributes), then capture
+    with torch.cuda.stream(stream):
+        step(stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(stream)
+    torch.cuda.synchronize()
+
+    rng = np.random.default_rng(cfg)
+    kc0, vc0 = kc.clone(), vc.clone()
+    for rep in range(3):
+        # new inputs in the same buffers
+        q.copy_(bf16_dev(W.f32_to_bf16_bits(
+            rng.standard_normal(d["q"].shape).astype(np.float32))))
+        kn.copy_(bf16_dev(W.f32_to_bf16_bits(
+            rng.standard_normal(d["k_new"].shape).astype(np.float32))))
+        kc.copy_(kc0)
+        vc.copy_(vc0)
+        graph.replay()
+        torch.cuda.synchronize()
+        got_out, got_k, got_h = dev_bits(out), dev_bits(kc), hashes[:nh].cpu().numpy()
+        # eager reference on fresh copies of the same inputs
+        kc.copy_(kc0)
+        vc.copy_(vc0)
+        out_e = torch.empty_like(q)
+        ws_e = pkv.alloc_decode_workspace(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, pkv.BF16)
+        sl_e = pkv.compute_slot_mapping(bt, pos, wl.BS)
+        pkv.kv_cache_write(kn, vn, sl_e, kc, vc)
+        pkv.paged_decode_attn(q, kc, vc, bt, sl, wl.scale, out=out_e, workspace=ws_e)
+        h_e = pkv.prefix_block_hash(toks, toffs, wl.hash_block, hoffs, nh, seed=7)
+        torch.cuda.synchronize()
+        assert np.array_equal(got_out, dev_bits(out_e)), f"replay {rep}: output differs"
+        assert np.array_equal(got_k, dev_bits(kc)), f"replay {rep}: cache differs"
+        assert np.array_equal(got_h, h_e.cpu().numpy()), f"replay {rep}: hashes differ"
+        assert pkv.read_device_error(ws) == 0

@@ -53,6 +53,8 @@ def parse():
                    help="copy_blocks: the copy-on-write block copy alone; prefill: paged "
                         "prefill attention on workload 8")
     p.add_argument("--pairs", type=int, default=4096, help="block pairs per copy_blocks launch")
+    p.add_argument("--prefill-kv", choices=["bf16", "fp8", "int8", "int4"], default="bf16",
+                   help="page kind of the cache the prefill reads (--op prefill)")
     return p.parse_args()
 
 
@@ -586,6 +588,8 @@ def run_prefill(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     wl = W.make(8, batch=args.batch)
+    kv = args.prefill_kv
+    wl.fp8, wl.int8, wl.int4 = kv == "fp8", kv == "int8", kv == "int4"
     dd = W.device_data(wl, dev)
     qo = torch.from_numpy(wl.q_offsets()).to(dev)
     bt = torch.from_numpy(wl.block_table).to(dev)
@@ -593,10 +597,27 @@ def run_prefill(args):
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty_like(dd["q"])
     main = torch.cuda.current_stream(dev)
+    ks = vs = ws = None
+    if wl.quant:
+        # quantised pages written by the library's own cache write from the source rows
+        kc = torch.zeros(wl.cache_shape, dtype=torch.int8 if wl.int8 else torch.uint8,
+                         device=dev)
+        vc = torch.zeros_like(kc)
+        req, pos = W.token_rows_order(wl)
+        slots = pkv.compute_slot_mapping(bt, torch.from_numpy(pos).to(dev), wl.BS,
+                                         req_idx=torch.from_numpy(req).to(dev))
+        ks, vs = dd["k_scale"], dd["v_scale"]
+        pkv.kv_cache_write(dd["k_rows"], dd["v_rows"], slots, kc, vc, ks, vs)
+        ws = torch.empty(pkv.prefill_workspace_size(wl.N, wl.MB, wl.Hkv, wl.D, wl.BS,
+                                                    wl.kv_kind), dtype=torch.uint8, device=dev)
+        torch.cuda.synchronize(dev)
+        del slots
+    else:
+        kc, vc = dd["k_cache"], dd["v_cache"]
 
     def launch():
-        pkv.paged_prefill_attn(dd["q"], qo, wl.max_q_len, dd["k_cache"], dd["v_cache"], bt, sl,
-                               wl.scale, out=out, error_word=err, stream=main)
+        pkv.paged_prefill_attn(dd["q"], qo, wl.max_q_len, kc, vc, bt, sl, wl.scale, out=out,
+                               k_scale=ks, v_scale=vs, workspace=ws, error_word=err, stream=main)
 
     K, Wm = args.steps, max(args.warmup, 3)
     for _ in range(Wm):
@@ -630,8 +651,14 @@ def run_prefill(args):
     achieved = flops / avg / 1e12
     # oracle: sampled rows of the same workload on the host cores, about 10 s
     q = dd["q"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    kc = dd["k_cache"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-    vc = dd["v_cache"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+    if wl.quant:
+        kc_h = kc.cpu().numpy()
+        vc_h = vc.cpu().numpy()
+        ks_h, vs_h = ks.cpu().numpy(), vs.cpu().numpy()
+    else:
+        kc_h = kc.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        vc_h = vc.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        ks_h = vs_h = None
     rng = np.random.default_rng(1)
     qo_np = wl.q_offsets()
     ql = wl.query_lens
@@ -639,7 +666,8 @@ def run_prefill(args):
     while tot_t < (0.0 if args.skip_cpu else 10.0):
         rows = rng.integers(0, wl.total_q * wl.Hq, size=64).astype(np.int64)
         t0 = time.perf_counter()
-        oracle.multiquery_rows(q, qo_np, kc, vc, wl.block_table, wl.seq_lens, wl.scale, rows)
+        oracle.multiquery_rows(q, qo_np, kc_h, vc_h, wl.block_table, wl.seq_lens, wl.scale, rows,
+                               ks_h, vs_h)
         tot_t += time.perf_counter() - t0
         for row in rows:
             tq_ = int(row) // wl.Hq
@@ -651,6 +679,8 @@ def run_prefill(args):
            "value": round(tot_f / tot_t / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
            "kind": "oracle", "sample": f"{n_rows} random (token, head) rows of {wl.name} "
                                        f"({tot_f/1e9:.1f} GFLOP in {tot_t:.1f} s), fp64 C + OpenMP"}
+    pages = "bf16" if not wl.quant else {1: "E4M3", 2: "int8", 3: "int4"}[wl.kv_kind]
+    kern = "pkv_prefill_kernel" if not wl.quant else "pkv_dequant_pages_kernel + pkv_prefill_kernel"
     line = {"metric": "paged prefill attention: causal-effective TFLOP/s (bf16 tensor cores)",
             "value": round(flops * K / t / 1e12, 2), "unit": "TFLOP/s", "n_gpus": 1,
             "steps": K, "warmup": Wm, "ms_per_step": round(t / K * 1e3, 4),
@@ -659,15 +689,17 @@ def run_prefill(args):
             "config": {"workload": wl.name, "batch": wl.N, "num_q_heads": wl.Hq,
                        "num_kv_heads": wl.Hkv, "head_dim": wl.D, "block_size": wl.BS,
                        "chunk_tokens": int(ql.max()), "context": "U[0, 6144] cached tokens",
+                       "pages": pages,
                        "flops_per_launch": flops,
                        "l2": "pages %.0f MB + q/out %.0f MB; no flush (compute-bound)" % (
-                           2 * wl.NB * wl.Hkv * wl.BS * wl.D * 2 / 1e6,
+                           2 * wl.NB * wl.Hkv * wl.BS * wl.D * wl.elt / 1e6,
                            2 * wl.total_q * wl.Hq * wl.D * 2 / 1e6)},
             "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
-                         "peak_source": peak_kind, "kernel": "pkv_prefill_kernel",
+                         "peak_source": peak_kind, "kernel": kern,
                          "flops_per_launch": flops, "avg_launch_ms": round(avg * 1e3, 4)},
-            "cpu_baseline": cpu, "e2e": None, "gpu_launches": K, "clocks": clocks}
+            "cpu_baseline": cpu, "e2e": None, "gpu_launches": K * (2 if wl.quant else 1),
+            "clocks": clocks}
     print(json.dumps(line), flush=True)
 
 

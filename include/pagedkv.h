@@ -280,20 +280,28 @@ PKV_API int pkv_prefix_block_hash(const int32_t *tokens, const int64_t *offsets,
  * A row that sees no token is zero.  Same result as pkv_paged_multiquery_attn, any
  * q_len.  max_q_len bounds every q_len_r: rows past it are not computed and
  * PKV_DEVERR_QLEN_CLAMPED is set; a request whose rows run past total_q is skipped
- * and flagged the same way.  Runs on the tcgen05 tensor cores: one CTA per 128 query rows
- * (128/G tokens x the G heads of a KV head).
+ * and flagged the same way.  Runs on the tcgen05 tensor cores: one CTA per 128 query
+ * rows (128/G tokens x the G heads of a KV head).
  *   q, out          bf16 [total_q][Hq][D], 16-byte aligned; rows of no request untouched
- *   k/v_cache       bf16 pages [NB][Hkv][BS][D]
+ *   k/v_cache       pages of cache_dtype (layouts above); k/v_scale for quantised kinds
+ *   workspace       quantised kinds only: pkv_prefill_workspace_size bytes, 256-byte
+ *                   aligned.  The batch's pages are first expanded to bf16 there
+ *                   (code * scale, rounded to nearest even) in request order, then the
+ *                   bf16 kernel runs on that pool.  bf16 pages need no workspace (NULL).
  *   error_word      device uint32 collecting PKV_DEVERR_* bits (sticky), or NULL
  * scale must be finite and > 0 (else PKV_ERR_INVALID_ARG).
- * Supported: bf16 pages, head_dim 64 or 128, block_size 16 or 32, G in {1, 2, 4, 8};
- * other shapes return PKV_ERR_UNSUPPORTED.  No workspace. */
+ * Supported: head_dim 64 or 128, block_size 16 or 32, G in {1, 2, 4, 8}; other shapes
+ * return PKV_ERR_UNSUPPORTED. */
+PKV_API size_t pkv_prefill_workspace_size(int batch, int max_blocks_per_seq, int num_kv_heads,
+                                          int head_dim, int block_size, int cache_dtype);
 PKV_API int pkv_paged_prefill_attn(const void *q, const int32_t *q_offsets, int total_q,
                                    int max_q_len, const void *k_cache, const void *v_cache,
+                                   const float *k_scale, const float *v_scale,
                                    const int32_t *block_table, int max_blocks_per_seq,
                                    const int32_t *seq_lens, int batch, int num_q_heads,
                                    int num_kv_heads, int head_dim, int block_size,
                                    int num_blocks, int cache_dtype, float scale, void *out,
+                                   void *workspace, size_t workspace_bytes,
                                    uint32_t *error_word, pkv_stream_t stream);
 
 /*

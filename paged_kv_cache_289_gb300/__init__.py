@@ -18,7 +18,7 @@ __all__ = [
     "paged_decode_attn_noalloc", "prefix_block_hash", "multiquery_workspace_size",
     "paged_multiquery_attn", "DEVERR_QLEN_CLAMPED", "kv_cache_write_rescale",
     "device_num_sms", "read_device_error", "copy_blocks", "BlockManager", "ERR_NO_BLOCKS",
-    "paged_prefill_attn",
+    "paged_prefill_attn", "prefill_workspace_size",
 ]
 
 BF16 = 0
@@ -86,9 +86,11 @@ def lib():
                                                         i, f, p, p]
             L.pkv_prefix_block_hash.restype = i
             L.pkv_prefix_block_hash.argtypes = [p, p, i, i, u64, p, p, p]
+            L.pkv_prefill_workspace_size.restype = sz
+            L.pkv_prefill_workspace_size.argtypes = [i, i, i, i, i, i]
             L.pkv_paged_prefill_attn.restype = i
-            L.pkv_paged_prefill_attn.argtypes = [p, p, i, i, p, p, p, i, p, i, i, i, i, i, i, i, f,
-                                                 p, p, p]
+            L.pkv_paged_prefill_attn.argtypes = [p, p, i, i, p, p, p, p, p, i, p, i, i, i, i, i,
+                                                 i, i, f, p, p, sz, p, p]
             L.pkv_copy_blocks.restype = i
             L.pkv_copy_blocks.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p]
             L.pkv_bm_create.restype = i
@@ -415,27 +417,41 @@ class BlockManager:
         return n
 
 
+def prefill_workspace_size(batch, max_blocks_per_seq, num_kv_heads, head_dim, block_size,
+                           cache_dtype) -> int:
+    return int(lib().pkv_prefill_workspace_size(batch, max_blocks_per_seq, num_kv_heads,
+                                                head_dim, block_size, cache_dtype))
+
+
 def paged_prefill_attn(q, q_offsets, max_q_len, k_cache, v_cache, block_table, seq_lens, scale,
-                       out=None, error_word=None, stream=None):
+                       out=None, k_scale=None, v_scale=None, workspace=None, error_word=None,
+                       stream=None):
     """Causal attention of prefill chunks over the paged cache on the tensor cores: request
     r's query rows q_offsets[r] .. q_offsets[r+1]-1 are its newest tokens (already written
-    to the pages); query i sees positions 0 .. seq_len - q_len + i.  bf16 pages.
+    to the pages); query i sees positions 0 .. seq_len - q_len + i.  Quantised pages (E4M3,
+    int8, int4) take their scales and a workspace (allocated here if not given).
     `error_word` (optional int32 CUDA tensor) collects the PKV_DEVERR_* bits."""
     import torch
     _need(q, "q", (torch.bfloat16,))
     _need(q_offsets, "q_offsets", (torch.int32,))
-    _need(k_cache, "k_cache", (torch.bfloat16,))
-    _need(v_cache, "v_cache", (torch.bfloat16,))
+    _need(k_cache, "k_cache", None)
+    _need(v_cache, "v_cache", None)
     _need(block_table, "block_table", (torch.int32,))
     _need(seq_lens, "seq_lens", (torch.int32,))
     if error_word is not None:
         _need(error_word, "error_word", (torch.int32,))
     T, Hq, D = q.shape
     NB, Hkv, BS, _ = k_cache.shape
+    dt = _cache_dtype(k_cache, D)
+    N, MB = seq_lens.shape[0], block_table.shape[1]
+    if dt != BF16 and workspace is None:
+        n = prefill_workspace_size(N, MB, Hkv, D, BS, dt)
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
     if out is None:
         out = torch.empty_like(q)
     _check("pkv_paged_prefill_attn", lib().pkv_paged_prefill_attn(
         _ptr(q), _ptr(q_offsets), T, int(max_q_len), _ptr(k_cache), _ptr(v_cache),
-        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), seq_lens.shape[0], Hq, Hkv, D,
-        BS, NB, BF16, float(scale), _ptr(out), _ptr(error_word), _stream(stream)))
+        _ptr(k_scale), _ptr(v_scale), _ptr(block_table), MB, _ptr(seq_lens), N, Hq, Hkv, D,
+        BS, NB, dt, float(scale), _ptr(out), _ptr(workspace),
+        0 if workspace is None else workspace.numel(), _ptr(error_word), _stream(stream)))
     return out

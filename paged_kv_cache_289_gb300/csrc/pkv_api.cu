@@ -221,16 +221,31 @@ int pkv_prefix_block_hash(const int32_t* tokens, const int64_t* offsets, int num
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+size_t pkv_prefill_workspace_size(int batch, int max_blocks_per_seq, int num_kv_heads,
+                                  int head_dim, int block_size, int cache_dtype) {
+    if (batch <= 0 || max_blocks_per_seq <= 0 || num_kv_heads <= 0 || head_dim <= 0 ||
+        block_size <= 0)
+        return 0;
+    if (cache_dtype == PKV_BF16) return 0;
+    const int64_t blocks = (int64_t)batch * max_blocks_per_seq;
+    const int64_t pool = blocks * num_kv_heads * block_size * head_dim * 2;   // bf16, K or V
+    return (size_t)(2 * pkv::align_up(pool, 256) + pkv::align_up(blocks * 4, 256));
+}
+
 int pkv_paged_prefill_attn(const void* q, const int32_t* q_offsets, int total_q, int max_q_len,
-                           const void* k_cache, const void* v_cache,
-                           const int32_t* block_table, int max_blocks_per_seq,
-                           const int32_t* seq_lens, int batch, int num_q_heads, int num_kv_heads,
-                           int head_dim, int block_size, int num_blocks, int cache_dtype,
-                           float scale, void* out, uint32_t* error_word, pkv_stream_t stream) {
+                           const void* k_cache, const void* v_cache, const float* k_scale,
+                           const float* v_scale, const int32_t* block_table,
+                           int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int num_blocks, int cache_dtype, float scale, void* out,
+                           void* workspace, size_t workspace_bytes, uint32_t* error_word,
+                           pkv_stream_t stream) {
     if (batch < 0 || total_q < 0 || max_q_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0)
         return PKV_ERR_INVALID_ARG;
-    if (!pkv::prefill_shape_supported(num_q_heads, num_kv_heads, head_dim, block_size,
-                                      cache_dtype))
+    if (cache_dtype != PKV_BF16 && cache_dtype != PKV_FP8_E4M3 && cache_dtype != PKV_INT8 &&
+        cache_dtype != PKV_INT4)
+        return PKV_ERR_UNSUPPORTED;
+    if (!pkv::prefill_shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, PKV_BF16))
         return PKV_ERR_UNSUPPORTED;
     if (!(scale > 0.f) || scale > 3.0e38f) return PKV_ERR_INVALID_ARG;   // finite, > 0
     if (batch == 0 || total_q == 0 || max_q_len == 0) return PKV_OK;
@@ -241,6 +256,7 @@ int pkv_paged_prefill_attn(const void* q, const int32_t* q_offsets, int total_q,
     if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
         !aligned(error_word, 4))
         return PKV_ERR_INVALID_ARG;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     pkv::PrefillLaunch L;
     L.q = q;
     L.q_offsets = q_offsets;
@@ -260,7 +276,32 @@ int pkv_paged_prefill_attn(const void* q, const int32_t* q_offsets, int total_q,
     L.MB = max_blocks_per_seq;
     L.NB = num_blocks;
     L.scale = scale;
-    return pkv::prefill_launch(L, reinterpret_cast<cudaStream_t>(stream));
+    if (cache_dtype != PKV_BF16) {
+        // quantised pages: expand the batch's pages to a bf16 pool, then the bf16 kernel
+        if (!k_scale || !v_scale) return PKV_ERR_INVALID_ARG;
+        const size_t need = pkv_prefill_workspace_size(batch, max_blocks_per_seq, num_kv_heads,
+                                                       head_dim, block_size, cache_dtype);
+        if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+        if (!aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
+        const int64_t blocks = (int64_t)batch * max_blocks_per_seq;
+        if ((blocks + 1) * num_kv_heads * block_size >= ((int64_t)1 << 31))
+            return PKV_ERR_UNSUPPORTED;
+        const int64_t pool = pkv::align_up(blocks * num_kv_heads * block_size * head_dim * 2, 256);
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        int sms = 0;
+        const int sst = current_num_sms(&sms);
+        if (sst != PKV_OK) return sst;
+        cudaError_t e = pkv::dequant_pages_launch(
+            k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, batch, max_blocks_per_seq,
+            num_blocks, num_kv_heads, block_size, head_dim, cache_dtype, ws, ws + pool,
+            reinterpret_cast<int32_t*>(ws + 2 * pool), error_word, sms, st);
+        if (e != cudaSuccess) return PKV_ERR_CUDA;
+        L.k_cache = ws;
+        L.v_cache = ws + pool;
+        L.block_table = reinterpret_cast<const int32_t*>(ws + 2 * pool);
+        L.NB = (int)blocks;
+    }
+    return pkv::prefill_launch(L, st);
 }
 
 int pkv_copy_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,

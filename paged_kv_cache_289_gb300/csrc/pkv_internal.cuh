@@ -105,6 +105,11 @@ struct PrefillLaunch {
     float scale;
 };
 bool prefill_shape_supported(int Hq, int Hkv, int D, int BS, int dtype);
+cudaError_t dequant_pages_launch(const void* k_cache, const void* v_cache, const float* k_scale,
+                                 const float* v_scale, const int32_t* block_table,
+                                 const int32_t* seq_lens, int N, int MB, int NB, int Hkv, int BS,
+                                 int D, int kt, void* kout, void* vout, int32_t* bt_out,
+                                 uint32_t* err, int num_sms, cudaStream_t st);
 int prefill_launch(const PrefillLaunch& L, cudaStream_t st);
 cudaError_t copy_blocks_launch(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
                                const int32_t* mapping, int pairs, int64_t block_bytes, int NB,

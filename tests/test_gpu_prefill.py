@@ -147,20 +147,53 @@ def test_prefill_rejects():
     L = pkv.lib()
     z = torch.zeros(64, dtype=torch.int32, device="cuda")
     p = z.data_ptr()
-    # fp8 pages, G = 3, head_dim 96 are not prefill shapes
-    assert L.pkv_paged_prefill_attn(p, p, 1, 1, p, p, p, 1, p, 1, 8, 8, 128, 16, 4, 1, 1.0, p,
-                                    None, None) == -2
-    assert L.pkv_paged_prefill_attn(p, p, 1, 1, p, p, p, 1, p, 1, 12, 4, 128, 16, 4, 0, 1.0, p,
-                                    None, None) == -2
-    assert L.pkv_paged_prefill_attn(p, p, 1, 1, p, p, p, 1, p, 1, 8, 8, 96, 16, 4, 0, 1.0, p,
-                                    None, None) == -2
-    assert L.pkv_paged_prefill_attn(p + 2, p, 1, 1, p, p, p, 1, p, 1, 8, 8, 128, 16, 4, 0, 1.0,
-                                    p, None, None) == -1
-    assert L.pkv_paged_prefill_attn(p, p, 0, 0, p, p, p, 1, p, 1, 8, 8, 128, 16, 4, 0, 1.0, p,
-                                    None, None) == 0
+
+    def call(q=None, total_q=1, max_q_len=1, Hq=8, Hkv=8, D=128, BS=16, dt=0, scale=1.0,
+             ks=None, ws=None, ws_bytes=0):
+        return L.pkv_paged_prefill_attn(p if q is None else q, p, total_q, max_q_len, p, p, ks,
+                                        ks, p, 1, p, 1, Hq, Hkv, D, BS, 4, dt, scale, p, ws,
+                                        ws_bytes, None, None)
+    assert call(dt=5) == -2                       # not a page kind
+    assert call(Hq=12, Hkv=4) == -2               # G = 3
+    assert call(D=96) == -2                       # head_dim 96
+    assert call(q=p + 2) == -1                    # misaligned q
+    assert call(total_q=0, max_q_len=0) == 0      # nothing to do
     for bad in (0.0, -1.0, float("nan"), float("inf")):    # scale must be finite and > 0
-        assert L.pkv_paged_prefill_attn(p, p, 1, 1, p, p, p, 1, p, 1, 8, 8, 128, 16, 4, 0, bad,
-                                        p, None, None) == -1
+        assert call(scale=bad) == -1
+    assert call(dt=1) == -1                       # quantised pages need their scales
+    assert call(dt=1, ks=p) == -3                 # ... and a workspace
+    n = L.pkv_prefill_workspace_size(1, 1, 8, 128, 16, 1)
+    assert n > 0 and L.pkv_prefill_workspace_size(1, 1, 8, 128, 16, 0) == 0
+    assert call(dt=1, ks=p, ws=p, ws_bytes=n - 1) == -3
+
+
+@pytest.mark.parametrize("kind", ["fp8", "int8", "int4"])
+def test_prefill_over_quantised_pages(kind):
+    """Ragged prefill chunks over E4M3 / int8 / int4 pages (the oracle quantises the same
+    source rows with its own write): the pages are expanded to bf16, then the tensor-core
+    kernel runs; the result is within the quantised-page tolerance of the oracle fed the
+    exact dequantised values."""
+    torch = torch_mod()
+    wl = W.make(8, small=True)
+    wl.fp8, wl.int8, wl.int4 = kind == "fp8", kind == "int8", kind == "int4"
+    case = HostCase(wl)
+    kc = torch.zeros(wl.cache_shape, dtype=torch.int8 if wl.int8 else torch.uint8, device="cuda")
+    vc = torch.zeros_like(kc)
+    ks, vs = to_dev(case.d["k_scale"]), to_dev(case.d["v_scale"])
+    slots = pkv.compute_slot_mapping(to_dev(wl.block_table), to_dev(case.pos_all), wl.BS,
+                                     req_idx=to_dev(case.req_all))
+    pkv.kv_cache_write(bf16_dev(case.d["k_rows"]), bf16_dev(case.d["v_rows"]), slots, kc, vc,
+                       ks, vs)
+    assert np.array_equal(dev_bits(kc), case.kc) and np.array_equal(dev_bits(vc), case.vc)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = pkv.paged_prefill_attn(bf16_dev(case.d["q"]), to_dev(wl.q_offsets()), wl.max_q_len, kc,
+                                 vc, to_dev(wl.block_table), to_dev(wl.seq_lens), wl.scale,
+                                 k_scale=ks, v_scale=vs, error_word=err)
+    torch.cuda.synchronize()
+    ref = oracle.multiquery_attn(case.d["q"], wl.q_offsets(), case.kc, case.vc, wl.block_table,
+                                 wl.seq_lens, wl.scale, case.d["k_scale"], case.d["v_scale"])
+    assert int(err.item()) == 0
+    compare(out_to_f64(out), ref, True)
 
 
 def test_prefill_full_size_sampled():

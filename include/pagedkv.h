@@ -236,8 +236,8 @@ PKV_API int pkv_paged_multiquery_attn(const void *q, const int32_t *q_offsets, i
  * until the process exits.
  *   - Shapes whose pkv_decode_workspace_size exceeds 16 MiB return
  *     PKV_ERR_WORKSPACE and launch nothing (at head_dim 128 on a 152-SM GPU:
- *     batch * num_kv_heads up to about 3,050 for bf16 pages and
- *     2,750 for quantised pages, whose plan runs more warps).
+ *     batch * num_kv_heads up to about 3,050 for bf16 pages, 2,750 for
+ *     E4M3 and int8 pages and 2,140 for int4 pages, whose plans run more warps).
  *   - The first call on a device, made with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress); make that first call before
  *     any stream capture.

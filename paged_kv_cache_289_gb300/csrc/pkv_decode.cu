@@ -86,9 +86,10 @@ struct Cfg {
     static constexpr int MT = TT / 16;                    // 16-token mma tiles per tile
     static constexpr int KS = D / 16;                     // QK k-steps
     static constexpr int DT = D / 16;                     // PV d-tiles
-    // 8/16-bit rows are whole 128-byte swizzle lines; int4 rows (64 bytes at D = 128)
-    // are stored unswizzled
+    // 8/16-bit rows are whole 128-byte swizzle lines; int4 rows are 64 bytes (D = 128),
+    // stored with the 64-byte swizzle
     static_assert(I4 || ROW_BYTES % 128 == 0, "rows must be whole 128-byte swizzle lines");
+    static_assert(!I4 || ROW_BYTES == 64, "int4 rows are 64 bytes");
     static_assert(BS % 16 == 0, "block size must be a multiple of 16");
     static_assert(SUB == 1 || SUB == 2, "one or two tiles per page");
 };
@@ -108,6 +109,14 @@ constexpr float kRescaleSlack = 8.f;
 template <int ROWS>
 __device__ __forceinline__ uint32_t swz(int t, int kc) {
     return (uint32_t)((kc >> 3) * (ROWS * 128) + t * 128 + (((kc & 7) ^ (t & 7)) << 4));
+}
+
+// Byte offset of 16-byte unit `u` (0-3) of row `t` inside an int4 tile of 64-byte rows
+// laid out by TMA with the 64-byte swizzle: address bits 4-5 XOR bits 7-8, i.e. the unit
+// index XOR (t / 2 mod 4).  The eight rows one ldmatrix matrix reads then fall in eight
+// different 16-byte bank groups (unswizzled they would share two, a 4-way conflict).
+__device__ __forceinline__ uint32_t swz64(int t, int u) {
+    return (uint32_t)(t * 64 + ((u ^ ((t >> 1) & 3)) << 4));
 }
 
 // Per-lane description of one page of a 32-page batch.
@@ -262,7 +271,7 @@ __device__ __noinline__ void merge_unit(const float* partials, uint16_t* out, in
 }
 
 template <int D, int BS, int KT, int QT>
-__global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
+__global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 1)
     pkv_decode_kernel(const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV, const DecodeArgs a) {
     constexpr bool FP8 = KT != 0;   // quantised pages (E4M3, int8, int4) with per-(block, head) scales
@@ -376,7 +385,7 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
             if constexpr (C::I4) {
-                // one box per tile: TT rows of D/2 bytes, unswizzled
+                // one box per tile: TT rows of D/2 bytes, 64-byte swizzle
                 tma_load_2d_hint(dst, &tmK, 0, y, bar, policy);
                 tma_load_2d_hint(dst + C::TILE_BYTES, &tmV, 0, y, bar, policy);
             } else {
@@ -634,8 +643,7 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
 #pragma unroll
                 for (int dblk = 0; dblk < D / 64; ++dblk) {
                     uint32_t r0, r1, r2, r3;
-                    ldsm_x4(kpg + (uint32_t)(tr * C::ROW_BYTES + dblk * 32 + (lane >> 4) * 16), r0,
-                            r1, r2, r3);
+                    ldsm_x4(kpg + swz64(tr, dblk * 2 + (lane >> 4)), r0, r1, r2, r3);
 #pragma unroll
                     for (int qi = 0; qi < QT; ++qi) {
                         mma_f16(e0[qi], i4pick_to_f16x2<0>(r0), i4pick_to_f16x2<0>(r1),
@@ -692,18 +700,26 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
         const float sc_page = FP8 ? qscale * ks : qscale;
         float mx0[QT], mx1[QT];
         bool need = false;
+        // every row of a full tile is a cached token every query sees: no mask
+        const bool full_tile = QT == 1 && ntok >= C::TT;
 #pragma unroll
         for (int qi = 0; qi < QT; ++qi) {
             mx0[qi] = mx1[qi] = -INFINITY;
 #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
+                if (full_tile) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int tok = mt * 16 + g + ((e & 2) ? 8 : 0);
-                    bool valid = tok < ntok;
-                    if constexpr (QT > 1) valid = valid && (tpos0 + tok <= seg_vis + qi);
-                    const float v = sacc[mt][qi][e] * sc_page;
-                    sacc[mt][qi][e] = valid ? v : -INFINITY;
+                    for (int e = 0; e < 4; ++e)
+                        sacc[mt][qi][e] *= sc_page;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int tok = mt * 16 + g + ((e & 2) ? 8 : 0);
+                        bool valid = tok < ntok;
+                        if constexpr (QT > 1) valid = valid && (tpos0 + tok <= seg_vis + qi);
+                        const float v = sacc[mt][qi][e] * sc_page;
+                        sacc[mt][qi][e] = valid ? v : -INFINITY;
+                    }
                 }
                 mx0[qi] = fmaxf(mx0[qi], fmaxf(sacc[mt][qi][0], sacc[mt][qi][2]));
                 mx1[qi] = fmaxf(mx1[qi], fmaxf(sacc[mt][qi][1], sacc[mt][qi][3]));
@@ -799,8 +815,7 @@ __global__ void __launch_bounds__((KT != 0 || QT > 1) ? 256 : 384, 1)
 #pragma unroll
                     for (int dblk = 0; dblk < D / 64; ++dblk) {
                         uint32_t r0, r1, r2, r3;
-                        ldsm_x4(vpg + (uint32_t)(tr * C::ROW_BYTES + dblk * 32 + (lane >> 4) * 16),
-                                r0, r1, r2, r3);
+                        ldsm_x4(vpg + swz64(tr, dblk * 2 + (lane >> 4)), r0, r1, r2, r3);
                         const uint32_t m0 = movmatrix_trans(r0);   // tokens 0-7,  d + 0
                         const uint32_t m1 = movmatrix_trans(r1);   // tokens 8-15, d + 0
                         const uint32_t m2 = movmatrix_trans(r2);   // tokens 0-7,  d + 32
@@ -1110,9 +1125,13 @@ DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int ba
     // instruction chain of a warp, not the bytes in flight, limits the rate, so the
     // CTA runs several warps per SM sub-partition.  Measured on GB300: 6 warps for
     // single-query bf16 pages, 8 for 8-bit pages (whose tiles carry twice the tokens)
-    // and for several query positions.
-    const int max_warps = (fp8 || qt > 1) ? 8 : 12;   // register budget of the launch bounds
-    p.warps = env_int("PKV_DECODE_WARPS", (fp8 || qt > 1) ? 8 : 6);
+    // and for several query positions, 12 for single-query int4 pages (compute-bound:
+    // 0.44 of the copy peak against 0.40 with 8; 10 warps split unevenly over the four
+    // sub-partitions and run slower).
+    // register budget of the launch bounds: 384 threads for single-query bf16 and int4
+    // pages, 256 otherwise
+    const int max_warps = ((fp8 && kt != 3) || qt > 1) ? 8 : 12;
+    p.warps = env_int("PKV_DECODE_WARPS", (kt == 3 && qt == 1) ? 12 : ((fp8 || qt > 1) ? 8 : 6));
     if (p.warps < 1) p.warps = 1;
     if (p.warps > max_warps) p.warps = max_warps;
     int stages = env_int("PKV_DECODE_STAGES", 0);
@@ -1163,13 +1182,13 @@ static bool encode_cache_map(CUtensorMap* m, const void* base, int fp8, int D, i
                              int64_t rows, int kt) {
     auto fn = encode_fn();
     if (!fn) return false;
-    if (kt == 3) {   // int4 rows: D/2 bytes, one unswizzled box of BS rows
+    if (kt == 3) {   // int4 rows: D/2 = 64 bytes, one box of BS rows, 64-byte swizzle
         cuuint64_t dims[2] = {(cuuint64_t)(D / 2), (cuuint64_t)rows};
         cuuint64_t strides[1] = {(cuuint64_t)(D / 2)};
         cuuint32_t box[2] = {(cuuint32_t)(D / 2), (cuuint32_t)BS};
         cuuint32_t estr[2] = {1, 1};
         return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
-                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
     }

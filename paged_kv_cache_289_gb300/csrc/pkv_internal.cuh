@@ -8,6 +8,7 @@
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -314,13 +315,19 @@ template <int I>
 __device__ __forceinline__ uint32_t i4pick_to_f16x2(uint32_t x) {
     const uint32_t w = (I >= 2) ? (x >> 8) : x;
     uint32_t r;
+    // the constants are literals the compiler can place in the instruction
     if constexpr ((I & 1) == 0) {
         const uint32_t y = (w & 0x000F000Fu) | 0x64006400u;      // (1024 + n, 1024 + n')
-        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(0x64086408u));   // - 1032
+        const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&y),
+                                  __half2half2(__ushort_as_half((unsigned short)0x6408u)));   // - 1032
+        r = *reinterpret_cast<const uint32_t*>(&h);
     } else {
         const uint32_t y = (w & 0x00F000F0u) | 0x64006400u;      // (1024 + 16 n, ...)
         // (1024 + 16 n) / 16 - 72 = n - 8
-        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(y), "r"(0x2C002C00u), "r"(0xD480D480u));
+        const __half2 h = __hfma2(*reinterpret_cast<const __half2*>(&y),
+                                  __half2half2(__ushort_as_half((unsigned short)0x2C00u)),
+                                  __half2half2(__ushort_as_half((unsigned short)0xD480u)));
+        r = *reinterpret_cast<const uint32_t*>(&h);
     }
     return r;
 }

@@ -9,16 +9,19 @@
 //
 // One CTA = one 128-row query tile of one (request, KV head): 128 / G query tokens x
 // the G query heads of the group, so every K/V tile staged in shared memory serves
-// the whole GQA group.  Per 128-token KV tile:
-//   S = Q K^T      tcgen05.mma, M = 128, N = 128, K = D; A and B K-major in shared
-//                  memory (128-byte swizzle, TMA), D in tensor memory (two S buffers)
-//   softmax        4 warps, one TMEM lane (= one query row) per thread: online max and
-//                  sum in the log2 domain, P rounded to bf16 into tensor memory
-//   O += P V       tcgen05.mma with A = P read from tensor memory and B = V, MN-major
-//                  (the page rows are tokens, d contiguous)
-// Warp roles: warps 0-3 softmax + epilogue, warp 4 TMA producer (and TMEM owner),
-// warp 5 MMA issuer.  K/V tiles are double-buffered; S is double-buffered so the
-// next tile's Q K^T runs while this tile's softmax does.  Every wait is bounded.
+// the whole GQA group.  Per 256-token KV tile:
+//   S = Q K^T      tcgen05.mma, M = 128, N = 256, K = D; A (Q) and B (K) K-major in
+//                  shared memory (128-byte swizzle), S in tensor memory (256 columns)
+//   softmax        2 x 4 warps, one TMEM lane (= one query row) per thread, each
+//                  warpgroup one half (128 columns) of every row: online max and sum in
+//                  the log2 domain, P rounded to bf16 into its own tensor-memory columns
+//   O += P V       tcgen05.mma, M = 128, N = D, A = P read from tensor memory and B = V
+//                  (MN-major: the page rows are tokens, d contiguous), in two 128-token
+//                  halves
+// The softmax warps release S as soon as they have loaded it, so the next tile's
+// Q K^T runs during this tile's softmax.  Warp roles: warps 0-7 softmax + epilogue,
+// warp 8 K producer (and TMEM owner), warp 9 V producer, warp 10 MMA issuer (lane 0).
+// Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -29,10 +32,11 @@ namespace pkv {
 namespace {
 
 constexpr int kRows = 128;        // query rows per tile (TMEM lanes)
-constexpr int kKvTile = 128;      // tokens per K/V tile
+constexpr int kKvTile = 256;      // tokens per K tile (and per score tile)
+constexpr int kVHalf = 128;       // tokens per V half-tile
 constexpr int kThreads = 352;     // 11 warps: 2 x 4 softmax, K producer, V producer, MMA
 constexpr uint64_t kWaitNs = 2000000000ull;
-constexpr uint32_t kColO = 256, kColP = 384, kColQ = 448, kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColP = 256, kColO = 384, kTmemCols = 512;
 
 // ------------------------------------------------------------ tcgen05 wrappers
 __device__ __forceinline__ void tc_fence_before() {
@@ -189,26 +193,35 @@ struct PrefillArgs {
     float scale_log2;
 };
 
-// Shared memory: K ring [NS][KB][128 rows][128 B] | V ring [NS][KB][128][128 B];
-// 1024-byte aligned (128-byte swizzle atoms).  Q lives in tensor memory.
+// Shared memory, one 1024-byte aligned block (128-byte swizzle atoms):
+//   Q [KB][128 rows][128 B] | K [2 slots][KB][256 rows][128 B] | V [2 half-slots][KB][128 rows][128 B]
+//   | row-max exchange [2 parities][2 halves][128 rows] fp32 | mbarriers | TMEM base, abort flag
+// At D = 128 that is 231,568 bytes of the 232,448 a CTA may use, with no slack for
+// realignment: the kernel checks that the block starts 1024-byte aligned.
 template <int D>
 struct PrefillSmem {
     static constexpr int KB = D / 64;
-    static constexpr int NS = 3;                    // ring depth
-    static constexpr int TILE = KB * kRows * 128;   // bytes of one 128-row operand tile
-    static constexpr int K_OFF = 0;
-    static constexpr int V_OFF = NS * TILE;
-    static constexpr int BYTES = 2 * NS * TILE;
-    static constexpr int ALLOC = BYTES + 1024;
+    static constexpr int Q_BYTES = KB * kRows * 128;
+    static constexpr int K_TILE = KB * kKvTile * 128;
+    static constexpr int V_HALF = KB * kVHalf * 128;
+    static constexpr int NK = 2, NV = 2;           // K slots, V half-slots
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = Q_OFF + Q_BYTES;
+    static constexpr int V_OFF = K_OFF + NK * K_TILE;
+    static constexpr int XCH_OFF = V_OFF + NV * V_HALF;
+    static constexpr int BAR_OFF = XCH_OFF + 2 * 2 * kRows * 4;
+    static constexpr int NBARS = 16;
+    static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;
+    static constexpr int BYTES = MISC_OFF + 16;
+    static_assert(BYTES <= 232448, "shared memory of one CTA");
 };
 
-// TMEM columns: S buffers 0 and 128 (fp32 scores of one K/V tile), O at 256 (fp32),
-// P at 384 (bf16 pairs, 64 columns), Q at 448 (bf16 pairs, D/2 columns).  Q K^T reads
-// its A operand (Q) and P V its A operand (P) from tensor memory, so each MMA streams
-// only its B operand (a K or V tile) from shared memory.
+// TMEM columns: S at 0 (fp32 scores of one 256-token tile, 256 columns), P at 256 (bf16
+// pairs, 128 columns), O at 384 (fp32, D columns).  P V reads its A operand (P) from
+// tensor memory.
 //
-// Softmax: two warpgroups split every score row: warps 0-3 take columns 0-63 of the
-// tile, warps 4-7 columns 64-127 (the same TMEM lanes, i.e. the same query rows).  The
+// Softmax: two warpgroups split every score row: warps 0-3 take columns 0-127 of the
+// tile, warps 4-7 columns 128-255 (the same TMEM lanes, i.e. the same query rows).  The
 // partners exchange their row max through shared memory once per tile; each keeps its
 // own partial row sum, the halves are added at the end.
 template <int D, int BS, int G>
@@ -217,24 +230,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const PrefillArgs a) {
     using SM = PrefillSmem<D>;
     constexpr int KB = SM::KB;
-    constexpr int NS = SM::NS;
     constexpr int TQ = kRows / G;            // query tokens per tile
-    constexpr int PAGES = kKvTile / BS;      // pages per K/V tile
+    constexpr int PAGES = kKvTile / BS;      // pages per K tile
+    constexpr int HPAGES = kVHalf / BS;      // pages per V half-tile
     constexpr int HALF = kKvTile / 2;        // score columns per softmax warpgroup
     constexpr int DH = D / 2;                // O / Q columns per warpgroup (d values)
     constexpr uint32_t ID_S = idesc_bf16(kRows, kKvTile, 0);
     constexpr uint32_t ID_O = idesc_bf16(kRows, D, 1);
 
-    extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t bars[8 + 4 * NS];
-    __shared__ uint32_t tmem_base_s;
-    __shared__ int abort_s;
-    __shared__ float xch[2][2][kRows];       // [tile parity][half][row]: partial row maxima
-    __shared__ float xl[2][kRows];           // [half][row]: partial row sums
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
 
     pdl_launch_dependents();
     pdl_wait();
 
+    if (smem_u32(smem_raw) & 1023u) {        // the swizzled layout needs the alignment
+        if (threadIdx.x == 0) flag_err(a.err, PKV_DEVERR_WAIT_TIMEOUT);
+        return;
+    }
     const int tile = a.tiles - 1 - (int)blockIdx.x;   // heavy (late) tiles first
     const int h = blockIdx.y;
     const int r = blockIdx.z;
@@ -258,44 +270,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kv_end > a.MB * BS) kv_end = a.MB * BS;
     if (kv_end < 0) kv_end = 0;
     const int n_tiles = (kv_end + kKvTile - 1) / kKvTile;
+    // V halves: both halves of every tile but the last, whose second half is loaded
+    // only if a token of it is visible
+    const int last_valid = n_tiles > 0 ? kv_end - (n_tiles - 1) * kKvTile : 0;   // 1..256
+    const int n_halves = n_tiles > 0 ? 2 * n_tiles - (last_valid <= kVHalf ? 1 : 0) : 0;
+    const int tail_valid = n_halves > 0 ? kv_end - (n_halves - 1) * kVHalf : 0;  // 1..128
 
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+    uint8_t* sm = smem_raw;
+    const uint32_t sQ = smem_u32(sm + SM::Q_OFF);
     const uint32_t sK = smem_u32(sm + SM::K_OFF);
     const uint32_t sV = smem_u32(sm + SM::V_OFF);
-    const uint32_t bar_q = smem_u32(&bars[0]);          // Q stored to TMEM (8 warps)
-    const uint32_t bar_p_ready = smem_u32(&bars[1]);    // P stored (8 warps)
-    const uint32_t bar_pv = smem_u32(&bars[2]);
-    const uint32_t bar_s_full = smem_u32(&bars[3]);     // [2]
-    const uint32_t bar_s_free = smem_u32(&bars[5]);     // [2] (8 warps)
-    const uint32_t bar_v_tail = smem_u32(&bars[7]);     // last V tile's tail zeroed
-    const uint32_t bar_k_full = smem_u32(&bars[8]);            // [NS]
-    const uint32_t bar_k_empty = smem_u32(&bars[8 + NS]);      // [NS]
-    const uint32_t bar_v_full = smem_u32(&bars[8 + 2 * NS]);   // [NS]
-    const uint32_t bar_v_empty = smem_u32(&bars[8 + 3 * NS]);  // [NS]
+    float* xch = reinterpret_cast<float*>(sm + SM::XCH_OFF);   // [parity][half][row]
+    const uint32_t bars = smem_u32(sm + SM::BAR_OFF);
+    uint32_t* tmem_base_s = reinterpret_cast<uint32_t*>(sm + SM::MISC_OFF);
+    volatile int* abort_v = reinterpret_cast<volatile int*>(sm + SM::MISC_OFF + 4);
+    const uint32_t bar_q = bars + 0;            // Q stored to shared memory (8 warps)
+    const uint32_t bar_s_full = bars + 8;       // S computed (commit)
+    const uint32_t bar_s_free = bars + 16;      // S loaded by the softmax (8 warps)
+    const uint32_t bar_p_ready = bars + 24;     // P stored (8 warps)
+    const uint32_t bar_pv = bars + 32;          // P V done (commit)
+    const uint32_t bar_v_tail = bars + 40;      // last V half's tail zeroed
+    const uint32_t bar_k_full = bars + 48;      // [2]
+    const uint32_t bar_k_empty = bars + 64;     // [2]
+    const uint32_t bar_v_full = bars + 80;      // [2]
+    const uint32_t bar_v_empty = bars + 96;     // [2]
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) {
         mbar_init(bar_q, 8);
+        mbar_init(bar_s_full, 1);
+        mbar_init(bar_s_free, 8);
         mbar_init(bar_p_ready, 8);
         mbar_init(bar_pv, 1);
         mbar_init(bar_v_tail, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_s_full + 8 * i, 1);
-            mbar_init(bar_s_free + 8 * i, 8);
-        }
-        for (int i = 0; i < NS; ++i) {
             mbar_init(bar_k_full + 8 * i, 1);
             mbar_init(bar_k_empty + 8 * i, 1);
             mbar_init(bar_v_full + 8 * i, 1);
             mbar_init(bar_v_empty + 8 * i, 1);
         }
-        abort_s = 0;
+        *abort_v = 0;
         fence_mbar_init();
     }
     if (warp == 8) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(&tmem_base_s)),
+                         smem_u32(tmem_base_s)),
                      "r"(kTmemCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -303,8 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = tmem_base_s;
-    volatile int* abort_v = &abort_s;
+    const uint32_t tmem = *tmem_base_s;
 
     // a bounded wait by lane 0, its outcome broadcast to the warp (a time-out also
     // raises the abort flag, which the other roles see at their next failed wait)
@@ -328,22 +346,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 8 || warp == 9) {
         // ---------------------------------------------------------- TMA producers
-        // warp 8 feeds the K ring, warp 9 the V ring; a K slot frees when its Q K^T
-        // completes, a V slot when its P V completes
+        // warp 8 feeds the K slots (one 256-token tile each), warp 9 the V half-slots
+        // (128 tokens each); a K slot frees when its Q K^T completes, a V half-slot
+        // when the P V MMAs reading it complete
         const bool is_k = warp == 8;
         if (lane == 0) prefetch_tensormap(is_k ? &tk : &tv);
         const CUtensorMap* map = is_k ? &tk : &tv;
         const uint32_t ring = is_k ? sK : sV;
+        const int slot_bytes = is_k ? SM::K_TILE : SM::V_HALF;
+        const int rows = is_k ? kKvTile : kVHalf;           // rows of one 64-d chunk region
+        const int per = is_k ? PAGES : HPAGES;              // pages per item
         const uint32_t full = is_k ? bar_k_full : bar_v_full;
         const uint32_t empty = is_k ? bar_k_empty : bar_v_empty;
+        const int items = is_k ? n_tiles : n_halves;
         const int64_t row_end = (int64_t)a.NB * a.Hkv * BS;   // first row past the pool
-        for (int j = 0; j < n_tiles; ++j) {
-            const int st = j % NS;
-            if (j >= NS && !warp_wait(empty + 8 * st, ((j / NS) - 1) & 1)) break;
+        for (int j = 0; j < items; ++j) {
+            const int st = j & 1;
+            if (j >= 2 && !warp_wait(empty + 8 * st, ((j >> 1) - 1) & 1)) break;
             if (*abort_v) break;
-            const int lb0 = j * PAGES;
+            const int lb0 = j * per;                        // first logical page of the item
             int npages = (kv_end - lb0 * BS + BS - 1) / BS;
-            if (npages > PAGES) npages = PAGES;
+            if (npages > per) npages = per;
             if (lane == 0)
                 mbar_arrive_expect_tx(full + 8 * st, (uint32_t)(npages * KB * BS * 128));
             __syncwarp();
@@ -359,20 +382,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t off = (uint32_t)(lane * BS * 128);
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb)
-                    tma_load_2d(ring + st * SM::TILE + kb * kRows * 128 + off, map, kb * 64,
+                    tma_load_2d(ring + st * slot_bytes + kb * rows * 128 + off, map, kb * 64,
                                 (int)row, full + 8 * st);
             }
         }
-        // V of the last tile: once it has landed, zero its rows at or past kv_end (the
+        // the last V half: once it has landed, zero its rows at or past kv_end (the
         // partial page, pages past the request), so P = 0 never meets stale or NaN bytes
-        const int tail = n_tiles - 1;
-        const int valid = kv_end - tail * kKvTile;
-        if (!is_k && n_tiles > 0 && valid < kKvTile && !*abort_v) {
-            if (warp_wait(bar_v_full + 8 * (tail % NS), (tail / NS) & 1)) {
-                uint8_t* vst = sm + SM::V_OFF + (tail % NS) * SM::TILE;
+        const int tail = n_halves - 1;
+        if (!is_k && n_halves > 0 && tail_valid < kVHalf && !*abort_v) {
+            if (warp_wait(bar_v_full + 8 * (tail & 1), (tail >> 1) & 1)) {
+                uint8_t* vst = sm + SM::V_OFF + (tail & 1) * SM::V_HALF;
                 for (int kb = 0; kb < KB; ++kb)
-                    for (int rr = valid + (lane >> 3); rr < kKvTile; rr += 4)
-                        *reinterpret_cast<uint4*>(vst + kb * kRows * 128 + rr * 128 +
+                    for (int rr = tail_valid + (lane >> 3); rr < kVHalf; rr += 4)
+                        *reinterpret_cast<uint4*>(vst + kb * kVHalf * 128 + rr * 128 +
                                                   (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -383,38 +405,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ---------------------------------------------------------- MMA issuer (lane 0)
         if (lane == 0) {
             auto issue_pv = [&](int t) -> bool {
-                const int vs = t % NS;
-                if (!thread_wait(bar_v_full + 8 * vs, (t / NS) & 1)) return false;
-                if (t == n_tiles - 1 && kv_end - t * kKvTile < kKvTile &&
-                    !thread_wait(bar_v_tail, 0))
-                    return false;
                 if (!thread_wait(bar_p_ready, t & 1)) return false;
-                tc_fence_after();
-                const uint32_t vbase = sV + vs * SM::TILE;
+                for (int hv = 0; hv < 2; ++hv) {
+                    const int t2 = 2 * t + hv;
+                    if (t2 >= n_halves) break;
+                    const int vs = t2 & 1;
+                    if (!thread_wait(bar_v_full + 8 * vs, (t2 >> 1) & 1)) return false;
+                    if (t2 == n_halves - 1 && tail_valid < kVHalf && !thread_wait(bar_v_tail, 0))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t vbase = sV + vs * SM::V_HALF;
 #pragma unroll
-                for (int k = 0; k < kKvTile / 16; ++k) {
-                    const uint64_t b = smem_desc_sw128(vbase + k * 2048, kRows * 128, 1024);
-                    mma_ts(tmem + kColO, tmem + kColP + k * 8, b, ID_O, (t > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < kVHalf / 16; ++k) {
+                        const uint64_t b = smem_desc_sw128(vbase + k * 2048, kVHalf * 128, 1024);
+                        mma_ts(tmem + kColO, tmem + kColP + (hv * (kVHalf / 16) + k) * 8, b, ID_O,
+                               (t > 0 || hv > 0 || k > 0) ? 1u : 0u);
+                    }
+                    mma_commit(bar_v_empty + 8 * vs);
                 }
                 mma_commit(bar_pv);
-                mma_commit(bar_v_empty + 8 * vs);
                 return true;
             };
             bool ok = thread_wait(bar_q, 0);
             tc_fence_after();
             for (int j = 0; ok && j < n_tiles; ++j) {
-                const int sb = j & 1, ks = j % NS;
-                if (!thread_wait(bar_k_full + 8 * ks, (j / NS) & 1)) { ok = false; break; }
-                if (j >= 2 && !thread_wait(bar_s_free + 8 * sb, ((j - 2) >> 1) & 1)) { ok = false; break; }
+                const int ks = j & 1;
+                if (!thread_wait(bar_k_full + 8 * ks, (j >> 1) & 1)) { ok = false; break; }
+                if (j >= 1 && !thread_wait(bar_s_free, (j - 1) & 1)) { ok = false; break; }
                 tc_fence_after();
-                const uint32_t kbase = sK + ks * SM::TILE;
+                const uint32_t kbase = sK + ks * SM::K_TILE;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (uint32_t)((k >> 2) * kRows * 128 + (k & 3) * 32);
-                    mma_ts(tmem + sb * 128, tmem + kColQ + k * 8,
-                           smem_desc_sw128(kbase + off, 16, 1024), ID_S, k > 0 ? 1u : 0u);
+                    const uint32_t col = (uint32_t)((k & 3) * 32);
+                    mma_ss(tmem + kColS,
+                           smem_desc_sw128(sQ + (k >> 2) * kRows * 128 + col, 16, 1024),
+                           smem_desc_sw128(kbase + (k >> 2) * kKvTile * 128 + col, 16, 1024), ID_S,
+                           k > 0 ? 1u : 0u);
                 }
-                mma_commit(bar_s_full + 8 * sb);
+                mma_commit(bar_s_full);
                 mma_commit(bar_k_empty + 8 * ks);
                 // the previous tile's P V runs after this tile's scores are queued
                 if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
@@ -434,27 +462,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (vis < 0) vis = 0;
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         const int nbar = 1 + (warp & 3);         // named barrier of this warp pair
-        // Q row (this half's D/2 values) into tensor memory
+        // this half's D/2 values of the Q row into shared memory, in the 128-byte
+        // swizzled K-major layout the MMA reads (16-byte unit c of row m at c ^ (m & 7))
         {
-            uint32_t w[DH / 2];
-            if (row_valid) {
-                const uint4* src = reinterpret_cast<const uint4*>(
-                    a.q + ((int64_t)(q0 + qi) * a.Hq + (int64_t)h * G + g) * D + hf * DH);
+            const uint4* src = reinterpret_cast<const uint4*>(
+                a.q + ((int64_t)(q0 + qi) * a.Hq + (int64_t)h * G + g) * D + hf * DH);
 #pragma unroll
-                for (int i = 0; i < DH / 8; ++i) {
-                    const uint4 v4 = src[i];
-                    w[4 * i] = v4.x;
-                    w[4 * i + 1] = v4.y;
-                    w[4 * i + 2] = v4.z;
-                    w[4 * i + 3] = v4.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < DH / 2; ++i) w[i] = 0u;
+            for (int i = 0; i < DH / 8; ++i) {
+                const int cu = hf * (DH / 8) + i;        // 16-byte unit of the D-value row
+                const uint4 v4 = row_valid ? src[i] : make_uint4(0u, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(sm + SM::Q_OFF + (cu >> 3) * kRows * 128 + m * 128 +
+                                          (((cu & 7) ^ (m & 7)) << 4)) = v4;
             }
-            tmem_st_words<DH / 2>(lane_base + kColQ + hf * (DH / 2), w);
-            tmem_st_wait();
-            tc_fence_before();
+            fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar_q);
         }
@@ -464,14 +484,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // loop: the partner warp must meet every named barrier below.
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            const int sb = j & 1;
-            if (ok && !warp_wait(bar_s_full + 8 * sb, (j >> 1) & 1)) ok = false;
+            if (ok && !warp_wait(bar_s_full, j & 1)) ok = false;
             tc_fence_after();
             float s[HALF];
-            tmem_ld64(lane_base + sb * 128 + hf * HALF, s);
+            tmem_ld64(lane_base + kColS + hf * HALF, *reinterpret_cast<float(*)[64]>(s));
+            tmem_ld64(lane_base + kColS + hf * HALF + 64, *reinterpret_cast<float(*)[64]>(s + 64));
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_s_free + 8 * sb);
+            if (lane == 0) mbar_arrive(bar_s_free);
             // mask (diagonal and tail tiles only), partial max on raw scores (scale > 0)
             const int lim = vis - j * kKvTile - hf * HALF;   // columns >= lim are masked
             if (lim < HALF) {
@@ -485,9 +505,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = 8; c < HALF; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
             const float pmx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-            xch[sb][hf][m] = pmx;
+            float* xj = xch + (j & 1) * 2 * kRows;
+            xj[hf * kRows + m] = pmx;
             named_barrier_sync(nbar, 64);
-            const float mx = fmaxf(pmx, xch[sb][hf ^ 1][m]) * a.scale_log2;
+            const float mx = fmaxf(pmx, xj[(hf ^ 1) * kRows + m]) * a.scale_log2;
             // raise the reference max only when a score passes it by more than 2^8
             // (both halves take the same decision from the same numbers)
             float alpha = 1.f;
@@ -527,7 +548,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32f(lane_base + kColO + hf * DH + c * 32, o);
                 }
             }
-            tmem_st32(lane_base + kColP + hf * (HALF / 2), p);
+            tmem_st32(lane_base + kColP + hf * (HALF / 2), *reinterpret_cast<uint32_t(*)[32]>(p));
+            tmem_st32(lane_base + kColP + hf * (HALF / 2) + 32,
+                      *reinterpret_cast<uint32_t(*)[32]>(p + 32));
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -538,9 +561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = warp_wait(bar_pv, (n_tiles - 1) & 1);
             tc_fence_after();
         }
-        xl[hf][m] = l;                           // the halves' partial sums
+        // the halves' partial sums, through the exchange parity no pending read uses
+        float* xl = xch + (n_tiles & 1) * 2 * kRows;
+        xl[hf * kRows + m] = l;
         named_barrier_sync(nbar, 64);
-        const float lt = l + xl[hf ^ 1][m];
+        const float lt = l + xl[(hf ^ 1) * kRows + m];
         const float inv = (lt > 0.f && ok) ? 1.f / lt : 0.f;
         uint16_t* orow = a.out + ((int64_t)(q0 + qi) * a.Hq + (int64_t)h * G + g) * D + hf * DH;
 #pragma unroll 1
@@ -599,7 +624,7 @@ cudaError_t prefill_launch_t(const PrefillLaunch& L, const PrefillArgs& a, const
     auto kern = pkv_prefill_kernel<D, BS, G>;
     // one CTA per SM (it holds all 512 TMEM columns); ask for enough shared memory
     // that no second CTA can be co-resident
-    int smem = PrefillSmem<D>::ALLOC;
+    int smem = PrefillSmem<D>::BYTES;
     if (smem < 120 * 1024) smem = 120 * 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

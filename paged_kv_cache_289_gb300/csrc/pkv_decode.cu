@@ -805,7 +805,7 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 #pragma unroll
                     for (int e = 0; e < 4; ++e) ot[dt][qi][e] = 0.f;
             if constexpr (C::I4) {
-                // the K-path matrices, transposed per 8x8 b16 block: a lane then holds
+                // the K-path matrices, transposed per 8x8 b16 block by the load: a lane holds
                 // tokens 2c, 2c+1 of b16 unit g (d = 64 dblk + 4g + 0..3), and nibble pair
                 // (j, j + 4) is one d for both tokens.  mma (dblk, i): V^T row g <-> d =
                 // 64 dblk + 4g + i, row g + 8 <-> d = 64 dblk + 32 + 4g + i.
@@ -814,12 +814,10 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                     const int tr = mt * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
                     for (int dblk = 0; dblk < D / 64; ++dblk) {
-                        uint32_t r0, r1, r2, r3;
-                        ldsm_x4(vpg + swz64(tr, dblk * 2 + (lane >> 4)), r0, r1, r2, r3);
-                        const uint32_t m0 = movmatrix_trans(r0);   // tokens 0-7,  d + 0
-                        const uint32_t m1 = movmatrix_trans(r1);   // tokens 8-15, d + 0
-                        const uint32_t m2 = movmatrix_trans(r2);   // tokens 0-7,  d + 32
-                        const uint32_t m3 = movmatrix_trans(r3);   // tokens 8-15, d + 32
+                        // m0: tokens 0-7, d + 0; m1: tokens 8-15, d + 0; m2: tokens 0-7,
+                        // d + 32; m3: tokens 8-15, d + 32
+                        uint32_t m0, m1, m2, m3;
+                        ldsm_x4_trans(vpg + swz64(tr, dblk * 2 + (lane >> 4)), m0, m1, m2, m3);
 #pragma unroll
                         for (int qi = 0; qi < QT; ++qi) {
                             mma_f16(ot[dblk * 4][qi], i4pick_to_f16x2<0>(m0), i4pick_to_f16x2<0>(m2),
@@ -843,12 +841,13 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt) {
                     const int t = mt * 16 + (lane & 15);
+                    // the four 8x8 b16 blocks, each transposed by the load
                     uint32_t r0, r1, r2, r3;
-                    ldsm_x4(vpg + swz<C::TT>(t, 2 * dp + (lane >> 4)), r0, r1, r2, r3);
+                    ldsm_x4_trans(vpg + swz<C::TT>(t, 2 * dp + (lane >> 4)), r0, r1, r2, r3);
 #pragma unroll
                     for (int half = 0; half < 2; ++half) {
-                        const uint32_t x = movmatrix_trans(half ? r2 : r0);   // tokens 0-7
-                        const uint32_t y = movmatrix_trans(half ? r3 : r1);   // tokens 8-15
+                        const uint32_t x = half ? r2 : r0;   // tokens 0-7
+                        const uint32_t y = half ? r3 : r1;   // tokens 8-15
                         uint32_t v0, v1, v2, v3;
                         if constexpr (KT == 2) {
                             // int8: the token regroup and the widening are one permute

@@ -176,6 +176,16 @@ __device__ __forceinline__ void tmem_st_words(uint32_t taddr, const uint32_t (&w
     }
 }
 
+// 3-D tiled bulk tensor copy global -> shared, completion on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -379,11 +389,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     row = ((int64_t)blk * a.Hkv + h) * BS;
                 }
-                const uint32_t off = (uint32_t)(lane * BS * 128);
+                if (is_k) {
+                    // K: [chunk][256 rows][128 B], one box per page and chunk
+                    const uint32_t off = (uint32_t)(lane * BS * 128);
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb)
-                    tma_load_2d(ring + st * slot_bytes + kb * rows * 128 + off, map, kb * 64,
-                                (int)row, full + 8 * st);
+                    for (int kb = 0; kb < KB; ++kb)
+                        tma_load_2d(ring + st * slot_bytes + kb * rows * 128 + off, map, kb * 64,
+                                    (int)row, full + 8 * st);
+                } else {
+                    // V: [page][chunk][BS rows][128 B], one box per page (all of D)
+                    tma_load_3d(ring + st * slot_bytes + (uint32_t)(lane * KB * BS * 128), map, 0,
+                                (int)row, 0, full + 8 * st);
+                }
             }
         }
         // the last V half: once it has landed, zero its rows at or past kv_end (the
@@ -394,8 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* vst = sm + SM::V_OFF + (tail & 1) * SM::V_HALF;
                 for (int kb = 0; kb < KB; ++kb)
                     for (int rr = tail_valid + (lane >> 3); rr < kVHalf; rr += 4)
-                        *reinterpret_cast<uint4*>(vst + kb * kVHalf * 128 + rr * 128 +
-                                                  (lane & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        *reinterpret_cast<uint4*>(vst + ((rr / BS) * KB + kb) * BS * 128 +
+                                                  (rr % BS) * 128 + (lane & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_v_tail);
@@ -417,7 +435,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t vbase = sV + vs * SM::V_HALF;
 #pragma unroll
                     for (int k = 0; k < kVHalf / 16; ++k) {
-                        const uint64_t b = smem_desc_sw128(vbase + k * 2048, kVHalf * 128, 1024);
+                        // 16 tokens inside one page: rows at 128 B, chunks BS * 128 B apart
+                        const uint32_t koff = (uint32_t)(((k * 16) / BS) * KB * BS * 128 +
+                                                         ((k * 16) % BS) * 128);
+                        const uint64_t b = smem_desc_sw128(vbase + koff, BS * 128, 1024);
                         mma_ts(tmem + kColO, tmem + kColP + (hv * (kVHalf / 16) + k) * 8, b, ID_O,
                                (t > 0 || hv > 0 || k > 0) ? 1u : 0u);
                     }
@@ -661,14 +682,24 @@ int prefill_launch(const PrefillLaunch& L, cudaStream_t st) {
     const int TQ = kRows / G;
     alignas(64) CUtensorMap tk, tv;
     const int64_t rows = (int64_t)L.NB * L.Hkv * L.BS;
-    for (int i = 0; i < 2; ++i) {
+    {   // K: 2-D, one box = one page's rows of one 64-d chunk
         cuuint64_t dims[2] = {(cuuint64_t)L.D, (cuuint64_t)rows};
         cuuint64_t strides[1] = {(cuuint64_t)L.D * 2};
         cuuint32_t box[2] = {64, (cuuint32_t)L.BS};
         cuuint32_t es[2] = {1, 1};
-        if (fn(i ? &tv : &tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-               const_cast<void*>(i ? L.v_cache : L.k_cache), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+        if (fn(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(L.k_cache), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return PKV_ERR_CUDA;
+    }
+    {   // V: 3-D (64 d, row, 64-d chunk), one box = one page's rows of all of D, laid
+        // out chunk by chunk
+        cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(L.D / 64)};
+        cuuint64_t strides[2] = {(cuuint64_t)L.D * 2, 128};
+        cuuint32_t box[3] = {64, (cuuint32_t)L.BS, (cuuint32_t)(L.D / 64)};
+        cuuint32_t es[3] = {1, 1, 1};
+        if (fn(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(L.v_cache), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return PKV_ERR_CUDA;
     }

@@ -181,12 +181,11 @@ PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_
  * Requirements: q, out, caches, workspace 16-byte aligned; workspace_bytes >=
  *   pkv_decode_workspace_size(...) for the same shape and device.
  * The work is one flat list of (request, kv head, page) items split evenly over
- * a persistent grid of warps.  A (request, kv head) unit split over at most six
- * warps is merged, with log-sum-exp weights, by the last of them to finish; wider
- * splits are merged by a small second kernel launched right behind the first
- * (programmatic dependent launch).  No host synchronisation.  The workspace's
- * arrival counters carry a per-call tag, so the workspace needs no clearing
- * between calls; calls that share a workspace must not overlap on the GPU.
+ * a persistent grid of warps.  The partial results of a (request, kv head) unit
+ * split over several warps are merged, with log-sum-exp weights, by a small second
+ * kernel launched right behind the first (programmatic dependent launch).  No host
+ * synchronisation.  The workspace needs no clearing between calls; calls that
+ * share a workspace must not overlap on the GPU.
  */
 PKV_API int pkv_paged_decode_attn(const void *q, const void *k_cache, const void *v_cache,
                           const float *k_scale, const float *v_scale,

@@ -36,7 +36,6 @@ __host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + 
 
 // Byte offsets inside the decode workspace.
 struct WorkspaceLayout {
-    int64_t counter_off;   // u64 [N * Hkv] arrival counters of split units (epoch << 32 | count)
     int64_t prefix_off;    // int32 [N + 1] page prefix over requests (times Hkv)
     int64_t partial_off;   // fp32 [slots][QT][kGroupPad][D + 4]: o[D], m, l, pad
     int64_t slots;         // N * Hkv + W
@@ -47,8 +46,7 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int batch, int num_k
                                                             int head_dim, int total_warps,
                                                             int qt) {
     WorkspaceLayout L;
-    L.counter_off = kWorkspaceHeader;
-    L.prefix_off = align_up(L.counter_off + 8 * (int64_t)batch * num_kv_heads, 256);
+    L.prefix_off = kWorkspaceHeader;
     L.partial_off = align_up(L.prefix_off + 4 * (int64_t)(batch + 1), 256);
     L.slots = (int64_t)batch * num_kv_heads + total_warps;
     L.total = L.partial_off + L.slots * qt * kGroupPad * (head_dim + 4) * 4;

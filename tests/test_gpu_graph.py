@@ -2,8 +2,8 @@
 算子优化要点: CUDA Graph wants static shapes and addresses).  Every entry point takes
 caller-owned buffers and never synchronises, so slot mapping, cache write, decode (with its
 split-unit merges) and the prefix hash record into one graph.  Each replay, fed new values in
-the same buffers, must equal the eager calls bit for bit.  Split units reuse the arrival
-counters across replays with the same call tag, and must still merge correctly."""
+the same buffers, must equal the eager calls bit for bit, split units (merged by the
+second kernel from the workspace's partial slots) included."""
 import numpy as np
 import pytest
 

@@ -318,8 +318,8 @@ def test_prefix_hash_long_sequence_and_odd_block_sizes():
 
 def test_decode_workspace_reuse_and_garbage_contents():
     """One workspace shared by successive calls of different shapes, starting from
-    garbage bytes: the split-unit counters carry a per-call tag and partial slots are
-    written before they are read, so nothing in the workspace needs clearing."""
+    garbage bytes: the page prefix and the partial slots are written before they are
+    read, so nothing in the workspace needs clearing."""
     torch = torch_mod()
     cases = [W.custom(3, 16, 2, 128, 16, [40, 5000, 700], seed=41),     # pages > warps
              W.custom(5, 16, 2, 128, 16, [3, 17, 1, 33, 64], seed=42),  # pages < warps

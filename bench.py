@@ -458,16 +458,19 @@ def run_ours(args):
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(main)
         up.wait_stream(main)                     # no upload starts before the timed region
+        h0 = time.perf_counter()
         for k in range(K):
             e2e_step(k)
         main.wait_stream(down)
         f1.record(main)
+        h1 = time.perf_counter()                 # host time to issue the K steps
         torch.cuda.synchronize(dev)
         te = aggregate_max(f0.elapsed_time(f1) / 1e3, world, dev)
         e2e = {"value": round(total_bytes / te / 1e9, 2), "unit": UNIT,
                "h2d_bytes_per_step": int(sum(n for _, n in in_offs.values())),
                "d2h_bytes_per_step": int(sum(n for _, n in out_offs.values())),
                "ms_per_step": round(te / K * 1e3, 4),
+               "host_issue_ms_per_step": round((h1 - h0) / K * 1e3, 4),
                "copies": "one packed H2D and one D2H per step on their own streams, "
                          "double-buffered (upload of step k+1 overlaps step k)"}
 

@@ -49,6 +49,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <type_traits>
 
 #include "pkv_internal.cuh"
 
@@ -879,77 +880,104 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 // Log-sum-exp merge of the units split over several warps:
 //   M = max_w m_w,  out = sum_w 2^(m_w - M) o_w / sum_w 2^(m_w - M) l_w
 // ("GPU推理深度拆解：KV Cache视角", 系统层：Context Parallel: the online-softmax merge
-// that ring attention also uses).  One CTA per unit, one warp per query head of the
-// group, each lane D/32 columns, for each of the request's query positions.  The loop over partials keeps several
-// independent loads in flight.  Runs after the decode kernel (programmatic
-// dependent launch: it waits for the decode grid to complete before reading).
+// that ring attention also uses).  One CTA per unit and one warp per (query head of the
+// group, query position); each lane owns D/32 columns.  Lane k holds partial k's (m, l),
+// so the weights reach the column loop by shuffle instead of another round of loads, and
+// the loop keeps several partials' loads in flight.  Runs after the decode kernel
+// (programmatic dependent launch: it waits for the decode grid to complete).
 template <int D, int QT>
-__global__ void __launch_bounds__(kGroupPad * 32)
+__global__ void __launch_bounds__(kGroupPad * 32 * QT)
     pkv_decode_merge_kernel(const DecodeArgs a) {
     constexpr int PER = D / 32;
     constexpr int QS = kGroupPad * (D + 4);
     constexpr int SLOT = QT * QS;
     pdl_wait();
     const int u = blockIdx.x;
-    const int gg = threadIdx.x >> 5;
+    const int wi = threadIdx.x >> 5;
+    const int gg = wi % kGroupPad, qi = wi / kGroupPad;
     const int lane = threadIdx.x & 31;
     if (gg >= a.G) return;
     const int r = u / a.Hkv;
     const int h = u - r * a.Hkv;
     const int P = a.g_prefix[a.N];
+    const int p0 = a.g_prefix[r], p1 = a.g_prefix[r + 1];
+    int qb, qlen;
+    uint32_t errbits = 0;
+    query_rows<QT>(a, r, qb, qlen, errbits);
     const int W = min(a.total_warps, P);
-    const int np = (a.g_prefix[r + 1] - a.g_prefix[r]) / a.Hkv;
-    if (np == 0) return;
-    const int64_t U = (int64_t)a.g_prefix[r] + (int64_t)h * np;
+    const int np = (p1 - p0) / a.Hkv;
+    if (np == 0 || qi >= qlen) return;
+    const int64_t U = (int64_t)p0 + (int64_t)h * np;
     const int64_t E = U + np - 1;
     const int wf = (int)(((U + 1) * W - 1) / P);
     const int wl = (int)(((E + 1) * W - 1) / P);
     const int n = wl - wf + 1;
     if (n == 1) return;   // a whole unit: the decode kernel wrote its output
-    int qb, qlen;
-    uint32_t errbits = 0;
-    query_rows<QT>(a, r, qb, qlen, errbits);
-    for (int qi = 0; qi < qlen; ++qi) {
-        const float* base = a.partials + ((int64_t)u + wf) * SLOT + qi * QS + gg * (D + 4);
-        float M = -INFINITY;
-        for (int k = lane; k < n; k += 32) M = fmaxf(M, base[(int64_t)k * SLOT + D]);
+    static_assert(PER == 2 || PER == 4, "head_dim 64 or 128");
+    using Row = typename std::conditional<PER == 4, float4, float2>::type;
+    const float* base = a.partials + ((int64_t)u + wf) * SLOT + qi * QS + gg * (D + 4);
+    // the first eight partials' rows go out with the (m, l) loads: their addresses do not
+    // depend on the maximum
+    Row v[8];
 #pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-        float acc[PER];
+    for (int j = 0; j < 8; ++j) {
+        if (j < n) v[j] = *reinterpret_cast<const Row*>(base + (int64_t)j * SLOT + lane * PER);
+        else v[j] = Row{};
+    }
+    // (m, l) of partial `lane` (and of lane + 32, ... for wider units)
+    const float2 ml0 = lane < n ? *reinterpret_cast<const float2*>(base + (int64_t)lane * SLOT + D)
+                                : make_float2(-INFINITY, 0.f);
+    float M = ml0.x;
+    for (int k = lane + 32; k < n; k += 32)
+        M = fmaxf(M, base[(int64_t)k * SLOT + D]);
 #pragma unroll
-        for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-        float L = 0.f;
-        if (M != -INFINITY) {   // else: the query saw no token: zero row
-            for (int k = lane; k < n; k += 32) {
-                const float2 ml = *reinterpret_cast<const float2*>(base + (int64_t)k * SLOT + D);
-                L = fmaf(exp2f(ml.x - M), ml.y, L);
-            }
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float acc[PER];
 #pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
-#pragma unroll 8
-            for (int k = 0; k < n; ++k) {
-                const float* ps = base + (int64_t)k * SLOT;
-                const float wt = exp2f(ps[D] - M);
-                if constexpr (PER == 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(ps + lane * 4);
-                    acc[0] = fmaf(wt, v.x, acc[0]);
-                    acc[1] = fmaf(wt, v.y, acc[1]);
-                    acc[2] = fmaf(wt, v.z, acc[2]);
-                    acc[3] = fmaf(wt, v.w, acc[3]);
-                } else {
-                    const float2 v = *reinterpret_cast<const float2*>(ps + lane * 2);
-                    acc[0] = fmaf(wt, v.x, acc[0]);
-                    acc[1] = fmaf(wt, v.y, acc[1]);
+    for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+    float L = 0.f;
+    if (M != -INFINITY) {   // else: the query saw no token: zero row
+        const float w0 = lane < n ? exp2f(ml0.x - M) : 0.f;   // weight of partial `lane`
+        L = w0 * ml0.y;
+        for (int k = lane + 32; k < n; k += 32) {
+            const float2 ml = *reinterpret_cast<const float2*>(base + (int64_t)k * SLOT + D);
+            L = fmaf(exp2f(ml.x - M), ml.y, L);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+        // 32 partials at a time: lane j holds the weight of partial c0 + j.  Rows are loaded
+        // eight at a time before any of them is used; a row past the end loads as zero and
+        // its lane's weight is zero, so the sum over k keeps its order and value.
+        for (int c0 = 0; c0 < n; c0 += 32) {
+            const float wc = c0 == 0 ? w0
+                             : (c0 + lane < n ? exp2f(base[(int64_t)(c0 + lane) * SLOT + D] - M)
+                                              : 0.f);
+            const int nc = min(n - c0, 32);
+            for (int k = 0; k < nc; k += 8) {
+                if (c0 != 0 || k != 0) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float* ps = base + (int64_t)(c0 + k + j) * SLOT + lane * PER;
+                        if (k + j < nc) v[j] = *reinterpret_cast<const Row*>(ps);
+                        else v[j] = Row{};
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const float wt = __shfl_sync(0xffffffffu, wc, k + j);
+                    const float* f = reinterpret_cast<const float*>(&v[j]);
+#pragma unroll
+                    for (int c = 0; c < PER; ++c) acc[c] = fmaf(wt, f[c], acc[c]);
                 }
             }
         }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        uint16_t* ob = a.out + ((int64_t)(qb + qi) * a.Hq + (int64_t)h * a.G + gg) * D;
-#pragma unroll
-        for (int k = 0; k < PER; k += 2)
-            *reinterpret_cast<uint32_t*>(ob + lane * PER + k) =
-                pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
     }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint16_t* ob = a.out + ((int64_t)(qb + qi) * a.Hq + (int64_t)h * a.G + gg) * D;
+#pragma unroll
+    for (int c = 0; c < PER; c += 2)
+        *reinterpret_cast<uint32_t*>(ob + lane * PER + c) =
+            pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
 }
 
 // ------------------------------------------------------------------ host side
@@ -1037,7 +1065,7 @@ static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const
     if (e != cudaSuccess) return e;
     // the wide-split merge, a programmatic dependent of the decode grid
     return launch_pdl(pkv_decode_merge_kernel<D, QT>, dim3((unsigned)(L.N * L.Hkv)),
-                      dim3(kGroupPad * 32), 0, st, args);
+                      dim3(kGroupPad * 32 * QT), 0, st, args);
 }
 
 template <int D, int BS, int KT>

@@ -324,13 +324,18 @@ def run_ours(args):
     launches_per_step = 5   # slot map, write, decode, wide-split merge, hash
 
     def step(I, O, dec_ev=None):
-        """One decode step on the per-step inputs I, writing the results O."""
+        """One decode step on the per-step inputs I, writing the results O.
+
+        The prefix hash reads only the step's tokens, so it starts first, on the side
+        stream, and runs beside the main-stream chain (slot mapping -> write -> decode ->
+        merge).  Started after the KV write instead, it lands on SMs that the decode grid
+        already fills and stretches the decode's tail (measured: +17 us per step)."""
+        side.wait_stream(main)                   # the step's inputs are in place
+        pkv.prefix_block_hash(I["tokens"], I["toffs"], wl.hash_block, I["hoffs"], nh, seed=0,
+                              out=O["hashes"], stream=side)
         pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, req_idx=I["req"], out=slots,
                                  stream=main)
         pkv.kv_cache_write(I["k_new"], I["v_new"], slots, kc, vc, ks, vs, stream=main)
-        side.wait_stream(main)
-        pkv.prefix_block_hash(I["tokens"], I["toffs"], wl.hash_block, I["hoffs"], nh, seed=0,
-                              out=O["hashes"], stream=side)
         if dec_ev is not None:
             dec_ev[0].record(main)
         if wl.q_len == 1:

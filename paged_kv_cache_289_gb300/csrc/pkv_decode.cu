@@ -318,6 +318,10 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
     float ot[FP8 ? C::DT : 1][QT][4];
     uint32_t qf[QSMEM ? 1 : C::KS][QT][2];
     float m0[QT], m1[QT], l0[QT], l1[QT];   // heads 2c, 2c+1 of this lane, per query
+    // int4 pages: the nibbles enter the mma offset (1024 + n or 1024 + 16 n, n = code + 8);
+    // cq = the scores' constant part per head (q . offsets), cr = sum over pages of
+    // v_scale * sum(P), which times 1032 or 72 is the output's constant part
+    float cq0[QT], cq1[QT], cr0[QT], cr1[QT];
     float qscale = a.scale_log2;
     bool seg_full = false;
     int seg_r = 0, seg_h = 0;
@@ -357,6 +361,7 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
             for (int qi = 0; qi < QT; ++qi) {
                 m0[qi] = m1[qi] = -INFINITY;
                 l0[qi] = l1[qi] = 0.f;
+                cr0[qi] = cr1[qi] = 0.f;
 #pragma unroll
                 for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
@@ -423,9 +428,24 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         for (int i = 0; i < 4; ++i) {
                             const uint4& A = raw4[2 * dblk][qi];
                             const uint4& B = raw4[2 * dblk + 1][qi];
-                            qf[dblk * 4 + i][qi][0] = pack_f16x2(qv(A, i) * sc, qv(A, i + 4) * sc);
-                            qf[dblk * 4 + i][qi][1] = pack_f16x2(qv(B, i) * sc, qv(B, i + 4) * sc);
+                            // odd picks hold 16 n: their q carries the 1/16 (exact)
+                            const float si = (i & 1) ? sc * 0.0625f : sc;
+                            qf[dblk * 4 + i][qi][0] = pack_f16x2(qv(A, i) * si, qv(A, i + 4) * si);
+                            qf[dblk * 4 + i][qi][1] = pack_f16x2(qv(B, i) * si, qv(B, i + 4) * si);
                         }
+                // the scores' constant part: the same mma over a tile of code-0 nibbles
+                // (1032 for even picks, 1152 for odd), one value per head
+#pragma unroll
+                for (int qi = 0; qi < QT; ++qi) {
+                    float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t k0 = (kk & 1) ? 0x64806480u : 0x64086408u;
+                        mma_f16(cacc, k0, k0, k0, k0, qf[kk][qi][0], qf[kk][qi][1]);
+                    }
+                    cq0[qi] = cacc[0];
+                    cq1[qi] = cacc[1];
+                }
                 qscale = a.scale_log2 * inv_sc;
             } else {
                 // k-slot mapping for E4M3 A fragments: slots 2c,2c+1 <-> d = 4c,4c+1 and
@@ -552,19 +572,19 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                     ldsm_x4(kpg + swz64(tr, dblk * 2 + (lane >> 4)), r0, r1, r2, r3);
 #pragma unroll
                     for (int qi = 0; qi < QT; ++qi) {
-                        mma_f16(e0[qi], i4pick_to_f16x2<0>(r0), i4pick_to_f16x2<0>(r1),
-                                i4pick_to_f16x2<0>(r2), i4pick_to_f16x2<0>(r3),
+                        mma_f16(e0[qi], i4pick_raw<0>(r0), i4pick_raw<0>(r1),
+                                i4pick_raw<0>(r2), i4pick_raw<0>(r3),
                                 qf[dblk * 4][qi][0], qf[dblk * 4][qi][1]);
-                        mma_f16(QT == 1 ? e1[qi] : e0[qi], i4pick_to_f16x2<1>(r0),
-                                i4pick_to_f16x2<1>(r1), i4pick_to_f16x2<1>(r2),
-                                i4pick_to_f16x2<1>(r3), qf[dblk * 4 + 1][qi][0],
+                        mma_f16(QT == 1 ? e1[qi] : e0[qi], i4pick_raw<1>(r0),
+                                i4pick_raw<1>(r1), i4pick_raw<1>(r2),
+                                i4pick_raw<1>(r3), qf[dblk * 4 + 1][qi][0],
                                 qf[dblk * 4 + 1][qi][1]);
-                        mma_f16(e0[qi], i4pick_to_f16x2<2>(r0), i4pick_to_f16x2<2>(r1),
-                                i4pick_to_f16x2<2>(r2), i4pick_to_f16x2<2>(r3),
+                        mma_f16(e0[qi], i4pick_raw<2>(r0), i4pick_raw<2>(r1),
+                                i4pick_raw<2>(r2), i4pick_raw<2>(r3),
                                 qf[dblk * 4 + 2][qi][0], qf[dblk * 4 + 2][qi][1]);
-                        mma_f16(QT == 1 ? e1[qi] : e0[qi], i4pick_to_f16x2<3>(r0),
-                                i4pick_to_f16x2<3>(r1), i4pick_to_f16x2<3>(r2),
-                                i4pick_to_f16x2<3>(r3), qf[dblk * 4 + 3][qi][0],
+                        mma_f16(QT == 1 ? e1[qi] : e0[qi], i4pick_raw<3>(r0),
+                                i4pick_raw<3>(r1), i4pick_raw<3>(r2),
+                                i4pick_raw<3>(r3), qf[dblk * 4 + 3][qi][0],
                                 qf[dblk * 4 + 3][qi][1]);
                     }
                 }
@@ -611,19 +631,24 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 #pragma unroll
         for (int qi = 0; qi < QT; ++qi) {
             mx0[qi] = mx1[qi] = -INFINITY;
+            // int4: score = (sum - cq) * scale, one fma
+            const float nc0 = C::I4 ? -cq0[qi] * sc_page : 0.f;
+            const float nc1 = C::I4 ? -cq1[qi] * sc_page : 0.f;
 #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
                 if (full_tile) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        sacc[mt][qi][e] *= sc_page;
+                        sacc[mt][qi][e] = C::I4 ? fmaf(sacc[mt][qi][e], sc_page, (e & 1) ? nc1 : nc0)
+                                                : sacc[mt][qi][e] * sc_page;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int tok = mt * 16 + g + ((e & 2) ? 8 : 0);
                         bool valid = tok < ntok;
                         if constexpr (QT > 1) valid = valid && (tpos0 + tok <= seg_vis + qi);
-                        const float v = sacc[mt][qi][e] * sc_page;
+                        const float v = C::I4 ? fmaf(sacc[mt][qi][e], sc_page, (e & 1) ? nc1 : nc0)
+                                              : sacc[mt][qi][e] * sc_page;
                         sacc[mt][qi][e] = valid ? v : -INFINITY;
                     }
                 }
@@ -653,6 +678,8 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                 m1[qi] = mn1;
                 l0[qi] *= al0;
                 l1[qi] *= al1;
+                cr0[qi] *= al0;
+                cr1[qi] *= al1;
 #pragma unroll
                 for (int dt = 0; dt < C::DT; ++dt) {
                     o[dt][qi][0] *= al0;
@@ -726,20 +753,32 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         ldsm_x4_trans(vpg + swz64(tr, dblk * 2 + (lane >> 4)), m0, m1, m2, m3);
 #pragma unroll
                         for (int qi = 0; qi < QT; ++qi) {
-                            mma_f16(ot[dblk * 4][qi], i4pick_to_f16x2<0>(m0), i4pick_to_f16x2<0>(m2),
-                                    i4pick_to_f16x2<0>(m1), i4pick_to_f16x2<0>(m3),
+                            mma_f16(ot[dblk * 4][qi], i4pick_raw<0>(m0), i4pick_raw<0>(m2),
+                                    i4pick_raw<0>(m1), i4pick_raw<0>(m3),
                                     pb[mt][qi][0], pb[mt][qi][1]);
-                            mma_f16(ot[dblk * 4 + 1][qi], i4pick_to_f16x2<1>(m0),
-                                    i4pick_to_f16x2<1>(m2), i4pick_to_f16x2<1>(m1),
-                                    i4pick_to_f16x2<1>(m3), pb[mt][qi][0], pb[mt][qi][1]);
-                            mma_f16(ot[dblk * 4 + 2][qi], i4pick_to_f16x2<2>(m0),
-                                    i4pick_to_f16x2<2>(m2), i4pick_to_f16x2<2>(m1),
-                                    i4pick_to_f16x2<2>(m3), pb[mt][qi][0], pb[mt][qi][1]);
-                            mma_f16(ot[dblk * 4 + 3][qi], i4pick_to_f16x2<3>(m0),
-                                    i4pick_to_f16x2<3>(m2), i4pick_to_f16x2<3>(m1),
-                                    i4pick_to_f16x2<3>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(ot[dblk * 4 + 1][qi], i4pick_raw<1>(m0),
+                                    i4pick_raw<1>(m2), i4pick_raw<1>(m1),
+                                    i4pick_raw<1>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(ot[dblk * 4 + 2][qi], i4pick_raw<2>(m0),
+                                    i4pick_raw<2>(m2), i4pick_raw<2>(m1),
+                                    i4pick_raw<2>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(ot[dblk * 4 + 3][qi], i4pick_raw<3>(m0),
+                                    i4pick_raw<3>(m2), i4pick_raw<3>(m1),
+                                    i4pick_raw<3>(m3), pb[mt][qi][0], pb[mt][qi][1]);
                         }
                     }
+                }
+                // sum(P) per head as the mma sees it (fp16 P against a tile of ones): the
+                // offset part of this page's P.V is 1032 (even picks) or 1152 (odd) times it
+#pragma unroll
+                for (int qi = 0; qi < QT; ++qi) {
+                    float psum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int mt = 0; mt < C::MT; ++mt)
+                        mma_f16(psum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u,
+                                pb[mt][qi][0], pb[mt][qi][1]);
+                    cr0[qi] = fmaf(vs, psum[0], cr0[qi]);
+                    cr1[qi] = fmaf(vs, psum[1], cr1[qi]);
                 }
             } else {
 #pragma unroll
@@ -776,12 +815,15 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                 }
             }
             }
+            // int4: odd picks accumulated 16 n, so their page scale carries the 1/16
+            const float vs16 = vs * 0.0625f;
 #pragma unroll
             for (int dt = 0; dt < C::DT; ++dt)
 #pragma unroll
                 for (int qi = 0; qi < QT; ++qi)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[dt][qi][e] = fmaf(vs, ot[dt][qi][e], o[dt][qi][e]);
+                    for (int e = 0; e < 4; ++e)
+                        o[dt][qi][e] = fmaf((C::I4 && (dt & 1)) ? vs16 : vs, ot[dt][qi][e], o[dt][qi][e]);
         }
 
         // ---- segment end ----
@@ -793,6 +835,18 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 #pragma unroll
             for (int qi = 0; qi < QT; ++qi) {
                 if (qi >= seg_qlen) break;
+                if constexpr (C::I4) {
+                    // remove the offsets' share: 1032 per unit of cr (even picks), 1152 / 16
+                    // = 72 (odd picks)
+#pragma unroll
+                    for (int dt = 0; dt < C::DT; ++dt) {
+                        const float k = (dt & 1) ? 72.f : 1032.f;
+                        o[dt][qi][0] = fmaf(-k, cr0[qi], o[dt][qi][0]);
+                        o[dt][qi][2] = fmaf(-k, cr0[qi], o[dt][qi][2]);
+                        o[dt][qi][1] = fmaf(-k, cr1[qi], o[dt][qi][1]);
+                        o[dt][qi][3] = fmaf(-k, cr1[qi], o[dt][qi][3]);
+                    }
+                }
                 float L0 = l0[qi], L1 = l1[qi];
 #pragma unroll
                 for (int o2 = 4; o2 < 32; o2 <<= 1) {

@@ -330,6 +330,16 @@ __device__ __forceinline__ uint32_t i4pick_to_f16x2(uint32_t x) {
     return r;
 }
 
+// The same nibble pick without the offset: (1024 + n) for I even, (1024 + 16 n) for I
+// odd, with n = code + 8.  A caller that folds the constant part into its sums (q prescaled
+// by 1/16 for odd I, the 1024 + 8 or 1024 + 128 term subtracted once per sum) saves the
+// half2 subtract or fma per pair.
+template <int I>
+__device__ __forceinline__ uint32_t i4pick_raw(uint32_t x) {
+    const uint32_t w = (I >= 2) ? (x >> 8) : x;
+    return ((I & 1) ? (w & 0x00F000F0u) : (w & 0x000F000Fu)) | 0x64006400u;
+}
+
 // Two 8-bit cache codes -> fp16x2 for page kind KT (1 = E4M3, 2 = int8).
 template <int KT>
 __device__ __forceinline__ uint32_t b8x2_to_f16x2(uint32_t x) {

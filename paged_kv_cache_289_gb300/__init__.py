@@ -47,6 +47,8 @@ class PkvError(RuntimeError):
 def lib():
     """Load libpagedkv.so (built by __graft_entry__.build())."""
     global _lib
+    if _lib is not None:             # loaded: no lock on the per-call path
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(library_path):

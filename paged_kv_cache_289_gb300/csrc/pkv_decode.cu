@@ -76,6 +76,9 @@ template <int D, int BS, int KT>
 struct Cfg {
     static constexpr bool FP8 = KT != 0;                  // quantised pages (one scale each)
     static constexpr bool I4 = KT == 3;                   // int4: two codes per byte
+    // int8 and int4 codes enter the mma with their offset (1024 + biased code); the
+    // offset's share is removed once per score and once per output
+    static constexpr bool FOLD = KT == 2 || KT == 3;
     static constexpr int ELT = FP8 ? 1 : 2;
     static constexpr int ROW_BYTES = I4 ? D / 2 : D * ELT;
     static constexpr int CH = I4 ? 1 : ROW_BYTES / 128;   // 128-byte column chunks per row
@@ -318,9 +321,10 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
     float ot[FP8 ? C::DT : 1][QT][4];
     uint32_t qf[QSMEM ? 1 : C::KS][QT][2];
     float m0[QT], m1[QT], l0[QT], l1[QT];   // heads 2c, 2c+1 of this lane, per query
-    // int4 pages: the nibbles enter the mma offset (1024 + n or 1024 + 16 n, n = code + 8);
-    // cq = the scores' constant part per head (q . offsets), cr = sum over pages of
-    // v_scale * sum(P), which times 1032 or 72 is the output's constant part
+    // int8 / int4 pages: the codes enter the mma with an offset (1024 + code + 128;
+    // 1024 + n or 1024 + 16 n with n = code + 8); cq = the scores' constant part per head
+    // (q . offsets), cr = sum over pages of v_scale * sum(P), which times 1152, 1032 or 72
+    // is the output's constant part
     float cq0[QT], cq1[QT], cr0[QT], cr1[QT];
     float qscale = a.scale_log2;
     bool seg_full = false;
@@ -485,6 +489,20 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         qf[ks2][qi][1] = pack_f16x2(bf16_lo_to_f32(raw_q[ks2][qi].y) * sc,
                                                     bf16_hi_to_f32(raw_q[ks2][qi].y) * sc);
                     }
+                if constexpr (KT == 2) {
+                    // the scores' constant part: the same mma over a tile of code-0 bytes
+                    // (1024 + 128), one value per head
+#pragma unroll
+                    for (int qi = 0; qi < QT; ++qi) {
+                        float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int ks2 = 0; ks2 < C::KS; ++ks2)
+                            mma_f16(cacc, 0x64806480u, 0x64806480u, 0x64806480u, 0x64806480u,
+                                    qf[ks2][qi][0], qf[ks2][qi][1]);
+                        cq0[qi] = cacc[0];
+                        cq1[qi] = cacc[1];
+                    }
+                }
                 qscale = a.scale_log2 * inv_sc;
             }
         }
@@ -598,10 +616,10 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         // int8: one sign flip per register, then gather + widen per pair
                         const uint32_t s0 = r0 ^ 0x80808080u, s1 = r1 ^ 0x80808080u;
                         const uint32_t s2 = r2 ^ 0x80808080u, s3 = r3 ^ 0x80808080u;
-                        k00 = i8pick_to_f16x2<0x5140>(s0); k02 = i8pick_to_f16x2<0x7362>(s0);
-                        k01 = i8pick_to_f16x2<0x5140>(s1); k03 = i8pick_to_f16x2<0x7362>(s1);
-                        k10 = i8pick_to_f16x2<0x5140>(s2); k12 = i8pick_to_f16x2<0x7362>(s2);
-                        k11 = i8pick_to_f16x2<0x5140>(s3); k13 = i8pick_to_f16x2<0x7362>(s3);
+                        k00 = i8pick_raw<0x5140>(s0); k02 = i8pick_raw<0x7362>(s0);
+                        k01 = i8pick_raw<0x5140>(s1); k03 = i8pick_raw<0x7362>(s1);
+                        k10 = i8pick_raw<0x5140>(s2); k12 = i8pick_raw<0x7362>(s2);
+                        k11 = i8pick_raw<0x5140>(s3); k13 = i8pick_raw<0x7362>(s3);
                     } else {
                         k00 = b8x2_to_f16x2<KT>(r0); k01 = b8x2_to_f16x2<KT>(r1);
                         k02 = b8x2_to_f16x2<KT>(r0 >> 16); k03 = b8x2_to_f16x2<KT>(r1 >> 16);
@@ -632,23 +650,23 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         for (int qi = 0; qi < QT; ++qi) {
             mx0[qi] = mx1[qi] = -INFINITY;
             // int4: score = (sum - cq) * scale, one fma
-            const float nc0 = C::I4 ? -cq0[qi] * sc_page : 0.f;
-            const float nc1 = C::I4 ? -cq1[qi] * sc_page : 0.f;
+            const float nc0 = C::FOLD ? -cq0[qi] * sc_page : 0.f;
+            const float nc1 = C::FOLD ? -cq1[qi] * sc_page : 0.f;
 #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
                 if (full_tile) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
-                        sacc[mt][qi][e] = C::I4 ? fmaf(sacc[mt][qi][e], sc_page, (e & 1) ? nc1 : nc0)
-                                                : sacc[mt][qi][e] * sc_page;
+                        sacc[mt][qi][e] = C::FOLD ? fmaf(sacc[mt][qi][e], sc_page, (e & 1) ? nc1 : nc0)
+                                                  : sacc[mt][qi][e] * sc_page;
                 } else {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int tok = mt * 16 + g + ((e & 2) ? 8 : 0);
                         bool valid = tok < ntok;
                         if constexpr (QT > 1) valid = valid && (tpos0 + tok <= seg_vis + qi);
-                        const float v = C::I4 ? fmaf(sacc[mt][qi][e], sc_page, (e & 1) ? nc1 : nc0)
-                                              : sacc[mt][qi][e] * sc_page;
+                        const float v = C::FOLD ? fmaf(sacc[mt][qi][e], sc_page, (e & 1) ? nc1 : nc0)
+                                                : sacc[mt][qi][e] * sc_page;
                         sacc[mt][qi][e] = valid ? v : -INFINITY;
                     }
                 }
@@ -768,18 +786,6 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         }
                     }
                 }
-                // sum(P) per head as the mma sees it (fp16 P against a tile of ones): the
-                // offset part of this page's P.V is 1032 (even picks) or 1152 (odd) times it
-#pragma unroll
-                for (int qi = 0; qi < QT; ++qi) {
-                    float psum[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int mt = 0; mt < C::MT; ++mt)
-                        mma_f16(psum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u,
-                                pb[mt][qi][0], pb[mt][qi][1]);
-                    cr0[qi] = fmaf(vs, psum[0], cr0[qi]);
-                    cr1[qi] = fmaf(vs, psum[1], cr1[qi]);
-                }
             } else {
 #pragma unroll
             for (int dp = 0; dp < C::DT / 2; ++dp) {
@@ -797,10 +803,10 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         if constexpr (KT == 2) {
                             // int8: the token regroup and the widening are one permute
                             const uint32_t xs = x ^ 0x80808080u, ys = y ^ 0x80808080u;
-                            v0 = i8pick_to_f16x2<0x5240>(xs);
-                            v1 = i8pick_to_f16x2<0x5341>(xs);
-                            v2 = i8pick_to_f16x2<0x5240>(ys);
-                            v3 = i8pick_to_f16x2<0x5341>(ys);
+                            v0 = i8pick_raw<0x5240>(xs);
+                            v1 = i8pick_raw<0x5341>(xs);
+                            v2 = i8pick_raw<0x5240>(ys);
+                            v3 = i8pick_raw<0x5341>(ys);
                         } else {
                             v0 = b8x2_to_f16x2<KT>(__byte_perm(x, 0u, 0x0020));
                             v1 = b8x2_to_f16x2<KT>(__byte_perm(x, 0u, 0x0031));
@@ -814,6 +820,21 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                     }
                 }
             }
+            }
+            if constexpr (C::FOLD) {
+                // sum(P) per head as the mma sees it (fp16 P against a tile of ones): the
+                // offset part of this page's P.V is that times 1032 (int4, even picks) or
+                // 1152 (int4 odd picks, int8)
+#pragma unroll
+                for (int qi = 0; qi < QT; ++qi) {
+                    float psum[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int mt = 0; mt < C::MT; ++mt)
+                        mma_f16(psum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u,
+                                pb[mt][qi][0], pb[mt][qi][1]);
+                    cr0[qi] = fmaf(vs, psum[0], cr0[qi]);
+                    cr1[qi] = fmaf(vs, psum[1], cr1[qi]);
+                }
             }
             // int4: odd picks accumulated 16 n, so their page scale carries the 1/16
             const float vs16 = vs * 0.0625f;
@@ -835,12 +856,12 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 #pragma unroll
             for (int qi = 0; qi < QT; ++qi) {
                 if (qi >= seg_qlen) break;
-                if constexpr (C::I4) {
-                    // remove the offsets' share: 1032 per unit of cr (even picks), 1152 / 16
-                    // = 72 (odd picks)
+                if constexpr (C::FOLD) {
+                    // remove the offsets' share: per unit of cr, 1152 (int8), 1032 (int4
+                    // even picks) or 1152 / 16 = 72 (int4 odd picks)
 #pragma unroll
                     for (int dt = 0; dt < C::DT; ++dt) {
-                        const float k = (dt & 1) ? 72.f : 1032.f;
+                        const float k = !C::I4 ? 1152.f : ((dt & 1) ? 72.f : 1032.f);
                         o[dt][qi][0] = fmaf(-k, cr0[qi], o[dt][qi][0]);
                         o[dt][qi][2] = fmaf(-k, cr0[qi], o[dt][qi][2]);
                         o[dt][qi][1] = fmaf(-k, cr1[qi], o[dt][qi][1]);

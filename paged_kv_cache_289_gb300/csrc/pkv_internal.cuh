@@ -294,46 +294,21 @@ __device__ __forceinline__ uint32_t i8x2_to_f16x2(uint32_t x) {
     return r;
 }
 
-// Two int8 codes picked from the 4 bytes of x by a byte-permute selector `sel`
-// (low pair first) -> fp16x2; `xs` is x with its sign bits already flipped
-// (x ^ 0x80808080), so the permute both gathers and widens.
+// Two int8 codes picked from the 4 bytes of xs by a byte-permute selector SEL (low pair
+// first), where xs is x with its sign bits flipped (x ^ 0x80808080, so byte = code + 128):
+// the permute gathers and widens at once, to fp16 (1024 + code + 128) per half.  fp16
+// 1024 + k (k < 1024) is the exponent of 1024 with k in the mantissa.  The offset 1152 is
+// left in: a caller subtracts it once per sum.
 template <uint32_t SEL>
-__device__ __forceinline__ uint32_t i8pick_to_f16x2(uint32_t xs) {
-    const uint32_t y = __byte_perm(xs, 0x64646464u, SEL);
-    uint32_t r;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(y), "r"(0x64806480u));
-    return r;
+__device__ __forceinline__ uint32_t i8pick_raw(uint32_t xs) {
+    return __byte_perm(xs, 0x64646464u, SEL);
 }
 
 // Two int4 codes picked from the 8 offset-binary nibbles n0..n7 of x (n_j at bits
-// 4j..4j+3) -> fp16x2 (n_I - 8, n_{I+4} - 8), exactly.  fp16 1024 + k (k < 1024)
-// is the exponent of 1024 with k in the mantissa: the mask-or puts a nibble there
-// directly (I even) or 16 times a nibble (I odd, then a multiply by 1/16 is exact).
-template <int I>
-__device__ __forceinline__ uint32_t i4pick_to_f16x2(uint32_t x) {
-    const uint32_t w = (I >= 2) ? (x >> 8) : x;
-    uint32_t r;
-    // the constants are literals the compiler can place in the instruction
-    if constexpr ((I & 1) == 0) {
-        const uint32_t y = (w & 0x000F000Fu) | 0x64006400u;      // (1024 + n, 1024 + n')
-        const __half2 h = __hsub2(*reinterpret_cast<const __half2*>(&y),
-                                  __half2half2(__ushort_as_half((unsigned short)0x6408u)));   // - 1032
-        r = *reinterpret_cast<const uint32_t*>(&h);
-    } else {
-        const uint32_t y = (w & 0x00F000F0u) | 0x64006400u;      // (1024 + 16 n, ...)
-        // (1024 + 16 n) / 16 - 72 = n - 8
-        const __half2 h = __hfma2(*reinterpret_cast<const __half2*>(&y),
-                                  __half2half2(__ushort_as_half((unsigned short)0x2C00u)),
-                                  __half2half2(__ushort_as_half((unsigned short)0xD480u)));
-        r = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    return r;
-}
-
-// The same nibble pick without the offset: (1024 + n) for I even, (1024 + 16 n) for I
-// odd, with n = code + 8.  A caller that folds the constant part into its sums (q prescaled
-// by 1/16 for odd I, the 1024 + 8 or 1024 + 128 term subtracted once per sum) saves the
-// half2 subtract or fma per pair.
+// 4j..4j+3, n = code + 8), pairing nibbles (I, I + 4): the mask-or places nibble n
+// directly in the mantissa of 1024 (I even, giving 1024 + n) or 16 n (I odd, giving
+// 1024 + 16 n).  The offsets are left in: a caller prescales q by 1/16 for odd picks
+// and subtracts the constant part once per sum.
 template <int I>
 __device__ __forceinline__ uint32_t i4pick_raw(uint32_t x) {
     const uint32_t w = (I >= 2) ? (x >> 8) : x;

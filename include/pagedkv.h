@@ -173,11 +173,14 @@ PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_
  * (likewise V), dequantised with k_scale/v_scale[block][h] for FP8 pages.
  * Accumulation is fp32; out is bf16.  seq_lens[r] == 0 gives out[r] = 0.
  * Supported: Hq % Hkv == 0, G = Hq / Hkv <= 8; block_size 16 or 32;
- *   PKV_BF16 with head_dim 64 or 128; PKV_FP8_E4M3 and PKV_INT8 with head_dim 128
- *   (FP8: the group's bf16 q values are rescaled by a power of two so the
- *   largest lands in [2^14, 2^15) and converted to fp16; this is exact except
- *   for nonzero elements more than 2^31 times smaller than the group's
- *   largest, which round to the fp16 subnormal grid).
+ *   PKV_BF16 with head_dim 64 or 128; PKV_FP8_E4M3, PKV_INT8 and PKV_INT4 with
+ *   head_dim 128 (quantised pages: the group's bf16 q values are rescaled by a
+ *   power of two so the largest lands in [2^14, 2^15) and converted to fp16; this
+ *   is exact except for nonzero elements more than 2^31 times smaller than the
+ *   group's largest, which round to the fp16 subnormal grid.  INT8 and INT4 codes
+ *   enter the fp16 mma with their offset, 1024 plus the biased code, which is
+ *   subtracted once per score and once per output; that cancellation adds fp32
+ *   rounding of about 2^-24 * 1152 * sqrt(pages) times v_scale to an output).
  * Requirements: q, out, caches, workspace 16-byte aligned; workspace_bytes >=
  *   pkv_decode_workspace_size(...) for the same shape and device.
  * The work is one flat list of (request, kv head, page) items split evenly over

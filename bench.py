@@ -88,12 +88,40 @@ def recorded_traffic(kernel_src_hash, workload_name):
         return None
 
 
+def strip_c_comments(src):
+    """C/C++/CUDA source without its comments, whitespace runs collapsed: the text
+    that decides the compiled code (string and character literals kept intact)."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            out.append(" ")
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_source_hash():
+    """sha256 of the decode kernel's sources with comments stripped, so a comment edit
+    keeps a recorded DRAM traffic figure valid and a code edit does not."""
     import hashlib
     h = hashlib.sha256()
     for name in ("pkv_decode.cu", "pkv_internal.cuh"):
-        with open(os.path.join(ROOT, "paged_kv_cache_289_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "paged_kv_cache_289_gb300", "csrc", name),
+                  encoding="utf-8") as f:
+            h.update(strip_c_comments(f.read()).encode())
     return h.hexdigest()
 
 

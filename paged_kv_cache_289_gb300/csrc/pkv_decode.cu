@@ -8,9 +8,10 @@
 // 的循环状态" and "PagedAttention与Cache管理"), with an online (running max / sum)
 // softmax ("GPU推理深度拆解：KV Cache视角", 算子优化要点) and the KV length split
 // across warps when the batch is small (same note: batch-1 decode leaves SMs idle).
-// With several query tokens per request (verifying speculative drafts, [P1]
-// "投机解码：打破每步一token的假设"), query i of the request's q_len newest tokens
-// attends causally to positions 0 .. seq_len - q_len + i.
+// With several query tokens per request (verifying speculative drafts,
+// "深入LLM推理：从KV Cache到PD分离的Serving全景解析", "投机解码：打破每步一token的假设"),
+// query i of the request's q_len newest tokens attends causally to positions
+// 0 .. seq_len - q_len + i.
 //
 // Work decomposition.  Unit u = (request r, kv head h) owns np_r = ceil(seq_r / BS)
 // pages.  All units' pages form one flat list of P items (request-major, then
@@ -21,7 +22,7 @@
 // it writes an unnormalised partial (o, running max m, sum l) to workspace slot
 // u + w (unique: unit and warp ranges are both ordered).  Every split unit is merged
 // with log-sum-exp weights by a small follow-up kernel (one CTA per unit, one warp
-// per query head), launched behind this one.  No warp waits for or merges after
+// per query head and query position), launched behind this one.  No warp waits for or merges after
 // another: a merge by the last warp to finish a unit kept that warp, and its SM,
 // busy past its peers (measured on GB300: up to 13 us for one query position and 46
 // us for four, with the step 2.5% and 14% slower).
@@ -40,10 +41,11 @@
 //                                     B = Q^T of the GQA group (8 heads, registers)
 //   O^T[d][g] += V^T[d][t] P^T[t][g]  A = V tile (ldmatrix.trans), B = P^T from
 //                                     the S^T accumulators via movmatrix.trans
-// 8-bit pages (E4M3 or int8) are widened exactly to fp16 in registers (cvt
-// e4m3x2 -> f16x2, or an exact int8 -> fp16 construction); the per-(block, head)
-// K scale multiplies S, the V scale multiplies the page's P.V contribution, so
-// neither scale is rounded into an fp16 operand.
+// Quantised pages are widened exactly to fp16 in registers: E4M3 by cvt e4m3x2 ->
+// f16x2; int8 and int4 codes by a byte permute or mask-or that yields 1024 plus the
+// biased code, whose constant share is subtracted once per score and once per output.
+// The per-(block, head) K scale multiplies S, the V scale multiplies the page's P.V
+// contribution, so neither scale is rounded into an fp16 operand.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>

@@ -20,10 +20,14 @@ Parity status per function (what pins it, see tests/test_oracle_pins.py):
   kv_bytes                                         -- the printed 327,680 B/token and ~10 GB at 32K
   slot_mapping, kv_cache_write                     -- worked example + write/gather round trip
   multiquery_attn                                  -- dense causal brute force, q_len = 1 case
-  decode_attn / decode_rows                        -- dense brute force, permutation invariance,
+  multiquery_rows                                  -- dense causal brute force on every row of a
+                                                      ragged batch (q_len 0 and q_len > seq_len)
+  decode_attn / decode_rows / decode_row_detail    -- dense brute force, permutation invariance,
                                                       GQA == replicated MHA, closed-form cases, LSE merge
   fnv1a64, fmix64                                  -- published FNV-1a and SplitMix64 test vectors
-  prefix_block_hash                                -- token-exact prefix equality properties
+  prefix_block_hash, hash_offsets                  -- token-exact prefix equality properties
+  prefix_block_hash_resume                         -- suffix of the published-vector-pinned chain
+                                                      at every cut point (the chain's definition)
   block_manager.BlockManagerModel, copy_blocks     -- hand-worked call sequences and invariants
                                                       (tests/test_block_manager.py)
 """
@@ -100,6 +104,8 @@ def lib():
             L.orc_multiquery_attn.restype = None
             L.orc_multiquery_attn.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i,
                                               _i, _i, _i, _d, _p]
+            L.orc_prefix_block_hash_resume.restype = None
+            L.orc_prefix_block_hash_resume.argtypes = [_p, _p, _i, _i, _p, _p, _p, _p]
             L.orc_multiquery_rows.restype = None
             L.orc_multiquery_rows.argtypes = [_p, _p, _p, _p, _p, _p, _p, _i, _p, _i, _i, _i,
                                               _i, _i, _i, _d, _p, _i64, _p]
@@ -319,3 +325,28 @@ def prefix_block_hash(tokens, offsets, block_size, seed):
                                 int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out) if out.size else None,
                                 _ptr(ho))
     return out, ho
+
+
+def prefix_block_hash_resume(tokens, offsets, block_size, prev_hashes, first_blocks,
+                             hash_offsets=None):
+    """The chain continued from h_k per sequence: prev_hashes[s] = h_{k_s},
+    first_blocks[s] = k_s full blocks already hashed.  Returns (hashes, hash_offsets)
+    with max(0, floor(L_s / B) - k_s) hashes per sequence unless hash_offsets gives
+    the room per sequence."""
+    tok = _c(tokens, np.int32)
+    off = _c(offsets, np.int64)
+    prev = _c(np.asarray(prev_hashes, dtype=np.uint64), np.uint64)
+    first = _c(first_blocks, np.int64)
+    if hash_offsets is None:
+        full = np.diff(off) // block_size
+        n = np.maximum(full - np.maximum(first, 0), 0)
+        ho = np.zeros(n.shape[0] + 1, dtype=np.int64)
+        np.cumsum(n, out=ho[1:])
+    else:
+        ho = _c(hash_offsets, np.int64)
+    out = np.zeros(max(int(ho[-1]), 1), dtype=np.uint64)
+    if tok.size == 0:
+        tok = np.zeros(1, np.int32)
+    lib().orc_prefix_block_hash_resume(_ptr(tok), _ptr(off), off.shape[0] - 1, block_size,
+                                       _ptr(prev), _ptr(first), _ptr(out), _ptr(ho))
+    return out[:int(ho[-1])], ho

@@ -559,3 +559,42 @@ void orc_prefix_block_hash(const int32_t *tokens, const int64_t *offsets,
     }
     free(buf);
 }
+
+/* Resuming the chain of [P3] "优化一：Prefix Cache" (工作原理：按块哈希): h_i depends
+ * only on h_{i-1} and the tokens of block i, so a sequence whose first k full
+ * blocks were hashed earlier continues from h_k and needs only the blocks after
+ * them.  Sequence s is tokens[offsets[s] .. offsets[s+1]) (all of its tokens);
+ * first_blocks[s] = k_s full blocks are already hashed and prev_hashes[s] = h_{k_s}
+ * (the seed when k_s = 0; a negative k_s is read as 0).  The hashes h_{k_s+1},
+ * h_{k_s+2}, ... of its later full blocks go to hashes[hash_offsets[s] ..], at most
+ * hash_offsets[s+1] - hash_offsets[s] of them; nothing is written when k_s is at or
+ * past floor(L_s / B).  The chain is re-derived here block by block from the
+ * definition above, independently of orc_prefix_block_hash. */
+void orc_prefix_block_hash_resume(const int32_t *tokens, const int64_t *offsets,
+                                  int num_seqs, int block_size,
+                                  const uint64_t *prev_hashes, const int64_t *first_blocks,
+                                  uint64_t *hashes, const int64_t *hash_offsets)
+{
+    uint8_t *buf = (uint8_t *)malloc((size_t)block_size * 4);
+    for (int s = 0; s < num_seqs; ++s) {
+        int64_t len = offsets[s + 1] - offsets[s];
+        int64_t full = len / block_size;            /* full blocks of the sequence */
+        int64_t k = first_blocks[s] < 0 ? 0 : first_blocks[s];
+        int64_t room = hash_offsets[s + 1] - hash_offsets[s];
+        uint64_t h = prev_hashes[s];                /* h_k */
+        int64_t written = 0;
+        /* block i (1-based) holds tokens (i-1)B .. iB-1 of the sequence */
+        for (int64_t i = k + 1; i <= full && written < room; ++i) {
+            const int32_t *blk = tokens + offsets[s] + (i - 1) * block_size;
+            for (int j = 0; j < block_size; ++j) {
+                uint32_t tok = (uint32_t)blk[j];
+                for (int b = 0; b < 4; ++b)
+                    buf[4 * j + b] = (uint8_t)(tok >> (8 * b));
+            }
+            h = orc_fmix64(h ^ orc_fnv1a64(buf, (int64_t)block_size * 4));
+            hashes[hash_offsets[s] + written] = h;
+            ++written;
+        }
+    }
+    free(buf);
+}

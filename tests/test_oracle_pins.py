@@ -427,6 +427,51 @@ def test_hash_empty_and_short_sequences():
     assert len(out[0]) == 0 and len(out[1]) == 0 and len(out[2]) == 1
 
 
+def test_hash_resume_continues_the_chain_at_every_cut():
+    """h_i = H(h_{i-1}, block i): continuing from h_k over the same tokens gives exactly
+    h_{k+1}, h_{k+2}, ... of the whole chain, for every cut k (the published-vector-pinned
+    chain above is the reference).  Several sequences at once, each cut independently."""
+    rng = np.random.default_rng(23)
+    B, seed = 16, 0x1234
+    seqs = [rng.integers(0, 128000, n).astype(np.int32) for n in (0, 5, 16, 16 * 7 + 3, 16 * 12)]
+    whole = _hash(seqs, B, seed)
+    toks = np.concatenate(seqs)
+    offs = np.zeros(len(seqs) + 1, np.int64)
+    np.cumsum([len(s) for s in seqs], out=offs[1:])
+    for cut in range(0, 14):
+        first = np.array([cut] * len(seqs), np.int64)
+        prev = np.array([seed if min(cut, len(w)) == 0 else int(w[min(cut, len(w)) - 1])
+                         for w in whole], np.uint64)
+        got, ho = oracle.prefix_block_hash_resume(toks, offs, B, prev, first)
+        for s, w in enumerate(whole):
+            assert np.array_equal(got[ho[s]:ho[s + 1]], w[cut:]), (cut, s)
+    # mixed cuts, one per sequence, including one past the last full block
+    first = np.array([0, 0, 1, 3, 12], np.int64)
+    prev = np.array([seed, seed, whole[2][0], whole[3][2], whole[4][11]], np.uint64)
+    got, ho = oracle.prefix_block_hash_resume(toks, offs, B, prev, first)
+    assert np.diff(ho).tolist() == [0, 0, 0, 4, 0]
+    assert np.array_equal(got, whole[3][3:])
+    # a negative count of blocks already hashed starts the chain at prev as h_0
+    got, _ = oracle.prefix_block_hash_resume(toks, offs, B, [seed] * 5, [-3] * 5)
+    assert np.array_equal(got, np.concatenate(whole))
+
+
+def test_hash_resume_respects_the_room_per_sequence():
+    """hash_offsets gives each sequence's room: a short room takes the first hashes of
+    the continued chain and nothing is written past it."""
+    rng = np.random.default_rng(24)
+    B, seed = 16, 99
+    seqs = [rng.integers(0, 128000, n).astype(np.int32) for n in (16 * 9, 16 * 5 + 1)]
+    whole = _hash(seqs, B, seed)
+    toks = np.concatenate(seqs)
+    offs = np.array([0, len(seqs[0]), len(seqs[0]) + len(seqs[1])], np.int64)
+    ho = np.array([0, 2, 2 + 10], np.int64)               # room 2 (needs 6), room 10 (needs 5)
+    got, _ = oracle.prefix_block_hash_resume(toks, offs, B, [whole[0][2], seed], [3, 0], ho)
+    assert np.array_equal(got[:2], whole[0][3:5])
+    assert np.array_equal(got[2:7], whole[1])
+    assert np.all(got[7:] == 0)                            # untouched past the chain's end
+
+
 # ---------------------------------------------------------------- multi-query (verify) attention
 def _dense_causal(q, qoffs, K, V, scale, G):
     """Query i of request r (its newest tokens) over positions 0..S-q_len+i, with scipy."""
@@ -461,6 +506,38 @@ def test_multiquery_matches_dense_causal_bruteforce():
     got = oracle.multiquery_attn(q, qoffs, kc, vc, bt, np.array(lens, np.int32), 0.1)
     ref = _dense_causal(q, qoffs, K, V, 0.1, G)
     np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_multiquery_rows_match_dense_causal_and_the_whole_output():
+    """Selected rows re-derive each row's request on their own, so they are pinned
+    separately: every row of every request, in shuffled order and with repeats, against
+    the dense causal brute force, and bit for bit against the whole-batch output.  The
+    batch has ragged q_lens, a request with more queries than cached tokens (its first
+    queries see nothing), and requests with no queries in the middle and at the end."""
+    rng = np.random.default_rng(72)
+    BS, Hkv, G, D = 16, 2, 4, 64
+    lens = [3, 5, 16, 9, 40, 77, 12]
+    qlens = [5, 2, 0, 4, 3, 8, 0]
+    K = [_bf16(rng.standard_normal((S, Hkv, D))) for S in lens]
+    V = [_bf16(rng.standard_normal((S, Hkv, D))) for S in lens]
+    qoffs = np.zeros(len(lens) + 1, np.int32)
+    np.cumsum(qlens, out=qoffs[1:])
+    Hq = Hkv * G
+    q = _bf16(rng.standard_normal((int(qoffs[-1]), Hq, D)))
+    kc, vc, bt = _paged_from_dense(rng, K, V, BS)
+    sl = np.array(lens, np.int32)
+    ref = _dense_causal(q, qoffs, K, V, 0.1, G).reshape(-1, D)
+    whole = oracle.multiquery_attn(q, qoffs, kc, vc, bt, sl, 0.1).reshape(-1, D)
+    rows = np.concatenate([rng.permutation(ref.shape[0]),
+                           rng.integers(0, ref.shape[0], size=40)]).astype(np.int64)
+    got = oracle.multiquery_rows(q, qoffs, kc, vc, bt, sl, 0.1, rows)
+    np.testing.assert_allclose(got, ref[rows], rtol=0, atol=1e-12)
+    assert np.array_equal(got, whole[rows])
+    # the rows that see no token: request 0's first two queries
+    zero = np.arange(2 * Hq)
+    assert np.all(ref[zero] == 0) and np.all(got[np.isin(rows, zero)] == 0)
+    # every other row saw at least one token
+    assert np.all(np.any(ref[2 * Hq:] != 0, axis=-1))
 
 
 def test_multiquery_single_query_is_decode_and_empty_rows_are_zero():

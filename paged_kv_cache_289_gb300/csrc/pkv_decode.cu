@@ -1075,12 +1075,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-int env_int(const char* name, int dflt) {
-    const char* v = getenv(name);
-    if (!v || !*v) return dflt;
-    return atoi(v);
-}
-
 }  // namespace
 
 // Compile-time query positions per request for a call with at most `max_q_len`
@@ -1107,14 +1101,12 @@ DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int ba
     // and for several query positions, 12 for single-query int4 pages (compute-bound:
     // 0.44 of the copy peak against 0.40 with 8; 10 warps split unevenly over the four
     // sub-partitions and run slower).
-    // register budget of the launch bounds: 384 threads for single-query bf16 and int4
-    // pages, 256 otherwise
-    const int max_warps = ((fp8 && kt != 3) || qt > 1) ? 8 : 12;
-    p.warps = env_int("PKV_DECODE_WARPS", (kt == 3 && qt == 1) ? 12 : ((fp8 || qt > 1) ? 8 : 6));
-    if (p.warps < 1) p.warps = 1;
-    if (p.warps > max_warps) p.warps = max_warps;
-    int stages = env_int("PKV_DECODE_STAGES", 0);
-    if (stages <= 0) stages = 131072 / (p.warps * p.stage_bytes);
+    // (within the launch bounds' register budget: 384 threads for single-query bf16
+    // and int4 pages, 256 otherwise)
+    // The plan is a pure function of its arguments: pkv_decode_workspace_size and the
+    // launch must agree on it in every process.
+    p.warps = (kt == 3 && qt == 1) ? 12 : ((fp8 || qt > 1) ? 8 : 6);
+    int stages = 131072 / (p.warps * p.stage_bytes);
     if (stages > 16) stages = 16;
     if (stages < 2) stages = 2;
     const int fixed = 1024 + (int)align_up(4 * (2 * (int64_t)batch + 1), 16);

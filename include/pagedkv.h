@@ -236,13 +236,19 @@ PKV_API int pkv_paged_multiquery_attn(const void *q, const int32_t *q_offsets, i
  * pkv_paged_decode_attn without the workspace: the scratch is a 16 MiB static
  * device array inside the library, which every GPU that loads the library holds
  * until the process exits.
- *   - Shapes whose pkv_decode_workspace_size exceeds 16 MiB return
- *     PKV_ERR_WORKSPACE and launch nothing (at head_dim 128 on a 152-SM GPU:
- *     batch * num_kv_heads up to about 3,050 for bf16 pages, 2,750 for
- *     E4M3 and int8 pages and 2,140 for int4 pages, whose plans run more warps).
+ *   - The limit: a call runs when pkv_decode_workspace_size(batch, ..., 0) on the
+ *     current device is at most 16 MiB; larger shapes return PKV_ERR_WORKSPACE and
+ *     launch nothing.  That size grows with batch * num_kv_heads and with the
+ *     device's SM count, so the bound depends on the GPU: on a 152-SM GPU at
+ *     head_dim 128 it is batch * num_kv_heads up to about 3,050 for bf16 pages,
+ *     2,750 for E4M3 and int8 pages and 2,140 for int4 pages (whose plans run more
+ *     warps per SM).
+ *   - Argument checks come in the same order and return the same statuses as
+ *     pkv_paged_decode_attn's; a failed CUDA query returns PKV_ERR_CUDA.
  *   - The first call on a device, made with that device current, looks up the
  *     array's device address (cudaGetSymbolAddress); make that first call before
- *     any stream capture.
+ *     any stream capture.  The address is kept per device and looked up again when
+ *     the device's current context has changed (after cudaDeviceReset, say).
  *   - Every call shares the one array and it keeps the last call's contents;
  *     nothing in it needs to start at zero.  Calls that overlap on the GPU (other
  *     streams, other threads) race on it: serialise them.  The device error word
@@ -263,13 +269,37 @@ PKV_API int pkv_paged_decode_attn_noalloc(const void *q, const void *k_cache,
  * with H(p, blk) = fmix64(p XOR FNV1a64(little-endian bytes of the block's int32
  * tokens)), fmix64 = the SplitMix64 output mixer.  Sequence s is
  * tokens[offsets[s] .. offsets[s+1]); its hashes go to
- * hashes[hash_offsets[s] .. hash_offsets[s] + floor(L_s / B)).  A partial last
- * block gets no hash.  tokens int32, offsets/hash_offsets int64 [num_seqs + 1],
+ * hashes[hash_offsets[s] .. hash_offsets[s] + floor(L_s / B)), and never more than
+ * hash_offsets[s+1] - hash_offsets[s] of them.  A partial last block gets no hash.  tokens int32, offsets/hash_offsets int64 [num_seqs + 1],
  * hashes uint64.  block_size in [1, 1024].
  */
 PKV_API int pkv_prefix_block_hash(const int32_t *tokens, const int64_t *offsets, int num_seqs,
                           int block_size, uint64_t seed, uint64_t *hashes,
                           const int64_t *hash_offsets, pkv_stream_t stream);
+
+/*
+ * The same chain, resumed ([P3] "优化一：Prefix Cache", 工作原理：按块哈希: h_i depends
+ * only on h_{i-1} and block i).  A serving step that has hashed a sequence's first
+ * k full blocks before passes h_k and k, and only the blocks filled since are read
+ * and hashed: a decode step typically hashes zero or one block per sequence
+ * instead of its whole history.
+ *   tokens, offsets  as pkv_prefix_block_hash: all tokens of sequence s
+ *   first_blocks     device int64 [num_seqs]: k_s, full blocks already hashed
+ *                    (negative reads as 0; at or past floor(L_s / B): nothing to do)
+ *   prev_hashes      device uint64 [num_seqs]: h_{k_s} (the seed when k_s = 0)
+ *   hashes           receives h_{k_s+1}, h_{k_s+2}, ... at hash_offsets[s] ..
+ *   hash_offsets     device int64 [num_seqs + 1]; sequence s gets at most
+ *                    hash_offsets[s+1] - hash_offsets[s] hashes, normally
+ *                    max(0, floor(L_s / B) - k_s).  Entries past what is written
+ *                    are left untouched.
+ * With k_s = 0 and prev_hashes[s] = seed this equals pkv_prefix_block_hash.
+ * block_size in [1, 1024]; any NULL pointer (num_seqs > 0) is PKV_ERR_INVALID_ARG.
+ */
+PKV_API int pkv_prefix_block_hash_resume(const int32_t *tokens, const int64_t *offsets,
+                                         int num_seqs, int block_size,
+                                         const uint64_t *prev_hashes,
+                                         const int64_t *first_blocks, uint64_t *hashes,
+                                         const int64_t *hash_offsets, pkv_stream_t stream);
 
 /*
  * Paged prefill attention ([P1] "推理的两阶段计算形态": prefill processes every prompt

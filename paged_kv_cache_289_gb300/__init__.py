@@ -15,7 +15,8 @@ __all__ = [
     "PkvError", "lib", "library_path", "BF16", "FP8_E4M3", "INT8", "INT4", "DEVERR_WAIT_TIMEOUT",
     "DEVERR_SEQ_CLAMPED", "DEVERR_BLOCK_RANGE", "compute_slot_mapping", "kv_cache_write",
     "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn",
-    "paged_decode_attn_noalloc", "prefix_block_hash", "multiquery_workspace_size",
+    "paged_decode_attn_noalloc", "prefix_block_hash", "prefix_block_hash_resume",
+    "multiquery_workspace_size",
     "paged_multiquery_attn", "DEVERR_QLEN_CLAMPED", "kv_cache_write_rescale",
     "device_num_sms", "read_device_error", "copy_blocks", "BlockManager", "ERR_NO_BLOCKS",
     "paged_prefill_attn", "prefill_workspace_size",
@@ -88,6 +89,8 @@ def lib():
                                                         i, f, p, p]
             L.pkv_prefix_block_hash.restype = i
             L.pkv_prefix_block_hash.argtypes = [p, p, i, i, u64, p, p, p]
+            L.pkv_prefix_block_hash_resume.restype = i
+            L.pkv_prefix_block_hash_resume.argtypes = [p, p, i, i, p, p, p, p, p]
             L.pkv_prefill_workspace_size.restype = sz
             L.pkv_prefill_workspace_size.argtypes = [i, i, i, i, i, i]
             L.pkv_paged_prefill_attn.restype = i
@@ -334,6 +337,25 @@ def prefix_block_hash(tokens, offsets, block_size, hash_offsets, num_hashes, see
     _check("pkv_prefix_block_hash", lib().pkv_prefix_block_hash(
         _ptr(tokens), _ptr(offsets), offsets.shape[0] - 1, block_size,
         int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out), _ptr(hash_offsets), _stream(stream)))
+    return out[:num_hashes]
+
+
+def prefix_block_hash_resume(tokens, offsets, block_size, prev_hashes, first_blocks,
+                             hash_offsets, num_hashes, out=None, stream=None):
+    """The chain continued per sequence from prev_hashes[s] = h_k after
+    first_blocks[s] = k full blocks (int64 tensors holding uint64 bit patterns /
+    block counts); returns the new hashes laid out by `hash_offsets`."""
+    import torch
+    _need(tokens, "tokens", (torch.int32,))
+    _need(offsets, "offsets", (torch.int64,))
+    _need(prev_hashes, "prev_hashes", (torch.int64,))
+    _need(first_blocks, "first_blocks", (torch.int64,))
+    _need(hash_offsets, "hash_offsets", (torch.int64,))
+    if out is None:
+        out = torch.empty(max(int(num_hashes), 1), dtype=torch.int64, device=tokens.device)
+    _check("pkv_prefix_block_hash_resume", lib().pkv_prefix_block_hash_resume(
+        _ptr(tokens), _ptr(offsets), offsets.shape[0] - 1, block_size, _ptr(prev_hashes),
+        _ptr(first_blocks), _ptr(out), _ptr(hash_offsets), _stream(stream)))
     return out[:num_hashes]
 
 

@@ -216,8 +216,23 @@ int pkv_prefix_block_hash(const int32_t* tokens, const int64_t* offsets, int num
     if (num_seqs < 0 || block_size <= 0 || block_size > 1024) return PKV_ERR_INVALID_ARG;
     if (num_seqs == 0) return PKV_OK;
     if (!tokens || !offsets || !hashes || !hash_offsets) return PKV_ERR_INVALID_ARG;
-    cudaError_t e = pkv::prefix_hash_launch(tokens, offsets, num_seqs, block_size, seed, hashes,
-                                            hash_offsets, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = pkv::prefix_hash_launch(tokens, offsets, num_seqs, block_size, seed, nullptr,
+                                            nullptr, hashes, hash_offsets,
+                                            reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+int pkv_prefix_block_hash_resume(const int32_t* tokens, const int64_t* offsets, int num_seqs,
+                                 int block_size, const uint64_t* prev_hashes,
+                                 const int64_t* first_blocks, uint64_t* hashes,
+                                 const int64_t* hash_offsets, pkv_stream_t stream) {
+    if (num_seqs < 0 || block_size <= 0 || block_size > 1024) return PKV_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PKV_OK;
+    if (!tokens || !offsets || !prev_hashes || !first_blocks || !hashes || !hash_offsets)
+        return PKV_ERR_INVALID_ARG;
+    cudaError_t e = pkv::prefix_hash_launch(tokens, offsets, num_seqs, block_size, 0, prev_hashes,
+                                            first_blocks, hashes, hash_offsets,
+                                            reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

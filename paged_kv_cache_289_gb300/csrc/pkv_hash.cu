@@ -48,15 +48,32 @@ __device__ __forceinline__ uint64_t fmix64(uint64_t z) {
     return z ^ (z >> 31);
 }
 
+// Full chain (prev_hashes == nullptr): every full block of the sequence, from h_0 =
+// seed.  Resumed chain: the first max(first_blocks[s], 0) full blocks were hashed
+// before and prev_hashes[s] is the last of them (h_k), so only the blocks after them
+// are digested and chained.  Either way at most hash_offsets[s+1] - hash_offsets[s]
+// hashes are written.
 __global__ void __launch_bounds__(kHashThreads)
     pkv_prefix_hash_kernel(const int32_t* __restrict__ tokens, const int64_t* __restrict__ offsets,
-                           int B, uint64_t seed, uint64_t* __restrict__ hashes,
+                           int B, uint64_t seed, const uint64_t* __restrict__ prev_hashes,
+                           const int64_t* __restrict__ first_blocks,
+                           uint64_t* __restrict__ hashes,
                            const int64_t* __restrict__ hash_offsets) {
     __shared__ uint64_t dig[2][kHashChunk];
     const int s = blockIdx.x;
-    const int64_t begin = offsets[s];
-    const int64_t len = offsets[s + 1] - begin;
-    const int64_t nb = len / B;
+    const int64_t full = (offsets[s + 1] - offsets[s]) / B;
+    int64_t k = 0;
+    uint64_t h0 = seed;
+    if (prev_hashes) {
+        k = first_blocks[s];
+        k = k < 0 ? 0 : (k > full ? full : k);
+        h0 = prev_hashes[s];
+    }
+    const int64_t room = hash_offsets[s + 1] - hash_offsets[s];
+    int64_t nb = full - k;                      // blocks to hash, from block k (0-based)
+    if (nb > room) nb = room;
+    if (nb < 0) nb = 0;
+    const int64_t begin = offsets[s] + k * B;
     const int nchunks = (int)((nb + kHashChunk - 1) / kHashChunk);
     uint64_t* out = hashes + hash_offsets[s];
     // digests of chunk c into buffer c & 1, by threads [t0, kHashThreads)
@@ -68,7 +85,7 @@ __global__ void __launch_bounds__(kHashThreads)
     };
     if (nchunks > 0) digest(0, 0);
     __syncthreads();
-    uint64_t h = seed;
+    uint64_t h = h0;
     for (int c = 0; c < nchunks; ++c) {
         if (threadIdx.x < 32) {
             if (threadIdx.x == 0) {
@@ -102,11 +119,12 @@ __global__ void __launch_bounds__(kHashThreads)
 }
 
 cudaError_t prefix_hash_launch(const int32_t* tokens, const int64_t* offsets, int num_seqs, int B,
-                               uint64_t seed, uint64_t* hashes, const int64_t* hash_offsets,
-                               cudaStream_t st) {
+                               uint64_t seed, const uint64_t* prev_hashes,
+                               const int64_t* first_blocks, uint64_t* hashes,
+                               const int64_t* hash_offsets, cudaStream_t st) {
     if (num_seqs == 0) return cudaSuccess;
-    pkv_prefix_hash_kernel<<<num_seqs, kHashThreads, 0, st>>>(tokens, offsets, B, seed, hashes,
-                                                              hash_offsets);
+    pkv_prefix_hash_kernel<<<num_seqs, kHashThreads, 0, st>>>(tokens, offsets, B, seed, prev_hashes,
+                                                              first_blocks, hashes, hash_offsets);
     return cudaGetLastError();
 }
 

@@ -88,9 +88,11 @@ cudaError_t cache_write_rescale_launch(const void* k, const void* v, const int64
                                        int Hkv, int D, int BS, int NB, int kt, void* k_cache,
                                        void* v_cache, float* k_scale, float* v_scale,
                                        void* workspace, cudaStream_t st);
+// prev_hashes / first_blocks == nullptr: the full chain from seed; else resumed
 cudaError_t prefix_hash_launch(const int32_t* tokens, const int64_t* offsets, int num_seqs, int B,
-                               uint64_t seed, uint64_t* hashes, const int64_t* hash_offsets,
-                               cudaStream_t st);
+                               uint64_t seed, const uint64_t* prev_hashes,
+                               const int64_t* first_blocks, uint64_t* hashes,
+                               const int64_t* hash_offsets, cudaStream_t st);
 struct PrefillLaunch {
     const void* q;
     const int32_t* q_offsets;

@@ -108,6 +108,13 @@ def test_write_slot_hash_reject_bad_arguments(L):
     assert h(16, 16, 2, 2000, 0, 16, 16, None) == -1
     assert h(None, 16, 2, 16, 0, 16, 16, None) == -1
     assert h(16, 16, 0, 16, 0, 16, 16, None) == 0
+    r = L.pkv_prefix_block_hash_resume
+    assert r(16, 16, 2, 0, 16, 16, 16, 16, None) == -1                  # block size
+    assert r(16, 16, -1, 16, 16, 16, 16, 16, None) == -1                # num_seqs
+    assert r(16, 16, 2, 16, None, 16, 16, 16, None) == -1               # no prev hashes
+    assert r(16, 16, 2, 16, 16, None, 16, 16, None) == -1               # no first blocks
+    assert r(16, 16, 2, 16, 16, 16, 16, None, None) == -1               # no hash offsets
+    assert r(16, 16, 0, 16, 16, 16, 16, 16, None) == 0                  # nothing to do
 
 
 def test_binding_raises_when_library_missing(monkeypatch):

@@ -316,6 +316,67 @@ def test_prefix_hash_long_sequence_and_odd_block_sizes():
         assert np.array_equal(got, ref)
 
 
+def _resume_both(tokens, offsets, B, prev, first, ho):
+    ref, _ = oracle.prefix_block_hash_resume(tokens, offsets, B, prev, first, ho)
+    torch = __import__("torch")
+    tok = to_dev(tokens if tokens.size else np.zeros(1, np.int32))
+    n = int(ho[-1])
+    out = torch.full((max(n, 1),), 0x5A5A5A5A, dtype=torch.int64, device="cuda")
+    got = pkv.prefix_block_hash_resume(tok, to_dev(offsets), B,
+                                       to_dev(np.asarray(prev, np.uint64).view(np.int64)),
+                                       to_dev(np.asarray(first, np.int64)), to_dev(ho), n, out=out)
+    g = out.cpu().numpy().view(np.uint64)
+    return g, ref, got
+
+
+@pytest.mark.parametrize("B", [16, 32, 7])
+def test_prefix_hash_resume_bit_exact(B):
+    """Resumed chains equal the oracle's bit for bit: every sequence cut at its own point
+    (none hashed, some, all, past the end, negative), the previous hash taken from the
+    full chain; a 131,072-token sequence resumed near its start (several digest chunks)
+    and at its last block (one block, the decode-step case)."""
+    rng = np.random.default_rng(41)
+    lens = [131072, 131072, 0, 5, 4097, 33, 16 * 40, 16 * 40 + 9, 3000]
+    toks = rng.integers(0, 128000, sum(lens)).astype(np.int32)
+    offs = np.zeros(len(lens) + 1, np.int64)
+    np.cumsum(lens, out=offs[1:])
+    full, fho = oracle.prefix_block_hash(toks, offs, B, 0xC0FFEE)
+    nfull = np.diff(offs) // B
+    first = np.array([3, nfull[1] - 1, 0, 0, nfull[4] // 2, nfull[5], nfull[6] + 4, -2, 1],
+                     np.int64)
+    prev = np.array([full[fho[s] + min(max(int(first[s]), 0), int(nfull[s])) - 1]
+                     if min(max(int(first[s]), 0), int(nfull[s])) > 0 else 0xC0FFEE
+                     for s in range(len(lens))], np.uint64)
+    n = np.maximum(nfull - np.clip(first, 0, None), 0)
+    ho = np.zeros(len(lens) + 1, np.int64)
+    np.cumsum(n, out=ho[1:])
+    got, ref, _ = _resume_both(toks, offs, B, prev, first, ho)
+    assert np.array_equal(got[:int(ho[-1])], ref)
+    # the resumed hashes are the full chain's suffixes
+    for s in range(len(lens)):
+        k = min(max(int(first[s]), 0), int(nfull[s]))
+        assert np.array_equal(ref[ho[s]:ho[s + 1]], full[fho[s] + k:fho[s + 1]])
+
+
+def test_prefix_hash_resume_room_limits_and_untouched_tail():
+    rng = np.random.default_rng(42)
+    B = 16
+    lens = [16 * 9, 16 * 5 + 1, 16 * 3000]
+    toks = rng.integers(0, 128000, sum(lens)).astype(np.int32)
+    offs = np.zeros(len(lens) + 1, np.int64)
+    np.cumsum(lens, out=offs[1:])
+    full, fho = oracle.prefix_block_hash(toks, offs, B, 7)
+    first = np.array([3, 0, 10], np.int64)
+    prev = np.array([full[fho[0] + 2], 7, full[fho[2] + 9]], np.uint64)
+    ho = np.array([0, 2, 12, 12 + 2500], np.int64)      # rooms 2 (needs 6), 10 (5), 2500 (2990)
+    got, ref, _ = _resume_both(toks, offs, B, prev, first, ho)
+    assert np.array_equal(got[:2], ref[:2]) and np.array_equal(got[:2], full[3:5])
+    assert np.array_equal(got[2:7], full[fho[1]:fho[2]])
+    assert np.all(got[7:12] == 0x5A5A5A5A)                # past the chain's end: untouched
+    assert np.array_equal(got[12:], full[fho[2] + 10:fho[2] + 10 + 2500])
+    assert np.array_equal(got[12:], ref[12:])
+
+
 def test_decode_workspace_reuse_and_garbage_contents():
     """One workspace shared by successive calls of different shapes, starting from
     garbage bytes: the page prefix and the partial slots are written before they are

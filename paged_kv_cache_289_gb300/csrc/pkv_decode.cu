@@ -123,7 +123,7 @@ __device__ __forceinline__ uint32_t swz64(int t, int u) {
 
 // Per-lane description of one page of a 32-page batch.
 struct PageBatch {
-    int id;        // physical block (NB = out of range sentinel)
+    int row;       // TMA row of the page's first token / BS: id * Hkv + h (id = NB past the end)
     int r, h;      // unit
     uint32_t fl;   // valid tokens | first << 8 | last << 9 | page index j << 10
     float ks, vs;  // FP8 scales
@@ -135,7 +135,7 @@ __device__ __forceinline__ void load_batch(PageBatch& b, int xbeg, int x1,
                                            const DecodeArgs& a, uint32_t& errbits) {
     const int lane = threadIdx.x & 31;
     const int x = xbeg + lane;
-    b.id = a.NB; b.r = 0; b.h = 0; b.fl = 0; b.ks = 1.f; b.vs = 1.f;
+    b.row = a.NB * a.Hkv; b.r = 0; b.h = 0; b.fl = 0; b.ks = 1.f; b.vs = 1.f;
     if (x >= x1) return;
     int lo = 0, hi = a.N;   // s_prefix[lo] <= x < s_prefix[hi]
     while (hi - lo > 1) {
@@ -153,7 +153,7 @@ __device__ __forceinline__ void load_batch(PageBatch& b, int xbeg, int x1,
         id = a.NB;   // TMA of rows past the tensor end reads zeros
     }
     const int ntok = min(BS, s_seq[r] - j * BS);
-    b.id = id;
+    b.row = id * a.Hkv + h;
     b.r = r;
     b.h = h;
     b.fl = (uint32_t)ntok | ((j == 0) ? 0x100u : 0u) | ((j == np - 1) ? 0x200u : 0u) |
@@ -281,18 +281,17 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
     int cb = 0;   // batch index held in `cur`
     const uint64_t policy = l2_policy_evict_first();
 
-    auto issue = [&](int i) {
+    // load item i (a tile) into stage s; the caller tracks s = i mod S
+    auto issue = [&](int i, int s) {
         const int pi = (C::SUB == 2) ? (i >> 1) : i;   // page of item i
         const int sub = i & (C::SUB - 1);               // tile within the page
         const int bi = pi >> 5;
         const int src = pi & 31;
-        const int id = __shfl_sync(0xffffffffu, bi == cb ? cur.id : nxt.id, src);
-        const int h = __shfl_sync(0xffffffffu, bi == cb ? cur.h : nxt.h, src);
+        const int row = __shfl_sync(0xffffffffu, bi == cb ? cur.row : nxt.row, src);
         if (lane == 0) {
-            const int s = i % S;
             const uint32_t bar = bars + 8u * s;
             const uint32_t dst = stage0 + (uint32_t)(s * C::STAGE_BYTES);
-            const int y = (id * a.Hkv + h) * BS + sub * C::TT;
+            const int y = row * BS + sub * C::TT;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
             if constexpr (C::I4) {
@@ -314,7 +313,7 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 
     const int total = count * C::SUB;   // pipeline items (tiles)
     const int npro = min(S, total);
-    for (int i = 0; i < npro; ++i) issue(i);
+    for (int i = 0; i < npro; ++i) issue(i, i);
 
     const int g = lane >> 2;   // mma row group: head column of B / token row of A
     const int c = lane & 3;
@@ -333,6 +332,8 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
     int seg_r = 0, seg_h = 0;
     int seg_qb = 0, seg_qlen = 1, seg_vis = 0;   // query rows; query qi sees positions <= seg_vis + qi
 
+    int s = 0;           // stage of item i (i mod S), kept by increment
+    uint32_t par = 0;    // phase of that stage's barrier ((i / S) & 1)
     for (int i = 0; i < total; ++i) {
         const int pi = (C::SUB == 2) ? (i >> 1) : i;
         const int sub = i & (C::SUB - 1);
@@ -342,8 +343,6 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
             load_batch<BS, FP8>(nxt, x0 + (cb + 1) * 32, x1, s_prefix, s_seq, a, errbits);
         }
         const int src = pi & 31;
-        const int r = __shfl_sync(0xffffffffu, cur.r, src);
-        const int h = __shfl_sync(0xffffffffu, cur.h, src);
         const uint32_t fl = __shfl_sync(0xffffffffu, cur.fl, src);
         float ks = 1.f, vs = 1.f;
         if (FP8) {
@@ -358,6 +357,8 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 
         // ---- segment start: load the GQA group's queries as mma B fragments ----
         if (i == 0 || first) {
+            const int r = __shfl_sync(0xffffffffu, cur.r, src);
+            const int h = __shfl_sync(0xffffffffu, cur.h, src);
             seg_full = first;
             seg_r = r;
             seg_h = h;
@@ -510,8 +511,6 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         }
 
         // ---- wait for the tile ----
-        const int s = i % S;
-        const uint32_t par = (uint32_t)((i / S) & 1);
         bool ok = mbar_wait_bounded(bars + 8u * s, par, kWaitLimitNs);
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) {
@@ -949,7 +948,11 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         // zero fill) before the async-proxy refill lane 0 is about to issue
         fence_proxy_async_smem();
         __syncwarp();
-        if (i + S < total) issue(i + S);
+        if (i + S < total) issue(i + S, s);   // item i + S reuses stage s
+        if (++s == S) {
+            s = 0;
+            par ^= 1u;
+        }
     }
     if (errbits) atomicOr(a.err, errbits);
 }

@@ -319,13 +319,14 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
     const int c = lane & 3;
 
     float o[C::DT][QT][4];
-    float ot[FP8 ? C::DT : 1][QT][4];
     uint32_t qf[QSMEM ? 1 : C::KS][QT][2];
     float m0[QT], m1[QT], l0[QT], l1[QT];   // heads 2c, 2c+1 of this lane, per query
-    // int8 / int4 pages: the codes enter the mma with an offset (1024 + code + 128;
-    // 1024 + n or 1024 + 16 n with n = code + 8); cq = the scores' constant part per head
-    // (q . offsets), cr = sum over pages of v_scale * sum(P), which times 1152, 1032 or 72
-    // is the output's constant part
+    // int8 / int4 pages: K codes enter the mma with an offset (1024 + code + 128;
+    // 1024 + n or 1024 + 16 n with n = code + 8), and cq = the scores' constant part per
+    // head (q . offsets).  V codes enter as fp16 subnormals ((code + 128) 2^-24; n 2^-24
+    // or 16 n 2^-24) against P * v_scale, so O accumulates across pages, and cr = the
+    // sum over pages of sum(P * v_scale), which times 128 (int8) or 8 (int4) is the
+    // output's constant part once O is scaled back by 2^24 (int4 odd picks: 2^20)
     float cq0[QT], cq1[QT], cr0[QT], cr1[QT];
     float qscale = a.scale_log2;
     bool seg_full = false;
@@ -727,8 +728,9 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                     pb[mt][qi][0] = movmatrix_trans(pack_bf16x2(p0, p1));
                     pb[mt][qi][1] = movmatrix_trans(pack_bf16x2(p2, p3));
                 } else {
-                    pb[mt][qi][0] = movmatrix_trans(pack_f16x2(p0, p1));
-                    pb[mt][qi][1] = movmatrix_trans(pack_f16x2(p2, p3));
+                    // quantised pages: P carries the page's V scale into the mma
+                    pb[mt][qi][0] = movmatrix_trans(pack_f16x2(p0 * vs, p1 * vs));
+                    pb[mt][qi][1] = movmatrix_trans(pack_f16x2(p2 * vs, p3 * vs));
                 }
             }
             l0[qi] += ps0;
@@ -750,12 +752,7 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                 }
             }
         } else {
-#pragma unroll
-            for (int dt = 0; dt < C::DT; ++dt)
-#pragma unroll
-                for (int qi = 0; qi < QT; ++qi)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) ot[dt][qi][e] = 0.f;
+            // P already holds P * v_scale (fp16), so every page accumulates into O
             if constexpr (C::I4) {
                 // the K-path matrices, transposed per 8x8 b16 block by the load: a lane holds
                 // tokens 2c, 2c+1 of b16 unit g (d = 64 dblk + 4g + 0..3), and nibble pair
@@ -772,18 +769,18 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         ldsm_x4_trans(vpg + swz64(tr, dblk * 2 + (lane >> 4)), m0, m1, m2, m3);
 #pragma unroll
                         for (int qi = 0; qi < QT; ++qi) {
-                            mma_f16(ot[dblk * 4][qi], i4pick_raw<0>(m0), i4pick_raw<0>(m2),
-                                    i4pick_raw<0>(m1), i4pick_raw<0>(m3),
+                            mma_f16(o[dblk * 4][qi], i4pick_sub<0>(m0), i4pick_sub<0>(m2),
+                                    i4pick_sub<0>(m1), i4pick_sub<0>(m3),
                                     pb[mt][qi][0], pb[mt][qi][1]);
-                            mma_f16(ot[dblk * 4 + 1][qi], i4pick_raw<1>(m0),
-                                    i4pick_raw<1>(m2), i4pick_raw<1>(m1),
-                                    i4pick_raw<1>(m3), pb[mt][qi][0], pb[mt][qi][1]);
-                            mma_f16(ot[dblk * 4 + 2][qi], i4pick_raw<2>(m0),
-                                    i4pick_raw<2>(m2), i4pick_raw<2>(m1),
-                                    i4pick_raw<2>(m3), pb[mt][qi][0], pb[mt][qi][1]);
-                            mma_f16(ot[dblk * 4 + 3][qi], i4pick_raw<3>(m0),
-                                    i4pick_raw<3>(m2), i4pick_raw<3>(m1),
-                                    i4pick_raw<3>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(o[dblk * 4 + 1][qi], i4pick_sub<1>(m0),
+                                    i4pick_sub<1>(m2), i4pick_sub<1>(m1),
+                                    i4pick_sub<1>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(o[dblk * 4 + 2][qi], i4pick_sub<2>(m0),
+                                    i4pick_sub<2>(m2), i4pick_sub<2>(m1),
+                                    i4pick_sub<2>(m3), pb[mt][qi][0], pb[mt][qi][1]);
+                            mma_f16(o[dblk * 4 + 3][qi], i4pick_sub<3>(m0),
+                                    i4pick_sub<3>(m2), i4pick_sub<3>(m1),
+                                    i4pick_sub<3>(m3), pb[mt][qi][0], pb[mt][qi][1]);
                         }
                     }
                 }
@@ -804,10 +801,10 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         if constexpr (KT == 2) {
                             // int8: the token regroup and the widening are one permute
                             const uint32_t xs = x ^ 0x80808080u, ys = y ^ 0x80808080u;
-                            v0 = i8pick_raw<0x5240>(xs);
-                            v1 = i8pick_raw<0x5341>(xs);
-                            v2 = i8pick_raw<0x5240>(ys);
-                            v3 = i8pick_raw<0x5341>(ys);
+                            v0 = i8pick_sub<0x5240>(xs);
+                            v1 = i8pick_sub<0x5341>(xs);
+                            v2 = i8pick_sub<0x5240>(ys);
+                            v3 = i8pick_sub<0x5341>(ys);
                         } else {
                             v0 = b8x2_to_f16x2<KT>(__byte_perm(x, 0u, 0x0020));
                             v1 = b8x2_to_f16x2<KT>(__byte_perm(x, 0u, 0x0031));
@@ -816,16 +813,16 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                         }
 #pragma unroll
                         for (int qi = 0; qi < QT; ++qi)
-                            mma_f16(ot[2 * dp + half][qi], v0, v1, v2, v3, pb[mt][qi][0],
+                            mma_f16(o[2 * dp + half][qi], v0, v1, v2, v3, pb[mt][qi][0],
                                     pb[mt][qi][1]);
                     }
                 }
             }
             }
             if constexpr (C::FOLD) {
-                // sum(P) per head as the mma sees it (fp16 P against a tile of ones): the
-                // offset part of this page's P.V is that times 1032 (int4, even picks) or
-                // 1152 (int4 odd picks, int8)
+                // sum(P * v_scale) per head as the mma sees it (fp16 against a tile of
+                // ones): the offset part of this page's P.V is that times 128 (int8) or 8
+                // (int4), in units of 2^-24
 #pragma unroll
                 for (int qi = 0; qi < QT; ++qi) {
                     float psum[4] = {0.f, 0.f, 0.f, 0.f};
@@ -833,19 +830,10 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                     for (int mt = 0; mt < C::MT; ++mt)
                         mma_f16(psum, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u,
                                 pb[mt][qi][0], pb[mt][qi][1]);
-                    cr0[qi] = fmaf(vs, psum[0], cr0[qi]);
-                    cr1[qi] = fmaf(vs, psum[1], cr1[qi]);
+                    cr0[qi] += psum[0];
+                    cr1[qi] += psum[1];
                 }
             }
-            // int4: odd picks accumulated 16 n, so their page scale carries the 1/16
-            const float vs16 = vs * 0.0625f;
-#pragma unroll
-            for (int dt = 0; dt < C::DT; ++dt)
-#pragma unroll
-                for (int qi = 0; qi < QT; ++qi)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        o[dt][qi][e] = fmaf((C::I4 && (dt & 1)) ? vs16 : vs, ot[dt][qi][e], o[dt][qi][e]);
         }
 
         // ---- segment end ----
@@ -858,15 +846,16 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
             for (int qi = 0; qi < QT; ++qi) {
                 if (qi >= seg_qlen) break;
                 if constexpr (C::FOLD) {
-                    // remove the offsets' share: per unit of cr, 1152 (int8), 1032 (int4
-                    // even picks) or 1152 / 16 = 72 (int4 odd picks)
+                    // back from subnormal units (2^24; int4 odd picks held 16 n: 2^20),
+                    // then remove the offsets' share: 128 (int8) or 8 (int4) per unit of cr
+                    const float k = C::I4 ? 8.f : 128.f;
 #pragma unroll
                     for (int dt = 0; dt < C::DT; ++dt) {
-                        const float k = !C::I4 ? 1152.f : ((dt & 1) ? 72.f : 1032.f);
-                        o[dt][qi][0] = fmaf(-k, cr0[qi], o[dt][qi][0]);
-                        o[dt][qi][2] = fmaf(-k, cr0[qi], o[dt][qi][2]);
-                        o[dt][qi][1] = fmaf(-k, cr1[qi], o[dt][qi][1]);
-                        o[dt][qi][3] = fmaf(-k, cr1[qi], o[dt][qi][3]);
+                        const float u = (C::I4 && (dt & 1)) ? 1048576.f : 16777216.f;
+                        o[dt][qi][0] = fmaf(o[dt][qi][0], u, -k * cr0[qi]);
+                        o[dt][qi][2] = fmaf(o[dt][qi][2], u, -k * cr0[qi]);
+                        o[dt][qi][1] = fmaf(o[dt][qi][1], u, -k * cr1[qi]);
+                        o[dt][qi][3] = fmaf(o[dt][qi][3], u, -k * cr1[qi]);
                     }
                 }
                 float L0 = l0[qi], L1 = l1[qi];

@@ -317,6 +317,24 @@ __device__ __forceinline__ uint32_t i4pick_raw(uint32_t x) {
     return ((I & 1) ? (w & 0x00F000F0u) : (w & 0x000F000Fu)) | 0x64006400u;
 }
 
+// The same picks as fp16 subnormals: the nibble (I even) or 16 x the nibble (I odd) is
+// the whole mantissa under a zero exponent, so each half is n * 2^-24 or 16 n * 2^-24
+// exactly, with no 1024 offset.  A sum over many of them keeps only the small offset of
+// the offset-binary code (8 per unit of the weights), so it can run across pages in one
+// fp32 accumulator without a large constant to cancel at the end.
+template <int I>
+__device__ __forceinline__ uint32_t i4pick_sub(uint32_t x) {
+    const uint32_t w = (I >= 2) ? (x >> 8) : x;
+    return (I & 1) ? (w & 0x00F000F0u) : (w & 0x000F000Fu);
+}
+
+// Two sign-flipped int8 codes (byte = code + 128) picked by SEL as fp16 subnormals:
+// (code + 128) * 2^-24 per half, the high byte of each half zero.
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t i8pick_sub(uint32_t xs) {
+    return __byte_perm(xs, 0u, SEL);
+}
+
 // Two 8-bit cache codes -> fp16x2 for page kind KT (1 = E4M3, 2 = int8).
 template <int KT>
 __device__ __forceinline__ uint32_t b8x2_to_f16x2(uint32_t x) {

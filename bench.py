@@ -2,17 +2,20 @@
 """Benchmark of the paged-KV decode step (libpagedkv on GB300).
 
 One step = the whole hot path over one batch: slot mapping of each request's new
-token, KV cache write, paged GQA decode attention (one kernel; split units are merged
-inside it), and the chained prefix block hash of every request's tokens (on a side
-stream).
+token, KV cache write, paged GQA decode attention (the decode kernel, then a merge
+kernel for requests split across warps), and the chained prefix block hash of every
+request's tokens (on a side stream).
 
 Workload: the Llama-3.3-70B-shaped decode layer -- batch 64, 64 query / 8 KV heads,
 head_dim 128, bf16, 16-token blocks, lengths U[1024, 8192], blocks randomly permuted
 in a pool 10% larger than needed.  Pages (~1.33 GB) exceed the 129 MB L2, so no flush
 is needed between steps.
 
-Prints ONE JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle instead,
-on bounded samples of the same workload.
+Prints ONE JSON line (rank 0).  With the default workload, the line also carries
+`per_workload`: decode-launch rooflines of workloads 3 (long context), 5 (E4M3 pages)
+and 4 (prefix sharing, logical and unique bytes, with and without an L2 flush), and
+workload 3's step with the full and the resumed prefix hash.  `--impl reference` times
+the fp64 CPU oracle instead, on bounded samples of the same workload.
 """
 from __future__ import annotations
 
@@ -46,6 +49,11 @@ def parse():
     p.add_argument("--workload", type=int, default=2, help="workload id (2 = the metric's)")
     p.add_argument("--skip-e2e", action="store_true")
     p.add_argument("--skip-cpu", action="store_true")
+    p.add_argument("--skip-per-workload", action="store_true",
+                   help="leave out the decode figures of workloads 3, 4 and 5 (workload 2 runs)")
+    p.add_argument("--hash", choices=["full", "resume"], default="full",
+                   help="full: the step re-hashes every token; resume: only the blocks the "
+                        "step completes (pkv_prefix_block_hash_resume)")
     p.add_argument("--seed", type=int, default=None)
     p.add_argument("--batch", type=int, default=None,
                    help="fewer requests of the same shapes (profiling captures only)")
@@ -277,10 +285,13 @@ def time_oracle(wl, sample, units):
     return dt, nbytes
 
 
-def cpu_baseline(wl, dd, budget_s=15.0):
+def cpu_baseline(wl, H, budget_s=15.0, single_budget_s=4.0):
     """The oracle timed on the host cores: the whole decode step of the first 16 requests
-    (all their units), repeated until about `budget_s` seconds of CPU work."""
+    (all their units), repeated until about `budget_s` seconds of CPU work; then the
+    same sample on one thread for about `single_budget_s` seconds."""
     import oracle
+    dd = {"q": H.inputs["q"], "k_cache": H.kc, "v_cache": H.vc, "k_scale": H.ks,
+          "v_scale": H.vs}
     reqs = list(range(min(wl.N, 16)))
     sample = oracle_sample(wl, dd, reqs)
     units = [(i, h) for i in range(len(reqs)) for h in range(wl.Hkv)]
@@ -291,11 +302,261 @@ def cpu_baseline(wl, dd, budget_s=15.0):
         dt, nb = time_oracle(wl, sample, units)
         tot_t += dt
         tot_b += nb
-    return {"value": round(tot_b / tot_t / 1e9, 4), "unit": UNIT, "cores": oracle.num_threads(),
+    cores = oracle.num_threads()
+    # one thread: whole units of request 0 until the budget is spent
+    oracle.set_num_threads(1)
+    try:
+        st, sb, n1 = 0.0, 0, 0
+        while st < single_budget_s:
+            dt, nb = time_oracle(wl, sample, units[:wl.Hkv])
+            st += dt
+            sb += nb
+            n1 += 1
+    finally:
+        oracle.set_num_threads(cores)
+    return {"value": round(tot_b / tot_t / 1e9, 4), "unit": UNIT, "cores": cores,
             "kind": "oracle",
             "sample": f"{reps} passes over all {len(units)} (request, kv head) units x {wl.G} query "
                       f"heads of requests 0..{len(reqs)-1} of {wl.name} ({tot_b/1e9:.1f} GB of K/V "
-                      f"in {tot_t:.1f} s); fp64 C + OpenMP"}
+                      f"in {tot_t:.1f} s); fp64 C + OpenMP",
+            "single_thread": {"value": round(sb / st / 1e9, 4), "unit": UNIT, "cores": 1,
+                              "sample": f"{n1} passes over the {wl.Hkv} units of request 0 "
+                                        f"({sb/1e9:.2f} GB in {st:.1f} s)"}}
+
+
+def l2_flush_buffer(torch, dev):
+    """A buffer twice the 129 MB L2, read between launches to evict their pages.  It is
+    written once here; reading it (rather than writing it every time) leaves no dirty
+    lines in L2 for the timed launch to write back."""
+    return torch.ones(2 * 129 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
+
+
+def median_of(ts):
+    return statistics.median(ts) if ts else float("nan")
+
+
+class StepHarness:
+    """Device buffers and the launch sequence of one decode step of a workload.
+
+    A step is slot mapping -> KV write -> decode (+ its merge kernel) on the main
+    stream and the prefix block hash on a side stream.  `hash_mode` "full" re-hashes
+    every request's whole token history (the chain from h_0); "resume" continues
+    each chain from the hash of its last block that was full before this step
+    (pkv_prefix_block_hash_resume), so only the blocks completed by the step's new
+    tokens are read."""
+
+    def __init__(self, wl, dev, hash_mode="full"):
+        import torch
+        import paged_kv_cache_289_gb300 as pkv
+        from paged_kv_cache_289_gb300 import workloads as W
+        self.wl, self.dev, self.hash_mode = wl, dev, hash_mode
+        self.torch, self.pkv = torch, pkv
+        dd = W.device_data(wl, dev)
+        bt = torch.from_numpy(wl.block_table).to(dev)
+        sl = torch.from_numpy(wl.seq_lens).to(dev)
+        req_new, pos_new = wl.new_token_rows()      # the step's new tokens (q_len per request)
+        if wl.quant:
+            kc = torch.zeros(wl.cache_shape, dtype=torch.int8 if wl.int8 else torch.uint8,
+                             device=dev)
+            vc = torch.zeros_like(kc)
+            req_all, pos_all = W.token_rows_order(wl)
+            sm_all = pkv.compute_slot_mapping(bt, torch.from_numpy(pos_all).to(dev), wl.BS,
+                                              req_idx=torch.from_numpy(req_all).to(dev))
+            pkv.kv_cache_write(dd["k_rows"], dd["v_rows"], sm_all, kc, vc, dd["k_scale"],
+                               dd["v_scale"])
+            del dd["k_rows"], dd["v_rows"], sm_all
+            self.ks, self.vs = dd["k_scale"], dd["v_scale"]
+        else:
+            kc, vc = dd["k_cache"], dd["v_cache"]
+            self.ks = self.vs = None
+        self.kc, self.vc = kc, vc
+        B = wl.hash_block
+        lens = np.diff(wl.token_offsets)
+        tokens = torch.from_numpy(wl.tokens).to(dev)
+        toffs = torch.from_numpy(wl.token_offsets).to(dev)
+        full = lens // B
+        if hash_mode == "full":
+            per_seq = full
+        else:
+            # blocks that were full before this step's q_len new tokens
+            self.first_np = np.maximum(lens - wl.q_len, 0) // B
+            per_seq = full - self.first_np
+        ho_np = np.zeros(wl.N + 1, np.int64)
+        np.cumsum(per_seq, out=ho_np[1:])
+        self.nh = int(ho_np[-1])
+        hoffs = torch.from_numpy(ho_np).to(dev)
+        self.inputs = {"q": dd["q"], "k_new": dd["k_new"], "v_new": dd["v_new"],
+                       "pos": torch.from_numpy(pos_new).to(dev),
+                       "req": torch.from_numpy(req_new).to(dev),
+                       "qoffs": torch.from_numpy(wl.q_offsets()).to(dev), "bt": bt, "sl": sl,
+                       "tokens": tokens, "toffs": toffs, "hoffs": hoffs}
+        if hash_mode == "resume":
+            # h_k of every sequence, carried over from the previous step in a serving
+            # loop; here taken once from the full chain
+            fho = np.zeros(wl.N + 1, np.int64)
+            np.cumsum(full, out=fho[1:])
+            chain = pkv.prefix_block_hash(tokens, toffs, B, torch.from_numpy(fho).to(dev),
+                                          int(fho[-1]), seed=0).cpu().numpy().view(np.uint64)
+            prev = np.array([chain[fho[s] + self.first_np[s] - 1] if self.first_np[s] > 0 else 0
+                             for s in range(wl.N)], np.uint64)
+            self.inputs["prev_hashes"] = torch.from_numpy(prev.view(np.int64)).to(dev)
+            self.inputs["first_blocks"] = torch.from_numpy(self.first_np.astype(np.int64)).to(dev)
+        self.outputs = {"out": torch.empty_like(dd["q"]),
+                        "hashes": torch.empty(max(self.nh, 1), dtype=torch.int64, device=dev)}
+        self.slots = torch.empty(wl.N * wl.q_len, dtype=torch.int64, device=dev)
+        self.ws = torch.zeros(pkv.multiquery_workspace_size(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS,
+                                                            wl.kv_kind, wl.q_len),
+                              dtype=torch.uint8, device=dev)
+        self.main = torch.cuda.current_stream(dev)
+        self.side = torch.cuda.Stream(dev)
+        self.launches_per_step = 5   # slot map, write, decode, wide-split merge, hash
+
+    def decode(self, I, O, stream):
+        wl, pkv = self.wl, self.pkv
+        if wl.q_len == 1:
+            pkv.paged_decode_attn(I["q"], self.kc, self.vc, I["bt"], I["sl"], wl.scale,
+                                  out=O["out"], k_scale=self.ks, v_scale=self.vs,
+                                  workspace=self.ws, stream=stream)
+        else:
+            pkv.paged_multiquery_attn(I["q"], I["qoffs"], wl.q_len, self.kc, self.vc, I["bt"],
+                                      I["sl"], wl.scale, out=O["out"], k_scale=self.ks,
+                                      v_scale=self.vs, workspace=self.ws, stream=stream)
+
+    def step(self, I, O, dec_ev=None):
+        """One decode step on the per-step inputs I, writing the results O.
+
+        The prefix hash reads only the step's tokens, so it starts first, on the side
+        stream, and runs beside the main-stream chain (slot mapping -> write -> decode ->
+        merge).  Started after the KV write instead, it lands on SMs that the decode grid
+        already fills and stretches the decode's tail (measured: +17 us per step)."""
+        wl, pkv, main, side = self.wl, self.pkv, self.main, self.side
+        side.wait_stream(main)                   # the step's inputs are in place
+        if self.hash_mode == "full":
+            pkv.prefix_block_hash(I["tokens"], I["toffs"], wl.hash_block, I["hoffs"], self.nh,
+                                  seed=0, out=O["hashes"], stream=side)
+        else:
+            pkv.prefix_block_hash_resume(I["tokens"], I["toffs"], wl.hash_block,
+                                         I["prev_hashes"], I["first_blocks"], I["hoffs"],
+                                         self.nh, out=O["hashes"], stream=side)
+        pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, req_idx=I["req"], out=self.slots,
+                                 stream=main)
+        pkv.kv_cache_write(I["k_new"], I["v_new"], self.slots, self.kc, self.vc, self.ks,
+                           self.vs, stream=main)
+        if dec_ev is not None:
+            dec_ev[0].record(main)
+        self.decode(I, O, main)
+        if dec_ev is not None:
+            dec_ev[1].record(main)
+        main.wait_stream(side)
+
+    def time_steps(self, K, warmup):
+        """Device time of K steps (seconds), after `warmup` untimed steps."""
+        torch = self.torch
+        for _ in range(max(warmup, 3)):
+            self.step(self.inputs, self.outputs)
+        torch.cuda.synchronize(self.dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(self.main)
+        for _ in range(K):
+            self.step(self.inputs, self.outputs)
+        e1.record(self.main)
+        torch.cuda.synchronize(self.dev)
+        return e0.elapsed_time(e1) / 1e3
+
+    def time_decode_launches(self, n=50, warmup=10, flush=None):
+        """Per-launch device times (seconds) of the decode call alone: `warmup` untimed
+        launches, then n launches each bracketed by events; `flush` (a buffer larger
+        than L2) is read through before every timed launch."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.decode(self.inputs, self.outputs, self.main)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        torch.cuda.synchronize(self.dev)
+        for i in range(n):
+            if flush is not None:
+                flush.sum()
+            ev[i][0].record(self.main)
+            self.decode(self.inputs, self.outputs, self.main)
+            ev[i][1].record(self.main)
+        torch.cuda.synchronize(self.dev)
+        return [a.elapsed_time(b) / 1e3 for a, b in ev]
+
+
+def per_workload_figures(dev, peak, main_harness=None):
+    """Decode-launch rooflines measured in the same run: the headline workload (2), long
+    contexts (3) and E4M3 pages (5) with an L2 flush between launches; prefix sharing
+    (4) on logical and on unique bytes, with and without the flush; and workload 3's
+    whole step with the full and the resumed prefix hash.  Each launch figure is the
+    median of 50 after 10 warm-ups."""
+    import torch
+    import paged_kv_cache_289_gb300 as pkv
+    from paged_kv_cache_289_gb300 import workloads as W
+    flush = l2_flush_buffer(torch, dev)
+    res = {}
+    sampler = ClockSampler(dev.index or 0)
+    sampler.start()
+    for cfg in (2, 3, 5, 4):
+        if cfg == 2 and main_harness is None:
+            continue
+        wl = main_harness.wl if cfg == 2 else W.make(cfg)
+        h = main_harness if cfg == 2 else StepHarness(wl, dev, "full")
+        alg = decode_algorithmic_bytes(wl)
+        entry = {"workload": wl.name, "batch": wl.N, "kv_dtype": ["bf16", "fp8_e4m3", "int8",
+                                                                  "int4"][wl.kv_kind],
+                 "algorithmic_bytes_per_launch": alg}
+        ts = h.time_decode_launches(flush=flush)
+        med, mean = median_of(ts), sum(ts) / len(ts)
+        entry.update({"median_launch_ms": round(med * 1e3, 4), "avg_launch_ms": round(mean * 1e3, 4),
+                      "achieved": round(alg / med / 1e9, 1), "frac": round(alg / med / 1e9 / peak, 4),
+                      "query_tokens_per_s": round(wl.N * wl.q_len / med, 1),
+                      "l2": "flushed (a 258 MB buffer read) before every timed launch"})
+        assert pkv.read_device_error(h.ws) == 0, "device error word set"
+        if cfg == 4:
+            uniq = wl.unique_kv_read_bytes()
+            logical = wl.kv_read_bytes()
+            ts_nf = h.time_decode_launches(flush=None)
+            med_nf = median_of(ts_nf)
+            entry.update({
+                "logical_kv_bytes": logical, "unique_kv_bytes": uniq,
+                "flushed": {"median_launch_ms": round(med * 1e3, 4),
+                            "logical_gbs": round(logical / med / 1e9, 1),
+                            "unique_gbs": round(uniq / med / 1e9, 1),
+                            "unique_frac": round(uniq / med / 1e9 / peak, 4)},
+                "no_flush": {"median_launch_ms": round(med_nf * 1e3, 4),
+                             "logical_gbs": round(logical / med_nf / 1e9, 1),
+                             "unique_gbs": round(uniq / med_nf / 1e9, 1),
+                             "unique_frac": round(uniq / med_nf / 1e9 / peak, 4)},
+                "note": "the shared 4096-token prefix (16 MB of pages) is read by every "
+                        "request; logical bytes count it per request, unique bytes once"})
+        if cfg == 3:
+            K = 50
+            t_full = h.time_steps(K, 10)
+            h = None                             # free its pages before the second harness
+            torch.cuda.empty_cache()
+            hr = StepHarness(wl, dev, "resume")
+            t_res = hr.time_steps(K, 10)
+            kvb = wl.kv_read_bytes()
+            entry["step"] = {
+                "full_hash": {"ms_per_step": round(t_full / K * 1e3, 4),
+                              "kv_gbs": round(kvb * K / t_full / 1e9, 1),
+                              "hashed_blocks_per_step": int(sum(np.diff(wl.token_offsets)
+                                                                // wl.hash_block))},
+                "resumed_hash": {"ms_per_step": round(t_res / K * 1e3, 4),
+                                 "kv_gbs": round(kvb * K / t_res / 1e9, 1),
+                                 "hashed_blocks_per_step": hr.nh},
+                "steps": K,
+                "what": "slot mapping + KV write + decode + prefix hash; full re-hashes "
+                        "every token of every request, resumed hashes only the blocks the "
+                        "step's new token completed (pkv_prefix_block_hash_resume)"}
+            del hr
+        res[str(cfg)] = entry
+        del h
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    res["clocks"] = sampler.stop()
+    return res
 
 
 # ------------------------------------------------------------------ our arm
@@ -314,79 +575,15 @@ def run_ours(args):
 
     wl = W.make(args.workload, seed=(args.seed if args.seed is not None else args.workload) + rank,
                 batch=args.batch)
-    dd = W.device_data(wl, dev)
-    quant = wl.quant                      # 8-bit pages (E4M3 or int8) with scales
-    dt_code = wl.kv_kind
-    bt = torch.from_numpy(wl.block_table).to(dev)
-    sl = torch.from_numpy(wl.seq_lens).to(dev)
-    req_new, pos_new = wl.new_token_rows()      # the step's new tokens (q_len per request)
-    pos = torch.from_numpy(pos_new).to(dev)
-    req = torch.from_numpy(req_new).to(dev)
-    qoffs = torch.from_numpy(wl.q_offsets()).to(dev)
-    if quant:
-        kc = torch.zeros(wl.cache_shape, dtype=torch.int8 if wl.int8 else torch.uint8, device=dev)
-        vc = torch.zeros_like(kc)
-        req_all, pos_all = W.token_rows_order(wl)
-        sm_all = pkv.compute_slot_mapping(bt, torch.from_numpy(pos_all).to(dev), wl.BS,
-                                          req_idx=torch.from_numpy(req_all).to(dev))
-        pkv.kv_cache_write(dd["k_rows"], dd["v_rows"], sm_all, kc, vc, dd["k_scale"], dd["v_scale"])
-        del dd["k_rows"], dd["v_rows"], sm_all
-        dd["k_cache"], dd["v_cache"] = kc, vc
-        ks, vs = dd["k_scale"], dd["v_scale"]
-    else:
-        kc, vc, ks, vs = dd["k_cache"], dd["v_cache"], None, None
-    tokens = torch.from_numpy(wl.tokens).to(dev)
-    toffs = torch.from_numpy(wl.token_offsets).to(dev)
-    lens = np.diff(wl.token_offsets)
-    ho_np = np.zeros(wl.N + 1, np.int64)
-    np.cumsum(lens // wl.hash_block, out=ho_np[1:])
-    hoffs = torch.from_numpy(ho_np).to(dev)
-    nh = int(ho_np[-1])
-    hashes = torch.empty(max(nh, 1), dtype=torch.int64, device=dev)
-    out = torch.empty_like(dd["q"])
-    slots = torch.empty(wl.N * wl.q_len, dtype=torch.int64, device=dev)
-    ws = torch.zeros(pkv.multiquery_workspace_size(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, dt_code,
-                                                   wl.q_len), dtype=torch.uint8, device=dev)
-    main = torch.cuda.current_stream(dev)
-    side = torch.cuda.Stream(dev)
-    launches_per_step = 5   # slot map, write, decode, wide-split merge, hash
-
-    def step(I, O, dec_ev=None):
-        """One decode step on the per-step inputs I, writing the results O.
-
-        The prefix hash reads only the step's tokens, so it starts first, on the side
-        stream, and runs beside the main-stream chain (slot mapping -> write -> decode ->
-        merge).  Started after the KV write instead, it lands on SMs that the decode grid
-        already fills and stretches the decode's tail (measured: +17 us per step)."""
-        side.wait_stream(main)                   # the step's inputs are in place
-        pkv.prefix_block_hash(I["tokens"], I["toffs"], wl.hash_block, I["hoffs"], nh, seed=0,
-                              out=O["hashes"], stream=side)
-        pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, req_idx=I["req"], out=slots,
-                                 stream=main)
-        pkv.kv_cache_write(I["k_new"], I["v_new"], slots, kc, vc, ks, vs, stream=main)
-        if dec_ev is not None:
-            dec_ev[0].record(main)
-        if wl.q_len == 1:
-            pkv.paged_decode_attn(I["q"], kc, vc, I["bt"], I["sl"], wl.scale, out=O["out"],
-                                  k_scale=ks, v_scale=vs, workspace=ws, stream=main)
-        else:
-            pkv.paged_multiquery_attn(I["q"], I["qoffs"], wl.q_len, kc, vc, I["bt"], I["sl"],
-                                      wl.scale, out=O["out"], k_scale=ks, v_scale=vs,
-                                      workspace=ws, stream=main)
-        if dec_ev is not None:
-            dec_ev[1].record(main)
-        main.wait_stream(side)
-
-    q, k_new, v_new = dd["q"], dd["k_new"], dd["v_new"]
-    inputs = {"q": q, "k_new": k_new, "v_new": v_new, "pos": pos, "req": req, "qoffs": qoffs,
-              "bt": bt, "sl": sl,
-              "tokens": tokens, "toffs": toffs, "hoffs": hoffs}
-    outputs = {"out": out, "hashes": hashes}
+    H = StepHarness(wl, dev, args.hash)
+    quant = wl.quant
+    main = H.main
+    inputs, outputs = H.inputs, H.outputs
+    step = H.step
     for _ in range(max(args.warmup, 3)):
         step(inputs, outputs)
     torch.cuda.synchronize(dev)
     if world > 1:
-        import torch.distributed as dist
         dist.barrier()
 
     # ---------------- device-timed region: exactly K steps
@@ -411,7 +608,8 @@ def run_ours(args):
     t_total = e0.elapsed_time(e1) / 1e3
     dec_times = [a.elapsed_time(b) / 1e3 for a, b in dec_events]
     dec_avg = sum(dec_times) / len(dec_times)
-    assert pkv.read_device_error(ws) == 0, "device error word set during the benchmark"
+    dec_med = median_of(dec_times)
+    assert pkv.read_device_error(H.ws) == 0, "device error word set during the benchmark"
 
     t_max = aggregate_max(t_total, world, dev)
     kv_bytes = wl.kv_read_bytes()
@@ -430,7 +628,11 @@ def run_ours(args):
                 "peak_source": f"{peak_kind} hbm_gbs (copy, read+write bytes)",
                 "kernel": "pkv_paged_decode_attn (pkv_decode_kernel)",
                 "algorithmic_bytes_per_launch": alg,
-                "avg_launch_ms": round(dec_avg * 1e3, 4)}
+                "avg_launch_ms": round(dec_avg * 1e3, 4),
+                "median_launch_ms": round(dec_med * 1e3, 4),
+                "note": "per-launch events inside the timed steps; an event between the KV "
+                        "write and the decode stops the decode's programmatic early launch, "
+                        "so the launch time includes that start-up (about 6 us)"}
 
     # ---------------- end to end through the public API with pinned host buffers
     e2e = None
@@ -507,9 +709,14 @@ def run_ours(args):
                "copies": "one packed H2D and one D2H per step on their own streams, "
                          "double-buffered (upload of step k+1 overlaps step k)"}
 
+    per_wl = None
+    if rank == 0 and world == 1 and not args.skip_per_workload and args.workload == 2 \
+            and args.batch is None:
+        per_wl = per_workload_figures(dev, peak, H)
+
     cpu = None
     if rank == 0 and world == 1 and not args.skip_cpu:
-        cpu = cpu_baseline(wl, dd)
+        cpu = cpu_baseline(wl, H)
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -518,12 +725,13 @@ def run_ours(args):
                 "dtype": ("bf16" if not quant else
                           ["", "fp8_e4m3", "int8", "int4"][wl.kv_kind] + " KV, bf16 q/out, fp32 accumulate"),
                 "data": "synthetic (seeded N(0,1) q/K/V, uniform token ids)",
-                "config": dict(workload_config(wl),
+                "config": dict(workload_config(wl), hash=args.hash,
                                parallelism=f"{world} independent replicas (no collective)"),
                 "query_tokens_per_s": round(total_q / t_max, 1),
                 "pct_of_hbm_peak": round(100 * value / peak, 2),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": launches_per_step * K, "clocks": clocks}
+                "gpu_launches": H.launches_per_step * K, "clocks": clocks,
+                "per_workload": per_wl}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()

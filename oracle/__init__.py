@@ -111,6 +111,8 @@ def lib():
                                               _i, _i, _i, _d, _p, _i64, _p]
             L.orc_num_threads.restype = _i
             L.orc_num_threads.argtypes = []
+            L.orc_set_num_threads.restype = None
+            L.orc_set_num_threads.argtypes = [_i]
             L.orc_fnv1a64.restype = _u64
             L.orc_fnv1a64.argtypes = [_p, _i64]
             L.orc_fmix64.restype = _u64
@@ -168,6 +170,11 @@ def kv_bytes(L: int, Hkv: int, d: int, S: int, b: int) -> int:
 
 def num_threads() -> int:
     return int(lib().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's parallel loops from now on (results do not change)."""
+    lib().orc_set_num_threads(int(n))
 
 
 # ---------------------------------------------------------------- steps

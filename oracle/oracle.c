@@ -503,6 +503,19 @@ int orc_num_threads(void)
 #endif
 }
 
+/* Threads used by the parallel loops from now on (n >= 1); for timing the oracle
+ * on one core as well as on all of them.  Changes no result: every output row is
+ * computed by one thread in the same order whatever the count. */
+void orc_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* ------------------------------------------------------------------------ */
 /* Prefix block hash  ([P3] "优化一：Prefix Cache", 工作原理：按块哈希:        */
 /* hash_i = H(hash_{i-1}, t_{(i-1)B+1}, ..., t_{iB}); token-exact matching)   */

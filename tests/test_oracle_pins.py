@@ -686,3 +686,20 @@ def test_rescale_write_scales_equal_the_amax_recipe(cfg):
     kc2, vc2 = np.zeros_like(kc), np.zeros_like(vc)
     oracle.kv_cache_write(d["k_rows"], d["v_rows"], slots, kc2, vc2, d["k_scale"], d["v_scale"])
     assert np.array_equal(kc, kc2) and np.array_equal(vc, vc2)
+
+
+def test_thread_count_changes_no_result():
+    """The single-core timing of the oracle computes the same bits as the all-core one."""
+    wl = W.make(2, small=True)
+    d = W.host_data(wl)
+    n0 = oracle.num_threads()
+    try:
+        a = oracle.decode_attn(d["q"], d["k_cache"], d["v_cache"], wl.block_table, wl.seq_lens,
+                               wl.scale)
+        oracle.set_num_threads(1)
+        assert oracle.num_threads() == 1
+        b = oracle.decode_attn(d["q"], d["k_cache"], d["v_cache"], wl.block_table, wl.seq_lens,
+                               wl.scale)
+    finally:
+        oracle.set_num_threads(n0)
+    assert np.array_equal(a, b)

@@ -85,8 +85,14 @@ struct Cfg {
     static constexpr int ROW_BYTES = I4 ? D / 2 : D * ELT;
     static constexpr int CH = I4 ? 1 : ROW_BYTES / 128;   // 128-byte column chunks per row
     static constexpr int CH_ELEMS = 128 / ELT;            // elements per chunk
-    static constexpr int TT = FP8 ? BS : 16;              // tokens per pipeline tile
-    static constexpr int SUB = BS / TT;                   // tiles per page (1 or 2)
+    // int4 pages are worked on two or four cache blocks at a time (64 tokens): the
+    // flat page list counts these groups, so each pipeline item carries twice the
+    // math of a 32-token block for the same waits, shuffles and branches
+    static constexpr int PPI = I4 ? 64 / BS : 1;          // cache blocks per list page
+    static constexpr int SPB = BS * PPI;                  // tokens per list page
+    static constexpr int TT = FP8 ? SPB : 16;             // tokens per pipeline tile
+    static constexpr int SUB = SPB / TT;                  // tiles per list page (1 or 2)
+    static constexpr int MTB = BS / 16;                   // 16-token mma tiles per block
     static constexpr int TILE_BYTES = TT * ROW_BYTES;     // K (or V) part of a stage
     static constexpr int STAGE_BYTES = 2 * TILE_BYTES;    // 8 KB at bf16 D=128 or E4M3 BS=32
     static constexpr int MT = TT / 16;                    // 16-token mma tiles per tile
@@ -98,6 +104,7 @@ struct Cfg {
     static_assert(!I4 || ROW_BYTES == 64, "int4 rows are 64 bytes");
     static_assert(BS % 16 == 0, "block size must be a multiple of 16");
     static_assert(SUB == 1 || SUB == 2, "one or two tiles per page");
+    static_assert(SPB <= 255, "token count of a list page fits the 8-bit field");
 };
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
@@ -121,21 +128,29 @@ __device__ __forceinline__ uint32_t swz64(int t, int u) {
     return (uint32_t)(t * 64 + ((u ^ ((t >> 1) & 3)) << 4));
 }
 
-// Per-lane description of one page of a 32-page batch.
+// Per-lane description of one list page (PPI cache blocks) of a 32-page batch.
+template <int PPI>
 struct PageBatch {
-    int row;       // TMA row of the page's first token / BS: id * Hkv + h (id = NB past the end)
+    int row[PPI];  // TMA row of each block's first token / BS: id * Hkv + h (id = NB: past
+                   // the end, read as zeros)
     int r, h;      // unit
     uint32_t fl;   // valid tokens | first << 8 | last << 9 | page index j << 10
-    float ks, vs;  // FP8 scales
+    float ks[PPI], vs[PPI];  // per-block scales of quantised pages
 };
 
-template <int BS, bool FP8>
-__device__ __forceinline__ void load_batch(PageBatch& b, int xbeg, int x1,
+template <int BS, int PPI, bool FP8>
+__device__ __forceinline__ void load_batch(PageBatch<PPI>& b, int xbeg, int x1,
                                            const int32_t* s_prefix, const int32_t* s_seq,
                                            const DecodeArgs& a, uint32_t& errbits) {
     const int lane = threadIdx.x & 31;
     const int x = xbeg + lane;
-    b.row = a.NB * a.Hkv; b.r = 0; b.h = 0; b.fl = 0; b.ks = 1.f; b.vs = 1.f;
+    b.r = 0; b.h = 0; b.fl = 0;
+#pragma unroll
+    for (int p = 0; p < PPI; ++p) {
+        b.row[p] = a.NB * a.Hkv;
+        b.ks[p] = 1.f;
+        b.vs[p] = 1.f;
+    }
     if (x >= x1) return;
     int lo = 0, hi = a.N;   // s_prefix[lo] <= x < s_prefix[hi]
     while (hi - lo > 1) {
@@ -147,21 +162,26 @@ __device__ __forceinline__ void load_batch(PageBatch& b, int xbeg, int x1,
     const int off = x - s_prefix[r];
     const int h = off / np;
     const int j = off - h * np;
-    int id = __ldg(a.block_table + (int64_t)r * a.MB + j);
-    if (id < 0 || id >= a.NB) {
-        errbits |= PKV_DEVERR_BLOCK_RANGE;
-        id = a.NB;   // TMA of rows past the tensor end reads zeros
+#pragma unroll
+    for (int p = 0; p < PPI; ++p) {
+        const int blk = j * PPI + p;
+        if (blk * BS >= s_seq[r]) break;   // past the request: stays a zero block
+        int id = __ldg(a.block_table + (int64_t)r * a.MB + blk);
+        if (id < 0 || id >= a.NB) {
+            errbits |= PKV_DEVERR_BLOCK_RANGE;
+            id = a.NB;   // TMA of rows past the tensor end reads zeros
+        }
+        b.row[p] = id * a.Hkv + h;
+        if (FP8 && id < a.NB) {
+            b.ks[p] = __ldg(a.k_scale + (int64_t)id * a.Hkv + h);
+            b.vs[p] = __ldg(a.v_scale + (int64_t)id * a.Hkv + h);
+        }
     }
-    const int ntok = min(BS, s_seq[r] - j * BS);
-    b.row = id * a.Hkv + h;
+    const int ntok = min(BS * PPI, s_seq[r] - j * BS * PPI);
     b.r = r;
     b.h = h;
     b.fl = (uint32_t)ntok | ((j == 0) ? 0x100u : 0u) | ((j == np - 1) ? 0x200u : 0u) |
            ((uint32_t)j << 10);
-    if (FP8 && id < a.NB) {
-        b.ks = __ldg(a.k_scale + (int64_t)id * a.Hkv + h);
-        b.vs = __ldg(a.v_scale + (int64_t)id * a.Hkv + h);
-    }
 }
 
 // The query rows of request r: first row and count (clamped to QT).
@@ -236,7 +256,7 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         int running = 0;
         for (int b0 = 0; b0 < a.N; b0 += 32) {
             const int i = b0 + lane;
-            int v = (i < a.N) ? a.Hkv * ((s_seq[i] + BS - 1) / BS) : 0;
+            int v = (i < a.N) ? a.Hkv * ((s_seq[i] + C::SPB - 1) / C::SPB) : 0;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const int n = __shfl_up_sync(0xffffffffu, v, o);
@@ -275,9 +295,9 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         return;
     }
 
-    PageBatch cur, nxt;
-    load_batch<BS, FP8>(cur, x0, x1, s_prefix, s_seq, a, errbits);
-    load_batch<BS, FP8>(nxt, x0 + 32, x1, s_prefix, s_seq, a, errbits);
+    PageBatch<C::PPI> cur, nxt;
+    load_batch<BS, C::PPI, FP8>(cur, x0, x1, s_prefix, s_seq, a, errbits);
+    load_batch<BS, C::PPI, FP8>(nxt, x0 + 32, x1, s_prefix, s_seq, a, errbits);
     int cb = 0;   // batch index held in `cur`
     const uint64_t policy = l2_policy_evict_first();
 
@@ -287,17 +307,26 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         const int sub = i & (C::SUB - 1);               // tile within the page
         const int bi = pi >> 5;
         const int src = pi & 31;
-        const int row = __shfl_sync(0xffffffffu, bi == cb ? cur.row : nxt.row, src);
+        int row[C::PPI];
+#pragma unroll
+        for (int p = 0; p < C::PPI; ++p)
+            row[p] = __shfl_sync(0xffffffffu, bi == cb ? cur.row[p] : nxt.row[p], src);
         if (lane == 0) {
             const uint32_t bar = bars + 8u * s;
             const uint32_t dst = stage0 + (uint32_t)(s * C::STAGE_BYTES);
-            const int y = row * BS + sub * C::TT;
+            const int y = row[0] * BS + sub * C::TT;
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(bar, C::STAGE_BYTES);
             if constexpr (C::I4) {
-                // one box per tile: TT rows of D/2 bytes, 64-byte swizzle
-                tma_load_2d_hint(dst, &tmK, 0, y, bar, policy);
-                tma_load_2d_hint(dst + C::TILE_BYTES, &tmV, 0, y, bar, policy);
+                // one box per cache block: BS rows of D/2 bytes, 64-byte swizzle; the
+                // blocks of a list page stack into one tile of PPI * BS rows
+#pragma unroll
+                for (int p = 0; p < C::PPI; ++p) {
+                    const uint32_t off = (uint32_t)(p * BS * C::ROW_BYTES);
+                    tma_load_2d_hint(dst + off, &tmK, 0, row[p] * BS, bar, policy);
+                    tma_load_2d_hint(dst + C::TILE_BYTES + off, &tmV, 0, row[p] * BS, bar,
+                                     policy);
+                }
             } else {
 #pragma unroll
                 for (int ch = 0; ch < C::CH; ++ch)
@@ -341,20 +370,21 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         if (sub == 0 && pi > 0 && (pi & 31) == 0) {
             cur = nxt;
             ++cb;
-            load_batch<BS, FP8>(nxt, x0 + (cb + 1) * 32, x1, s_prefix, s_seq, a, errbits);
+            load_batch<BS, C::PPI, FP8>(nxt, x0 + (cb + 1) * 32, x1, s_prefix, s_seq, a, errbits);
         }
         const int src = pi & 31;
         const uint32_t fl = __shfl_sync(0xffffffffu, cur.fl, src);
-        float ks = 1.f, vs = 1.f;
-        if (FP8) {
-            ks = __shfl_sync(0xffffffffu, cur.ks, src);
-            vs = __shfl_sync(0xffffffffu, cur.vs, src);
+        float ks[C::PPI], vs[C::PPI];   // scales of the page's blocks (quantised pages)
+#pragma unroll
+        for (int p = 0; p < C::PPI; ++p) {
+            ks[p] = FP8 ? __shfl_sync(0xffffffffu, cur.ks[p], src) : 1.f;
+            vs[p] = FP8 ? __shfl_sync(0xffffffffu, cur.vs[p], src) : 1.f;
         }
         // valid tokens of this tile (<= 0 only for the empty second half of a last page)
         const int ntok = (int)(fl & 0xFFu) - sub * C::TT;
         const bool first = ((fl >> 8) & 1u) && sub == 0;
         const bool last = ((fl >> 9) & 1u) && sub == C::SUB - 1;
-        const int tpos0 = (int)(fl >> 10) * BS + sub * C::TT;   // position of tile row 0
+        const int tpos0 = (int)(fl >> 10) * C::SPB + sub * C::TT;   // position of tile row 0
 
         // ---- segment start: load the GQA group's queries as mma B fragments ----
         if (i == 0 || first) {
@@ -643,7 +673,6 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         }
 
         // ---- online softmax (log2 domain), heads 2c and 2c+1 of this lane ----
-        const float sc_page = FP8 ? qscale * ks : qscale;
         float mx0[QT], mx1[QT];
         bool need = false;
         // every row of a full tile is a cached token every query sees: no mask
@@ -651,11 +680,13 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 #pragma unroll
         for (int qi = 0; qi < QT; ++qi) {
             mx0[qi] = mx1[qi] = -INFINITY;
-            // int4: score = (sum - cq) * scale, one fma
-            const float nc0 = C::FOLD ? -cq0[qi] * sc_page : 0.f;
-            const float nc1 = C::FOLD ? -cq1[qi] * sc_page : 0.f;
 #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
+                // the K scale of the block holding these 16 tokens; int8 / int4:
+                // score = (sum - cq) * scale, one fma
+                const float sc_page = FP8 ? qscale * ks[mt / C::MTB] : qscale;
+                const float nc0 = C::FOLD ? -cq0[qi] * sc_page : 0.f;
+                const float nc1 = C::FOLD ? -cq1[qi] * sc_page : 0.f;
                 if (full_tile) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e)
@@ -688,7 +719,7 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                     mx1[qi] = fmaxf(mx1[qi], __shfl_xor_sync(0xffffffffu, mx1[qi], o2));
                 }
                 const float mn0 = fmaxf(m0[qi], mx0[qi]), mn1 = fmaxf(m1[qi], mx1[qi]);
-                float al0 = exp2f(m0[qi] - mn0), al1 = exp2f(m1[qi] - mn1);
+                float al0 = ex2_approx(m0[qi] - mn0), al1 = ex2_approx(m1[qi] - mn1);
                 if constexpr (QT > 1) {
                     // a query that has seen no token yet keeps -inf without a NaN
                     if (mn0 == -INFINITY) al0 = 1.f;
@@ -720,17 +751,18 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
             float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
             for (int mt = 0; mt < C::MT; ++mt) {
-                const float p0 = exp2f(sacc[mt][qi][0] - r0m), p1 = exp2f(sacc[mt][qi][1] - r1m);
-                const float p2 = exp2f(sacc[mt][qi][2] - r0m), p3 = exp2f(sacc[mt][qi][3] - r1m);
+                const float p0 = ex2_approx(sacc[mt][qi][0] - r0m), p1 = ex2_approx(sacc[mt][qi][1] - r1m);
+                const float p2 = ex2_approx(sacc[mt][qi][2] - r0m), p3 = ex2_approx(sacc[mt][qi][3] - r1m);
                 ps0 += p0 + p2;
                 ps1 += p1 + p3;
                 if (!FP8) {
                     pb[mt][qi][0] = movmatrix_trans(pack_bf16x2(p0, p1));
                     pb[mt][qi][1] = movmatrix_trans(pack_bf16x2(p2, p3));
                 } else {
-                    // quantised pages: P carries the page's V scale into the mma
-                    pb[mt][qi][0] = movmatrix_trans(pack_f16x2(p0 * vs, p1 * vs));
-                    pb[mt][qi][1] = movmatrix_trans(pack_f16x2(p2 * vs, p3 * vs));
+                    // quantised pages: P carries the block's V scale into the mma
+                    const float vsb = vs[mt / C::MTB];
+                    pb[mt][qi][0] = movmatrix_trans(pack_f16x2(p0 * vsb, p1 * vsb));
+                    pb[mt][qi][1] = movmatrix_trans(pack_f16x2(p2 * vsb, p3 * vsb));
                 }
             }
             l0[qi] += ps0;
@@ -1084,7 +1116,9 @@ DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int ba
     DecodePlan p;
     const int fp8 = kt != 0;
     const int row_bytes = kt == 3 ? head_dim / 2 : head_dim * (fp8 ? 1 : 2);
-    const int tile_tokens = fp8 ? block_size : 16;
+    // int4 tiles hold 64 tokens (two or four cache blocks); 8-bit tiles one block;
+    // bf16 tiles 16 tokens
+    const int tile_tokens = kt == 3 ? 64 : (fp8 ? block_size : 16);
     p.stage_bytes = 2 * tile_tokens * row_bytes;
     // Each warp streams its pages through its own 2-stage pipeline; the per-page
     // instruction chain of a warp, not the bytes in flight, limits the rate, so the

@@ -364,6 +364,15 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return y;
 }
 
+// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero): one instruction;
+// -inf gives +0.  Relative error about 2^-22; results below 2^-126 flush to zero, far
+// below what a softmax weight relative to its running maximum contributes.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float bf16_lo_to_f32(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf16_hi_to_f32(uint32_t x) {
     return __uint_as_float(x & 0xFFFF0000u);

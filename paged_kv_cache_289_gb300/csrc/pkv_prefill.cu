@@ -125,13 +125,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&w)[32
         : "memory");
 }
 
-// 2^x on the special-function unit (PTX ex2.approx, flush-to-zero): one MUFU op;
-// -inf gives +0.
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32]) {
     asm volatile(

@@ -120,6 +120,10 @@ PKV_API int pkv_compute_slot_mapping(const int32_t *block_table, int max_blocks_
  *   PKV_INT8:     byte = clamp(round_half_even(float(x) / scale[blk][h]), -127, 127)
  *                 as int8, same division and scales ([P3] "优化五：KV 本体压缩":
  *                 FP16 -> FP8/INT8/INT4).  NaN inputs give 0.
+ *   PKV_INT4:     code = clamp(round_half_even(float(x) / scale[blk][h]), -7, 7),
+ *                 same division and scales, stored offset-binary (code + 8) two per
+ *                 byte in the nibble layout of the cache-type note above.  NaN
+ *                 inputs give code 0.
  * Bytes not addressed by a slot are untouched.  Two tokens with the same slot
  * race (last writer wins, undefined which).
  * Requirements: head_dim % 8 == 0; k, v, caches 16-byte aligned.
@@ -134,7 +138,7 @@ PKV_API int pkv_kv_cache_write(const void *k, const void *v, const int64_t *slot
  * 8-bit KV with a scale; here the scale is derived from the data being written).
  * For every (block, kv head) that receives at least one row in this call, its scale
  * becomes amax / QMAX over the |values| of the rows written to it by this call
- * (QMAX = 448 for PKV_FP8_E4M3, 127 for PKV_INT8; binary32 divide; NaN values
+ * (QMAX = 448 for PKV_FP8_E4M3, 127 for PKV_INT8, 7 for PKV_INT4; binary32 divide; NaN values
  * ignored; an all-zero block gets 1); the rows are then coded exactly as
  * pkv_kv_cache_write does with those scales.  Scales of blocks receiving no row are
  * unchanged; bytes written to a touched block by earlier calls are not re-coded, so
@@ -177,10 +181,12 @@ PKV_API size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_
  *   head_dim 128 (quantised pages: the group's bf16 q values are rescaled by a
  *   power of two so the largest lands in [2^14, 2^15) and converted to fp16; this
  *   is exact except for nonzero elements more than 2^31 times smaller than the
- *   group's largest, which round to the fp16 subnormal grid.  INT8 and INT4 codes
- *   enter the fp16 mma with their offset, 1024 plus the biased code, which is
- *   subtracted once per score and once per output; that cancellation adds fp32
- *   rounding of about 2^-24 * 1152 * sqrt(pages) times v_scale to an output).
+ *   group's largest, which round to the fp16 subnormal grid.  INT8 and INT4 K codes
+ *   enter the fp16 mma with their offset, 1024 plus the biased code, subtracted once
+ *   per score.  V codes enter as fp16 subnormals (biased code * 2^-24) against
+ *   P * v_scale rounded to fp16; the small offset of the biased code (128 or 8) is
+ *   subtracted once per output.  E4M3 V codes are widened exactly and also meet
+ *   P * v_scale in fp16).
  * Requirements: q, out, caches, workspace 16-byte aligned; workspace_bytes >=
  *   pkv_decode_workspace_size(...) for the same shape and device.
  * The work is one flat list of (request, kv head, page) items split evenly over

@@ -28,7 +28,8 @@
 // us for four, with the step 2.5% and 14% slower).
 //
 // Per-warp pipeline.  Each warp owns `stages` shared-memory stages, each holding
-// the K and V tile (TT tokens) of one (block, head) page.  Lane 0 issues 2-D bulk
+// the K and V tile (TT tokens) of one (block, head) page (of one 64-token group of
+// blocks for int4).  Lane 0 issues 2-D bulk
 // tensor copies (TMA, 128-byte swizzle, box = 128 bytes x TT rows) that complete on
 // the stage's mbarrier; all lanes wait on it (bounded), compute, and the stage is
 // refilled with the tile `stages` ahead.  Block ids for the next 32 pages are looked
@@ -42,10 +43,13 @@
 //   O^T[d][g] += V^T[d][t] P^T[t][g]  A = V tile (ldmatrix.trans), B = P^T from
 //                                     the S^T accumulators via movmatrix.trans
 // Quantised pages are widened exactly to fp16 in registers: E4M3 by cvt e4m3x2 ->
-// f16x2; int8 and int4 codes by a byte permute or mask-or that yields 1024 plus the
-// biased code, whose constant share is subtracted once per score and once per output.
-// The per-(block, head) K scale multiplies S, the V scale multiplies the page's P.V
-// contribution, so neither scale is rounded into an fp16 operand.
+// f16x2; int8 and int4 K codes by a byte permute or mask-or that yields 1024 plus the
+// biased code, whose constant share is subtracted once per score; int8 and int4 V
+// codes by the same picks under a zero exponent (fp16 subnormals, biased code *
+// 2^-24), whose small constant share is subtracted once per output.  The
+// per-(block, head) K scale multiplies S in fp32; the V scale multiplies P before P is
+// rounded to fp16, so O accumulates every page in the same mma accumulators.  int4
+// caches are worked 64 tokens (two or four blocks of one unit) per pipeline item.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>

@@ -66,8 +66,8 @@ struct DecodeLaunch {
     const int32_t* seq_lens;
     void* out;
     void* workspace;
-    int N, Hq, Hkv, D, BS, MB, NB, fp8;   // fp8: any 8-bit page kind (E4M3 or int8)
-    int kt;                               // page kind: 0 bf16, 1 E4M3, 2 int8
+    int N, Hq, Hkv, D, BS, MB, NB, fp8;   // fp8: any quantised page kind (E4M3, int8, int4)
+    int kt;                               // page kind: 0 bf16, 1 E4M3, 2 int8, 3 int4
     float scale;
     int num_sms;
 };

@@ -331,6 +331,14 @@ def l2_flush_buffer(torch, dev):
     return torch.ones(2 * 129 * 1024 * 1024 // 4, dtype=torch.int32, device=dev)
 
 
+def gate(torch, stream):
+    """A bounded GPU sleep (about 1 ms) queued just before a timed region opens: the host
+    enqueues the region's first launches while it runs, so the first timed step does not
+    wait on the host.  It sits before the start event and is not timed."""
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(2_000_000)
+
+
 def median_of(ts):
     return statistics.median(ts) if ts else float("nan")
 
@@ -457,6 +465,7 @@ class StepHarness:
         torch.cuda.synchronize(self.dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        gate(torch, self.main)
         e0.record(self.main)
         for _ in range(K):
             self.step(self.inputs, self.outputs)
@@ -597,6 +606,7 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    gate(torch, main)
     e0.record(main)
     for k in range(K):
         step(inputs, outputs, dec_events[k])
@@ -773,6 +783,7 @@ def run_copy_blocks(args):
     sampler.start()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gate(torch, main)
     e0.record(main)
     for k in range(K):
         ev[k][0].record(main)
@@ -873,6 +884,7 @@ def run_prefill(args):
     sampler.start()
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gate(torch, main)
     e0.record(main)
     for k in range(K):
         ev[k][0].record(main)

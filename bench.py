@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--skip-cpu", action="store_true")
     p.add_argument("--skip-per-workload", action="store_true",
                    help="leave out the decode figures of workloads 3, 4 and 5 (workload 2 runs)")
+    p.add_argument("--shared-prefix", action="store_true",
+                   help="workload 4: decode through pkv_paged_decode_attn_shared_prefix (the "
+                        "shared pages attended once for the batch)")
     p.add_argument("--hash", choices=["full", "resume"], default="full",
                    help="full: the step re-hashes every token; resume: only the blocks the "
                         "step completes (pkv_prefix_block_hash_resume)")
@@ -231,11 +234,12 @@ def workload_config(wl):
                   % (2 * wl.NB * wl.Hkv * wl.BS * wl.D * wl.elt / 1e9)}
 
 
-def decode_algorithmic_bytes(wl):
+def decode_algorithmic_bytes(wl, unique=False):
     """Bytes one decode launch must move: every cached K/V row once, plus the block
-    table entries, FP8 scales, q and out."""
+    table entries, FP8 scales, q and out.  unique: rows of shared pages counted once
+    (the shared-prefix call reads them once)."""
     nblk = sum(len(wl.blocks_of(r)) for r in range(wl.N))
-    b = wl.kv_read_bytes()
+    b = wl.unique_kv_read_bytes() if unique else wl.kv_read_bytes()
     b += nblk * 4                                        # block table entries read
     if wl.quant:
         b += nblk * wl.Hkv * 2 * 4                       # K and V scales
@@ -353,11 +357,13 @@ class StepHarness:
     (pkv_prefix_block_hash_resume), so only the blocks completed by the step's new
     tokens are read."""
 
-    def __init__(self, wl, dev, hash_mode="full"):
+    def __init__(self, wl, dev, hash_mode="full", shared_prefix=False):
         import torch
         import paged_kv_cache_289_gb300 as pkv
         from paged_kv_cache_289_gb300 import workloads as W
         self.wl, self.dev, self.hash_mode = wl, dev, hash_mode
+        # decode through the shared-prefix call (the prefix-sharing workload only)
+        self.prefix = wl.notes.get("shared_prefix_blocks", 0) * wl.BS if shared_prefix else 0
         self.torch, self.pkv = torch, pkv
         dd = W.device_data(wl, dev)
         bt = torch.from_numpy(wl.block_table).to(dev)
@@ -415,13 +421,21 @@ class StepHarness:
         self.ws = torch.zeros(pkv.multiquery_workspace_size(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS,
                                                             wl.kv_kind, wl.q_len),
                               dtype=torch.uint8, device=dev)
+        if self.prefix:
+            self.ws = torch.zeros(pkv.shared_prefix_workspace_size(wl.N, wl.Hq, wl.Hkv, wl.D,
+                                                                   wl.BS, self.prefix),
+                                  dtype=torch.uint8, device=dev)
         self.main = torch.cuda.current_stream(dev)
         self.side = torch.cuda.Stream(dev)
         self.launches_per_step = 5   # slot map, write, decode, wide-split merge, hash
 
     def decode(self, I, O, stream):
         wl, pkv = self.wl, self.pkv
-        if wl.q_len == 1:
+        if self.prefix:
+            pkv.paged_decode_attn_shared_prefix(I["q"], self.kc, self.vc, I["bt"], I["sl"],
+                                                wl.scale, self.prefix, out=O["out"],
+                                                workspace=self.ws, stream=stream)
+        elif wl.q_len == 1:
             pkv.paged_decode_attn(I["q"], self.kc, self.vc, I["bt"], I["sl"], wl.scale,
                                   out=O["out"], k_scale=self.ks, v_scale=self.vs,
                                   workspace=self.ws, stream=stream)
@@ -539,6 +553,21 @@ def per_workload_figures(dev, peak, main_harness=None):
                              "unique_frac": round(uniq / med_nf / 1e9 / peak, 4)},
                 "note": "the shared 4096-token prefix (16 MB of pages) is read by every "
                         "request; logical bytes count it per request, unique bytes once"})
+            # the same batch through the shared-prefix call: the shared pages once
+            hs = StepHarness(wl, dev, "full", shared_prefix=True)
+            fig = {}
+            for key, fl in (("flushed", flush), ("no_flush", None)):
+                t = median_of(hs.time_decode_launches(flush=fl))
+                fig[key] = {"median_launch_ms": round(t * 1e3, 4),
+                            "logical_gbs": round(logical / t / 1e9, 1),
+                            "unique_gbs": round(uniq / t / 1e9, 1),
+                            "unique_frac": round(uniq / t / 1e9 / peak, 4)}
+            assert pkv.read_device_error(hs.ws) == 0, "device error word set"
+            fig["what"] = ("pkv_paged_decode_attn_shared_prefix: the 4096 shared tokens "
+                           "attended once for all 128 requests on the tensor cores, the tails "
+                           "by the decode kernel, a log-sum-exp merge")
+            entry["shared_prefix_call"] = fig
+            hs = None
         if cfg == 3:
             K = 50
             t_full = h.time_steps(K, 10)
@@ -584,7 +613,7 @@ def run_ours(args):
 
     wl = W.make(args.workload, seed=(args.seed if args.seed is not None else args.workload) + rank,
                 batch=args.batch)
-    H = StepHarness(wl, dev, args.hash)
+    H = StepHarness(wl, dev, args.hash, shared_prefix=args.shared_prefix)
     quant = wl.quant
     main = H.main
     inputs, outputs = H.inputs, H.outputs
@@ -630,13 +659,15 @@ def run_ours(args):
 
     # ---------------- roofline of the dominant launch (decode: main + merge kernels)
     peak, peak_kind = peak_hbm()
-    alg = decode_algorithmic_bytes(wl)
+    alg = decode_algorithmic_bytes(wl, unique=bool(H.prefix))
     achieved = alg / dec_avg / 1e9
     traffic = recorded_traffic(kernel_source_hash(), wl.name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": f"{peak_kind} hbm_gbs (copy, read+write bytes)",
-                "kernel": "pkv_paged_decode_attn (pkv_decode_kernel)",
+                "kernel": ("pkv_paged_decode_attn_shared_prefix (pkv_prefill_kernel over the "
+                           "shared pages, pkv_decode_kernel over the tails, merge)"
+                           if H.prefix else "pkv_paged_decode_attn (pkv_decode_kernel)"),
                 "algorithmic_bytes_per_launch": alg,
                 "avg_launch_ms": round(dec_avg * 1e3, 4),
                 "median_launch_ms": round(dec_med * 1e3, 4),
@@ -736,6 +767,7 @@ def run_ours(args):
                           ["", "fp8_e4m3", "int8", "int4"][wl.kv_kind] + " KV, bf16 q/out, fp32 accumulate"),
                 "data": "synthetic (seeded N(0,1) q/K/V, uniform token ids)",
                 "config": dict(workload_config(wl), hash=args.hash,
+                               shared_prefix_tokens=H.prefix,
                                parallelism=f"{world} independent replicas (no collective)"),
                 "query_tokens_per_s": round(total_q / t_max, 1),
                 "pct_of_hbm_peak": round(100 * value / peak, 2),

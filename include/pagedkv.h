@@ -234,6 +234,41 @@ PKV_API int pkv_paged_multiquery_attn(const void *q, const int32_t *q_offsets, i
                                       pkv_stream_t stream);
 
 /*
+ * Paged decode attention over a shared prefix ([P3] "优化一：Prefix Cache": requests whose
+ * first blocks hash alike share those physical blocks; [P2] "缓存命中与复用").  The same
+ * result as pkv_paged_decode_attn (bf16 pages, one query per request) when every request
+ * of the batch begins with the same prefix_len tokens held in the same blocks: the
+ * first prefix_len / block_size entries of every block-table row equal row 0's, and
+ * seq_lens[r] >= prefix_len (the caller's contract, not checked on the device).  The
+ * shared pages are read once for the whole batch instead of once per request:
+ *   1. all the batch's queries, stacked as the rows of the tensor-core prefill kernel,
+ *      attend without mask to row 0's first prefix_len tokens (split in a few KV chunks
+ *      so that the SMs are covered); each (request, query head) leaves an unnormalised
+ *      partial (o, m, l) per chunk in the workspace;
+ *   2. the decode kernel attends each request to its tokens prefix_len .. seq_lens[r]-1
+ *      and leaves a partial for every (request, KV head);
+ *   3. a merge combines each row's partials with log-sum-exp weights into out.
+ * prefix_len must be a multiple of block_size and at most max_blocks_per_seq *
+ * block_size (else PKV_ERR_INVALID_ARG); 0 runs the plain decode.  scale finite and > 0.
+ * Supported: bf16 pages, head_dim 64 or 128, block_size 16 or 32, G = Hq / Hkv in
+ * {1, 2, 4, 8}; otherwise PKV_ERR_UNSUPPORTED.  workspace: at least
+ * pkv_shared_prefix_workspace_size(...) bytes (0 for an unsupported shape), 256-byte
+ * aligned, no clearing needed; its first word is the device error word.  Three
+ * launches on stream, no host synchronisation.
+ */
+PKV_API size_t pkv_shared_prefix_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                                int head_dim, int block_size, int prefix_len,
+                                                int num_sms);
+PKV_API int pkv_paged_decode_attn_shared_prefix(const void *q, const void *k_cache,
+                                                const void *v_cache, const int32_t *block_table,
+                                                int max_blocks_per_seq, const int32_t *seq_lens,
+                                                int batch, int num_q_heads, int num_kv_heads,
+                                                int head_dim, int block_size, int num_blocks,
+                                                int prefix_len, float scale, void *out,
+                                                void *workspace, size_t workspace_bytes,
+                                                pkv_stream_t stream);
+
+/*
  * Paged decode attention that allocates nothing.  The sources describe no such
  * call: it exists for callers that cannot call cudaMalloc -- for example a plugin
  * hosted by an engine that owns all device memory and offers no workspace hook,

@@ -16,6 +16,7 @@ __all__ = [
     "DEVERR_SEQ_CLAMPED", "DEVERR_BLOCK_RANGE", "compute_slot_mapping", "kv_cache_write",
     "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn",
     "paged_decode_attn_noalloc", "prefix_block_hash", "prefix_block_hash_resume",
+    "shared_prefix_workspace_size", "paged_decode_attn_shared_prefix",
     "multiquery_workspace_size",
     "paged_multiquery_attn", "DEVERR_QLEN_CLAMPED", "kv_cache_write_rescale",
     "device_num_sms", "read_device_error", "copy_blocks", "BlockManager", "ERR_NO_BLOCKS",
@@ -89,6 +90,11 @@ def lib():
                                                         i, f, p, p]
             L.pkv_prefix_block_hash.restype = i
             L.pkv_prefix_block_hash.argtypes = [p, p, i, i, u64, p, p, p]
+            L.pkv_shared_prefix_workspace_size.restype = sz
+            L.pkv_shared_prefix_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.pkv_paged_decode_attn_shared_prefix.restype = i
+            L.pkv_paged_decode_attn_shared_prefix.argtypes = [p, p, p, p, i, p, i, i, i, i, i, i,
+                                                              i, f, p, p, sz, p]
             L.pkv_prefix_block_hash_resume.restype = i
             L.pkv_prefix_block_hash_resume.argtypes = [p, p, i, i, p, p, p, p, p]
             L.pkv_prefill_workspace_size.restype = sz
@@ -300,6 +306,39 @@ def paged_multiquery_attn(q, q_offsets, max_q_len, k_cache, v_cache, block_table
         _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D,
         BS, NB, dt, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
         _stream(stream)))
+    return out
+
+
+def shared_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                 prefix_len, num_sms=0) -> int:
+    return int(lib().pkv_shared_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
+                                                      block_size, prefix_len, num_sms))
+
+
+def paged_decode_attn_shared_prefix(q, k_cache, v_cache, block_table, seq_lens, scale,
+                                    prefix_len, out=None, workspace=None, stream=None):
+    """paged_decode_attn for a batch whose requests all begin with the same prefix_len
+    tokens in the same blocks: the shared pages are attended once for the whole batch
+    (bf16 pages)."""
+    import torch
+    _need(q, "q", (torch.bfloat16,))
+    _need(k_cache, "k_cache", (torch.bfloat16,))
+    _need(v_cache, "v_cache", (torch.bfloat16,))
+    _need(block_table, "block_table", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    N, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        n = shared_prefix_workspace_size(N, Hq, Hkv, D, BS, prefix_len)
+        if n == 0:
+            raise PkvError("pkv_shared_prefix_workspace_size", -2)
+        workspace = torch.zeros(n, dtype=torch.uint8, device=q.device)
+    _check("pkv_paged_decode_attn_shared_prefix", lib().pkv_paged_decode_attn_shared_prefix(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), block_table.shape[1],
+        _ptr(seq_lens), N, Hq, Hkv, D, BS, NB, int(prefix_len), float(scale), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

@@ -3,6 +3,7 @@
 // Every entry point validates its host-side scalars and pointer alignment
 // first and launches nothing when a check fails.  No entry point synchronises
 // the device or copies device memory to the host.
+#include <math.h>
 #include <stdint.h>
 
 #include "pkv_internal.cuh"
@@ -234,6 +235,154 @@ int pkv_prefix_block_hash_resume(const int32_t* tokens, const int64_t* offsets, 
                                             first_blocks, hashes, hash_offsets,
                                             reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ shared prefix
+namespace {
+
+// KV chunks of the prefix pass: enough (query tile, KV head, chunk) CTAs to cover the
+// SMs, each chunk a whole number of 256-token tiles.
+int shared_prefix_split(int batch, int Hq, int Hkv, int prefix_len, int num_sms,
+                        int* chunk_tokens) {
+    const int G = Hq / Hkv;
+    const int TQ = 128 / G;
+    const int tiles = (batch + TQ - 1) / TQ;
+    const int ktiles = (prefix_len + 255) / 256;
+    if (ktiles == 0 || tiles == 0) {
+        *chunk_tokens = 0;
+        return 0;
+    }
+    int want = (num_sms + tiles * Hkv - 1) / (tiles * Hkv);
+    if (want < 1) want = 1;
+    if (want > ktiles) want = ktiles;
+    const int per = (ktiles + want - 1) / want;
+    *chunk_tokens = per * 256;
+    return (ktiles + per - 1) / per;
+}
+
+bool shared_prefix_supported(int Hq, int Hkv, int D, int BS) {
+    return shape_supported(Hq, Hkv, D, BS, PKV_BF16) &&
+           pkv::prefill_shape_supported(Hq, Hkv, D, BS, PKV_BF16);
+}
+
+}  // namespace
+
+size_t pkv_shared_prefix_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                        int head_dim, int block_size, int prefix_len,
+                                        int num_sms) {
+    if (batch < 0 || batch > pkv::kMaxBatch || prefix_len < 0) return 0;
+    if (!shared_prefix_supported(num_q_heads, num_kv_heads, head_dim, block_size)) return 0;
+    if (num_sms <= 0 && current_num_sms(&num_sms) != PKV_OK) return 0;
+    const size_t dec = pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
+                                                   PKV_BF16, num_sms, 1);
+    int chunk = 0;
+    const int split = shared_prefix_split(batch, num_q_heads, num_kv_heads, prefix_len, num_sms,
+                                          &chunk);
+    return (size_t)pkv::align_up((int64_t)dec, 256) +
+           (size_t)batch * num_q_heads * split * (head_dim + 4) * 4;
+}
+
+int pkv_paged_decode_attn_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_table, int max_blocks_per_seq,
+                                        const int32_t* seq_lens, int batch, int num_q_heads,
+                                        int num_kv_heads, int head_dim, int block_size,
+                                        int num_blocks, int prefix_len, float scale, void* out,
+                                        void* workspace, size_t workspace_bytes,
+                                        pkv_stream_t stream) {
+    if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || prefix_len < 0)
+        return PKV_ERR_INVALID_ARG;
+    if (!shared_prefix_supported(num_q_heads, num_kv_heads, head_dim, block_size))
+        return PKV_ERR_UNSUPPORTED;
+    if (batch > pkv::kMaxBatch) return PKV_ERR_UNSUPPORTED;
+    if (block_size <= 0 || prefix_len % block_size != 0 ||
+        prefix_len > max_blocks_per_seq * block_size)
+        return PKV_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !(scale < INFINITY)) return PKV_ERR_INVALID_ARG;
+    if (prefix_len == 0)   // nothing shared: the plain decode
+        return pkv_paged_decode_attn(q, k_cache, v_cache, nullptr, nullptr, block_table,
+                                     max_blocks_per_seq, seq_lens, batch, num_q_heads,
+                                     num_kv_heads, head_dim, block_size, num_blocks, PKV_BF16,
+                                     scale, out, workspace, workspace_bytes, stream);
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t rows = ((int64_t)num_blocks + 1) * num_kv_heads * block_size;
+    const int64_t max_pages = (int64_t)batch * num_kv_heads * max_blocks_per_seq;
+    if (rows >= (int64_t)1 << 31 || max_pages >= (int64_t)1 << 31 ||
+        (int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 22)
+        return PKV_ERR_UNSUPPORTED;
+    int num_sms = 0;
+    if (current_num_sms(&num_sms) != PKV_OK) return PKV_ERR_CUDA;
+    const size_t need = pkv_shared_prefix_workspace_size(batch, num_q_heads, num_kv_heads,
+                                                         head_dim, block_size, prefix_len,
+                                                         num_sms);
+    if (!workspace || need == 0 || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 256)) return PKV_ERR_INVALID_ARG;
+    const size_t dec = pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
+                                                   PKV_BF16, num_sms, 1);
+    float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                           pkv::align_up((int64_t)dec, 256));
+    int chunk = 0;
+    const int split = shared_prefix_split(batch, num_q_heads, num_kv_heads, prefix_len, num_sms,
+                                          &chunk);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // 1) the shared pages once for every request: all queries as the rows of a
+    //    non-causal pass over block-table row 0's first prefix_len tokens
+    pkv::PrefillLaunch P;
+    P.q = q;
+    P.q_offsets = nullptr;
+    P.k_cache = k_cache;
+    P.v_cache = v_cache;
+    P.block_table = block_table;
+    P.seq_lens = nullptr;
+    P.out = nullptr;
+    P.err = static_cast<uint32_t*>(workspace);   // the decode workspace's error word
+    P.total_q = batch;
+    P.max_q_len = batch;
+    P.N = 1;
+    P.Hq = num_q_heads;
+    P.Hkv = num_kv_heads;
+    P.D = head_dim;
+    P.BS = block_size;
+    P.MB = max_blocks_per_seq;
+    P.NB = num_blocks;
+    P.scale = scale;
+    P.prefix_split = split;
+    P.prefix_len = prefix_len;
+    P.chunk_tokens = chunk;
+    P.part = part;
+    int stp = pkv::prefill_launch(P, st);
+    if (stp != PKV_OK) return stp;
+    // 2) each request's private pages, every unit as a partial, 3) the merge
+    pkv::DecodeLaunch L;
+    L.q = q;
+    L.q_offsets = nullptr;
+    L.max_q_len = 1;
+    L.k_cache = k_cache;
+    L.v_cache = v_cache;
+    L.k_scale = nullptr;
+    L.v_scale = nullptr;
+    L.block_table = block_table;
+    L.seq_lens = seq_lens;
+    L.out = out;
+    L.workspace = workspace;
+    L.N = batch;
+    L.Hq = num_q_heads;
+    L.Hkv = num_kv_heads;
+    L.D = head_dim;
+    L.BS = block_size;
+    L.MB = max_blocks_per_seq;
+    L.NB = num_blocks;
+    L.fp8 = 0;
+    L.kt = PKV_BF16;
+    L.scale = scale;
+    L.num_sms = num_sms;
+    L.skip_blocks = prefix_len / block_size;
+    L.cascade_part = part;
+    L.cascade_split = split;
+    return pkv::decode_launch(L, st);
 }
 
 size_t pkv_prefill_workspace_size(int batch, int max_blocks_per_seq, int num_kv_heads,

@@ -76,6 +76,13 @@ struct DecodeArgs {
     float scale_log2;   // scale * log2(e): scores kept in the log2 domain
     int stages;
     int total_warps;
+    // Shared-prefix decode: the first skip_blocks blocks of every request are attended
+    // by the prefix pass, this kernel takes the rest; every unit then writes a partial
+    // (none writes its output) and the cascade merge adds the prefix partials
+    // cascade_part[(r * Hq + hq) * cascade_split + c].
+    int skip_blocks;
+    const float* cascade_part;
+    int cascade_split;
 };
 
 template <int D, int BS, int KT>
@@ -170,7 +177,7 @@ __device__ __forceinline__ void load_batch(PageBatch<PPI>& b, int xbeg, int x1,
     for (int p = 0; p < PPI; ++p) {
         const int blk = j * PPI + p;
         if (blk * BS >= s_seq[r]) break;   // past the request: stays a zero block
-        int id = __ldg(a.block_table + (int64_t)r * a.MB + blk);
+        int id = __ldg(a.block_table + (int64_t)r * a.MB + a.skip_blocks + blk);
         if (id < 0 || id >= a.NB) {
             errbits |= PKV_DEVERR_BLOCK_RANGE;
             id = a.NB;   // TMA of rows past the tensor end reads zeros
@@ -248,9 +255,9 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
 
     // ---- page prefix over requests (every CTA computes its own copy) ----
     uint32_t errbits = 0;
-    const int maxlen = a.MB * BS;
+    const int maxlen = (a.MB - a.skip_blocks) * BS;
     for (int i = threadIdx.x; i < a.N; i += blockDim.x) {
-        const int s = __ldg(a.seq_lens + i);
+        const int s = __ldg(a.seq_lens + i) - a.skip_blocks * BS;   // tokens after the skip
         const int c = min(max(s, 0), maxlen);
         if (c != s) errbits |= PKV_DEVERR_SEQ_CLAMPED;
         s_seq[i] = c;
@@ -275,8 +282,9 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i <= a.N; i += blockDim.x) a.g_prefix[i] = s_prefix[i];
     }
-    // requests with no cached tokens get zero output rows (grid-strided over requests)
-    for (int r = blockIdx.x; r < a.N; r += gridDim.x) {
+    // requests with no cached tokens get zero output rows (grid-strided over requests);
+    // with a shared prefix the cascade merge writes every row
+    for (int r = blockIdx.x; r < (a.cascade_part ? 0 : a.N); r += gridDim.x) {
         if (s_seq[r] != 0) continue;
         int qb, qlen;
         query_rows<QT>(a, r, qb, qlen, errbits);
@@ -875,7 +883,7 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
         // ---- segment end ----
         if (last || i == total - 1) {
             const int g0 = 2 * c, g1 = 2 * c + 1;
-            const bool complete = seg_full && last;
+            const bool complete = seg_full && last && a.cascade_part == nullptr;
             const int64_t u = (int64_t)seg_r * a.Hkv + seg_h;
             const int64_t slot = u + gw;
 #pragma unroll
@@ -1085,6 +1093,88 @@ __global__ void __launch_bounds__(kGroupPad * 32 * QT)
             pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
 }
 
+// The shared-prefix merge: per (request, query head), the unit's decode partials over
+// its private pages and the prefix pass's partials over the shared pages, merged with
+// the same log-sum-exp weights as pkv_decode_merge_kernel (one query position).  One
+// CTA per unit, one warp per query head; lane k holds partial k's (m, l) and each lane
+// owns D/32 columns.
+template <int D>
+__global__ void __launch_bounds__(kGroupPad * 32)
+    pkv_cascade_merge_kernel(const DecodeArgs a) {
+    constexpr int PER = D / 32;
+    constexpr int QS = kGroupPad * (D + 4);
+    pdl_wait();
+    const int u = blockIdx.x;
+    const int gg = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gg >= a.G) return;
+    const int r = u / a.Hkv;
+    const int h = u - r * a.Hkv;
+    const int P = a.g_prefix[a.N];
+    const int p0 = a.g_prefix[r], p1 = a.g_prefix[r + 1];
+    const int np = (p1 - p0) / a.Hkv;
+    int wf = 0, n = 0;   // the unit's decode partials: slots u + wf .. u + wf + n - 1
+    if (np > 0) {
+        const int W = min(a.total_warps, P);
+        const int64_t U = (int64_t)p0 + (int64_t)h * np;
+        const int64_t E = U + np - 1;
+        wf = (int)(((U + 1) * W - 1) / P);
+        n = (int)(((E + 1) * W - 1) / P) - wf + 1;
+    }
+    const int C = a.cascade_split;
+    const int T = n + C;   // all partials of this (request, head)
+    const float* dp = a.partials + ((int64_t)u + wf) * QS + gg * (D + 4);
+    const float* pp = a.cascade_part + ((int64_t)r * a.Hq + (int64_t)h * a.G + gg) * C * (D + 4);
+    auto row = [&](int k) { return k < n ? dp + (int64_t)k * QS : pp + (int64_t)(k - n) * (D + 4); };
+    static_assert(PER == 2 || PER == 4, "head_dim 64 or 128");
+    using Row = typename std::conditional<PER == 4, float4, float2>::type;
+    // lane k holds partial k's (m, l); further partials (more than 32) are folded in by
+    // the lane-strided loops
+    float2 ml0 = make_float2(-INFINITY, 0.f);
+    if (lane < T) ml0 = *reinterpret_cast<const float2*>(row(lane) + D);
+    float M = ml0.x;
+    for (int k = lane + 32; k < T; k += 32) M = fmaxf(M, row(k)[D]);
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+    float acc[PER];
+#pragma unroll
+    for (int c = 0; c < PER; ++c) acc[c] = 0.f;
+    float L = 0.f;
+    if (M != -INFINITY) {
+        const float w0 = lane < T ? exp2f(ml0.x - M) : 0.f;   // weight of partial `lane`
+        L = w0 * ml0.y;
+        for (int k = lane + 32; k < T; k += 32) {
+            const float2 ml = *reinterpret_cast<const float2*>(row(k) + D);
+            L = fmaf(exp2f(ml.x - M), ml.y, L);
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+        // rows eight at a time, all loads issued before any is used; a row past the end
+        // loads as zero with weight zero, so the sum keeps its order over k
+        for (int k0 = 0; k0 < T; k0 += 8) {
+            Row v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = k0 + j < T ? *reinterpret_cast<const Row*>(row(k0 + j) + lane * PER) : Row{};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int k = k0 + j;
+                float wt = __shfl_sync(0xffffffffu, w0, k & 31);
+                if (k >= 32) wt = k < T ? exp2f(row(k)[D] - M) : 0.f;
+                if (k >= T) wt = 0.f;
+                const float* f = reinterpret_cast<const float*>(&v[j]);
+#pragma unroll
+                for (int c = 0; c < PER; ++c) acc[c] = fmaf(wt, f[c], acc[c]);
+            }
+        }
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint16_t* ob = a.out + ((int64_t)r * a.Hq + (int64_t)h * a.G + gg) * D;
+#pragma unroll
+    for (int c = 0; c < PER; c += 2)
+        *reinterpret_cast<uint32_t*>(ob + lane * PER + c) = pack_bf16x2(acc[c] * inv, acc[c + 1] * inv);
+}
+
 // ------------------------------------------------------------------ host side
 namespace {
 
@@ -1162,7 +1252,13 @@ static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const
     e = launch_pdl(kern, dim3(grid), dim3(plan.warps * 32), (size_t)plan.smem_bytes, st, tk, tv,
                    args);
     if (e != cudaSuccess) return e;
-    // the wide-split merge, a programmatic dependent of the decode grid
+    // the wide-split merge, a programmatic dependent of the decode grid (with a shared
+    // prefix: the merge of every unit with its prefix partials)
+    if constexpr (QT == 1) {
+        if (L.cascade_part != nullptr)
+            return launch_pdl(pkv_cascade_merge_kernel<D>, dim3((unsigned)(L.N * L.Hkv)),
+                              dim3(kGroupPad * 32), 0, st, args);
+    }
     return launch_pdl(pkv_decode_merge_kernel<D, QT>, dim3((unsigned)(L.N * L.Hkv)),
                       dim3(kGroupPad * 32 * QT), 0, st, args);
 }
@@ -1237,6 +1333,9 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     a.scale_log2 = L.scale * 1.4426950408889634f;
     a.stages = plan.stages;
     a.total_warps = plan.total_warps;
+    a.skip_blocks = L.skip_blocks;
+    a.cascade_part = L.cascade_part;
+    a.cascade_split = L.cascade_split;
     cudaError_t e = cudaErrorInvalidValue;
     if (L.kt == 0) {
         if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, 0>(qt, L, plan, tk, tv, a, st);

@@ -70,6 +70,11 @@ struct DecodeLaunch {
     int kt;                               // page kind: 0 bf16, 1 E4M3, 2 int8, 3 int4
     float scale;
     int num_sms;
+    // shared-prefix decode (one query position): the first skip_blocks blocks are left
+    // to the prefix pass whose partials cascade_part holds, cascade_split per row
+    int skip_blocks = 0;
+    const float* cascade_part = nullptr;
+    int cascade_split = 0;
 };
 
 int query_tile(int fp8, int max_q_len);
@@ -104,6 +109,10 @@ struct PrefillLaunch {
     uint32_t* err;                     // device error word, may be null
     int total_q, max_q_len, N, Hq, Hkv, D, BS, MB, NB;
     float scale;
+    // shared-prefix mode: the total_q rows all see block-table row 0's first prefix_len
+    // tokens, split in prefix_split chunks of chunk_tokens; partials go to part
+    int prefix_split = 0, prefix_len = 0, chunk_tokens = 0;
+    float* part = nullptr;
 };
 bool prefill_shape_supported(int Hq, int Hkv, int D, int BS, int dtype);
 cudaError_t dequant_pages_launch(const void* k_cache, const void* v_cache, const float* k_scale,

@@ -194,6 +194,12 @@ struct PrefillArgs {
     uint32_t* err;
     int N, Hq, Hkv, MB, NB, total_q, max_q_len, tiles;
     float scale_log2;
+    // Shared-prefix mode (prefix_split > 0): the total_q query rows all see, unmasked, the
+    // first prefix_len tokens of block-table row 0; blockIdx.z picks a chunk of
+    // chunk_tokens of them, and each row writes its unnormalised partial over that chunk,
+    // part[(row * Hq + head) * prefix_split + chunk] = (o[D], m, l), instead of an output.
+    int prefix_split, prefix_len, chunk_tokens;
+    float* part;
 };
 
 // Shared memory, one 1024-byte aligned block (128-byte swizzle atoms):
@@ -227,7 +233,9 @@ struct PrefillSmem {
 // tile, warps 4-7 columns 128-255 (the same TMEM lanes, i.e. the same query rows).  The
 // partners exchange their row max through shared memory once per tile; each keeps its
 // own partial row sum, the halves are added at the end.
-template <int D, int BS, int G>
+// SHARED: the shared-prefix pass (every row sees block-table row 0's first prefix_len
+// tokens, partials out); otherwise causal prefill chunks with bf16 outputs.
+template <int D, int BS, int G, bool SHARED>
 __global__ void __launch_bounds__(kThreads, 1)
     pkv_prefill_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const PrefillArgs a) {
@@ -252,26 +260,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int tile = a.tiles - 1 - (int)blockIdx.x;   // heavy (late) tiles first
     const int h = blockIdx.y;
-    const int r = blockIdx.z;
-    const int q0 = a.q_offsets[r];
-    int q_len = a.q_offsets[r + 1] - q0;
-    const int seq = a.seq_lens[r];
-    if (q_len < 0) q_len = 0;
-    if (q0 < 0 || q0 + q_len > a.total_q) {
-        if (threadIdx.x == 0 && tile == 0 && h == 0) flag_err(a.err, PKV_DEVERR_QLEN_CLAMPED);
-        return;
+    constexpr bool shared = SHARED;
+    const int r = shared ? 0 : (int)blockIdx.z;
+    const int zc = shared ? (int)blockIdx.z : 0;      // shared mode: KV chunk
+    int q0 = 0, q_len = a.total_q, seq = a.prefix_len;
+    if (!shared) {
+        q0 = a.q_offsets[r];
+        q_len = a.q_offsets[r + 1] - q0;
+        seq = a.seq_lens[r];
+        if (q_len < 0) q_len = 0;
+        if (q0 < 0 || q0 + q_len > a.total_q) {
+            if (threadIdx.x == 0 && tile == 0 && h == 0) flag_err(a.err, PKV_DEVERR_QLEN_CLAMPED);
+            return;
+        }
     }
-    const int ctx = seq - q_len;             // tokens before the chunk
+    const int ctx = seq - q_len;             // tokens before the chunk (causal mode)
     if (q_len > a.max_q_len) {               // rows past max_q_len are not computed
         if (threadIdx.x == 0 && h == 0 && (int)blockIdx.x == 0)
             flag_err(a.err, PKV_DEVERR_QLEN_CLAMPED);
         q_len = a.max_q_len;
     }
     if (tile * TQ >= q_len) return;          // past this request's queries: no work
-    int kv_end = ctx + min(tile * TQ + TQ, q_len);   // tokens the tile's last query sees
-    if (kv_end > seq) kv_end = seq;
-    if (kv_end > a.MB * BS) kv_end = a.MB * BS;
+    // KV range of this CTA: tokens kv_lo .. kv_lo + kv_end - 1 of the request's cache
+    int kv_lo = 0, kv_end;
+    if (shared) {
+        kv_lo = zc * a.chunk_tokens;
+        kv_end = min(seq, kv_lo + a.chunk_tokens) - kv_lo;
+        if (kv_lo + kv_end > a.MB * BS) kv_end = a.MB * BS - kv_lo;
+    } else {
+        kv_end = ctx + min(tile * TQ + TQ, q_len);   // tokens the tile's last query sees
+        if (kv_end > seq) kv_end = seq;
+        if (kv_end > a.MB * BS) kv_end = a.MB * BS;
+    }
     if (kv_end < 0) kv_end = 0;
+    const int pg0 = kv_lo / BS;              // first page of the range (kv_lo % BS == 0)
     const int n_tiles = (kv_end + kKvTile - 1) / kKvTile;
     // V halves: both halves of every tile but the last, whose second half is loaded
     // only if a token of it is visible
@@ -367,14 +389,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int st = j & 1;
             if (j >= 2 && !warp_wait(empty + 8 * st, ((j >> 1) - 1) & 1)) break;
             if (*abort_v) break;
-            const int lb0 = j * per;                        // first logical page of the item
+            const int lb0 = j * per;                        // first page of the item in the range
             int npages = (kv_end - lb0 * BS + BS - 1) / BS;
             if (npages > per) npages = per;
             if (lane == 0)
                 mbar_arrive_expect_tx(full + 8 * st, (uint32_t)(npages * KB * BS * 128));
             __syncwarp();
             if (lane < npages) {
-                int blk = a.block_table[(int64_t)r * a.MB + lb0 + lane];
+                int blk = a.block_table[(int64_t)r * a.MB + pg0 + lb0 + lane];
                 int64_t row;
                 if (blk < 0 || blk >= a.NB) {
                     if (is_k) flag_err(a.err, PKV_DEVERR_BLOCK_RANGE);
@@ -471,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tq_i = m / G, g = m - (m / G) * G;
         const int qi = tile * TQ + tq_i;
         const bool row_valid = qi < q_len;
-        int vis = row_valid ? ctx + qi + 1 : 0;  // tokens this row sees
+        int vis = row_valid ? (shared ? kv_end : ctx + qi + 1) : 0;   // tokens this row sees
         if (vis > kv_end) vis = kv_end;
         if (vis < 0) vis = 0;
         const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -580,10 +602,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         xl[hf * kRows + m] = l;
         named_barrier_sync(nbar, 64);
         const float lt = l + xl[(hf ^ 1) * kRows + m];
+        if (shared) {
+            // the row's unnormalised partial over this chunk: o, its reference max m
+            // (log2 domain, scale applied) and sum l; no contribution if nothing was seen.
+            // The tensor-memory loads are warp-collective: every lane takes part (n_tiles
+            // and ok are the same across the warp), only the stores depend on the row.
+            float* prow = a.part + (((int64_t)qi * a.Hq + (int64_t)h * G + g) * a.prefix_split +
+                                    zc) * (D + 4);
+            const bool has = n_tiles > 0 && ok && lt > 0.f;
+#pragma unroll 1
+            for (int c = 0; c < DH / 32; ++c) {
+                float o[32];
+                if (n_tiles > 0 && ok) {
+                    tmem_ld32(lane_base + kColO + hf * DH + c * 32, o);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0.f;
+                }
+                if (row_valid) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(prow + hf * DH + c * 32 + i) =
+                            has ? make_float4(o[i], o[i + 1], o[i + 2], o[i + 3])
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+            if (row_valid && hf == 0)
+                *reinterpret_cast<float2*>(prow + D) =
+                    has ? make_float2(m_ref, lt) : make_float2(-INFINITY, 0.f);
+        }
         const float inv = (lt > 0.f && ok) ? 1.f / lt : 0.f;
         uint16_t* orow = a.out + ((int64_t)(q0 + qi) * a.Hq + (int64_t)h * G + g) * D + hf * DH;
 #pragma unroll 1
-        for (int c = 0; c < DH / 32; ++c) {
+        for (int c = 0; c < (shared ? 0 : DH / 32); ++c) {
             float o[32];
             if (n_tiles > 0 && ok) {
                 tmem_ld32(lane_base + kColO + hf * DH + c * 32, o);
@@ -635,15 +686,17 @@ PFN_cuTensorMapEncodeTiled_v12000 prefill_encode_fn() {
 template <int D, int BS, int G>
 cudaError_t prefill_launch_t(const PrefillLaunch& L, const PrefillArgs& a, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t st) {
-    auto kern = pkv_prefill_kernel<D, BS, G>;
+    auto kern = a.prefix_split > 0 ? pkv_prefill_kernel<D, BS, G, true>
+                                   : pkv_prefill_kernel<D, BS, G, false>;
     // one CTA per SM (it holds all 512 TMEM columns); ask for enough shared memory
     // that no second CTA can be co-resident
     int smem = PrefillSmem<D>::BYTES;
     if (smem < 120 * 1024) smem = 120 * 1024;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(kern, dim3((unsigned)a.tiles, (unsigned)L.Hkv, (unsigned)L.N),
-                      dim3(kThreads), (size_t)smem, st, tk, tv, a);
+    const unsigned gz = (unsigned)(a.prefix_split > 0 ? a.prefix_split : L.N);
+    return launch_pdl(kern, dim3((unsigned)a.tiles, (unsigned)L.Hkv, gz), dim3(kThreads),
+                      (size_t)smem, st, tk, tv, a);
 }
 
 template <int D, int BS>
@@ -712,6 +765,10 @@ int prefill_launch(const PrefillLaunch& L, cudaStream_t st) {
     a.max_q_len = L.max_q_len;
     a.tiles = (L.max_q_len + TQ - 1) / TQ;   // query tiles per request
     a.scale_log2 = L.scale * 1.4426950408889634f;
+    a.prefix_split = L.prefix_split;
+    a.prefix_len = L.prefix_len;
+    a.chunk_tokens = L.chunk_tokens;
+    a.part = L.part;
     if (a.tiles <= 0) return PKV_OK;
     cudaError_t e = cudaErrorInvalidValue;
     if (L.D == 128 && L.BS == 16) e = prefill_launch_g<128, 16>(G, L, a, tk, tv, st);

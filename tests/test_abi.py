@@ -117,6 +117,29 @@ def test_write_slot_hash_reject_bad_arguments(L):
     assert r(16, 16, 0, 16, 16, 16, 16, 16, None) == 0                  # nothing to do
 
 
+def test_shared_prefix_rejects_bad_arguments_without_launching(L):
+    f = L.pkv_paged_decode_attn_shared_prefix
+    # (fake pointers; every call fails a host check before any CUDA call)
+    args = [16, 16, 16, 16, 8, 16, 4, 32, 8, 128, 16, 64, 32, 0.1, 16, 16, 1 << 30, None]
+
+    def call(**kw):
+        a = list(args)
+        for k, v in kw.items():
+            a[{"MB": 4, "N": 6, "Hq": 7, "D": 9, "BS": 10, "prefix": 12, "scale": 13}[k]] = v
+        return f(*a)
+    assert call(prefix=24) == -1               # not a whole number of blocks
+    assert call(prefix=16 * 9) == -1           # past the block table
+    assert call(prefix=-16) == -1
+    assert call(N=-1) == -1
+    assert call(scale=0.0) == -1
+    assert call(D=96) == -2
+    assert call(Hq=24) == -2                   # G = 3: the prefix pass takes 1, 2, 4, 8
+    assert call(BS=8) == -2
+    assert L.pkv_shared_prefix_workspace_size(128, 32, 8, 128, 16, 4096, 152) > \
+        L.pkv_decode_workspace_size(128, 32, 8, 128, 16, 0, 152)
+    assert L.pkv_shared_prefix_workspace_size(128, 32, 8, 96, 16, 4096, 152) == 0
+
+
 def test_binding_raises_when_library_missing(monkeypatch):
     monkeypatch.setattr(pkv, "_lib", None)
     monkeypatch.setattr(pkv, "library_path", "/nonexistent/libpagedkv.so")

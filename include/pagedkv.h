@@ -281,7 +281,7 @@ PKV_API int pkv_paged_decode_attn_shared_prefix(const void *q, const void *k_cac
  *     current device is at most 16 MiB; larger shapes return PKV_ERR_WORKSPACE and
  *     launch nothing.  That size grows with batch * num_kv_heads and with the
  *     device's SM count, so the bound depends on the GPU: on a 152-SM GPU at
- *     head_dim 128 it is batch * num_kv_heads up to about 3,050 for bf16 pages,
+ *     head_dim 128 it is batch * num_kv_heads up to about 2,900 for bf16 pages,
  *     2,750 for E4M3 and int8 pages and 2,140 for int4 pages (whose plans run more
  *     warps per SM).
  *   - Argument checks come in the same order and return the same statuses as

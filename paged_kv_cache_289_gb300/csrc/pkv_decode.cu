@@ -1216,8 +1216,9 @@ DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int ba
     p.stage_bytes = 2 * tile_tokens * row_bytes;
     // Each warp streams its pages through its own 2-stage pipeline; the per-page
     // instruction chain of a warp, not the bytes in flight, limits the rate, so the
-    // CTA runs several warps per SM sub-partition.  Measured on GB300: 6 warps for
-    // single-query bf16 pages, 8 for 8-bit pages (whose tiles carry twice the tokens)
+    // CTA runs several warps per SM sub-partition.  Measured on GB300: 7 warps for
+    // single-query bf16 pages (6 and 8 ran slower), 8 for 8-bit pages (whose tiles carry
+    // twice the tokens)
     // and for several query positions, 12 for single-query int4 pages (compute-bound:
     // 0.44 of the copy peak against 0.40 with 8; 10 warps split unevenly over the four
     // sub-partitions and run slower).
@@ -1225,7 +1226,7 @@ DecodePlan decode_plan(int kt, int head_dim, int block_size, int num_sms, int ba
     // and int4 pages, 256 otherwise)
     // The plan is a pure function of its arguments: pkv_decode_workspace_size and the
     // launch must agree on it in every process.
-    p.warps = (kt == 3 && qt == 1) ? 12 : ((fp8 || qt > 1) ? 8 : 6);
+    p.warps = (kt == 3 && qt == 1) ? 12 : ((fp8 || qt > 1) ? 8 : 7);
     int stages = 131072 / (p.warps * p.stage_bytes);
     if (stages > 16) stages = 16;
     if (stages < 2) stages = 2;

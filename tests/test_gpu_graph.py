@@ -88,3 +88,77 @@ def test_decode_step_graph_replay_equals_eager(cfg):
         assert np.array_equal(got_k, dev_bits(kc)), f"replay {rep}: cache differs"
         assert np.array_equal(got_h, h_e.cpu().numpy()), f"replay {rep}: hashes differ"
         assert pkv.read_device_error(ws) == 0
+
+
+def test_shared_prefix_step_with_resumed_hash_graph_replay_equals_eager():
+    """The serving-style step of the prefix-sharing workload (small): slot mapping, write,
+    shared-prefix decode (prefix pass, tail decode, merge) and the resumed hash chains,
+    captured once and replayed with new queries and new K rows; bit for bit the eager
+    calls."""
+    torch = torch_mod()
+    wl = W.make(4, small=True)
+    d = W.host_data(wl)
+    prefix = wl.notes["shared_prefix_blocks"] * wl.BS
+    bt, sl = to_dev(wl.block_table), to_dev(wl.seq_lens)
+    pos = to_dev(wl.new_token_positions())
+    toks, toffs = to_dev(wl.tokens), to_dev(wl.token_offsets)
+    lens = np.diff(wl.token_offsets)
+    first = ((lens - 1) // wl.hash_block).astype(np.int64)   # blocks full before the step
+    ho = np.zeros(wl.N + 1, np.int64)
+    np.cumsum(lens // wl.hash_block - first, out=ho[1:])
+    nh = int(ho[-1])
+    fho = np.zeros(wl.N + 1, np.int64)
+    np.cumsum(lens // wl.hash_block, out=fho[1:])
+    chain = pkv.prefix_block_hash(toks, toffs, wl.hash_block, to_dev(fho), int(fho[-1]), seed=3)
+    chain = chain.cpu().numpy().view(np.uint64)
+    prev = np.array([chain[fho[s] + first[s] - 1] if first[s] > 0 else 3 for s in range(wl.N)],
+                    np.uint64)
+    prev_t, first_t, hoffs = to_dev(prev.view(np.int64)), to_dev(first), to_dev(ho)
+    q = bf16_dev(d["q"])
+    kn, vn = bf16_dev(d["k_new"]), bf16_dev(d["v_new"])
+    kc, vc = bf16_dev(d["k_cache"]), bf16_dev(d["v_cache"])
+    slots = torch.empty(wl.N, dtype=torch.int64, device="cuda")
+    out = torch.empty_like(q)
+    hashes = torch.empty(max(nh, 1), dtype=torch.int64, device="cuda")
+    nws = pkv.shared_prefix_workspace_size(wl.N, wl.Hq, wl.Hkv, wl.D, wl.BS, prefix)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step(st, o, w, h):
+        pkv.compute_slot_mapping(bt, pos, wl.BS, out=slots, stream=st)
+        pkv.kv_cache_write(kn, vn, slots, kc, vc, stream=st)
+        pkv.paged_decode_attn_shared_prefix(q, kc, vc, bt, sl, wl.scale, prefix, out=o,
+                                            workspace=w, stream=st)
+        pkv.prefix_block_hash_resume(toks, toffs, wl.hash_block, prev_t, first_t, hoffs, nh,
+                                     out=h, stream=st)
+
+    with torch.cuda.stream(stream):
+        step(stream, out, ws, hashes)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step(stream, out, ws, hashes)
+    torch.cuda.synchronize()
+
+    rng = np.random.default_rng(9)
+    kc0, vc0 = kc.clone(), vc.clone()
+    for rep in range(3):
+        q.copy_(bf16_dev(W.f32_to_bf16_bits(
+            rng.standard_normal(d["q"].shape).astype(np.float32))))
+        kn.copy_(bf16_dev(W.f32_to_bf16_bits(
+            rng.standard_normal(d["k_new"].shape).astype(np.float32))))
+        kc.copy_(kc0)
+        vc.copy_(vc0)
+        graph.replay()
+        torch.cuda.synchronize()
+        got_out, got_h = dev_bits(out), hashes[:nh].cpu().numpy()
+        kc.copy_(kc0)
+        vc.copy_(vc0)
+        out_e = torch.empty_like(q)
+        ws_e = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+        h_e = torch.empty(max(nh, 1), dtype=torch.int64, device="cuda")
+        step(torch.cuda.current_stream(), out_e, ws_e, h_e)
+        torch.cuda.synchronize()
+        assert np.array_equal(got_out, dev_bits(out_e)), f"replay {rep}: output differs"
+        assert np.array_equal(got_h, h_e[:nh].cpu().numpy()), f"replay {rep}: hashes differ"
+        assert pkv.read_device_error(ws) == 0

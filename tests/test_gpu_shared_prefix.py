@@ -72,6 +72,7 @@ def _run(q, kc, vc, bt, seq, scale, prefix):
     (33, 8, 8, 64, 16, 1024, "u0-100", 3),            # G = 1: 33 rows over 128-row tiles
     (1, 16, 4, 128, 16, 4096, [37], 4),               # one request, a long shared prefix
     (130, 32, 8, 128, 16, 768, "u0-64", 5),           # two query tiles per KV head
+    (7, 32, 8, 128, 32, 320, [0] * 7, 6),             # every tail empty: prefix partials only
 ])
 def test_shared_prefix_matches_full_attention(N, Hq, Hkv, D, BS, prefix, tails, seed):
     if isinstance(tails, str):

@@ -427,7 +427,9 @@ class StepHarness:
                                   dtype=torch.uint8, device=dev)
         self.main = torch.cuda.current_stream(dev)
         self.side = torch.cuda.Stream(dev)
-        self.launches_per_step = 5   # slot map, write, decode, wide-split merge, hash
+        # slot map, write, decode, wide-split merge, hash (+ the prefix pass of the
+        # shared-prefix call)
+        self.launches_per_step = 6 if self.prefix else 5
 
     def decode(self, I, O, stream):
         wl, pkv = self.wl, self.pkv

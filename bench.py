@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--skip-cpu", action="store_true")
     p.add_argument("--skip-per-workload", action="store_true",
                    help="leave out the decode figures of workloads 3, 4 and 5 (workload 2 runs)")
+    p.add_argument("--append", action="store_true",
+                   help="the decode writes each request's new K/V rows itself "
+                        "(pkv_paged_decode_attn_append; bf16 pages); slot mapping runs beside it")
     p.add_argument("--shared-prefix", action="store_true",
                    help="workload 4: decode through pkv_paged_decode_attn_shared_prefix (the "
                         "shared pages attended once for the batch)")
@@ -234,7 +237,7 @@ def workload_config(wl):
                   % (2 * wl.NB * wl.Hkv * wl.BS * wl.D * wl.elt / 1e9)}
 
 
-def decode_algorithmic_bytes(wl, unique=False):
+def decode_algorithmic_bytes(wl, unique=False, append=False):
     """Bytes one decode launch must move: every cached K/V row once, plus the block
     table entries, FP8 scales, q and out.  unique: rows of shared pages counted once
     (the shared-prefix call reads them once)."""
@@ -244,6 +247,8 @@ def decode_algorithmic_bytes(wl, unique=False):
     if wl.quant:
         b += nblk * wl.Hkv * 2 * 4                       # K and V scales
     b += 2 * wl.N * wl.q_len * wl.Hq * wl.D * 2          # q in, out
+    if append:
+        b += 4 * wl.N * wl.Hkv * wl.D * 2                # new K/V rows read and written
     return b
 
 
@@ -357,13 +362,15 @@ class StepHarness:
     (pkv_prefix_block_hash_resume), so only the blocks completed by the step's new
     tokens are read."""
 
-    def __init__(self, wl, dev, hash_mode="full", shared_prefix=False):
+    def __init__(self, wl, dev, hash_mode="full", shared_prefix=False, append=False):
         import torch
         import paged_kv_cache_289_gb300 as pkv
         from paged_kv_cache_289_gb300 import workloads as W
         self.wl, self.dev, self.hash_mode = wl, dev, hash_mode
         # decode through the shared-prefix call (the prefix-sharing workload only)
         self.prefix = wl.notes.get("shared_prefix_blocks", 0) * wl.BS if shared_prefix else 0
+        # the decode writes the step's new rows itself (bf16 pages, one query)
+        self.append = append and not wl.quant and wl.q_len == 1 and not self.prefix
         self.torch, self.pkv = torch, pkv
         dd = W.device_data(wl, dev)
         bt = torch.from_numpy(wl.block_table).to(dev)
@@ -429,7 +436,7 @@ class StepHarness:
         self.side = torch.cuda.Stream(dev)
         # slot map, write, decode, wide-split merge, hash (+ the prefix pass of the
         # shared-prefix call)
-        self.launches_per_step = 6 if self.prefix else 5
+        self.launches_per_step = 6 if self.prefix else (4 if self.append else 5)
 
     def decode(self, I, O, stream):
         wl, pkv = self.wl, self.pkv
@@ -455,6 +462,11 @@ class StepHarness:
         already fills and stretches the decode's tail (measured: +17 us per step)."""
         wl, pkv, main, side = self.wl, self.pkv, self.main, self.side
         side.wait_stream(main)                   # the step's inputs are in place
+        if self.append:
+            # slot mapping feeds nothing on the main stream when the decode writes the
+            # new rows itself: it runs beside the decode
+            pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, req_idx=I["req"], out=self.slots,
+                                     stream=side)
         if self.hash_mode == "full":
             pkv.prefix_block_hash(I["tokens"], I["toffs"], wl.hash_block, I["hoffs"], self.nh,
                                   seed=0, out=O["hashes"], stream=side)
@@ -462,13 +474,19 @@ class StepHarness:
             pkv.prefix_block_hash_resume(I["tokens"], I["toffs"], wl.hash_block,
                                          I["prev_hashes"], I["first_blocks"], I["hoffs"],
                                          self.nh, out=O["hashes"], stream=side)
-        pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, req_idx=I["req"], out=self.slots,
-                                 stream=main)
-        pkv.kv_cache_write(I["k_new"], I["v_new"], self.slots, self.kc, self.vc, self.ks,
-                           self.vs, stream=main)
+        if not self.append:
+            pkv.compute_slot_mapping(I["bt"], I["pos"], wl.BS, req_idx=I["req"], out=self.slots,
+                                     stream=main)
+            pkv.kv_cache_write(I["k_new"], I["v_new"], self.slots, self.kc, self.vc, self.ks,
+                               self.vs, stream=main)
         if dec_ev is not None:
             dec_ev[0].record(main)
-        self.decode(I, O, main)
+        if self.append:
+            pkv.paged_decode_attn_append(I["q"], I["k_new"], I["v_new"], self.kc, self.vc,
+                                         I["bt"], I["sl"], wl.scale, out=O["out"],
+                                         workspace=self.ws, stream=main)
+        else:
+            self.decode(I, O, main)
         if dec_ev is not None:
             dec_ev[1].record(main)
         main.wait_stream(side)
@@ -538,6 +556,21 @@ def per_workload_figures(dev, peak, main_harness=None):
                       "query_tokens_per_s": round(wl.N * wl.q_len / med, 1),
                       "l2": "flushed (a 258 MB buffer read) before every timed launch"})
         assert pkv.read_device_error(h.ws) == 0, "device error word set"
+        if cfg == 2:
+            # the serving form of the same step: each chain resumed from its last full
+            # block, the new rows written by the decode kernel (slot mapping beside it)
+            K = 50
+            hs = StepHarness(wl, dev, "resume", append=True)
+            t_s = hs.time_steps(K, 10)
+            assert pkv.read_device_error(hs.ws) == 0, "device error word set"
+            entry["serving_step"] = {
+                "ms_per_step": round(t_s / K * 1e3, 4),
+                "kv_gbs": round(wl.kv_read_bytes() * K / t_s / 1e9, 1),
+                "steps": K,
+                "what": "slot mapping (beside the decode) + pkv_paged_decode_attn_append (the "
+                        "new rows written by the decode kernel) + merge + "
+                        "pkv_prefix_block_hash_resume (only the blocks the step completes)"}
+            hs = None
         if cfg == 4:
             uniq = wl.unique_kv_read_bytes()
             logical = wl.kv_read_bytes()
@@ -615,7 +648,7 @@ def run_ours(args):
 
     wl = W.make(args.workload, seed=(args.seed if args.seed is not None else args.workload) + rank,
                 batch=args.batch)
-    H = StepHarness(wl, dev, args.hash, shared_prefix=args.shared_prefix)
+    H = StepHarness(wl, dev, args.hash, shared_prefix=args.shared_prefix, append=args.append)
     quant = wl.quant
     main = H.main
     inputs, outputs = H.inputs, H.outputs
@@ -661,7 +694,7 @@ def run_ours(args):
 
     # ---------------- roofline of the dominant launch (decode: main + merge kernels)
     peak, peak_kind = peak_hbm()
-    alg = decode_algorithmic_bytes(wl, unique=bool(H.prefix))
+    alg = decode_algorithmic_bytes(wl, unique=bool(H.prefix), append=H.append)
     achieved = alg / dec_avg / 1e9
     traffic = recorded_traffic(kernel_source_hash(), wl.name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -669,7 +702,9 @@ def run_ours(args):
                 "peak_source": f"{peak_kind} hbm_gbs (copy, read+write bytes)",
                 "kernel": ("pkv_paged_decode_attn_shared_prefix (pkv_prefill_kernel over the "
                            "shared pages, pkv_decode_kernel over the tails, merge)"
-                           if H.prefix else "pkv_paged_decode_attn (pkv_decode_kernel)"),
+                           if H.prefix else
+                           ("pkv_paged_decode_attn_append (pkv_decode_kernel writing the new rows)"
+                            if H.append else "pkv_paged_decode_attn (pkv_decode_kernel)")),
                 "algorithmic_bytes_per_launch": alg,
                 "avg_launch_ms": round(dec_avg * 1e3, 4),
                 "median_launch_ms": round(dec_med * 1e3, 4),
@@ -770,6 +805,8 @@ def run_ours(args):
                 "data": "synthetic (seeded N(0,1) q/K/V, uniform token ids)",
                 "config": dict(workload_config(wl), hash=args.hash,
                                shared_prefix_tokens=H.prefix,
+                               cache_write=("in the decode kernel (append)" if H.append
+                                            else "pkv_kv_cache_write before the decode"),
                                parallelism=f"{world} independent replicas (no collective)"),
                 "query_tokens_per_s": round(total_q / t_max, 1),
                 "pct_of_hbm_peak": round(100 * value / peak, 2),

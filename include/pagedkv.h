@@ -234,6 +234,29 @@ PKV_API int pkv_paged_multiquery_attn(const void *q, const int32_t *q_offsets, i
                                       pkv_stream_t stream);
 
 /*
+ * Decode with the step's cache write folded in (bf16 pages, one query per request):
+ * the same result and the same cache contents as pkv_compute_slot_mapping +
+ * pkv_kv_cache_write of each request's newest token (position seq_lens[r] - 1) followed
+ * by pkv_paged_decode_attn ([P1] "KV Cache：Transformer的循环状态": the new token's K/V
+ * join the cache and the query attends to them; [P3] "组合拳：一次请求的完整旅程": the
+ * new K/V go back into the pool).  k_new, v_new: bf16 [batch][Hkv][D], the newest token's
+ * rows.  The warp whose tile holds that position writes the rows into the token's slot
+ * (block_table[r][(seq_lens[r]-1) / BS], row (seq_lens[r]-1) % BS; a block id outside the
+ * pool is not written and is flagged) and uses them in place of the page's stored row, so
+ * the attention needs no write kernel before it.  seq_lens[r] == 0: nothing is written,
+ * out[r] = 0.  Shapes, workspace (pkv_decode_workspace_size with PKV_BF16) and every
+ * other argument as pkv_paged_decode_attn; k_new / v_new 16-byte aligned.
+ */
+PKV_API int pkv_paged_decode_attn_append(const void *q, const void *k_new, const void *v_new,
+                                         void *k_cache, void *v_cache,
+                                         const int32_t *block_table, int max_blocks_per_seq,
+                                         const int32_t *seq_lens, int batch, int num_q_heads,
+                                         int num_kv_heads, int head_dim, int block_size,
+                                         int num_blocks, float scale, void *out,
+                                         void *workspace, size_t workspace_bytes,
+                                         pkv_stream_t stream);
+
+/*
  * Paged decode attention over a shared prefix ([P3] "优化一：Prefix Cache": requests whose
  * first blocks hash alike share those physical blocks; [P2] "缓存命中与复用").  The same
  * result as pkv_paged_decode_attn (bf16 pages, one query per request) when every request

@@ -16,7 +16,7 @@ __all__ = [
     "DEVERR_SEQ_CLAMPED", "DEVERR_BLOCK_RANGE", "compute_slot_mapping", "kv_cache_write",
     "decode_workspace_size", "alloc_decode_workspace", "paged_decode_attn",
     "paged_decode_attn_noalloc", "prefix_block_hash", "prefix_block_hash_resume",
-    "shared_prefix_workspace_size", "paged_decode_attn_shared_prefix",
+    "shared_prefix_workspace_size", "paged_decode_attn_shared_prefix", "paged_decode_attn_append",
     "multiquery_workspace_size",
     "paged_multiquery_attn", "DEVERR_QLEN_CLAMPED", "kv_cache_write_rescale",
     "device_num_sms", "read_device_error", "copy_blocks", "BlockManager", "ERR_NO_BLOCKS",
@@ -90,6 +90,9 @@ def lib():
                                                         i, f, p, p]
             L.pkv_prefix_block_hash.restype = i
             L.pkv_prefix_block_hash.argtypes = [p, p, i, i, u64, p, p, p]
+            L.pkv_paged_decode_attn_append.restype = i
+            L.pkv_paged_decode_attn_append.argtypes = [p, p, p, p, p, p, i, p, i, i, i, i, i, i,
+                                                       f, p, p, sz, p]
             L.pkv_shared_prefix_workspace_size.restype = sz
             L.pkv_shared_prefix_workspace_size.argtypes = [i, i, i, i, i, i, i]
             L.pkv_paged_decode_attn_shared_prefix.restype = i
@@ -306,6 +309,32 @@ def paged_multiquery_attn(q, q_offsets, max_q_len, k_cache, v_cache, block_table
         _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D,
         BS, NB, dt, float(scale), _ptr(out), _ptr(workspace), workspace.numel(),
         _stream(stream)))
+    return out
+
+
+def paged_decode_attn_append(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, scale,
+                             out=None, workspace=None, stream=None):
+    """paged_decode_attn with each request's newest token (k_new, v_new [N, Hkv, D] bf16,
+    position seq_len - 1) written into the cache by the decode kernel itself: the same
+    output and cache contents as slot mapping + kv_cache_write + paged_decode_attn."""
+    import torch
+    _need(q, "q", (torch.bfloat16,))
+    _need(k_new, "k_new", (torch.bfloat16,))
+    _need(v_new, "v_new", (torch.bfloat16,))
+    _need(k_cache, "k_cache", (torch.bfloat16,))
+    _need(v_cache, "v_cache", (torch.bfloat16,))
+    _need(block_table, "block_table", (torch.int32,))
+    _need(seq_lens, "seq_lens", (torch.int32,))
+    N, Hq, D = q.shape
+    NB, Hkv, BS, _ = k_cache.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = alloc_decode_workspace(N, Hq, Hkv, D, BS, BF16, device=q.device)
+    _check("pkv_paged_decode_attn_append", lib().pkv_paged_decode_attn_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        block_table.shape[1], _ptr(seq_lens), N, Hq, Hkv, D, BS, NB, float(scale), _ptr(out),
+        _ptr(workspace), workspace.numel(), _stream(stream)))
     return out
 
 

@@ -237,6 +237,61 @@ int pkv_prefix_block_hash_resume(const int32_t* tokens, const int64_t* offsets, 
     return e == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
+int pkv_paged_decode_attn_append(const void* q, const void* k_new, const void* v_new,
+                                 void* k_cache, void* v_cache, const int32_t* block_table,
+                                 int max_blocks_per_seq, const int32_t* seq_lens, int batch,
+                                 int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                                 int num_blocks, float scale, void* out, void* workspace,
+                                 size_t workspace_bytes, pkv_stream_t stream) {
+    if (batch < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (!shape_supported(num_q_heads, num_kv_heads, head_dim, block_size, PKV_BF16))
+        return PKV_ERR_UNSUPPORTED;
+    if (batch > pkv::kMaxBatch) return PKV_ERR_UNSUPPORTED;
+    if (batch == 0) return PKV_OK;
+    if (!q || !k_new || !v_new || !k_cache || !v_cache || !block_table || !seq_lens || !out)
+        return PKV_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(k_new, 16) || !aligned(v_new, 16))
+        return PKV_ERR_INVALID_ARG;
+    const int64_t rows = ((int64_t)num_blocks + 1) * num_kv_heads * block_size;
+    const int64_t max_pages = (int64_t)batch * num_kv_heads * max_blocks_per_seq;
+    if (rows >= (int64_t)1 << 31 || max_pages >= (int64_t)1 << 31 ||
+        (int64_t)max_blocks_per_seq * block_size >= (int64_t)1 << 22)
+        return PKV_ERR_UNSUPPORTED;
+    int num_sms = 0;
+    if (current_num_sms(&num_sms) != PKV_OK) return PKV_ERR_CUDA;
+    const size_t need = pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
+                                                    PKV_BF16, num_sms, 1);
+    if (!workspace || workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (!aligned(workspace, 16)) return PKV_ERR_INVALID_ARG;
+    pkv::DecodeLaunch L;
+    L.q = q;
+    L.q_offsets = nullptr;
+    L.max_q_len = 1;
+    L.k_cache = k_cache;
+    L.v_cache = v_cache;
+    L.k_scale = nullptr;
+    L.v_scale = nullptr;
+    L.block_table = block_table;
+    L.seq_lens = seq_lens;
+    L.out = out;
+    L.workspace = workspace;
+    L.N = batch;
+    L.Hq = num_q_heads;
+    L.Hkv = num_kv_heads;
+    L.D = head_dim;
+    L.BS = block_size;
+    L.MB = max_blocks_per_seq;
+    L.NB = num_blocks;
+    L.fp8 = 0;
+    L.kt = PKV_BF16;
+    L.scale = scale;
+    L.num_sms = num_sms;
+    L.k_new = k_new;
+    L.v_new = v_new;
+    return pkv::decode_launch(L, reinterpret_cast<cudaStream_t>(stream));
+}
+
 // ------------------------------------------------------------------ shared prefix
 namespace {
 

@@ -83,6 +83,14 @@ struct DecodeArgs {
     int skip_blocks;
     const float* cascade_part;
     int cascade_split;
+    // Append (bf16 pages, one query): each request's newest token (position seq_len - 1)
+    // has K/V rows k_new / v_new [N][Hkv][D]; the warp whose tile holds that position
+    // writes them into the cache pages (k_cache_w / v_cache_w) and into its tile, so the
+    // call needs no cache write before it.
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint16_t* k_cache_w;
+    uint16_t* v_cache_w;
 };
 
 template <int D, int BS, int KT>
@@ -589,6 +597,43 @@ __global__ void __launch_bounds__(((KT != 0 && KT != 3) || QT > 1) ? 256 : 384, 
                     make_uint4(0u, 0u, 0u, 0u);
             }
             __syncwarp();
+        }
+
+        // ---- append: the request's newest token into the cache and into this tile ----
+        if constexpr (KT == 0 && QT == 1) {
+            if (a.k_new != nullptr && ((fl >> 9) & 1u) && ntok >= 1 && ntok <= C::TT &&
+                tpos0 + ntok == s_seq[seg_r]) {
+                const int tr = ntok - 1;                   // tile row of the token
+                const int prow = __shfl_sync(0xffffffffu, cur.row[0], src);   // block * Hkv + h
+                constexpr int EPL = D / 32;                // elements per lane
+                const int d0 = lane * EPL;
+                const int64_t in = ((int64_t)seg_r * a.Hkv + seg_h) * D + d0;
+                // the 128-byte swizzled tile layout the TMA wrote
+                const uint32_t so = (uint32_t)((d0 / 64) * (C::TT * 128) + tr * 128 +
+                                               ((((d0 % 64) / 8) ^ (tr & 7)) << 4) + (d0 % 8) * 2);
+                const bool in_pool = prow < a.NB * a.Hkv;
+                const int64_t go = ((int64_t)prow * BS + (tpos0 % BS) + tr) * D + d0;
+                if constexpr (EPL == 4) {
+                    const uint2 kv = __ldg(reinterpret_cast<const uint2*>(a.k_new + in));
+                    const uint2 vv = __ldg(reinterpret_cast<const uint2*>(a.v_new + in));
+                    *reinterpret_cast<uint2*>(basep + (kpg - base) + so) = kv;
+                    *reinterpret_cast<uint2*>(basep + (vpg - base) + so) = vv;
+                    if (in_pool) {
+                        *reinterpret_cast<uint2*>(a.k_cache_w + go) = kv;
+                        *reinterpret_cast<uint2*>(a.v_cache_w + go) = vv;
+                    }
+                } else {
+                    const uint32_t kv = __ldg(reinterpret_cast<const uint32_t*>(a.k_new + in));
+                    const uint32_t vv = __ldg(reinterpret_cast<const uint32_t*>(a.v_new + in));
+                    *reinterpret_cast<uint32_t*>(basep + (kpg - base) + so) = kv;
+                    *reinterpret_cast<uint32_t*>(basep + (vpg - base) + so) = vv;
+                    if (in_pool) {
+                        *reinterpret_cast<uint32_t*>(a.k_cache_w + go) = kv;
+                        *reinterpret_cast<uint32_t*>(a.v_cache_w + go) = vv;
+                    }
+                }
+                __syncwarp();
+            }
         }
 
         // ---- S^T = K Q^T (tokens x heads), one n-tile per query position ----
@@ -1337,6 +1382,10 @@ int decode_launch(const DecodeLaunch& L, cudaStream_t st) {
     a.skip_blocks = L.skip_blocks;
     a.cascade_part = L.cascade_part;
     a.cascade_split = L.cascade_split;
+    a.k_new = static_cast<const uint16_t*>(L.k_new);
+    a.v_new = static_cast<const uint16_t*>(L.v_new);
+    a.k_cache_w = static_cast<uint16_t*>(const_cast<void*>(L.k_cache));
+    a.v_cache_w = static_cast<uint16_t*>(const_cast<void*>(L.v_cache));
     cudaError_t e = cudaErrorInvalidValue;
     if (L.kt == 0) {
         if (L.D == 128 && L.BS == 16) e = launch_q<128, 16, 0>(qt, L, plan, tk, tv, a, st);

@@ -75,6 +75,10 @@ struct DecodeLaunch {
     int skip_blocks = 0;
     const float* cascade_part = nullptr;
     int cascade_split = 0;
+    // append (bf16, one query): the newest token's K/V rows [N][Hkv][D], written by the
+    // decode kernel into the cache and used in place of the page's stored row
+    const void* k_new = nullptr;
+    const void* v_new = nullptr;
 };
 
 int query_tile(int fp8, int max_q_len);

@@ -140,6 +140,25 @@ def test_shared_prefix_rejects_bad_arguments_without_launching(L):
     assert L.pkv_shared_prefix_workspace_size(128, 32, 8, 96, 16, 4096, 152) == 0
 
 
+def test_append_rejects_bad_arguments_without_launching(L):
+    f = L.pkv_paged_decode_attn_append
+    # q, k_new, v_new, k_cache, v_cache, bt, MB, sl, N, Hq, Hkv, D, BS, NB, scale, out, ws,
+    # ws_bytes, stream (fake pointers: each call fails a host check first)
+    a = [16, 16, 16, 16, 16, 16, 4, 16, 2, 8, 2, 128, 16, 8, 0.1, 16, 16, 1 << 20, None]
+
+    def call(i, v):
+        b = list(a)
+        b[i] = v
+        return f(*b)
+    assert call(8, -1) == -1          # batch
+    assert call(6, 0) == -1           # max blocks per sequence
+    assert call(11, 96) == -2         # head_dim
+    assert call(9, 9) == -2           # Hq % Hkv
+    assert call(1, None) == -1        # no k_new
+    assert call(2, 8) == -1           # v_new misaligned
+    assert call(8, 0) == 0            # empty batch
+
+
 def test_binding_raises_when_library_missing(monkeypatch):
     monkeypatch.setattr(pkv, "_lib", None)
     monkeypatch.setattr(pkv, "library_path", "/nonexistent/libpagedkv.so")

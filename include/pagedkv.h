@@ -271,13 +271,22 @@ PKV_API int pkv_paged_decode_attn_append(const void *q, const void *k_new, const
  *   2. the decode kernel attends each request to its tokens prefix_len .. seq_lens[r]-1
  *      and leaves a partial for every (request, KV head);
  *   3. a merge combines each row's partials with log-sum-exp weights into out.
+ * When step 1 needs few CTAs (its 128-row query tiles x num_kv_heads at most a third of
+ * the SMs) and, by a cost estimate that takes each tail as half the room the block table
+ * leaves after the prefix, finishes sooner that way, it runs as one KV chunk per CTA on a
+ * second stream the library keeps per device, while step 2 runs on stream sized to the
+ * remaining SMs; stream waits for it before step 3.  That second stream and its two
+ * events are created by the first such call with the device current (make that call
+ * outside stream capture; later calls capture into a CUDA graph, the fork and join
+ * becoming graph edges) and again after the device's context changes.
  * prefix_len must be a multiple of block_size and at most max_blocks_per_seq *
  * block_size (else PKV_ERR_INVALID_ARG); 0 runs the plain decode.  scale finite and > 0.
  * Supported: bf16 pages, head_dim 64 or 128, block_size 16 or 32, G = Hq / Hkv in
  * {1, 2, 4, 8}; otherwise PKV_ERR_UNSUPPORTED.  workspace: at least
  * pkv_shared_prefix_workspace_size(...) bytes (0 for an unsupported shape), 256-byte
  * aligned, no clearing needed; its first word is the device error word.  Three
- * launches on stream, no host synchronisation.
+ * launches, no host synchronisation; PKV_ERR_CUDA if the second stream or its events
+ * cannot be created.
  */
 PKV_API size_t pkv_shared_prefix_workspace_size(int batch, int num_q_heads, int num_kv_heads,
                                                 int head_dim, int block_size, int prefix_len,

@@ -6,6 +6,10 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
+#include <cuda.h>
+
 #include "pkv_internal.cuh"
 
 
@@ -297,22 +301,107 @@ namespace {
 
 // KV chunks of the prefix pass: enough (query tile, KV head, chunk) CTAs to cover the
 // SMs, each chunk a whole number of 256-token tiles.
-int shared_prefix_split(int batch, int Hq, int Hkv, int prefix_len, int num_sms,
-                        int* chunk_tokens) {
+// How the shared-prefix call divides the GPU.  The prefix pass has rows = batch x G query
+// rows per KV head, in 128-row tiles: CTAs = tiles x Hkv x split.
+//   sequential: the prefix pass split into chunks so that its CTAs fill the SMs, then the
+//     tail decode over every SM, then the merge.
+//   overlapped: the prefix pass with one chunk per CTA (few CTAs) on a second stream,
+//     while the tail decode runs on the remaining SMs, then the merge.  Chosen when those
+//     CTAs take at most a third of the SMs and, by a cost estimate, finish sooner: the
+//     prefix pass at about 2.1 us per 256-token tile plus 6.5 us per CTA, the tails
+//     streamed at about 6.5 TB/s, each tail taken as half the room the block table leaves
+//     after the prefix (the host does not see the lengths).
+struct SharedPrefixPlan {
+    int split;        // chunks of the prefix (one per CTA along the third grid axis)
+    int chunk;        // tokens per chunk
+    int dec_sms;      // SMs the tail decode is sized for
+    bool overlap;
+};
+
+SharedPrefixPlan shared_prefix_plan(int batch, int Hq, int Hkv, int D, int BS, int MB,
+                                    int prefix_len, int num_sms) {
+    SharedPrefixPlan p{0, 0, num_sms, false};
     const int G = Hq / Hkv;
     const int TQ = 128 / G;
     const int tiles = (batch + TQ - 1) / TQ;
     const int ktiles = (prefix_len + 255) / 256;
-    if (ktiles == 0 || tiles == 0) {
-        *chunk_tokens = 0;
-        return 0;
-    }
+    if (ktiles == 0 || tiles == 0) return p;
     int want = (num_sms + tiles * Hkv - 1) / (tiles * Hkv);
     if (want < 1) want = 1;
     if (want > ktiles) want = ktiles;
     const int per = (ktiles + want - 1) / want;
-    *chunk_tokens = per * 256;
-    return (ktiles + per - 1) / per;
+    p.chunk = per * 256;
+    p.split = (ktiles + per - 1) / per;
+    const int k = tiles * Hkv;                  // prefix CTAs with one chunk each
+    if (3 * k <= num_sms) {
+        const double tile_us = 2.1, cta_us = 6.5, gbs = 6500.0;
+        const double tail_tokens = 0.5 * ((double)MB * BS - prefix_len);
+        const double tail_us =
+            (double)batch * tail_tokens * Hkv * D * 2.0 * 2.0 / (gbs * 1e3);
+        const double seq_us = per * tile_us + cta_us + tail_us;
+        const double ovl_us = fmax(ktiles * tile_us + cta_us,
+                                   tail_us * num_sms / (double)(num_sms - k));
+        if (ovl_us < seq_us) {
+            p.split = 1;
+            p.chunk = ktiles * 256;
+            p.dec_sms = num_sms - k;
+            p.overlap = true;
+        }
+    }
+    return p;
+}
+
+// A second stream and two events per device for the overlapped prefix pass, created on
+// the first overlapped call with that device current (make that call outside stream
+// capture) and again after the device's context changes.  One lock serialises the fork
+// and join of concurrent callers.
+typedef CUresult (*ctx_get_current_fn)(CUcontext*);
+
+ctx_get_current_fn side_ctx_get_current() {
+    static ctx_get_current_fn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &qr) == cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<ctx_get_current_fn>(p);
+    });
+    return fn;
+}
+
+struct SideStream {
+    CUcontext ctx = nullptr;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxSideDevices = 64;
+std::mutex g_side_mu;
+SideStream g_side[kMaxSideDevices];
+
+// With g_side_mu held.
+int side_stream(SideStream** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxSideDevices) return PKV_ERR_UNSUPPORTED;
+    ctx_get_current_fn get = side_ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS || !ctx) return PKV_ERR_CUDA;
+    SideStream& s = g_side[dev];
+    if (s.ctx != ctx || !s.stream) {
+        // a new context: the old handles belonged to a context that is gone
+        SideStream n;
+        if (cudaStreamCreateWithFlags(&n.stream, cudaStreamNonBlocking) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        if (cudaEventCreateWithFlags(&n.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&n.join, cudaEventDisableTiming) != cudaSuccess)
+            return PKV_ERR_CUDA;
+        n.ctx = ctx;
+        s = n;
+    }
+    *out = &s;
+    return PKV_OK;
 }
 
 bool shared_prefix_supported(int Hq, int Hkv, int D, int BS) {
@@ -330,11 +419,13 @@ size_t pkv_shared_prefix_workspace_size(int batch, int num_q_heads, int num_kv_h
     if (num_sms <= 0 && current_num_sms(&num_sms) != PKV_OK) return 0;
     const size_t dec = pkv::decode_workspace_bytes(batch, num_kv_heads, head_dim, block_size,
                                                    PKV_BF16, num_sms, 1);
-    int chunk = 0;
-    const int split = shared_prefix_split(batch, num_q_heads, num_kv_heads, prefix_len, num_sms,
-                                          &chunk);
+    // the prefix partials for the sequential plan's split, which is at least the
+    // overlapped plan's one chunk; the decode part for every SM, at least the tail
+    // decode's share of them
+    const SharedPrefixPlan p = shared_prefix_plan(batch, num_q_heads, num_kv_heads, head_dim,
+                                                  block_size, 0, prefix_len, num_sms);
     return (size_t)pkv::align_up((int64_t)dec, 256) +
-           (size_t)batch * num_q_heads * split * (head_dim + 4) * 4;
+           (size_t)batch * num_q_heads * p.split * (head_dim + 4) * 4;
 }
 
 int pkv_paged_decode_attn_shared_prefix(const void* q, const void* k_cache, const void* v_cache,
@@ -379,9 +470,10 @@ int pkv_paged_decode_attn_shared_prefix(const void* q, const void* k_cache, cons
                                                    PKV_BF16, num_sms, 1);
     float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                            pkv::align_up((int64_t)dec, 256));
-    int chunk = 0;
-    const int split = shared_prefix_split(batch, num_q_heads, num_kv_heads, prefix_len, num_sms,
-                                          &chunk);
+    const SharedPrefixPlan plan =
+        shared_prefix_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                           max_blocks_per_seq, prefix_len, num_sms);
+    const int split = plan.split, chunk = plan.chunk;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // 1) the shared pages once for every request: all queries as the rows of a
     //    non-causal pass over block-table row 0's first prefix_len tokens
@@ -408,8 +500,20 @@ int pkv_paged_decode_attn_shared_prefix(const void* q, const void* k_cache, cons
     P.prefix_len = prefix_len;
     P.chunk_tokens = chunk;
     P.part = part;
-    int stp = pkv::prefill_launch(P, st);
+    // overlapped: the prefix pass forks onto the side stream and joins before the merge
+    std::unique_lock<std::mutex> side_lock;
+    SideStream* side = nullptr;
+    if (plan.overlap) {
+        side_lock = std::unique_lock<std::mutex>(g_side_mu);
+        const int sst = side_stream(&side);
+        if (sst != PKV_OK) return sst;
+        if (cudaEventRecord(side->fork, st) != cudaSuccess ||
+            cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    int stp = pkv::prefill_launch(P, side ? side->stream : st);
     if (stp != PKV_OK) return stp;
+    if (side && cudaEventRecord(side->join, side->stream) != cudaSuccess) return PKV_ERR_CUDA;
     // 2) each request's private pages, every unit as a partial, 3) the merge
     pkv::DecodeLaunch L;
     L.q = q;
@@ -433,10 +537,11 @@ int pkv_paged_decode_attn_shared_prefix(const void* q, const void* k_cache, cons
     L.fp8 = 0;
     L.kt = PKV_BF16;
     L.scale = scale;
-    L.num_sms = num_sms;
+    L.num_sms = plan.dec_sms;
     L.skip_blocks = prefix_len / block_size;
     L.cascade_part = part;
     L.cascade_split = split;
+    L.merge_after = side ? side->join : nullptr;
     return pkv::decode_launch(L, st);
 }
 

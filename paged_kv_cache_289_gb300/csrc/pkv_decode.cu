@@ -1298,6 +1298,10 @@ static cudaError_t launch_t(const DecodeLaunch& L, const DecodePlan& plan, const
     e = launch_pdl(kern, dim3(grid), dim3(plan.warps * 32), (size_t)plan.smem_bytes, st, tk, tv,
                    args);
     if (e != cudaSuccess) return e;
+    if (L.merge_after != nullptr) {
+        e = cudaStreamWaitEvent(st, L.merge_after, 0);
+        if (e != cudaSuccess) return e;
+    }
     // the wide-split merge, a programmatic dependent of the decode grid (with a shared
     // prefix: the merge of every unit with its prefix partials)
     if constexpr (QT == 1) {

@@ -79,6 +79,9 @@ struct DecodeLaunch {
     // decode kernel into the cache and used in place of the page's stored row
     const void* k_new = nullptr;
     const void* v_new = nullptr;
+    // when set, the merge waits for this event (recorded after work on another stream
+    // whose results it reads, e.g. a prefix pass run beside the decode)
+    cudaEvent_t merge_after = nullptr;
 };
 
 int query_tile(int fp8, int max_q_len);

@@ -162,3 +162,59 @@ def test_shared_prefix_step_with_resumed_hash_graph_replay_equals_eager():
         assert np.array_equal(got_out, dev_bits(out_e)), f"replay {rep}: output differs"
         assert np.array_equal(got_h, h_e[:nh].cpu().numpy()), f"replay {rep}: hashes differ"
         assert pkv.read_device_error(ws) == 0
+
+
+def test_overlapped_shared_prefix_call_graph_replay_equals_eager():
+    """A batch whose shared-prefix call takes the overlapped plan (the prefix pass on the
+    library's second stream beside the tail decode, joined before the merge), captured
+    once: the fork and join become graph edges, and every replay with new queries equals
+    the eager call bit for bit."""
+    torch = torch_mod()
+    rng = np.random.default_rng(31)
+    N, Hq, Hkv, D, BS, prefix = 40, 32, 8, 128, 16, 256
+    tails = rng.integers(600, 1201, size=N)
+    npre = prefix // BS
+    ntail = [-(-int(t) // BS) for t in tails]
+    NB = npre + sum(ntail) + 4
+    ids = rng.permutation(NB).astype(np.int32)
+    MB = npre + max(ntail)
+    bt = np.zeros((N, MB), np.int32)
+    o = npre
+    for r in range(N):
+        bt[r, :npre] = ids[:npre]
+        bt[r, npre:npre + ntail[r]] = ids[o:o + ntail[r]]
+        o += ntail[r]
+    seq = (prefix + tails).astype(np.int32)
+    kc = bf16_dev(W.f32_to_bf16_bits(rng.standard_normal((NB, Hkv, BS, D), dtype=np.float32)))
+    vc = bf16_dev(W.f32_to_bf16_bits(rng.standard_normal((NB, Hkv, BS, D), dtype=np.float32)))
+    q = bf16_dev(W.f32_to_bf16_bits(rng.standard_normal((N, Hq, D), dtype=np.float32)))
+    btd, sld = to_dev(bt), to_dev(seq)
+    nws = pkv.shared_prefix_workspace_size(N, Hq, Hkv, D, BS, prefix)
+    ws = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(q)
+    stream = torch.cuda.Stream()
+    scale = 1.0 / np.sqrt(D)
+
+    def call(st, o_, w_):
+        pkv.paged_decode_attn_shared_prefix(q, kc, vc, btd, sld, scale, prefix, out=o_,
+                                            workspace=w_, stream=st)
+
+    with torch.cuda.stream(stream):
+        call(stream, out, ws)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        call(stream, out, ws)
+    torch.cuda.synchronize()
+    for rep in range(3):
+        q.copy_(bf16_dev(W.f32_to_bf16_bits(
+            rng.standard_normal((N, Hq, D)).astype(np.float32))))
+        graph.replay()
+        torch.cuda.synchronize()
+        got = dev_bits(out)
+        out_e = torch.empty_like(q)
+        ws_e = torch.zeros(nws, dtype=torch.uint8, device="cuda")
+        call(torch.cuda.current_stream(), out_e, ws_e)
+        torch.cuda.synchronize()
+        assert np.array_equal(got, dev_bits(out_e)), f"replay {rep}: output differs"
+        assert pkv.read_device_error(ws) == 0

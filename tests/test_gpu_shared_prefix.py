@@ -73,6 +73,10 @@ def _run(q, kc, vc, bt, seq, scale, prefix):
     (1, 16, 4, 128, 16, 4096, [37], 4),               # one request, a long shared prefix
     (130, 32, 8, 128, 16, 768, "u0-64", 5),           # two query tiles per KV head
     (7, 32, 8, 128, 32, 320, [0] * 7, 6),             # every tail empty: prefix partials only
+    # few prefix CTAs (2 tiles x 8 heads) and long tails: the prefix pass runs on its own
+    # stream beside a tail decode sized to the remaining SMs
+    (40, 32, 8, 128, 16, 256, "u600-1200", 8),
+    (64, 16, 8, 128, 32, 512, "u900-1500", 9),
 ])
 def test_shared_prefix_matches_full_attention(N, Hq, Hkv, D, BS, prefix, tails, seed):
     if isinstance(tails, str):

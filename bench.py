@@ -529,10 +529,13 @@ class StepHarness:
 
 def per_workload_figures(dev, peak, main_harness=None):
     """Decode-launch rooflines measured in the same run: the headline workload (2), long
-    contexts (3) and E4M3 pages (5) with an L2 flush between launches; prefix sharing
-    (4) on logical and on unique bytes, with and without the flush; and workload 3's
-    whole step with the full and the resumed prefix hash.  Each launch figure is the
-    median of 50 after 10 warm-ups."""
+    contexts (3), E4M3 / INT8 / INT4 pages (5, 7, 9) and four query positions (6) with an
+    L2 flush between launches; prefix sharing (4) on logical and on unique bytes, with and
+    without the flush; and workload 3's whole step with the full and the resumed prefix
+    hash.  Each launch figure is the median of 50 after 10 warm-ups.  Launched alone, the
+    decode kernels of workloads 6, 7 and 9 do not meet the full re-hash's CTAs, which in a
+    step (hash first, on the side stream) hold SM resources those register-heavy plans
+    need and delay some of their persistent CTAs."""
     import torch
     import paged_kv_cache_289_gb300 as pkv
     from paged_kv_cache_289_gb300 import workloads as W
@@ -540,7 +543,7 @@ def per_workload_figures(dev, peak, main_harness=None):
     res = {}
     sampler = ClockSampler(dev.index or 0)
     sampler.start()
-    for cfg in (2, 3, 5, 4):
+    for cfg in (2, 3, 5, 7, 9, 6, 4):
         if cfg == 2 and main_harness is None:
             continue
         wl = main_harness.wl if cfg == 2 else W.make(cfg)

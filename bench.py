@@ -321,6 +321,19 @@ def cpu_baseline(wl, H, budget_s=15.0, single_budget_s=4.0):
             st += dt
             sb += nb
             n1 += 1
+        # the tiny configuration (4 requests of 17..100 tokens, one KV head), whole
+        # batch per pass, on the same one thread
+        from paged_kv_cache_289_gb300 import workloads as W
+        tw = W.make(1)
+        td = W.host_data(tw)
+        tb = int(tw.seq_lens.sum()) * tw.Hkv * tw.D * 2 * 2
+        tt, tn = 0.0, 0
+        while tt < 1.0:
+            t0 = time.perf_counter()
+            oracle.decode_attn(td["q"], td["k_cache"], td["v_cache"], tw.block_table,
+                               tw.seq_lens, tw.scale)
+            tt += time.perf_counter() - t0
+            tn += 1
     finally:
         oracle.set_num_threads(cores)
     return {"value": round(tot_b / tot_t / 1e9, 4), "unit": UNIT, "cores": cores,
@@ -330,7 +343,12 @@ def cpu_baseline(wl, H, budget_s=15.0, single_budget_s=4.0):
                       f"in {tot_t:.1f} s); fp64 C + OpenMP",
             "single_thread": {"value": round(sb / st / 1e9, 4), "unit": UNIT, "cores": 1,
                               "sample": f"{n1} passes over the {wl.Hkv} units of request 0 "
-                                        f"({sb/1e9:.2f} GB in {st:.1f} s)"}}
+                                        f"({sb/1e9:.2f} GB in {st:.1f} s)"},
+            "single_thread_tiny": {"value": round(tb * tn / tt / 1e9, 4), "unit": UNIT,
+                                   "cores": 1,
+                                   "sample": f"{tn} passes over the whole tiny batch "
+                                             f"({tw.name}: {tw.N} requests, {tb} B of K/V per "
+                                             f"pass, {tt:.2f} s)"}}
 
 
 def l2_flush_buffer(torch, dev):

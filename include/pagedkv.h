@@ -299,6 +299,17 @@ PKV_API int pkv_paged_decode_attn_shared_prefix(const void *q, const void *k_cac
                                                 int prefix_len, float scale, void *out,
                                                 void *workspace, size_t workspace_bytes,
                                                 pkv_stream_t stream);
+/*
+ * The plan pkv_paged_decode_attn_shared_prefix takes for these arguments on a device with
+ * num_sms SMs (num_sms <= 0: the current device's): 1 overlapped (the prefix pass on the
+ * library's second stream beside the tail decode), 0 sequential; negative: the status the
+ * call would return for an invalid or unsupported shape.  When not null, *prefix_ctas
+ * receives the prefix pass's CTAs and *decode_sms the SMs the tail decode is sized for.
+ * Host only: launches nothing.
+ */
+PKV_API int pkv_shared_prefix_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int max_blocks_per_seq, int prefix_len,
+                                   int num_sms, int *prefix_ctas, int *decode_sms);
 
 /*
  * Paged decode attention that allocates nothing.  The sources describe no such

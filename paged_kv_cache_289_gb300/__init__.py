@@ -95,6 +95,8 @@ def lib():
                                                        f, p, p, sz, p]
             L.pkv_shared_prefix_workspace_size.restype = sz
             L.pkv_shared_prefix_workspace_size.argtypes = [i, i, i, i, i, i, i]
+            L.pkv_shared_prefix_plan.restype = i
+            L.pkv_shared_prefix_plan.argtypes = [i, i, i, i, i, i, i, i, p, p]
             L.pkv_paged_decode_attn_shared_prefix.restype = i
             L.pkv_paged_decode_attn_shared_prefix.argtypes = [p, p, p, p, i, p, i, i, i, i, i, i,
                                                               i, f, p, p, sz, p]
@@ -342,6 +344,20 @@ def shared_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, blo
                                  prefix_len, num_sms=0) -> int:
     return int(lib().pkv_shared_prefix_workspace_size(batch, num_q_heads, num_kv_heads, head_dim,
                                                       block_size, prefix_len, num_sms))
+
+
+def shared_prefix_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                       max_blocks_per_seq, prefix_len, num_sms=0):
+    """(overlapped, prefix_ctas, decode_sms) that paged_decode_attn_shared_prefix takes for
+    these arguments (num_sms 0: the current device's SMs); raises PkvError for a shape
+    the call would refuse."""
+    ctas, sms = ctypes.c_int(0), ctypes.c_int(0)
+    r = lib().pkv_shared_prefix_plan(batch, num_q_heads, num_kv_heads, head_dim, block_size,
+                                     max_blocks_per_seq, prefix_len, num_sms,
+                                     ctypes.byref(ctas), ctypes.byref(sms))
+    if r < 0:
+        _check("pkv_shared_prefix_plan", r)
+    return bool(r), ctas.value, sms.value
 
 
 def paged_decode_attn_shared_prefix(q, k_cache, v_cache, block_table, seq_lens, scale,

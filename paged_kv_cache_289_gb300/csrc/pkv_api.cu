@@ -411,6 +411,26 @@ bool shared_prefix_supported(int Hq, int Hkv, int D, int BS) {
 
 }  // namespace
 
+int pkv_shared_prefix_plan(int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                           int block_size, int max_blocks_per_seq, int prefix_len, int num_sms,
+                           int* prefix_ctas, int* decode_sms) {
+    if (batch < 0 || max_blocks_per_seq <= 0 || prefix_len < 0) return PKV_ERR_INVALID_ARG;
+    if (!shared_prefix_supported(num_q_heads, num_kv_heads, head_dim, block_size))
+        return PKV_ERR_UNSUPPORTED;
+    if (batch > pkv::kMaxBatch) return PKV_ERR_UNSUPPORTED;
+    if (prefix_len % block_size != 0 || prefix_len > max_blocks_per_seq * block_size)
+        return PKV_ERR_INVALID_ARG;
+    if (num_sms <= 0 && current_num_sms(&num_sms) != PKV_OK) return PKV_ERR_CUDA;
+    const SharedPrefixPlan p = shared_prefix_plan(batch, num_q_heads, num_kv_heads, head_dim,
+                                                  block_size, max_blocks_per_seq, prefix_len,
+                                                  num_sms);
+    const int G = num_q_heads / num_kv_heads;
+    const int tiles = (batch + 128 / G - 1) / (128 / G);
+    if (prefix_ctas) *prefix_ctas = p.split > 0 ? tiles * num_kv_heads * p.split : 0;
+    if (decode_sms) *decode_sms = p.dec_sms;
+    return p.overlap ? 1 : 0;
+}
+
 size_t pkv_shared_prefix_workspace_size(int batch, int num_q_heads, int num_kv_heads,
                                         int head_dim, int block_size, int prefix_len,
                                         int num_sms) {

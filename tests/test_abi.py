@@ -140,6 +140,36 @@ def test_shared_prefix_rejects_bad_arguments_without_launching(L):
     assert L.pkv_shared_prefix_workspace_size(128, 32, 8, 96, 16, 4096, 152) == 0
 
 
+def test_shared_prefix_plan_query(L):
+    """The plan query (host only) for the overlapped and the sequential shared-prefix
+    plans: the overlapped one keeps the prefix pass to a third of the SMs and sizes the
+    tail decode to the rest."""
+    import ctypes
+    f = L.pkv_shared_prefix_plan
+    f.restype = ctypes.c_int
+    ctas, sms = ctypes.c_int(-7), ctypes.c_int(-7)
+
+    def plan(*a):
+        r = f(*a, ctypes.byref(ctas), ctypes.byref(sms))
+        return r, ctas.value, sms.value
+    # 40 requests x 4 query heads per KV head = 2 tiles of 128 rows, x 8 KV heads; tails of
+    # up to (128 x 16 - 256) tokens: overlapped, 16 prefix CTAs, the decode on 136 SMs
+    assert plan(40, 32, 8, 128, 16, 128, 256, 152) == (1, 16, 136)
+    # 128 requests over a 4096-token prefix: 4 tiles x 8 heads, split into 4 chunks of
+    # 1024 tokens to fill the SMs, then the tails on every SM
+    assert plan(128, 32, 8, 128, 16, 512, 4096, 152) == (0, 128, 152)
+    # a third of 40 SMs is under 16 prefix CTAs: sequential
+    assert plan(40, 32, 8, 128, 16, 128, 256, 40)[0] == 0
+    for a in [(40, 32, 8, 128, 16, 128, 256, 152), (64, 16, 8, 128, 32, 64, 512, 152),
+              (5, 64, 8, 128, 32, 15, 160, 152)]:
+        r, c, s = plan(*a)
+        assert r == 1 and 3 * c <= a[-1] and s == a[-1] - c
+    assert f(40, 32, 8, 128, 16, 128, 24, 152, None, None) == -1   # not whole blocks
+    assert f(40, 32, 8, 128, 16, 8, 256, 152, None, None) == -1    # past the block table
+    assert f(40, 24, 8, 128, 16, 128, 256, 152, None, None) == -2  # G = 3
+    assert f(40, 32, 8, 96, 16, 128, 256, 152, None, None) == -2   # head_dim
+
+
 def test_append_rejects_bad_arguments_without_launching(L):
     f = L.pkv_paged_decode_attn_append
     # q, k_new, v_new, k_cache, v_cache, bt, MB, sl, N, Hq, Hkv, D, BS, NB, scale, out, ws,

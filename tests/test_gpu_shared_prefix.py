@@ -66,23 +66,27 @@ def _run(q, kc, vc, bt, seq, scale, prefix):
     return out
 
 
-@pytest.mark.parametrize("N,Hq,Hkv,D,BS,prefix,tails,seed", [
-    (12, 32, 8, 128, 16, 512, "u16-200", 1),        # the prefix-sharing shape, small
-    (5, 64, 8, 128, 32, 160, [0, 1, 300, 31, 32], 2),   # G = 8, prefix not a 256 multiple
-    (33, 8, 8, 64, 16, 1024, "u0-100", 3),            # G = 1: 33 rows over 128-row tiles
-    (1, 16, 4, 128, 16, 4096, [37], 4),               # one request, a long shared prefix
-    (130, 32, 8, 128, 16, 768, "u0-64", 5),           # two query tiles per KV head
-    (7, 32, 8, 128, 32, 320, [0] * 7, 6),             # every tail empty: prefix partials only
-    # few prefix CTAs (2 tiles x 8 heads) and long tails: the prefix pass runs on its own
-    # stream beside a tail decode sized to the remaining SMs
-    (40, 32, 8, 128, 16, 256, "u600-1200", 8),
-    (64, 16, 8, 128, 32, 512, "u900-1500", 9),
+# ovl: the plan the call takes on a 152-SM device (checked first, so that both plans are
+# known to be covered): True = the prefix pass on its own stream beside a tail decode sized
+# to the remaining SMs (few prefix CTAs, long tails), False = prefix pass, then tails.
+@pytest.mark.parametrize("N,Hq,Hkv,D,BS,prefix,tails,seed,ovl", [
+    (12, 32, 8, 128, 16, 512, "u16-200", 1, False),   # the prefix-sharing shape, small
+    (5, 64, 8, 128, 32, 160, [0, 1, 300, 31, 32], 2, True),   # G = 8, prefix not 256k
+    (33, 8, 8, 64, 16, 1024, "u0-100", 3, False),     # G = 1: 33 rows over 128-row tiles
+    (1, 16, 4, 128, 16, 4096, [37], 4, False),        # one request, a long shared prefix
+    (130, 32, 8, 128, 16, 768, "u0-64", 5, False),    # two query tiles per KV head
+    (7, 32, 8, 128, 32, 320, [0] * 7, 6, False),      # every tail empty: prefix partials only
+    (40, 32, 8, 128, 16, 256, "u600-1200", 8, True),  # 2 tiles x 8 heads, long tails
+    (64, 16, 8, 128, 32, 512, "u900-1500", 9, True),
 ])
-def test_shared_prefix_matches_full_attention(N, Hq, Hkv, D, BS, prefix, tails, seed):
+def test_shared_prefix_matches_full_attention(N, Hq, Hkv, D, BS, prefix, tails, seed, ovl):
     if isinstance(tails, str):
         lo, hi = (int(x) for x in tails[1:].split("-"))
         tails = np.random.default_rng(seed + 100).integers(lo, hi + 1, size=N)
     q, kc, vc, bt, seq, scale = _case(N, Hq, Hkv, D, BS, prefix, tails, seed)
+    sms = torch_mod().cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert pkv.shared_prefix_plan(N, Hq, Hkv, D, BS, bt.shape[1], prefix)[0] == ovl
     got = out_to_f64(_run(q, kc, vc, bt, seq, scale, prefix))
     ref = oracle.decode_attn(q, kc, vc, bt, seq, scale)
     compare(got, ref, False)

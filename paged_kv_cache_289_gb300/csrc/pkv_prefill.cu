@@ -34,7 +34,13 @@ namespace {
 constexpr int kRows = 128;        // query rows per tile (TMEM lanes)
 constexpr int kKvTile = 256;      // tokens per K tile (and per score tile)
 constexpr int kVHalf = 128;       // tokens per V half-tile
-constexpr int kThreads = 352;     // 11 warps: 2 x 4 softmax, K producer, V producer, MMA
+constexpr int kThreads = 384;     // 12 warps: 2 x 4 softmax; K producer, V producer, MMA, idle
+// Registers per thread after the start-up: the producer/MMA warpgroup gives registers
+// back and the softmax warpgroups take them (setmaxnreg).  The block is launched with
+// kThreads x (launch registers, 168 under the launch bounds); the split must fit in that.
+constexpr int kRegsSoftmax = 216;
+constexpr int kRegsOther = 56;
+constexpr int kRegsSplit = 2 * 128 * kRegsSoftmax + 128 * kRegsOther;   // 62,464
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr uint32_t kColS = 0, kColP = 256, kColO = 384, kTmemCols = 512;
 
@@ -82,6 +88,33 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
         : "memory");
+}
+
+// Packed fp32 pairs (sm_100 family): one instruction does two fp32 FMAs or adds, each
+// rounded as its scalar form would be.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f32x2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// max of three (sm_100 family); like fmaxf, a NaN operand is ignored
+__device__ __forceinline__ float fmax3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 // 32 consecutive fp32 columns of this thread's lane.  The load and its wait sit in
@@ -369,6 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
     };
 
+    // warps 8-11 (producers, MMA issuer, one idle warp) run on few registers, the two
+    // softmax warpgroups on many; each warpgroup executes its setmaxnreg as a whole, at
+    // the head of its own branch
+    if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
     if (warp == 8 || warp == 9) {
         // ---------------------------------------------------------- TMA producers
         // warp 8 feeds the K slots (one 256-token tile each), warp 9 the V half-slots
@@ -486,7 +524,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
         }
         __syncwarp();
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ---------------------------------------------------------- softmax, 2 x 4 warps
         const int hf = warp >> 2;                // column half of every score row
         const int m = tid & 127;                 // query row = TMEM lane
@@ -534,13 +574,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int c = 0; c < HALF; ++c) s[c] = c < lim ? s[c] : -INFINITY;
             }
+            static_assert(HALF % 16 == 0, "score columns in groups of 16");
             float m8[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) m8[i] = s[i];
+            for (int i = 0; i < 8; ++i) m8[i] = fmaxf(s[i], s[i + 8]);
 #pragma unroll
-            for (int c = 8; c < HALF; ++c) m8[c & 7] = fmaxf(m8[c & 7], s[c]);
-            const float pmx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                    fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+            for (int c = 16; c < HALF; c += 16)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m8[i] = fmax3f(m8[i], s[c + i], s[c + 8 + i]);
+            const float pmx = fmaxf(fmax3f(m8[0], m8[1], m8[2]),
+                                    fmax3f(fmax3f(m8[3], m8[4], m8[5]), m8[6], m8[7]));
             float* xj = xch + (j & 1) * 2 * kRows;
             xj[hf * kRows + m] = pmx;
             named_barrier_sync(nbar, 64);
@@ -557,16 +600,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
             uint32_t p[HALF / 2];
-            float l8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) l8[i] = 0.f;
+            // column pairs: the exponent arguments by one packed FMA, the sums in four
+            // packed accumulators
+            const uint64_t sc2 = f32x2_pack(a.scale_log2, a.scale_log2);
+            const uint64_t nmu2 = f32x2_pack(nmu, nmu);
+            uint64_t l4[4] = {0ull, 0ull, 0ull, 0ull};   // (+0, +0) pairs
 #pragma unroll
             for (int c = 0; c < HALF; c += 2) {
-                const float e0 = ex2_approx(fmaf(s[c], a.scale_log2, nmu));
-                const float e1 = ex2_approx(fmaf(s[c + 1], a.scale_log2, nmu));
+                float t0, t1;
+                f32x2_unpack(f32x2_fma(f32x2_pack(s[c], s[c + 1]), sc2, nmu2), t0, t1);
+                const float e0 = ex2_approx(t0);
+                const float e1 = ex2_approx(t1);
                 p[c / 2] = pack_bf16x2(e0, e1);
-                l8[(c >> 1) & 7] += e0 + e1;
+                l4[(c >> 1) & 3] = f32x2_add(l4[(c >> 1) & 3], f32x2_pack(e0, e1));
             }
+            float l8[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) f32x2_unpack(l4[i], l8[2 * i], l8[2 * i + 1]);
             l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
             // P buffer and O are free once the previous P V has completed
             if (j >= 1) {
@@ -683,11 +733,23 @@ PFN_cuTensorMapEncodeTiled_v12000 prefill_encode_fn() {
     return fn;
 }
 
+template <typename K>
+int launch_regs(K kern) {
+    cudaFuncAttributes fa;
+    return cudaFuncGetAttributes(&fa, kern) == cudaSuccess ? fa.numRegs : 0;
+}
+
 template <int D, int BS, int G>
 cudaError_t prefill_launch_t(const PrefillLaunch& L, const PrefillArgs& a, const CUtensorMap& tk,
                              const CUtensorMap& tv, cudaStream_t st) {
     auto kern = a.prefix_split > 0 ? pkv_prefill_kernel<D, BS, G, true>
                                    : pkv_prefill_kernel<D, BS, G, false>;
+    // the register split must fit in what the block is launched with, else the softmax
+    // warps' setmaxnreg.inc could never be granted
+    static const int regs_c = launch_regs(pkv_prefill_kernel<D, BS, G, false>);
+    static const int regs_s = launch_regs(pkv_prefill_kernel<D, BS, G, true>);
+    if ((a.prefix_split > 0 ? regs_s : regs_c) * kThreads < kRegsSplit)
+        return cudaErrorInvalidConfiguration;
     // one CTA per SM (it holds all 512 TMEM columns); ask for enough shared memory
     // that no second CTA can be co-resident
     int smem = PrefillSmem<D>::BYTES;

@@ -423,18 +423,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t empty = is_k ? bar_k_empty : bar_v_empty;
         const int items = is_k ? n_tiles : n_halves;
         const int64_t row_end = (int64_t)a.NB * a.Hkv * BS;   // first row past the pool
+        // pages of item jj, and lane's block id for it: read one item ahead, so the
+        // table read overlaps the wait for the slot instead of following it
+        auto item_pages = [&](int jj) {
+            const int np = (kv_end - jj * per * BS + BS - 1) / BS;
+            return np > per ? per : np;
+        };
+        auto item_block = [&](int jj) {
+            return lane < item_pages(jj)
+                       ? a.block_table[(int64_t)r * a.MB + pg0 + jj * per + lane] : 0;
+        };
+        int blk_next = items > 0 ? item_block(0) : 0;
         for (int j = 0; j < items; ++j) {
             const int st = j & 1;
+            const int blk = blk_next;
+            if (j + 1 < items) blk_next = item_block(j + 1);
             if (j >= 2 && !warp_wait(empty + 8 * st, ((j >> 1) - 1) & 1)) break;
             if (*abort_v) break;
-            const int lb0 = j * per;                        // first page of the item in the range
-            int npages = (kv_end - lb0 * BS + BS - 1) / BS;
-            if (npages > per) npages = per;
+            const int npages = item_pages(j);
             if (lane == 0)
                 mbar_arrive_expect_tx(full + 8 * st, (uint32_t)(npages * KB * BS * 128));
             __syncwarp();
             if (lane < npages) {
-                int blk = a.block_table[(int64_t)r * a.MB + pg0 + lb0 + lane];
                 int64_t row;
                 if (blk < 0 || blk >= a.NB) {
                     if (is_k) flag_err(a.err, PKV_DEVERR_BLOCK_RANGE);

@@ -406,135 +406,136 @@ __global__ void __launch_bounds__(kThreads, 1)
     // softmax warpgroups on many; each warpgroup executes its setmaxnreg as a whole, at
     // the head of its own branch
     if (warp >= 8) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
-    if (warp == 8 || warp == 9) {
-        // ---------------------------------------------------------- TMA producers
-        // warp 8 feeds the K slots (one 256-token tile each), warp 9 the V half-slots
-        // (128 tokens each); a K slot frees when its Q K^T completes, a V half-slot
-        // when the P V MMAs reading it complete
-        const bool is_k = warp == 8;
-        if (lane == 0) prefetch_tensormap(is_k ? &tk : &tv);
-        const CUtensorMap* map = is_k ? &tk : &tv;
-        const uint32_t ring = is_k ? sK : sV;
-        const int slot_bytes = is_k ? SM::K_TILE : SM::V_HALF;
-        const int rows = is_k ? kKvTile : kVHalf;           // rows of one 64-d chunk region
-        const int per = is_k ? PAGES : HPAGES;              // pages per item
-        const uint32_t full = is_k ? bar_k_full : bar_v_full;
-        const uint32_t empty = is_k ? bar_k_empty : bar_v_empty;
-        const int items = is_k ? n_tiles : n_halves;
-        const int64_t row_end = (int64_t)a.NB * a.Hkv * BS;   // first row past the pool
-        // pages of item jj, and lane's block id for it: read one item ahead, so the
-        // table read overlaps the wait for the slot instead of following it
-        auto item_pages = [&](int jj) {
-            const int np = (kv_end - jj * per * BS + BS - 1) / BS;
-            return np > per ? per : np;
-        };
-        auto item_block = [&](int jj) {
-            return lane < item_pages(jj)
-                       ? a.block_table[(int64_t)r * a.MB + pg0 + jj * per + lane] : 0;
-        };
-        int blk_next = items > 0 ? item_block(0) : 0;
-        for (int j = 0; j < items; ++j) {
-            const int st = j & 1;
-            const int blk = blk_next;
-            if (j + 1 < items) blk_next = item_block(j + 1);
-            if (j >= 2 && !warp_wait(empty + 8 * st, ((j >> 1) - 1) & 1)) break;
-            if (*abort_v) break;
-            const int npages = item_pages(j);
-            if (lane == 0)
-                mbar_arrive_expect_tx(full + 8 * st, (uint32_t)(npages * KB * BS * 128));
-            __syncwarp();
-            if (lane < npages) {
-                int64_t row;
-                if (blk < 0 || blk >= a.NB) {
-                    if (is_k) flag_err(a.err, PKV_DEVERR_BLOCK_RANGE);
-                    row = row_end;                 // past the end: TMA fills zeros
-                } else {
-                    row = ((int64_t)blk * a.Hkv + h) * BS;
-                }
-                if (is_k) {
-                    // K: [chunk][256 rows][128 B], one box per page and chunk
-                    const uint32_t off = (uint32_t)(lane * BS * 128);
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
-                        tma_load_2d(ring + st * slot_bytes + kb * rows * 128 + off, map, kb * 64,
-                                    (int)row, full + 8 * st);
-                } else {
-                    // V: [page][chunk][BS rows][128 B], one box per page (all of D)
-                    tma_load_3d(ring + st * slot_bytes + (uint32_t)(lane * KB * BS * 128), map, 0,
-                                (int)row, 0, full + 8 * st);
-                }
-            }
-        }
-        // the last V half: once it has landed, zero its rows at or past kv_end (the
-        // partial page, pages past the request), so P = 0 never meets stale or NaN bytes
-        const int tail = n_halves - 1;
-        if (!is_k && n_halves > 0 && tail_valid < kVHalf && !*abort_v) {
-            if (warp_wait(bar_v_full + 8 * (tail & 1), (tail >> 1) & 1)) {
-                uint8_t* vst = sm + SM::V_OFF + (tail & 1) * SM::V_HALF;
-                for (int kb = 0; kb < KB; ++kb)
-                    for (int rr = tail_valid + (lane >> 3); rr < kVHalf; rr += 4)
-                        *reinterpret_cast<uint4*>(vst + ((rr / BS) * KB + kb) * BS * 128 +
-                                                  (rr % BS) * 128 + (lane & 7) * 16) =
-                            make_uint4(0u, 0u, 0u, 0u);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_v_tail);
-            }
-        }
-    } else if (warp == 10) {
-        // ---------------------------------------------------------- MMA issuer (lane 0)
-        if (lane == 0) {
-            auto issue_pv = [&](int t) -> bool {
-                if (!thread_wait(bar_p_ready, t & 1)) return false;
-                for (int hv = 0; hv < 2; ++hv) {
-                    const int t2 = 2 * t + hv;
-                    if (t2 >= n_halves) break;
-                    const int vs = t2 & 1;
-                    if (!thread_wait(bar_v_full + 8 * vs, (t2 >> 1) & 1)) return false;
-                    if (t2 == n_halves - 1 && tail_valid < kVHalf && !thread_wait(bar_v_tail, 0))
-                        return false;
-                    tc_fence_after();
-                    const uint32_t vbase = sV + vs * SM::V_HALF;
-#pragma unroll
-                    for (int k = 0; k < kVHalf / 16; ++k) {
-                        // 16 tokens inside one page: rows at 128 B, chunks BS * 128 B apart
-                        const uint32_t koff = (uint32_t)(((k * 16) / BS) * KB * BS * 128 +
-                                                         ((k * 16) % BS) * 128);
-                        const uint64_t b = smem_desc_sw128(vbase + koff, BS * 128, 1024);
-                        mma_ts(tmem + kColO, tmem + kColP + (hv * (kVHalf / 16) + k) * 8, b, ID_O,
-                               (t > 0 || hv > 0 || k > 0) ? 1u : 0u);
-                    }
-                    mma_commit(bar_v_empty + 8 * vs);
-                }
-                mma_commit(bar_pv);
-                return true;
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsOther));
+        if (warp == 8 || warp == 9) {
+            // ---------------------------------------------------------- TMA producers
+            // warp 8 feeds the K slots (one 256-token tile each), warp 9 the V half-slots
+            // (128 tokens each); a K slot frees when its Q K^T completes, a V half-slot
+            // when the P V MMAs reading it complete
+            const bool is_k = warp == 8;
+            if (lane == 0) prefetch_tensormap(is_k ? &tk : &tv);
+            const CUtensorMap* map = is_k ? &tk : &tv;
+            const uint32_t ring = is_k ? sK : sV;
+            const int slot_bytes = is_k ? SM::K_TILE : SM::V_HALF;
+            const int rows = is_k ? kKvTile : kVHalf;           // rows of one 64-d chunk region
+            const int per = is_k ? PAGES : HPAGES;              // pages per item
+            const uint32_t full = is_k ? bar_k_full : bar_v_full;
+            const uint32_t empty = is_k ? bar_k_empty : bar_v_empty;
+            const int items = is_k ? n_tiles : n_halves;
+            const int64_t row_end = (int64_t)a.NB * a.Hkv * BS;   // first row past the pool
+            // pages of item jj, and lane's block id for it: read one item ahead, so the
+            // table read overlaps the wait for the slot instead of following it
+            auto item_pages = [&](int jj) {
+                const int np = (kv_end - jj * per * BS + BS - 1) / BS;
+                return np > per ? per : np;
             };
-            bool ok = thread_wait(bar_q, 0);
-            tc_fence_after();
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                const int ks = j & 1;
-                if (!thread_wait(bar_k_full + 8 * ks, (j >> 1) & 1)) { ok = false; break; }
-                if (j >= 1 && !thread_wait(bar_s_free, (j - 1) & 1)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t kbase = sK + ks * SM::K_TILE;
+            auto item_block = [&](int jj) {
+                return lane < item_pages(jj)
+                           ? a.block_table[(int64_t)r * a.MB + pg0 + jj * per + lane] : 0;
+            };
+            int blk_next = items > 0 ? item_block(0) : 0;
+            for (int j = 0; j < items; ++j) {
+                const int st = j & 1;
+                const int blk = blk_next;
+                if (j + 1 < items) blk_next = item_block(j + 1);
+                if (j >= 2 && !warp_wait(empty + 8 * st, ((j >> 1) - 1) & 1)) break;
+                if (*abort_v) break;
+                const int npages = item_pages(j);
+                if (lane == 0)
+                    mbar_arrive_expect_tx(full + 8 * st, (uint32_t)(npages * KB * BS * 128));
+                __syncwarp();
+                if (lane < npages) {
+                    int64_t row;
+                    if (blk < 0 || blk >= a.NB) {
+                        if (is_k) flag_err(a.err, PKV_DEVERR_BLOCK_RANGE);
+                        row = row_end;                 // past the end: TMA fills zeros
+                    } else {
+                        row = ((int64_t)blk * a.Hkv + h) * BS;
+                    }
+                    if (is_k) {
+                        // K: [chunk][256 rows][128 B], one box per page and chunk
+                        const uint32_t off = (uint32_t)(lane * BS * 128);
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t col = (uint32_t)((k & 3) * 32);
-                    mma_ss(tmem + kColS,
-                           smem_desc_sw128(sQ + (k >> 2) * kRows * 128 + col, 16, 1024),
-                           smem_desc_sw128(kbase + (k >> 2) * kKvTile * 128 + col, 16, 1024), ID_S,
-                           k > 0 ? 1u : 0u);
+                        for (int kb = 0; kb < KB; ++kb)
+                            tma_load_2d(ring + st * slot_bytes + kb * rows * 128 + off, map,
+                                        kb * 64, (int)row, full + 8 * st);
+                    } else {
+                        // V: [page][chunk][BS rows][128 B], one box per page (all of D)
+                        tma_load_3d(ring + st * slot_bytes + (uint32_t)(lane * KB * BS * 128),
+                                    map, 0, (int)row, 0, full + 8 * st);
+                    }
                 }
-                mma_commit(bar_s_full);
-                mma_commit(bar_k_empty + 8 * ks);
-                // the previous tile's P V runs after this tile's scores are queued
-                if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
             }
-            if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
+            // the last V half: once it has landed, zero its rows at or past kv_end (the
+            // partial page, pages past the request), so P = 0 never meets stale or NaN bytes
+            const int tail = n_halves - 1;
+            if (!is_k && n_halves > 0 && tail_valid < kVHalf && !*abort_v) {
+                if (warp_wait(bar_v_full + 8 * (tail & 1), (tail >> 1) & 1)) {
+                    uint8_t* vst = sm + SM::V_OFF + (tail & 1) * SM::V_HALF;
+                    for (int kb = 0; kb < KB; ++kb)
+                        for (int rr = tail_valid + (lane >> 3); rr < kVHalf; rr += 4)
+                            *reinterpret_cast<uint4*>(vst + ((rr / BS) * KB + kb) * BS * 128 +
+                                                      (rr % BS) * 128 + (lane & 7) * 16) =
+                                make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_v_tail);
+                }
+            }
+        } else if (warp == 10) {
+            // ---------------------------------------------------------- MMA issuer (lane 0)
+            if (lane == 0) {
+                auto issue_pv = [&](int t) -> bool {
+                    if (!thread_wait(bar_p_ready, t & 1)) return false;
+                    for (int hv = 0; hv < 2; ++hv) {
+                        const int t2 = 2 * t + hv;
+                        if (t2 >= n_halves) break;
+                        const int vs = t2 & 1;
+                        if (!thread_wait(bar_v_full + 8 * vs, (t2 >> 1) & 1)) return false;
+                        if (t2 == n_halves - 1 && tail_valid < kVHalf &&
+                            !thread_wait(bar_v_tail, 0))
+                            return false;
+                        tc_fence_after();
+                        const uint32_t vbase = sV + vs * SM::V_HALF;
+#pragma unroll
+                        for (int k = 0; k < kVHalf / 16; ++k) {
+                            // 16 tokens inside one page: rows at 128 B, chunks BS * 128 B apart
+                            const uint32_t koff = (uint32_t)(((k * 16) / BS) * KB * BS * 128 +
+                                                             ((k * 16) % BS) * 128);
+                            const uint64_t b = smem_desc_sw128(vbase + koff, BS * 128, 1024);
+                            mma_ts(tmem + kColO, tmem + kColP + (hv * (kVHalf / 16) + k) * 8, b,
+                                   ID_O, (t > 0 || hv > 0 || k > 0) ? 1u : 0u);
+                        }
+                        mma_commit(bar_v_empty + 8 * vs);
+                    }
+                    mma_commit(bar_pv);
+                    return true;
+                };
+                bool ok = thread_wait(bar_q, 0);
+                tc_fence_after();
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    const int ks = j & 1;
+                    if (!thread_wait(bar_k_full + 8 * ks, (j >> 1) & 1)) { ok = false; break; }
+                    if (j >= 1 && !thread_wait(bar_s_free, (j - 1) & 1)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t kbase = sK + ks * SM::K_TILE;
+#pragma unroll
+                    for (int k = 0; k < D / 16; ++k) {
+                        const uint32_t col = (uint32_t)((k & 3) * 32);
+                        mma_ss(tmem + kColS,
+                               smem_desc_sw128(sQ + (k >> 2) * kRows * 128 + col, 16, 1024),
+                               smem_desc_sw128(kbase + (k >> 2) * kKvTile * 128 + col, 16, 1024),
+                               ID_S, k > 0 ? 1u : 0u);
+                    }
+                    mma_commit(bar_s_full);
+                    mma_commit(bar_k_empty + 8 * ks);
+                    // the previous tile's P V runs after this tile's scores are queued
+                    if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
+                }
+                if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
+            }
+            __syncwarp();
         }
-        __syncwarp();
-    }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
         // ---------------------------------------------------------- softmax, 2 x 4 warps

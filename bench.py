@@ -550,7 +550,9 @@ def per_workload_figures(dev, peak, main_harness=None):
     contexts (3), E4M3 / INT8 / INT4 pages (5, 7, 9) and four query positions (6) with an
     L2 flush between launches; prefix sharing (4) on logical and on unique bytes, with and
     without the flush; and workload 3's whole step with the full and the resumed prefix
-    hash.  Each launch figure is the median of 50 after 10 warm-ups.  Launched alone, the
+    hash; then the tensor-core prefill (workload 8, bf16 and INT4 pages) and the
+    copy-on-write block copy.  Each decode launch figure is the median of 50 after 10
+    warm-ups.  Launched alone, the
     decode kernels of workloads 6, 7 and 9 do not meet the full re-hash's CTAs, which in a
     step (hash first, on the side stream) hold SM resources those register-heavy plans
     need and delay some of their persistent CTAs."""
@@ -649,7 +651,70 @@ def per_workload_figures(dev, peak, main_harness=None):
         del h
         torch.cuda.synchronize(dev)
         torch.cuda.empty_cache()
+    res.update(prefill_and_copy_figures(dev, peak))
     res["clocks"] = sampler.stop()
+    return res
+
+
+def launch_times(torch, stream, launch, n, warmup, flush=None):
+    """Device times (seconds) of n launches of launch(i), each bracketed by events on
+    `stream`, after `warmup` untimed ones; `flush` (a buffer larger than L2) is read
+    before every timed launch when given."""
+    for i in range(warmup):
+        launch(i)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for k in range(n):
+        if flush is not None:
+            flush.sum()
+        ev[k][0].record(stream)
+        launch(warmup + k)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) / 1e3 for a, b in ev]
+
+
+def prefill_and_copy_figures(dev, hbm_peak):
+    """The tensor-core prefill (workload 8, bf16 and INT4 pages: median of 30 launches after
+    5, no flush: compute-bound) and the copy-on-write block copy (4,096 random pairs of the
+    70B pool, a fresh mapping per launch: median of 50 after 10), measured in the same run
+    as the decode figures."""
+    import torch
+    res = {}
+    main = torch.cuda.current_stream(dev)
+    peak, peak_kind = bf16_peak()
+    for kv in ("bf16", "int4"):
+        wl, dd, kc, vc, ks, vs, launch, err = prefill_case(dev, kv, None, main)
+        ts = launch_times(torch, main, lambda i: launch(), 30, 5)
+        assert int(err.item()) == 0, "device error word set"
+        med = median_of(ts)
+        flops = wl.prefill_flops()
+        res["8" if kv == "bf16" else "8_int4"] = {
+            "workload": wl.name, "batch": wl.N, "pages": kv,
+            "kernel": "pkv_prefill_kernel" if kv == "bf16"
+                      else "pkv_dequant_pages_kernel + pkv_prefill_kernel",
+            "flops_per_launch": flops, "median_launch_ms": round(med * 1e3, 4),
+            "achieved_tflops": round(flops / med / 1e12, 1),
+            "frac": round(flops / med / 1e12 / peak, 4), "peak": peak, "peak_source": peak_kind,
+            "l2": "no flush (compute-bound)"}
+        del wl, dd, kc, vc, ks, vs, launch, err
+        torch.cuda.synchronize(dev)
+        torch.cuda.empty_cache()
+    import paged_kv_cache_289_gb300 as pkv
+    NB, Hkv, BS, D, P, kc, vc, maps = copy_case(dev, 4096, 60)
+    ts = launch_times(torch, main, lambda i: pkv.copy_blocks(kc, vc, maps[i % len(maps)],
+                                                             stream=main), 50, 10)
+    med = median_of(ts)
+    alg = copy_algorithmic_bytes(P, Hkv, BS, D)
+    res["copy_blocks"] = {
+        "workload": "copy_blocks_llama70b_pool", "pairs_per_launch": P, "num_blocks": NB,
+        "algorithmic_bytes_per_launch": alg, "median_launch_ms": round(med * 1e3, 4),
+        "achieved": round(alg / med / 1e9, 1), "frac": round(alg / med / 1e9 / hbm_peak, 4),
+        "l2": "fresh random mapping per launch"}
+    del kc, vc, maps
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
     return res
 
 
@@ -841,6 +906,30 @@ def run_ours(args):
 
 
 # ------------------------------------------------------------------ block copy alone
+def copy_case(dev, pairs, n_maps):
+    """The 70B-layer pool (20,480 blocks of 8 KV heads x 16 tokens x 128 bf16 per cache)
+    and n_maps fresh random (source, destination) mappings of `pairs` pairs each."""
+    import torch
+    NB, Hkv, BS, D = 20480, 8, 16, 128
+    P = min(pairs, NB // 2)
+    g = torch.Generator(device=dev)
+    g.manual_seed(5)
+    kc = torch.randn((NB, Hkv, BS, D), generator=g, device=dev, dtype=torch.bfloat16)
+    vc = torch.randn((NB, Hkv, BS, D), generator=g, device=dev, dtype=torch.bfloat16)
+    rng = np.random.default_rng(6)
+    maps = []
+    for _ in range(n_maps):
+        ids = rng.permutation(NB)
+        maps.append(torch.from_numpy(np.stack([ids[:P], ids[P:2 * P]], 1).astype(np.int32))
+                    .to(dev))
+    return NB, Hkv, BS, D, P, kc, vc, maps
+
+
+def copy_algorithmic_bytes(P, Hkv, BS, D):
+    """K and V blocks read and written per pair, plus the pair's two int32 ids."""
+    return P * (2 * 2 * Hkv * BS * D * 2 + 2 * 4)
+
+
 def run_copy_blocks(args):
     """pkv_copy_blocks on the 70B-layer pool (8 KV heads x 16 tokens x 128 bf16: 32 KB per
     block and cache, 20,480 blocks, 1.34 GB for K and V): `--pairs` (source, destination)
@@ -852,19 +941,8 @@ def run_copy_blocks(args):
 
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    NB, Hkv, BS, D = 20480, 8, 16, 128
-    P = min(args.pairs, NB // 2)
-    g = torch.Generator(device=dev)
-    g.manual_seed(5)
-    kc = torch.randn((NB, Hkv, BS, D), generator=g, device=dev, dtype=torch.bfloat16)
-    vc = torch.randn((NB, Hkv, BS, D), generator=g, device=dev, dtype=torch.bfloat16)
-    rng = np.random.default_rng(6)
     K, Wm = args.steps, max(args.warmup, 3)
-    maps = []
-    for _ in range(min(K + Wm, 64)):
-        ids = rng.permutation(NB)
-        maps.append(torch.from_numpy(np.stack([ids[:P], ids[P:2 * P]], 1).astype(np.int32))
-                    .to(dev))
+    NB, Hkv, BS, D, P, kc, vc, maps = copy_case(dev, args.pairs, min(K + Wm, 64))
     main = torch.cuda.current_stream(dev)
     for i in range(Wm):
         pkv.copy_blocks(kc, vc, maps[i % len(maps)], stream=main)
@@ -887,7 +965,7 @@ def run_copy_blocks(args):
     t = e0.elapsed_time(e1) / 1e3
     avg = sum(a.elapsed_time(b) for a, b in ev) / K / 1e3
     block_bytes = Hkv * BS * D * 2
-    alg = P * (2 * 2 * block_bytes + 2 * 4)      # K and V blocks read + written, one pair entry
+    alg = copy_algorithmic_bytes(P, Hkv, BS, D)
     peak, peak_kind = peak_hbm()
     # oracle: the same copy on host memory, a bounded sample of pairs
     kh = np.zeros((2048, Hkv, BS, D), np.uint16)
@@ -923,19 +1001,14 @@ def run_copy_blocks(args):
 
 
 # ------------------------------------------------------------------ prefill attention
-def run_prefill(args):
-    """pkv_paged_prefill_attn on workload 8: 8 requests, each a 2048-token prompt chunk
-    after a cached context of U[0, 6144] tokens, Llama-3.3-70B layer shape (64/8 heads,
-    head_dim 128, bf16, 16-token blocks).  Metric: causal-effective attention TFLOP/s."""
+def prefill_case(dev, kv="bf16", batch=None, stream=None):
+    """Workload 8 on the device, ready to launch: (wl, device data, K/V caches, scales,
+    launch(), device error word).  kv picks the page kind; quantised pages are written by
+    the library's own cache write from the source rows."""
     import torch
-    import oracle
     import paged_kv_cache_289_gb300 as pkv
     from paged_kv_cache_289_gb300 import workloads as W
-
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
-    wl = W.make(8, batch=args.batch)
-    kv = args.prefill_kv
+    wl = W.make(8, batch=batch)
     wl.fp8, wl.int8, wl.int4 = kv == "fp8", kv == "int8", kv == "int4"
     dd = W.device_data(wl, dev)
     qo = torch.from_numpy(wl.q_offsets()).to(dev)
@@ -943,10 +1016,8 @@ def run_prefill(args):
     sl = torch.from_numpy(wl.seq_lens).to(dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     out = torch.empty_like(dd["q"])
-    main = torch.cuda.current_stream(dev)
     ks = vs = ws = None
     if wl.quant:
-        # quantised pages written by the library's own cache write from the source rows
         kc = torch.zeros(wl.cache_shape, dtype=torch.int8 if wl.int8 else torch.uint8,
                          device=dev)
         vc = torch.zeros_like(kc)
@@ -964,7 +1035,33 @@ def run_prefill(args):
 
     def launch():
         pkv.paged_prefill_attn(dd["q"], qo, wl.max_q_len, kc, vc, bt, sl, wl.scale, out=out,
-                               k_scale=ks, v_scale=vs, workspace=ws, error_word=err, stream=main)
+                               k_scale=ks, v_scale=vs, workspace=ws, error_word=err,
+                               stream=stream)
+    return wl, dd, kc, vc, ks, vs, launch, err
+
+
+def bf16_peak():
+    """The bf16 tensor peak the prefill is read against: MEASURED_PEAKS.json's cuBLAS
+    burst figure, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), "measured bf16_tflops (cuBLAS burst)"
+    except Exception:
+        return 1900.0, "fallback bf16 burst"
+
+
+def run_prefill(args):
+    """pkv_paged_prefill_attn on workload 8: 8 requests, each a 2048-token prompt chunk
+    after a cached context of U[0, 6144] tokens, Llama-3.3-70B layer shape (64/8 heads,
+    head_dim 128, bf16, 16-token blocks).  Metric: causal-effective attention TFLOP/s."""
+    import torch
+    import oracle
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    main = torch.cuda.current_stream(dev)
+    wl, dd, kc, vc, ks, vs, launch, err = prefill_case(dev, args.prefill_kv, args.batch, main)
 
     K, Wm = args.steps, max(args.warmup, 3)
     for _ in range(Wm):
@@ -989,13 +1086,7 @@ def run_prefill(args):
     t = e0.elapsed_time(e1) / 1e3
     avg = sum(a.elapsed_time(b) for a, b in ev) / K / 1e3
     flops = wl.prefill_flops()
-    peak = None
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            pk = json.load(f)
-        peak, peak_kind = float(pk["bf16_tflops"]), "measured bf16_tflops (cuBLAS burst)"
-    except Exception:
-        peak, peak_kind = 1900.0, "fallback bf16 burst"
+    peak, peak_kind = bf16_peak()
     achieved = flops / avg / 1e12
     # oracle: sampled rows of the same workload on the host cores, about 10 s
     q = dd["q"].contiguous().view(torch.int16).cpu().numpy().view(np.uint16)

@@ -34,7 +34,7 @@ namespace {
 constexpr int kRows = 128;        // query rows per tile (TMEM lanes)
 constexpr int kKvTile = 256;      // tokens per K tile (and per score tile)
 constexpr int kVHalf = 128;       // tokens per V half-tile
-constexpr int kThreads = 384;     // 12 warps: 2 x 4 softmax; K producer, V producer, MMA, idle
+constexpr int kThreads = 384;     // 12 warps: 2 x 4 softmax; K producer, V producer, 2 MMA issuers
 // Registers per thread after the start-up: the producer/MMA warpgroup gives registers
 // back and the softmax warpgroups take them (setmaxnreg).  The block is launched with
 // kThreads x (launch registers, 168 under the launch bounds); the split must fit in that.
@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
     };
 
-    // warps 8-11 (producers, MMA issuer, one idle warp) run on few registers, the two
+    // warps 8-11 (the two producers and the two MMA issuers) run on few registers, the two
     // softmax warpgroups on many; each warpgroup executes its setmaxnreg as a whole, at
     // the head of its own branch
     if (warp >= 8) {
@@ -482,9 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(bar_v_tail);
                 }
             }
-        } else if (warp == 10) {
-            // ---------------------------------------------------------- MMA issuer (lane 0)
-            if (lane == 0) {
+        } else if (warp == 10 || warp == 11) {
+            // ---------------------------------------------------------- MMA issuers (lane 0)
+            // warp 10 issues every Q K^T, warp 11 every P V.  They write disjoint TMEM
+            // columns (S; O), each commit tracks only its own thread's MMAs, and the
+            // barriers order what depends on what: Q K^T(j + 1) waits for S(j) to be
+            // loaded, P V(j) for P(j), and P(j + 1) is stored only after P V(j).
+            if (lane == 0 && warp == 11) {
                 auto issue_pv = [&](int t) -> bool {
                     if (!thread_wait(bar_p_ready, t & 1)) return false;
                     for (int hv = 0; hv < 2; ++hv) {
@@ -511,6 +515,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit(bar_pv);
                     return true;
                 };
+                for (int t = 0; t < n_tiles; ++t)
+                    if (!issue_pv(t)) break;
+            } else if (lane == 0) {
                 bool ok = thread_wait(bar_q, 0);
                 tc_fence_after();
                 for (int j = 0; ok && j < n_tiles; ++j) {
@@ -529,10 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(bar_s_full);
                     mma_commit(bar_k_empty + 8 * ks);
-                    // the previous tile's P V runs after this tile's scores are queued
-                    if (j >= 1 && !issue_pv(j - 1)) { ok = false; break; }
                 }
-                if (ok && n_tiles > 0) issue_pv(n_tiles - 1);
             }
             __syncwarp();
         }

@@ -20,8 +20,8 @@
 //                  halves
 // The softmax warps release S as soon as they have loaded it, so the next tile's
 // Q K^T runs during this tile's softmax.  Warp roles: warps 0-7 softmax + epilogue,
-// warp 8 K producer (and TMEM owner), warp 9 V producer, warp 10 MMA issuer (lane 0).
-// Every wait is bounded.
+// warp 8 K producer (and TMEM owner), warp 9 V producer, warp 10 the Q K^T issuer and
+// warp 11 the P V issuer (lane 0 of each).  Every wait is bounded.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
